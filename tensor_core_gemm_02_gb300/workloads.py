@@ -1,0 +1,173 @@
+"""Seeded synthetic inputs for the GEMM workloads (host side, CPU tensors).
+
+This module holds none of the GEMM arithmetic: it only draws random numbers and
+rounds them to the operand dtypes.  Both the CUDA path's tests/bench and the
+oracle consume what it returns; neither side generates inputs on its own.
+
+Recipe (numpy ``default_rng(seed)``, draws in the order listed, the dtype cast
+after each draw; float32 -> f16 by numpy ``astype`` and float32 -> bf16 by
+torch ``.to(torch.bfloat16)``, both round-to-nearest-even):
+
+  worked_16x8x32   seed 0: a = integers(-4, 5, (16, 32)) / 4, b likewise
+                   (8, 32), both f16; no C; fp32 out.  This is the input of the
+                   "mma.sync" page's worked example ("Example: a 16x8 result
+                   with two K16 issues").
+  f16_1024         seed 1: A, B (1024, 1024) N(0,1) -> f16; C (1024, 1024)
+                   N(0,1) float32; alpha = beta = 1; fp32 out.
+  bf16_8192        seed 2: A (8192, 8192) N(0,1), B (8192, 8192) 0.02 * N(0,1),
+                   both -> bf16; no C; bf16 out.
+  mlp_8192x28672x4096
+                   seed 3: A (8192, 4096) N(0,1), B (28672, 4096) 0.02 * N(0,1)
+                   -> bf16; C (8192, 28672) N(0,1) float32; alpha = 0.5,
+                   beta = 1; fp32 out.
+  skinny_16x28672x4096
+                   the same draws; A[:16] and C[:16] (numpy fills row-major, so
+                   C[:16] is the first 16 rows of the C draw and only those are
+                   drawn).
+  gather_16384_of_65536
+                   seed 4: table (65536, 4096) N(0,1) -> bf16, idx =
+                   integers(0, 65536, 16384) int32 (repeats allowed),
+                   B (4096, 4096) 0.02 * N(0,1) -> bf16; no C; fp32 out.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+OUT_TORCH = {OUT_F32: torch.float32, OUT_BF16: torch.bfloat16, OUT_F16: torch.float16}
+
+
+@dataclass
+class Problem:
+    """One GEMM problem: D = alpha * A @ B.T + beta * C, or the gathered form."""
+    name: str
+    A: torch.Tensor                 # M x K operand, or the gather table
+    B: torch.Tensor                 # N x K
+    C: torch.Tensor | None = None   # M x N float32
+    idx: torch.Tensor | None = None  # int32 row indices into A (gathered form)
+    alpha: float = 1.0
+    beta: float = 1.0
+    out: int = OUT_F32
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def M(self) -> int:
+        return int(self.idx.shape[0]) if self.idx is not None else int(self.A.shape[0])
+
+    @property
+    def N(self) -> int:
+        return int(self.B.shape[0])
+
+    @property
+    def K(self) -> int:
+        return int(self.A.shape[1])
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+def _f16(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x.astype(np.float16)))
+
+
+def _bf16(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _cast(x: np.ndarray, dtype: str) -> torch.Tensor:
+    return _f16(x) if dtype == "f16" else _bf16(x)
+
+
+def worked_16x8x32() -> Problem:
+    rng = np.random.default_rng(0)
+    a = rng.integers(-4, 5, (16, 32)) / 4
+    b = rng.integers(-4, 5, (8, 32)) / 4
+    return Problem("worked_16x8x32", _f16(a), _f16(b), None, alpha=1.0, beta=0.0,
+                   out=OUT_F32)
+
+
+def f16_1024() -> Problem:
+    rng = np.random.default_rng(1)
+    A = _f16(rng.standard_normal((1024, 1024), dtype=np.float32))
+    B = _f16(rng.standard_normal((1024, 1024), dtype=np.float32))
+    C = torch.from_numpy(rng.standard_normal((1024, 1024), dtype=np.float32))
+    return Problem("f16_1024", A, B, C, alpha=1.0, beta=1.0, out=OUT_F32)
+
+
+def bf16_8192() -> Problem:
+    rng = np.random.default_rng(2)
+    A = _bf16(rng.standard_normal((8192, 8192), dtype=np.float32))
+    B = _bf16(0.02 * rng.standard_normal((8192, 8192), dtype=np.float32))
+    return Problem("bf16_8192", A, B, None, alpha=1.0, beta=0.0, out=OUT_BF16)
+
+
+def _mlp_draws(c_rows: int):
+    rng = np.random.default_rng(3)
+    A = _bf16(rng.standard_normal((8192, 4096), dtype=np.float32))
+    B = _bf16(0.02 * rng.standard_normal((28672, 4096), dtype=np.float32))
+    C = torch.from_numpy(rng.standard_normal((c_rows, 28672), dtype=np.float32))
+    return A, B, C
+
+
+def mlp_8192x28672x4096() -> Problem:
+    A, B, C = _mlp_draws(8192)
+    return Problem("mlp_8192x28672x4096", A, B, C, alpha=0.5, beta=1.0, out=OUT_F32)
+
+
+def skinny_16x28672x4096() -> Problem:
+    A, B, C = _mlp_draws(16)
+    return Problem("skinny_16x28672x4096", A[:16].contiguous(), B, C, alpha=0.5,
+                   beta=1.0, out=OUT_F32)
+
+
+def gather_16384_of_65536() -> Problem:
+    rng = np.random.default_rng(4)
+    table = _bf16(rng.standard_normal((65536, 4096), dtype=np.float32))
+    idx = torch.from_numpy(rng.integers(0, 65536, 16384).astype(np.int32))
+    B = _bf16(0.02 * rng.standard_normal((4096, 4096), dtype=np.float32))
+    return Problem("gather_16384_of_65536", table, B, None, idx=idx, alpha=1.0,
+                   beta=0.0, out=OUT_F32)
+
+
+WORKLOADS = {
+    "worked_16x8x32": worked_16x8x32,
+    "f16_1024": f16_1024,
+    "bf16_8192": bf16_8192,
+    "mlp_8192x28672x4096": mlp_8192x28672x4096,
+    "skinny_16x28672x4096": skinny_16x28672x4096,
+    "gather_16384_of_65536": gather_16384_of_65536,
+}
+
+
+def random_problem(seed: int, M: int, N: int, K: int, dtype: str = "bf16",
+                   values: str = "normal", with_c: bool = False, alpha: float = 1.0,
+                   beta: float = 1.0, out: int = OUT_F32, gather_rows: int | None = None,
+                   b_scale: float = 1.0) -> Problem:
+    """A seeded problem of any size.
+
+    values="quarter": entries are integers in [-4, 4] divided by 4 (the worked
+    example's recipe; C likewise), so every partial sum is exact in float32.
+    values="normal": N(0,1) entries (B scaled by b_scale, C N(0,1)).
+    gather_rows: if set, A is a table of that many rows and M random indices
+    (with repeats) are drawn into it.
+    """
+    rng = np.random.default_rng(seed)
+    a_rows = gather_rows if gather_rows is not None else M
+
+    def draw(shape, scale=1.0):
+        if values == "quarter":
+            return (rng.integers(-4, 5, shape) / 4).astype(np.float32)
+        return (scale * rng.standard_normal(shape, dtype=np.float32)).astype(np.float32)
+
+    A = _cast(draw((a_rows, K)), dtype)
+    idx = None
+    if gather_rows is not None:
+        idx = torch.from_numpy(rng.integers(0, gather_rows, M).astype(np.int32))
+    B = _cast(draw((N, K), b_scale), dtype)
+    C = torch.from_numpy(draw((M, N))) if with_c else None
+    return Problem(f"random_{values}_{M}x{N}x{K}_{dtype}", A, B, C, idx=idx,
+                   alpha=alpha, beta=beta, out=out)

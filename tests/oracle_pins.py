@@ -1,0 +1,173 @@
+"""Checks that pin the oracle to facts other than itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with
+something the pages or the mathematics fix.  They run against the real oracle
+in test_oracle_pins.py and against deliberately broken copies of oracle.c in
+test_oracle_mutants.py (where at least one pin must fail).
+"""
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+from tensor_core_gemm_02_gb300 import workloads
+
+
+def _f64(t):
+    """Library widening of an f16/bf16 tensor to float64 (torch/numpy, not the oracle)."""
+    return t.to(torch.float64).numpy()
+
+
+def pin_decode_f16():
+    # every binary16 pattern against numpy's float16 -> float64 widening
+    bits = np.arange(65536, dtype=np.uint16)
+    want = bits.view(np.float16).astype(np.float64)
+    got = oracle.decode(bits, "f16")
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def pin_decode_bf16():
+    # every bfloat16 pattern against torch's bfloat16 -> float64 widening
+    bits = np.arange(65536, dtype=np.uint16)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.decode(bits, "bf16")
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def pin_worked_example_exact():
+    """The "mma.sync" page's worked example: exact rational brute force.
+
+    Entries are quarter-integers, products are multiples of 1/16 and 32 of them
+    sum exactly, so the result is a multiple of 1/16 with |value| <= 32.
+    """
+    p = workloads.worked_16x8x32()
+    ref, _, bad = oracle.gemm(p.A, p.B)
+    assert not bad
+    a = p.A.to(torch.float64).numpy()
+    b = p.B.to(torch.float64).numpy()
+    for i in range(16):
+        for j in range(8):
+            exact = sum(Fraction(float(a[i, k])) * Fraction(float(b[j, k])) for k in range(32))
+            assert Fraction(float(ref[i, j])) == exact, (i, j)
+    assert np.all(np.abs(ref) <= 32)
+    assert np.all(ref * 16 == np.round(ref * 16))
+    # the page checks against a @ b.T in float32 (rtol = atol = 2e-4)
+    np.testing.assert_allclose(ref, p.A.float().numpy() @ p.B.float().numpy().T,
+                               rtol=2e-4, atol=2e-4)
+
+
+def pin_matches_numpy_random_shapes():
+    """Non-square shapes catch transposed operands and wrong strides."""
+    for seed, (M, N, K) in enumerate([(5, 7, 3), (13, 3, 40), (2, 11, 17), (9, 9, 64), (1, 6, 129)]):
+        for dtype in ("f16", "bf16"):
+            pr = workloads.random_problem(seed, M, N, K, dtype=dtype, with_c=True,
+                                          alpha=0.75, beta=-1.5)
+            ref, absprod, bad = oracle.gemm(pr.A, pr.B, pr.C, pr.alpha, pr.beta)
+            a, b, c = _f64(pr.A), _f64(pr.B), pr.C.numpy().astype(np.float64)
+            want = pr.alpha * (a @ b.T) + pr.beta * c
+            tol = 1e-12 * (np.abs(a) @ np.abs(b).T + np.abs(c) + 1)
+            assert np.all(np.abs(ref - want) <= tol), (M, N, K, dtype)
+            np.testing.assert_allclose(absprod, np.abs(a) @ np.abs(b).T, rtol=1e-12, atol=0)
+
+
+def pin_two_a_plus_one():
+    """The "fma" page's example: with small integers the reference is exactly 2*A+1.
+
+    B = identity (N = K), C = ones, alpha = 2, beta = 1  =>  D = 2 X + 1.
+    """
+    rng = np.random.default_rng(7)
+    K = 24
+    X = rng.integers(-64, 65, (10, K)).astype(np.float16)
+    eye = np.eye(K, dtype=np.float16)
+    ones = np.ones((10, K), np.float32)
+    ref, _, _ = oracle.gemm(X, eye, ones, alpha=2.0, beta=1.0)
+    assert np.array_equal(ref, 2 * X.astype(np.float64) + 1)
+
+
+def pin_fma_separation():
+    """A case whose exact result lies between float32 neighbours of a rounded multiply.
+
+    acc = 1 + 2^-12, alpha = 1 + 2^-12, C = -1, beta = 1:
+    alpha * acc + C = 2^-11 + 2^-24 exactly (fused, one rounding); a rounded
+    multiply first gives 1 + 2^-11 (tie to even) and then 2^-11.
+    """
+    K = 8
+    a = np.zeros((1, K), np.float16)
+    a[0, 0], a[0, 1] = 1.0, 2.0 ** -12
+    b = np.zeros((1, K), np.float16)
+    b[0, 0], b[0, 1] = 1.0, 1.0
+    c = np.full((1, 1), -1.0, np.float32)
+    alpha = float(np.float32(1 + 2.0 ** -12))
+    ref, _, _ = oracle.gemm(a, b, c, alpha=alpha, beta=1.0)
+    fused = 2.0 ** -11 + 2.0 ** -24
+    assert ref[0, 0] == fused
+    assert np.float32(ref[0, 0]) == np.float32(fused)
+    unfused = np.float32(np.float32(alpha) * np.float32(1 + 2.0 ** -12)) - np.float32(1)
+    assert unfused == np.float32(2.0 ** -11) != np.float32(fused)
+
+
+def pin_alpha_beta_c_cases():
+    pr = workloads.random_problem(11, 6, 5, 32, dtype="bf16", values="quarter", with_c=True)
+    a, b, c = _f64(pr.A), _f64(pr.B), pr.C.numpy().astype(np.float64)
+    # alpha = 0 leaves beta * C exactly
+    ref, _, _ = oracle.gemm(pr.A, pr.B, pr.C, alpha=0.0, beta=2.0)
+    assert np.array_equal(ref, 2.0 * c)
+    # C absent equals an explicit zero C
+    r0, _, _ = oracle.gemm(pr.A, pr.B, None, alpha=1.0, beta=1.0)
+    rz, _, _ = oracle.gemm(pr.A, pr.B, np.zeros((6, 5), np.float32), alpha=1.0, beta=1.0)
+    assert np.array_equal(r0, rz)
+    assert np.array_equal(r0, a @ b.T)  # exact on quarter-integers
+    # beta = 0 means C is not read: NaN in C does not reach the result
+    cn = np.full((6, 5), np.nan, np.float32)
+    rn, _, _ = oracle.gemm(pr.A, pr.B, cn, alpha=1.0, beta=0.0)
+    assert np.array_equal(rn, a @ b.T)
+    # alpha = -1, beta = 0.5, all exact
+    rs, _, _ = oracle.gemm(pr.A, pr.B, pr.C, alpha=-1.0, beta=0.5)
+    assert np.array_equal(rs, -(a @ b.T) + 0.5 * c)
+
+
+def pin_gather_invariants():
+    rng = np.random.default_rng(5)
+    pr = workloads.random_problem(12, 9, 7, 20, dtype="bf16", with_c=True)
+    table = pr.A  # 9 x 20
+    plain, _, _ = oracle.gemm(table, pr.B, pr.C, 1.0, 1.0)
+    ar = torch.arange(9, dtype=torch.int32)
+    g, _, bad = oracle.gemm(table, pr.B, pr.C, 1.0, 1.0, idx=ar)
+    assert not bad and np.array_equal(g, plain)
+    perm = rng.permutation(9).astype(np.int32)
+    g2, _, _ = oracle.gemm(table, pr.B, None, 1.0, 0.0, idx=torch.from_numpy(perm))
+    want, _, _ = oracle.gemm(table[torch.from_numpy(perm).long()].contiguous(), pr.B, None, 1.0, 0.0)
+    assert np.array_equal(g2, want)
+    dup = torch.tensor([3, 3, 0, 3], dtype=torch.int32)
+    g3, _, _ = oracle.gemm(table, pr.B, None, 1.0, 0.0, idx=dup)
+    assert np.array_equal(g3[0], g3[1]) and np.array_equal(g3[0], g3[3])
+    assert np.array_equal(g3[0], plain[3] - pr.C.numpy()[3].astype(np.float64))
+    # an index outside the table makes the row zero and is reported
+    badidx = torch.tensor([1, 9, -1, 2], dtype=torch.int32)
+    c4 = pr.C[:4].contiguous()
+    g4, _, bad4 = oracle.gemm(table, pr.B, c4, 1.0, 0.5, idx=badidx)
+    assert bad4
+    assert np.array_equal(g4[1], 0.5 * c4.numpy()[1].astype(np.float64))
+    assert np.array_equal(g4[2], 0.5 * c4.numpy()[2].astype(np.float64))
+
+
+def pin_entries_match_rows():
+    pr = workloads.random_problem(13, 17, 19, 40, dtype="f16", with_c=True, alpha=0.5,
+                                  beta=2.0)
+    full, fabs_, _ = oracle.gemm(pr.A, pr.B, pr.C, pr.alpha, pr.beta)
+    ii = np.array([0, 16, 5, 7, 16], np.int64)
+    jj = np.array([0, 18, 3, 18, 0], np.int64)
+    e, eabs, _ = oracle.gemm_entries(pr.A, pr.B, ii, jj, pr.C, pr.alpha, pr.beta)
+    assert np.array_equal(e, full[ii, jj]) and np.array_equal(eabs, fabs_[ii, jj])
+    part, _, _ = oracle.gemm(pr.A, pr.B, pr.C, pr.alpha, pr.beta, rows=(4, 11))
+    assert np.array_equal(part, full[4:11])
+
+
+ALL_PINS = [pin_decode_f16, pin_decode_bf16, pin_worked_example_exact,
+            pin_matches_numpy_random_shapes, pin_two_a_plus_one, pin_fma_separation,
+            pin_alpha_beta_c_cases, pin_gather_invariants, pin_entries_match_rows]
