@@ -1,0 +1,189 @@
+/*
+ * tcgemm.h -- C ABI of the GB300 (sm_103a) tensor-core GEMM library.
+ *
+ * Operation (all entry points):
+ *
+ *     D[i][j] = fma.rn.f32(alpha, sum_k A[i][k] * B[j][k], beta * C[i][j])
+ *
+ *  - A is row-major M x K and B is stored N x K, so the product is A times B
+ *    transposed ("mma.sync" page, section "Operand coordinates and ownership":
+ *    B's atom axes are (N, K/2) although the product uses B transposed).
+ *  - A and B are both f16 or both bf16; the sum is accumulated in float32
+ *    ("mma.sync" page, introduction); C is float32 (same page, operand table).
+ *  - alpha and beta are applied after the product at the call site as one
+ *    single-rounded fma.rn.f32 ("mma.sync" page, section "Accumulation,
+ *    transpose and alpha/beta"; "fma" page, section "Operand specification":
+ *    a*b+c is one fused atom, not a rounded multiply and a rounded add).
+ *    With C == NULL or beta == 0, C is not read and D = alpha * sum
+ *    (mul.rn.f32).  beta * C is formed with mul.rn.f32 before the fma.
+ *  - The K recurrence starts from zero ("mma.sync" page, worked example: the
+ *    first K issue uses scalar C = 0, later issues read D); C enters in the
+ *    epilogue fma above.
+ *  - D is float32, bf16 or f16.  The 16-bit outputs are the float32 result
+ *    rounded to nearest even (cvt.rn).
+ *
+ * Layout: every matrix is row-major with an explicit leading dimension
+ * (elements between the starts of consecutive rows).  Rows of A, B and the
+ * gather table are K contiguous elements; rows of C and D are N contiguous
+ * elements.
+ *
+ * Ownership: every pointer argument is caller-owned device memory (any
+ * allocator; typically PyTorch).  The library never frees or retains caller
+ * memory beyond the asynchronous execution of the call.  It holds, per
+ * device, a small status word in its own device globals and a host-side cache
+ * of TMA descriptors; the skinny (M <= 64) path also keeps a per-device
+ * workspace that it allocates once and grows on demand.
+ *
+ * Execution: calls are asynchronous on `stream` (a cudaStream_t; NULL means
+ * the legacy default stream) on the current device.
+ *
+ * Errors:
+ *  - Argument, alignment, aliasing and type errors are returned synchronously
+ *    before anything is launched, following the descriptor legality rule that
+ *    invalid fields are rejected rather than promoted, folded or reinterpreted
+ *    ("cp.async.bulk.tensor" page, section "Operands and descriptor fields").
+ *  - Launch failures return GEMM_ERR_CUDA.
+ *  - Errors found on the device (a pipeline wait that ran out of time, a
+ *    gather index outside the table) are recorded in the device status word
+ *    and returned by gemm_check_device_status().  No kernel traps.
+ */
+#ifndef TCGEMM_H
+#define TCGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* negative size, NULL required pointer, bad leading dim, bad enum */
+    GEMM_ERR_ALIGNMENT = 2,   /* pointer not 16-byte aligned or row pitch not a multiple of 16 bytes */
+    GEMM_ERR_UNSUPPORTED = 3, /* a size of 2^31 or more, or a device without tcgen05 (not sm_103) */
+    GEMM_ERR_ALIAS = 4,       /* D overlaps A, B, idx, or C other than exactly in place */
+    GEMM_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed */
+    GEMM_ERR_TIMEOUT = 6,     /* device: a pipeline wait ran out of time; the kernel returned */
+    GEMM_ERR_INDEX = 7        /* device: a gather index was outside [0, table_rows) */
+} gemm_status;
+
+typedef enum {
+    GEMM_OUT_F32 = 0,
+    GEMM_OUT_BF16 = 1,
+    GEMM_OUT_F16 = 2
+} gemm_out_t;
+
+/*
+ * D = fma.rn(alpha, A * B^T, beta * C) with f16 operands.
+ *
+ *  M, N, K     sizes, each in [0, 2^31).  M == 0 or N == 0: nothing is done.
+ *              K == 0: D = beta * C (or 0 when C is absent).
+ *  A, lda      M x K f16, lda >= K, lda % 8 == 0, 16-byte aligned.
+ *              May be NULL only when K == 0.
+ *  B, ldb      N x K f16, ldb >= K, ldb % 8 == 0, 16-byte aligned.
+ *              May be NULL only when K == 0.
+ *  C, ldc      M x N float32 or NULL (absent).  ldc >= N, ldc % 4 == 0,
+ *              16-byte aligned.  Not read when beta == 0.
+ *  D, ldd      M x N output of type `out`; ldd >= N, ldd * sizeof(out) a
+ *              multiple of 16, 16-byte aligned.  D may be C exactly (same
+ *              pointer, ldd == ldc, out == GEMM_OUT_F32); any other overlap
+ *              of D with A, B or C is GEMM_ERR_ALIAS.
+ *  out         a gemm_out_t value.
+ *  stream      cudaStream_t to run on.
+ */
+gemm_status gemm_f16(int64_t M, int64_t N, int64_t K,
+                     const void *A, int64_t lda,
+                     const void *B, int64_t ldb,
+                     const float *C, int64_t ldc,
+                     void *D, int64_t ldd,
+                     int out, float alpha, float beta, void *stream);
+
+/* As gemm_f16 with bf16 operands. */
+gemm_status gemm_bf16(int64_t M, int64_t N, int64_t K,
+                      const void *A, int64_t lda,
+                      const void *B, int64_t ldb,
+                      const float *C, int64_t ldc,
+                      void *D, int64_t ldd,
+                      int out, float alpha, float beta, void *stream);
+
+/*
+ * Row-gathered form: D[i][:] = fma.rn(alpha, table[idx[i]][:] * B^T, beta * C[i][:])
+ * for i < M.  The A rows are fetched four at a time with TMA tile::gather4
+ * loads ("cp.async.bulk.tensor" page, section "Gather4 and scatter4": four
+ * runtime row coordinates per issue, not necessarily consecutive; choosing
+ * them is the caller's logic).  Indices may repeat.
+ *
+ *  dtype_is_bf16  0: table and B are f16; 1: bf16.
+ *  table, lda     table_rows x K, lda >= K, lda % 8 == 0, 16-byte aligned.
+ *  table_rows     rows in the table, in [1, 2^31).
+ *  idx            M int32 row indices in device memory, 4-byte aligned.
+ *                 An index outside [0, table_rows) makes that A row zero (so
+ *                 D[i][:] = beta * C[i][:]) and records GEMM_ERR_INDEX in the
+ *                 device status word.
+ *  Other arguments as in gemm_f16.  D must not overlap idx or the table.
+ */
+gemm_status gemm_gather_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
+                             const void *table, int64_t table_rows, int64_t lda,
+                             const int32_t *idx,
+                             const void *B, int64_t ldb,
+                             const float *C, int64_t ldc,
+                             void *D, int64_t ldd,
+                             int out, float alpha, float beta, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the first error the device
+ * recorded since the last call on the current device (GEMM_OK if none).
+ * Returns GEMM_ERR_CUDA if the synchronisation itself failed.  After a
+ * device-side error it also resets the library's scratch state on this
+ * device, so later calls start clean.
+ */
+gemm_status gemm_check_device_status(void *stream);
+
+/* Static, NUL-terminated name of a status code ("GEMM_OK", ...). */
+const char *gemm_status_string(int status);
+
+/*
+ * The kernel choice the library makes for a problem, without launching
+ * anything and without touching the GPU (for diagnostics and tests).
+ *
+ *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles),
+ *           2 = skinny swap-AB kernel (M <= 64), 3 = K == 0 epilogue only
+ *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
+ *  stages   shared-memory ring depth
+ *  tiles    output tiles; splits = K slices per tile (skinny kernel)
+ *  grid     CTAs launched for `sm_count` SMs
+ */
+typedef struct {
+    int32_t kernel;
+    int32_t bm;
+    int32_t bn;
+    int32_t stages;
+    int64_t tiles;
+    int32_t splits;
+    int32_t grid;
+} gemm_plan;
+
+gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather,
+                            int sm_count, gemm_plan *plan);
+
+/*
+ * Time limit, in nanoseconds, of every bounded pipeline wait in the kernels
+ * (default 2e9).  A wait that runs out records GEMM_ERR_TIMEOUT, the kernel
+ * stops its pipeline, releases its tensor memory and returns.  ns == 0
+ * restores the default.  Applies to launches made after the call.
+ */
+gemm_status gemm_set_wait_timeout(uint64_t ns);
+
+/*
+ * Test hook.  mode 1: the next launches add 16 bytes to the transaction
+ * count the first shared-memory stage expects, so that stage never completes
+ * and its bounded wait runs out (all copies still land; nothing faults).
+ * mode 0 turns it off.
+ */
+gemm_status gemm_debug_inject(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCGEMM_H */

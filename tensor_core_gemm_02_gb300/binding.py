@@ -1,0 +1,178 @@
+"""ctypes binding of libtcgemm.so (include/tcgemm.h).  Marshalling only.
+
+The raw entry points keep the C names and argument lists (``lib().gemm_bf16``
+etc. via :func:`load_library`).  The functions below take torch CUDA tensors,
+read their pointers, leading dimensions and the current stream, call the
+C function of the same name and raise :class:`GemmError` on a non-OK status.
+Every step of the computation runs in the library's CUDA kernels; there is no
+fallback.  If the library is missing this module raises instead of computing
+anything some other way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libtcgemm.so")
+
+GEMM_OK = 0
+GEMM_ERR_TIMEOUT = 6
+GEMM_ERR_INDEX = 7
+OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+_OUT_OF_DTYPE = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16, torch.float16: OUT_F16}
+_DTYPE_OF_OUT = {v: k for k, v in _OUT_OF_DTYPE.items()}
+
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = int(status)
+        super().__init__(f"{where}: {gemm_status_string(status)} ({status})")
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("bm", ctypes.c_int32), ("bn", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("tiles", ctypes.c_int64),
+                ("splits", ctypes.c_int32), ("grid", ctypes.c_int32)]
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libtcgemm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it first (python -m tensor_core_gemm_02_gb300.build)")
+    lib = ctypes.CDLL(path)
+    i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+    plain = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, f32, f32, vp]
+    lib.gemm_f16.argtypes = plain
+    lib.gemm_bf16.argtypes = plain
+    lib.gemm_gather_rows.argtypes = [i64, i64, i64, i32, vp, i64, i64, vp, vp, i64, vp, i64,
+                                     vp, i64, i32, f32, f32, vp]
+    lib.gemm_check_device_status.argtypes = [vp]
+    lib.gemm_status_string.argtypes = [i32]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_query_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(Plan)]
+    lib.gemm_set_wait_timeout.argtypes = [ctypes.c_uint64]
+    lib.gemm_debug_inject.argtypes = [i32]
+    for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_check_device_status",
+                 "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def gemm_status_string(status: int) -> str:
+    return load_library().gemm_status_string(int(status)).decode()
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ld(t: torch.Tensor) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("matrices must be 2-D with unit column stride")
+    return int(t.stride(0)) if t.shape[0] > 1 else max(int(t.stride(0)), int(t.shape[1]))
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _check(status: int, where: str):
+    if status != GEMM_OK:
+        raise GemmError(status, where)
+
+
+def _out_tensor(D, M, N, out, device):
+    if D is None:
+        return torch.empty((M, N), dtype=_DTYPE_OF_OUT[out], device=device)
+    if _OUT_OF_DTYPE.get(D.dtype) != out:
+        raise TypeError("D's dtype does not match `out`")
+    return D
+
+
+def _plain(name, dtype, A, B, C, D, alpha, beta, out, stream):
+    if A.dtype != dtype or B.dtype != dtype:
+        raise TypeError(f"{name} needs {dtype} A and B")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    if C is not None and (C.dtype != torch.float32 or tuple(C.shape) != (M, N)):
+        raise ValueError("C must be float32 M x N")
+    D = _out_tensor(D, M, N, out, A.device)
+    st = getattr(load_library(), name)(
+        M, N, K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C) if C is not None else 0,
+        _ptr(D), _ld(D), out, float(alpha), float(beta), _stream_ptr(stream))
+    _check(st, name)
+    return D
+
+
+def gemm_f16(A, B, C=None, D=None, *, alpha=1.0, beta=1.0, out=OUT_F32, stream=None):
+    """D = fma.rn(alpha, A @ B.T, beta * C) with f16 A (M x K) and B (N x K)."""
+    return _plain("gemm_f16", torch.float16, A, B, C, D, alpha, beta, out, stream)
+
+
+def gemm_bf16(A, B, C=None, D=None, *, alpha=1.0, beta=1.0, out=OUT_F32, stream=None):
+    """D = fma.rn(alpha, A @ B.T, beta * C) with bf16 A (M x K) and B (N x K)."""
+    return _plain("gemm_bf16", torch.bfloat16, A, B, C, D, alpha, beta, out, stream)
+
+
+def gemm_gather_rows(table, idx, B, C=None, D=None, *, alpha=1.0, beta=1.0, out=OUT_F32,
+                     stream=None):
+    """D[i] = fma.rn(alpha, table[idx[i]] @ B.T, beta * C[i])."""
+    if table.dtype not in (torch.float16, torch.bfloat16) or B.dtype != table.dtype:
+        raise TypeError("table and B must both be f16 or both bf16")
+    if idx.dtype != torch.int32 or idx.dim() != 1:
+        raise TypeError("idx must be a 1-D int32 tensor")
+    M = int(idx.shape[0])
+    rows, K = table.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("table and B disagree on K")
+    if C is not None and (C.dtype != torch.float32 or tuple(C.shape) != (M, N)):
+        raise ValueError("C must be float32 M x N")
+    D = _out_tensor(D, M, N, out, table.device)
+    st = load_library().gemm_gather_rows(
+        M, N, K, 1 if table.dtype == torch.bfloat16 else 0, _ptr(table), rows, _ld(table),
+        _ptr(idx), _ptr(B), _ld(B), _ptr(C), _ld(C) if C is not None else 0, _ptr(D), _ld(D),
+        out, float(alpha), float(beta), _stream_ptr(stream))
+    _check(st, "gemm_gather_rows")
+    return D
+
+
+def gemm(A, B, C=None, *, alpha=1.0, beta=1.0, out_dtype=torch.float32, D=None, stream=None):
+    """Dispatch on A's dtype to gemm_f16 / gemm_bf16."""
+    out = _OUT_OF_DTYPE[out_dtype]
+    fn = gemm_bf16 if A.dtype == torch.bfloat16 else gemm_f16
+    return fn(A, B, C, D, alpha=alpha, beta=beta, out=out, stream=stream)
+
+
+def gemm_check_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device-side status code."""
+    return int(load_library().gemm_check_device_status(_stream_ptr(stream)))
+
+
+def gemm_query_plan(M, N, K, gather=False, sm_count=148) -> Plan:
+    p = Plan()
+    _check(load_library().gemm_query_plan(M, N, K, int(bool(gather)), sm_count,
+                                          ctypes.byref(p)), "gemm_query_plan")
+    return p
+
+
+def gemm_set_wait_timeout(ns: int) -> None:
+    _check(load_library().gemm_set_wait_timeout(int(ns)), "gemm_set_wait_timeout")
+
+
+def gemm_debug_inject(mode: int) -> None:
+    _check(load_library().gemm_debug_inject(int(mode)), "gemm_debug_inject")

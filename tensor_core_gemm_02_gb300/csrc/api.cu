@@ -1,0 +1,456 @@
+// api.cu -- the C ABI declared in include/tcgemm.h: argument validation,
+// TMA descriptor encoding (with a small cache), kernel choice and launch, and
+// the per-device status word.
+//
+// Validation follows the descriptor legality rule of the "cp.async.bulk.tensor"
+// page (section "Operands and descriptor fields"): unit innermost stride,
+// 16-byte aligned bases and row pitches; invalid fields are rejected, never
+// promoted or reinterpreted.  Every check runs before any CUDA call, so it
+// needs no GPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "launch.h"
+#include "tcgemm.h"
+
+// First device-side error code [0] and where it arose [1], one per device.
+static __device__ uint32_t g_device_status[4];
+
+namespace {
+
+using tcg::GemmArgs;
+using tcg::GemmMaps;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    uint32_t *status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_inject{0};
+
+gemm_status device_info(DeviceInfo **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return GEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (major != 10 || minor != 3)
+            return GEMM_ERR_UNSUPPORTED;  // kernels are built for sm_103a only
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return GEMM_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.sm_count = sms;
+        d.status = static_cast<uint32_t *>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------- descriptors
+
+struct MapKey {
+    uint64_t ptr, inner, outer, stride;
+    uint32_t box_inner, box_outer, dtype, swizzle;
+    bool operator==(const MapKey &o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
+};
+
+struct MapSlot {
+    bool used = false;
+    MapKey key{};
+    CUtensorMap map{};
+};
+
+constexpr int kCacheSlots = 1024;
+MapSlot g_cache[kCacheSlots];
+std::mutex g_cache_mu;
+
+uint64_t hash_key(const MapKey &k)
+{
+    uint64_t h = 1469598103934665603ull;
+    const unsigned char *p = reinterpret_cast<const unsigned char *>(&k);
+    for (size_t i = 0; i < sizeof(k); ++i) {
+        h ^= p[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+// A 2-D row-major tensor: `inner` contiguous elements per row, `outer` rows
+// `stride_bytes` apart, copied in boxes of box_inner x box_outer.
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dtype, const void *ptr, uint64_t inner,
+               uint64_t outer, uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle)
+{
+    MapKey key;
+    std::memset(&key, 0, sizeof(key));
+    key.ptr = reinterpret_cast<uint64_t>(ptr);
+    key.inner = inner;
+    key.outer = outer;
+    key.stride = stride_bytes;
+    key.box_inner = box_inner;
+    key.box_outer = box_outer;
+    key.dtype = static_cast<uint32_t>(dtype);
+    key.swizzle = static_cast<uint32_t>(swizzle);
+    const int slot = static_cast<int>(hash_key(key) % kCacheSlots);
+    {
+        std::lock_guard<std::mutex> lock(g_cache_mu);
+        if (g_cache[slot].used && g_cache[slot].key == key) {
+            *m = g_cache[slot].map;
+            return true;
+        }
+    }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    g_cache[slot].used = true;
+    g_cache[slot].key = key;
+    g_cache[slot].map = *m;
+    return true;
+}
+
+// ------------------------------------------------------------- validation
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// bytes spanned by a rows x cols matrix with leading dimension ld
+uint64_t span_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t esize)
+{
+    if (rows <= 0 || cols <= 0)
+        return 0;
+    return static_cast<uint64_t>(((rows - 1) * ld + cols) * esize);
+}
+
+bool overlap(const void *a, uint64_t an, const void *b, uint64_t bn)
+{
+    if (!a || !b || an == 0 || bn == 0)
+        return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int out_size(int out) { return out == GEMM_OUT_F32 ? 4 : 2; }
+
+struct Problem {
+    int64_t M, N, K;
+    bool bf16;
+    const void *A;
+    int64_t a_rows;  // rows of A, or of the gather table
+    int64_t lda;
+    const int32_t *idx;
+    const void *B;
+    int64_t ldb;
+    const float *C;
+    int64_t ldc;
+    void *D;
+    int64_t ldd;
+    int out;
+    float alpha, beta;
+    bool gather;
+    cudaStream_t stream;
+};
+
+gemm_status validate(const Problem &p, bool *empty)
+{
+    *empty = false;
+    if (p.M < 0 || p.N < 0 || p.K < 0 || p.a_rows < 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (p.out != GEMM_OUT_F32 && p.out != GEMM_OUT_BF16 && p.out != GEMM_OUT_F16)
+        return GEMM_ERR_INVALID_ARG;
+    if (p.M > kMaxDim || p.N > kMaxDim || p.K > kMaxDim || p.a_rows > kMaxDim)
+        return GEMM_ERR_UNSUPPORTED;
+    if (p.M == 0 || p.N == 0) {
+        *empty = true;
+        return GEMM_OK;
+    }
+    const bool c_used = p.C != nullptr && p.beta != 0.0f;
+    if (!p.D)
+        return GEMM_ERR_INVALID_ARG;
+    if (p.K > 0 && (!p.A || !p.B))
+        return GEMM_ERR_INVALID_ARG;
+    if (p.gather && (!p.idx || p.a_rows < 1))
+        return GEMM_ERR_INVALID_ARG;
+    if (p.ldd < p.N)
+        return GEMM_ERR_INVALID_ARG;
+    if (c_used && p.ldc < p.N)
+        return GEMM_ERR_INVALID_ARG;
+    if (p.K > 0 && (p.lda < p.K || p.ldb < p.K))
+        return GEMM_ERR_INVALID_ARG;
+    if (p.lda > kMaxDim || p.ldb > kMaxDim || p.ldc > kMaxDim || p.ldd > kMaxDim)
+        return GEMM_ERR_UNSUPPORTED;
+    // alignment: 16-byte bases, row pitches that are multiples of 16 bytes
+    if (p.K > 0 && (!aligned16(p.A) || !aligned16(p.B) || (p.lda * 2) % 16 || (p.ldb * 2) % 16))
+        return GEMM_ERR_ALIGNMENT;
+    if (c_used && (!aligned16(p.C) || (p.ldc * 4) % 16))
+        return GEMM_ERR_ALIGNMENT;
+    if (!aligned16(p.D) || (p.ldd * out_size(p.out)) % 16)
+        return GEMM_ERR_ALIGNMENT;
+    if (p.gather && (reinterpret_cast<uintptr_t>(p.idx) & 3u))
+        return GEMM_ERR_ALIGNMENT;
+    // aliasing: D may only coincide exactly with C (fp32 in-place update)
+    const uint64_t d_span = span_bytes(p.M, p.N, p.ldd, out_size(p.out));
+    if (p.K > 0) {
+        if (overlap(p.D, d_span, p.A, span_bytes(p.a_rows, p.K, p.lda, 2)))
+            return GEMM_ERR_ALIAS;
+        if (overlap(p.D, d_span, p.B, span_bytes(p.N, p.K, p.ldb, 2)))
+            return GEMM_ERR_ALIAS;
+    }
+    if (p.gather && overlap(p.D, d_span, p.idx, static_cast<uint64_t>(p.M) * 4))
+        return GEMM_ERR_ALIAS;
+    if (c_used && overlap(p.D, d_span, p.C, span_bytes(p.M, p.N, p.ldc, 4))) {
+        const bool exact_in_place = static_cast<const void *>(p.C) == p.D &&
+                                    p.out == GEMM_OUT_F32 && p.ldc == p.ldd;
+        if (!exact_in_place)
+            return GEMM_ERR_ALIAS;
+    }
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------- planning
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Tile width for the 128-row tile kernel: the fewest waves of persistent
+// CTAs, weighting each wave by the tile width plus a fixed per-tile cost.
+int choose_bn(int64_t M, int64_t N, int sm_count)
+{
+    static const int widths[3] = {256, 128, 64};
+    int best = 256;
+    int64_t best_cost = -1;
+    for (int w : widths) {
+        const int64_t tiles = ceil_div(M, 128) * ceil_div(N, w);
+        const int64_t waves = ceil_div(tiles, sm_count);
+        const int64_t cost = waves * (w + 32);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = w;
+        }
+    }
+    return best;
+}
+
+gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, int sm_count)
+{
+    (void)K;
+    (void)gather;
+    gemm_plan p;
+    std::memset(&p, 0, sizeof(p));
+    if (M == 0 || N == 0)
+        return p;
+    const int bn = choose_bn(M, N, sm_count);
+    p.kernel = 1;
+    p.bm = 128;
+    p.bn = bn;
+    p.stages = tcg::tile_stages(bn);
+    p.tiles = ceil_div(M, 128) * ceil_div(N, bn);
+    p.splits = 1;
+    p.grid = static_cast<int32_t>(p.tiles < sm_count ? p.tiles : sm_count);
+    return p;
+}
+
+CUtensorMapDataType ab_type(bool bf16)
+{
+    return bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+gemm_status run(const Problem &p)
+{
+    bool empty = false;
+    gemm_status st = validate(p, &empty);
+    if (st != GEMM_OK || empty)
+        return st;
+    DeviceInfo *dev = nullptr;
+    if ((st = device_info(&dev)) != GEMM_OK)
+        return st;
+    const gemm_plan plan = make_plan(p.M, p.N, p.K, p.gather, dev->sm_count);
+    const bool c_used = p.C != nullptr && p.beta != 0.0f;
+
+    GemmMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const int bn = plan.bn;
+    if (p.K > 0) {
+        const bool ok_a =
+            p.gather ? encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.a_rows, p.lda * 2, 64, 1,
+                                 CU_TENSOR_MAP_SWIZZLE_128B)
+                     : encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.M, p.lda * 2, 64, 128,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+        const bool ok_b = encode_2d(&maps.b, ab_type(p.bf16), p.B, p.K, p.N, p.ldb * 2, 64,
+                                    static_cast<uint32_t>(bn), CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!ok_a || !ok_b)
+            return GEMM_ERR_CUDA;
+    }
+    if (c_used && !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.C, p.N, p.M, p.ldc * 4,
+                             32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GEMM_ERR_CUDA;
+    {
+        const CUtensorMapDataType dt = p.out == GEMM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : p.out == GEMM_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const CUtensorMapSwizzle sw =
+            p.out == GEMM_OUT_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        if (!encode_2d(&maps.d, dt, p.D, p.N, p.M, p.ldd * out_size(p.out), 32, 32, sw))
+            return GEMM_ERR_CUDA;
+    }
+
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.M = static_cast<int32_t>(p.M);
+    a.N = static_cast<int32_t>(p.N);
+    a.K = static_cast<int32_t>(p.K);
+    a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, 128));
+    a.num_n_blocks = static_cast<int32_t>(ceil_div(p.N, bn));
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, 64));
+    a.num_tiles = static_cast<int32_t>(plan.tiles);
+    a.group_m = a.num_m_blocks < 16 ? a.num_m_blocks : 16;
+    a.splits = 1;
+    a.kb_per_split = a.num_k_blocks;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.has_c = c_used ? 1 : 0;
+    a.out_kind = p.out;
+    a.ab_bf16 = p.bf16 ? 1 : 0;
+    a.gather = p.gather ? 1 : 0;
+    a.idx = p.idx;
+    a.table_rows = static_cast<int32_t>(p.a_rows);
+    a.extra_tx = g_inject.load() == 1 ? 16u : 0u;
+    a.status = dev->status;
+    a.timeout_ns = g_timeout_ns.load();
+
+    const cudaError_t e = tcg::launch_tile(bn, maps, a, plan.grid, p.stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------- exported ABI
+
+extern "C" {
+
+gemm_status gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                     int64_t ldb, const float *C, int64_t ldc, void *D, int64_t ldd, int out,
+                     float alpha, float beta, void *stream)
+{
+    Problem p{M, N, K, false, A, M, lda, nullptr, B, ldb, C, ldc, D, ldd, out, alpha, beta,
+              false, static_cast<cudaStream_t>(stream)};
+    return run(p);
+}
+
+gemm_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                      int64_t ldb, const float *C, int64_t ldc, void *D, int64_t ldd, int out,
+                      float alpha, float beta, void *stream)
+{
+    Problem p{M, N, K, true, A, M, lda, nullptr, B, ldb, C, ldc, D, ldd, out, alpha, beta,
+              false, static_cast<cudaStream_t>(stream)};
+    return run(p);
+}
+
+gemm_status gemm_gather_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
+                             const void *table, int64_t table_rows, int64_t lda,
+                             const int32_t *idx, const void *B, int64_t ldb, const float *C,
+                             int64_t ldc, void *D, int64_t ldd, int out, float alpha, float beta,
+                             void *stream)
+{
+    if (dtype_is_bf16 != 0 && dtype_is_bf16 != 1)
+        return GEMM_ERR_INVALID_ARG;
+    Problem p{M, N, K, dtype_is_bf16 == 1, table, table_rows, lda, idx, B, ldb, C, ldc, D, ldd,
+              out, alpha, beta, true, static_cast<cudaStream_t>(stream)};
+    return run(p);
+}
+
+gemm_status gemm_check_device_status(void *stream)
+{
+    DeviceInfo *dev = nullptr;
+    gemm_status st = device_info(&dev);
+    if (st != GEMM_OK)
+        return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    uint32_t h[2] = {0, 0};
+    if (cudaMemcpy(h, dev->status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (h[0] != 0) {
+        if (cudaMemset(dev->status, 0, sizeof(h)) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    return static_cast<gemm_status>(h[0]);
+}
+
+const char *gemm_status_string(int status)
+{
+    switch (status) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+    case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    case GEMM_ERR_INDEX: return "GEMM_ERR_INDEX";
+    default: return "GEMM_ERR_UNKNOWN";
+    }
+}
+
+gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather, int sm_count,
+                            gemm_plan *plan)
+{
+    if (!plan || sm_count < 1 || M < 0 || N < 0 || K < 0)
+        return GEMM_ERR_INVALID_ARG;
+    *plan = make_plan(M, N, K, gather != 0, sm_count);
+    return GEMM_OK;
+}
+
+gemm_status gemm_set_wait_timeout(uint64_t ns)
+{
+    g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
+    return GEMM_OK;
+}
+
+gemm_status gemm_debug_inject(int mode)
+{
+    if (mode != 0 && mode != 1)
+        return GEMM_ERR_INVALID_ARG;
+    g_inject.store(mode);
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,382 @@
+// kernel_tile.cuh -- persistent warp-specialised tcgen05 GEMM, 128 x BN tiles.
+//
+//   warp 0      producer: TMA loads of A (tiled, or tile::gather4 rows of a
+//               table) and B boxes into a STAGES-deep shared ring, each stage
+//               completing on an mbarrier armed with its byte count
+//               ("cp.async.bulk.tensor" page, sections "Example: two explicit
+//               8x16 boxes" and "Gather4 and scatter4").
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16)
+//               into one of two TMEM accumulators; the first K step starts
+//               from zero and later ones accumulate ("mma.sync" page, section
+//               "Accumulation, transpose and alpha/beta": only the first K
+//               issue reads the start value).  tcgen05.commit frees stages.
+//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), optional C box via
+//               TMA, D = fma.rn(alpha, acc, beta*C) ("fma" page), convert,
+//               swizzled shared image, TMA store ("cp.async.bulk.tensor"
+//               page, section "Stores, reductions, and completion").
+//
+// Two accumulators let the epilogue of tile i overlap the mainloop of tile
+// i+1.  Every wait is bounded (common.cuh); on a timeout all roles leave
+// their loops, the copies in flight are drained, TMEM is freed and the
+// kernel returns with the error recorded.
+#pragma once
+
+#include "common.cuh"
+
+namespace tcg {
+
+template <int BN_, int STAGES_>
+struct TileCfg {
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr int BK = 64;  // 64 x 16-bit = one 128-byte swizzle row
+    static constexpr int STAGES = STAGES_;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t EPI_BUF = 32 * 128;  // 32 rows x 128 B
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = STAGES * A_BYTES;
+    static constexpr uint32_t OFF_EPI = STAGES * STAGE_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_EPI + 8 * EPI_BUF;  // 4 warps x 2 buffers
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 8;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+    static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base
+    static constexpr uint32_t TMEM_COLS = 2 * BN;               // two fp32 accumulators
+    static constexpr int THREADS = 192;
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "TMEM allocation must be a power of two in [32, 512]");
+};
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled box image
+// whose rows are `row_bytes` long (128: 128-byte swizzle, 64: 64-byte).  The
+// image base is aligned to the swizzle period.
+__device__ __forceinline__ uint32_t swz_off(uint32_t row, uint32_t chunk, uint32_t row_bytes)
+{
+    const uint32_t lin = row * row_bytes + chunk * 16u;
+    const uint32_t mask = row_bytes / 16u - 1u;  // 7 or 3
+    return lin ^ (((lin >> 7) & mask) << 4);
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC,
+                     const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
+{
+    using Cfg = TileCfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x / 32u, 0);
+    const uint32_t lane = threadIdx.x % 32u;
+
+    const uint32_t bar0 = base + Cfg::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    auto c_bar = [&](int q, int j) { return bar0 + 8u * (2 * STAGES + 4 + 2 * q + j); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
+        }
+        for (int q = 0; q < 4; ++q)
+            for (int j = 0; j < 2; ++j)
+                mbar_init(c_bar(q, j), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        if (args.num_k_blocks > 0) {  // with K == 0 the A/B descriptors are left empty
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+        }
+        if (args.has_c)
+            tma_prefetch_desc(&tmC);
+        tma_prefetch_desc(&tmD);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int s = 0;
+        uint32_t ph = 0;
+        int pending = 0;  // stages issued and not yet seen consumed (for teardown)
+        bool first = true;
+        bool alive = true;
+        for (int32_t t = blockIdx.x; t < args.num_tiles && alive; t += gridDim.x) {
+            int32_t mb, nb;
+            tile_coords(t, args, mb, nb);
+            const int32_t m0 = mb * Cfg::BM, n0 = nb * BN;
+            int32_t rows[4] = {0, 0, 0, 0};
+            if (args.gather) {
+                // lane l fetches rows 4l .. 4l+3 of the tile, four per gather4
+                for (int r = 0; r < 4; ++r) {
+                    const int32_t m = m0 + 4 * (int32_t)lane + r;
+                    int32_t v = 0;
+                    if (m < args.M) {
+                        v = args.idx[m];
+                        if (v < 0 || v >= args.table_rows) {
+                            record_error(args.status, kStatusIndex, 0);
+                            v = 0;  // fetch a valid row; the epilogue zeroes this one
+                        }
+                    }
+                    rows[r] = v;
+                }
+            }
+            for (int32_t kb = 0; kb < args.num_k_blocks; ++kb) {
+                if (!warp_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status,
+                                       args.timeout_ns, kWhereProducerEmpty)) {
+                    alive = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t bytes = Cfg::STAGE_BYTES + (first ? args.extra_tx : 0u);
+                    mbar_arrive_expect_tx(full_bar(s), bytes);
+                }
+                first = false;
+                __syncwarp();
+                const int32_t k0 = kb * Cfg::BK;
+                const uint32_t sa = base + Cfg::OFF_A + s * Cfg::A_BYTES;
+                const uint32_t sb = base + Cfg::OFF_B + s * Cfg::B_BYTES;
+                if (args.gather)
+                    tma_gather4(sa + lane * 512u, &tmA, full_bar(s), k0, rows[0], rows[1], rows[2],
+                                rows[3]);
+                else if (lane == 0)
+                    tma_load_2d(sa, &tmA, full_bar(s), k0, m0);
+                if (lane == 0)
+                    tma_load_2d(sb, &tmB, full_bar(s), k0, n0);
+                pending = min(pending + 1, STAGES);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (!alive) {
+            // Drain: every issued stage's bytes land before shared memory is
+            // released.  The waits are bounded again; a stage whose expected
+            // count can never be met (the test hook) simply times out here.
+            int ds = s;
+            uint32_t dph = ph;
+            for (int i = 0; i < pending; ++i) {
+                if (--ds < 0) {
+                    ds = STAGES - 1;
+                    dph ^= 1u;
+                }
+                wait_drain(full_bar(ds), dph, 10000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32acc(args.ab_bf16 != 0, Cfg::BM, BN);
+            int s = 0;
+            uint32_t ph = 0;
+            int ab = 0;
+            uint32_t aph = 0;
+            bool alive = true;
+            for (int32_t t = blockIdx.x; t < args.num_tiles && alive; t += gridDim.x) {
+                if (!wait_bounded(acce_bar(ab), aph ^ 1u, abort_flag, args.status,
+                                  args.timeout_ns, kWhereMmaAccEmpty))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BN);
+                for (int32_t kb = 0; kb < args.num_k_blocks; ++kb) {
+                    if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
+                                      kWhereMmaFull)) {
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES);
+                    const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < Cfg::BK / 16; ++k)  // +32 B per K=16 step
+                        tc_mma_f16(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
+                                   (kb | k) != 0 ? 1u : 0u);
+                    tc_commit(empty_bar(s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!alive)
+                    break;
+                if (args.num_k_blocks == 0)
+                    mbar_arrive(accf_bar(ab));  // nothing to multiply: acc reads as zero
+                else
+                    tc_commit(accf_bar(ab));
+                if (++ab == 2) {
+                    ab = 0;
+                    aph ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may read
+        const uint32_t buf0 = base + Cfg::OFF_EPI + q * 2u * Cfg::EPI_BUF;
+        const bool has_c = args.has_c != 0;
+        const bool acc_zero = args.num_k_blocks == 0;
+        const int out_kind = args.out_kind;
+        int ab = 0;
+        uint32_t aph = 0;
+        uint32_t cph[2] = {0u, 0u};
+        bool alive = true;
+        for (int32_t t = blockIdx.x; t < args.num_tiles && alive; t += gridDim.x) {
+            int32_t mb, nb;
+            tile_coords(t, args, mb, nb);
+            const int32_t m0 = mb * Cfg::BM, n0 = nb * BN;
+            const int32_t row0 = m0 + 32 * (int32_t)q;
+            const bool rows_ok = row0 < args.M;
+            const int32_t nchunks = min(BN / 32, (args.N - n0 + 31) / 32);
+
+            if (lane == 0)
+                bulk_wait_group_read<0>();  // last tile's stores are done with the buffers
+            __syncwarp();
+            if (has_c && rows_ok && lane == 0) {
+                for (int j = 0; j < 2 && j < nchunks; ++j) {
+                    mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
+                    tma_load_2d(buf0 + j * Cfg::EPI_BUF, &tmC, c_bar(q, j), n0 + 32 * j, row0);
+                }
+            }
+            if (!warp_wait_bounded(accf_bar(ab), aph, abort_flag, args.status, args.timeout_ns,
+                                   kWhereEpiAccFull)) {
+                alive = false;
+                break;
+            }
+            tc_fence_after_sync();
+
+            bool zero_row = acc_zero;
+            const int32_t my_row = row0 + (int32_t)lane;
+            if (args.gather && my_row < args.M) {
+                const int32_t v = args.idx[my_row];
+                zero_row = zero_row || v < 0 || v >= args.table_rows;
+            }
+
+            for (int32_t c = 0; c < nchunks; ++c) {
+                const int j = c & 1;
+                const uint32_t buf = buf0 + j * Cfg::EPI_BUF;
+                uint32_t acc[32];
+                tc_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * BN + 32 * c),
+                                 acc);
+                tc_wait_ld(acc);
+                if (c == nchunks - 1) {
+                    // the accumulator is fully read: hand it back to the MMA warp
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(acce_bar(ab));
+                }
+                if (!rows_ok)
+                    continue;
+                float v[32];
+                if (has_c) {
+                    if (!warp_wait_bounded(c_bar(q, j), cph[j], abort_flag, args.status,
+                                           args.timeout_ns, kWhereEpiC)) {
+                        alive = false;
+                        break;
+                    }
+                    cph[j] ^= 1u;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        uint32_t x0, x1, x2, x3;
+                        ld_shared_v4(buf + swz_off(lane, i, 128u), x0, x1, x2, x3);
+                        const float a0 = zero_row ? 0.f : __uint_as_float(acc[4 * i + 0]);
+                        const float a1 = zero_row ? 0.f : __uint_as_float(acc[4 * i + 1]);
+                        const float a2 = zero_row ? 0.f : __uint_as_float(acc[4 * i + 2]);
+                        const float a3 = zero_row ? 0.f : __uint_as_float(acc[4 * i + 3]);
+                        v[4 * i + 0] = fma_rn(args.alpha, a0, mul_rn(args.beta, __uint_as_float(x0)));
+                        v[4 * i + 1] = fma_rn(args.alpha, a1, mul_rn(args.beta, __uint_as_float(x1)));
+                        v[4 * i + 2] = fma_rn(args.alpha, a2, mul_rn(args.beta, __uint_as_float(x2)));
+                        v[4 * i + 3] = fma_rn(args.alpha, a3, mul_rn(args.beta, __uint_as_float(x3)));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = mul_rn(args.alpha, zero_row ? 0.f : __uint_as_float(acc[i]));
+                    if (lane == 0)
+                        bulk_wait_group_read<1>();  // the store two chunks back left buffer j
+                }
+                __syncwarp();  // all of C read (in-place D) and buffer j free
+                if (out_kind == kOutF32) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        st_shared_v4(buf + swz_off(lane, i, 128u), __float_as_uint(v[4 * i]),
+                                     __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                                     __float_as_uint(v[4 * i + 3]));
+                } else if (out_kind == kOutBF16) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_shared_v4(buf + swz_off(lane, i, 64u), pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                     pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                     pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                     pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_shared_v4(buf + swz_off(lane, i, 64u), pack_f16x2(v[8 * i], v[8 * i + 1]),
+                                     pack_f16x2(v[8 * i + 2], v[8 * i + 3]),
+                                     pack_f16x2(v[8 * i + 4], v[8 * i + 5]),
+                                     pack_f16x2(v[8 * i + 6], v[8 * i + 7]));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmD, buf, n0 + 32 * c, row0);
+                    bulk_commit_group();
+                    if (has_c && c + 2 < nchunks) {
+                        bulk_wait_group_read<0>();  // this store is done with buffer j
+                        mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
+                        tma_load_2d(buf, &tmC, c_bar(q, j), n0 + 32 * (c + 2), row0);
+                    }
+                }
+                __syncwarp();
+            }
+            if (++ab == 2) {
+                ab = 0;
+                aph ^= 1u;
+            }
+        }
+        if (!alive && has_c && lane == 0) {
+            // C loads issued for this tile may still be landing: let them finish
+            for (int j = 0; j < 2; ++j)
+                wait_drain(c_bar(q, j), cph[j], 10000000ull);
+        }
+        if (lane == 0)
+            bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace tcg

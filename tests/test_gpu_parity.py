@@ -1,0 +1,256 @@
+"""GPU path vs the oracle, element by element (needs a GB300)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (DEV, assert_bits, assert_within, device_status, oracle_full, run,
+                         to_f64)
+from tensor_core_gemm_02_gb300 import binding, workloads
+from tensor_core_gemm_02_gb300.workloads import OUT_BF16, OUT_F16, OUT_F32
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    binding.gemm_debug_inject(0)
+    binding.gemm_set_wait_timeout(0)
+    assert device_status() == binding.GEMM_OK
+    yield
+    assert device_status() == binding.GEMM_OK
+
+
+def test_worked_example_bit_exact():
+    """The mma.sync page's 16 x 8 x 32 example: D equals the stored exact result."""
+    p = workloads.worked_16x8x32()
+    D = run(p)
+    stored = np.loadtxt(os.path.join(GOLDEN, "worked_16x8x32.txt"))
+    assert np.array_equal(to_f64(D), stored)
+
+
+QUARTER_SHAPES = [(1, 1, 8), (16, 8, 32), (5, 3, 24), (127, 255, 64), (128, 256, 64),
+                  (129, 257, 72), (300, 520, 264), (257, 129, 520), (64, 640, 136),
+                  (384, 96, 1000)]
+
+
+@pytest.mark.parametrize("M,N,K", QUARTER_SHAPES)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_quarter_integers_bit_exact(M, N, K, dtype):
+    """Quarter-integer inputs make every partial sum exact: D must match bit for bit."""
+    for out, with_c, alpha, beta in [(OUT_F32, False, 1.0, 1.0), (OUT_F32, True, 0.5, 2.0),
+                                     (OUT_BF16, True, -1.0, 0.5), (OUT_F16, False, 2.0, 0.0)]:
+        p = workloads.random_problem(M * 7 + N + K, M, N, K, dtype=dtype, values="quarter",
+                                     with_c=with_c, alpha=alpha, beta=beta, out=out)
+        ref, _, _ = oracle_full(p)
+        assert_bits(run(p), ref, out, f"{M}x{N}x{K} {dtype} out={out} C={with_c}")
+
+
+def test_fma_single_rounding():
+    """alpha*acc + C must be one fused rounding (fma page): 2^-11 + 2^-24, not 2^-11."""
+    K = 8
+    a = torch.zeros((1, K), dtype=torch.float16)
+    a[0, 0], a[0, 1] = 1.0, 2.0 ** -12
+    b = torch.zeros((1, K), dtype=torch.float16)
+    b[0, 0], b[0, 1] = 1.0, 1.0
+    c = torch.full((1, 1), -1.0)
+    alpha = float(np.float32(1 + 2.0 ** -12))
+    D = binding.gemm_f16(a.to(DEV), b.to(DEV), c.to(DEV), alpha=alpha, beta=1.0)
+    assert D.item() == 2.0 ** -11 + 2.0 ** -24
+
+
+def test_two_a_plus_one():
+    """The fma page's example through the GEMM: X * I^T * 2 + 1 == 2X + 1 exactly."""
+    rng = np.random.default_rng(7)
+    K = 64
+    X = torch.from_numpy(rng.integers(-64, 65, (40, K)).astype(np.float16))
+    eye = torch.eye(K, dtype=torch.float16)
+    ones = torch.ones((40, K))
+    D = binding.gemm_f16(X.to(DEV), eye.to(DEV), ones.to(DEV), alpha=2.0, beta=1.0)
+    assert torch.equal(D.cpu(), 2 * X.float() + 1)
+
+
+NORMAL_SHAPES = [(777, 1000, 520), (128, 4096, 64), (1000, 333, 1032), (2, 5000, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", NORMAL_SHAPES)
+@pytest.mark.parametrize("out", [OUT_F32, OUT_BF16, OUT_F16])
+def test_normal_within_tolerance(M, N, K, out):
+    p = workloads.random_problem(M + N + K + out, M, N, K, dtype="bf16", with_c=True,
+                                 alpha=0.5, beta=1.0, out=out, b_scale=0.02)
+    ref, absprod, _ = oracle_full(p)
+    assert_within(run(p), ref, absprod, out, f"{M}x{N}x{K}")
+
+
+def test_f16_1024_full():
+    """f16 1024^3 with C (alpha = beta = 1), every element."""
+    p = workloads.f16_1024()
+    ref, absprod, _ = oracle_full(p)
+    assert_within(run(p), ref, absprod, p.out, p.name)
+
+
+def _sample_coords(M, N, n, seed):
+    rng = np.random.default_rng(seed)
+    ii = rng.integers(0, M, n)
+    jj = rng.integers(0, N, n)
+    # tile corners and the last row / column
+    edge_i = np.array([0, 127, 128, M - 1, M - 1, 0, 255, 256])
+    edge_j = np.array([0, 255, 256, N - 1, 0, N - 1, 31, 32])
+    return np.concatenate([ii, edge_i]), np.concatenate([jj, edge_j])
+
+
+def _sampled_check(p, n=4096, seed=0):
+    D = run(p)
+    torch.cuda.synchronize()
+    ii, jj = _sample_coords(p.M, p.N, n, seed)
+    ref, absprod, _ = oracle.gemm_entries(p.A, p.B, ii, jj, p.C, p.alpha, p.beta, idx=p.idx)
+    got = D[torch.from_numpy(ii).to(DEV), torch.from_numpy(jj).to(DEV)]
+    assert_within(to_f64(got), ref, absprod, p.out, p.name)
+    return D
+
+
+def test_bf16_8192_sampled():
+    _sampled_check(workloads.bf16_8192())
+
+
+def test_mlp_sampled():
+    _sampled_check(workloads.mlp_8192x28672x4096())
+
+
+def test_skinny_full():
+    p = workloads.skinny_16x28672x4096()
+    ref, absprod, _ = oracle_full(p)
+    assert_within(run(p), ref, absprod, p.out, p.name)
+
+
+def test_gather_sampled():
+    _sampled_check(workloads.gather_16384_of_65536())
+
+
+def test_gather_identity_matches_plain():
+    """idx = arange(M) must give exactly the plain GEMM on the same rows."""
+    p = workloads.random_problem(21, 300, 400, 264, dtype="bf16", with_c=True, alpha=0.5)
+    plain = run(p)
+    p.idx = torch.arange(300, dtype=torch.int32)
+    gathered = run(p)
+    assert torch.equal(plain, gathered)
+
+
+def test_gather_duplicates_identical_rows():
+    p = workloads.random_problem(22, 256, 300, 200, dtype="f16", gather_rows=50)
+    p.idx[:] = torch.from_numpy(np.random.default_rng(1).integers(0, 4, 256).astype(np.int32))
+    D = run(p).cpu()
+    for r in range(4):
+        rows = (p.idx == r).nonzero().flatten()
+        assert all(torch.equal(D[rows[0]], D[k]) for k in rows)
+    ref, absprod, _ = oracle_full(p)
+    assert_within(D, ref, absprod, p.out, "duplicates")
+
+
+def test_gather_bad_index_reports_and_zeroes():
+    p = workloads.random_problem(23, 130, 96, 64, dtype="bf16", with_c=True, beta=0.5,
+                                 gather_rows=40)
+    p.idx[3] = 40
+    p.idx[129] = -7
+    D = run(p)
+    assert device_status() == binding.GEMM_ERR_INDEX
+    ref, absprod, bad = oracle_full(p)
+    assert bad
+    assert_within(D, ref, absprod, p.out, "bad index")
+    assert torch.equal(D[3].cpu(), 0.5 * p.C[3])
+
+
+def test_c_absent_equals_zero_c():
+    p = workloads.random_problem(24, 200, 300, 128, dtype="bf16", alpha=1.5)
+    D0 = run(p)
+    p.C = torch.zeros((200, 300))
+    Dz = run(p)
+    assert torch.equal(D0, Dz)
+
+
+def test_beta_zero_does_not_read_c():
+    p = workloads.random_problem(25, 130, 70, 64, dtype="bf16", beta=0.0)
+    D0 = run(p)
+    p.C = torch.full((130, 70), float("nan"))
+    assert torch.equal(run(p), D0)
+
+
+def test_in_place_d_is_c():
+    p = workloads.random_problem(26, 260, 300, 136, dtype="f16", values="quarter",
+                                 with_c=True, alpha=0.5, beta=2.0)
+    ref, _, _ = oracle_full(p)
+    C = p.C.to(DEV)
+    D = binding.gemm_f16(p.A.to(DEV), p.B.to(DEV), C, C, alpha=0.5, beta=2.0)
+    assert D.data_ptr() == C.data_ptr()
+    assert_bits(D, ref, OUT_F32, "in place")
+
+
+def test_k_zero_gives_beta_c():
+    C = torch.randn(70, 90)
+    A = torch.empty((70, 0), dtype=torch.bfloat16)
+    B = torch.empty((90, 0), dtype=torch.bfloat16)
+    D = binding.gemm_bf16(A.to(DEV), B.to(DEV), C.to(DEV), alpha=3.0, beta=0.5)
+    assert torch.equal(D.cpu(), 0.5 * C)
+    D2 = binding.gemm_bf16(A.to(DEV), B.to(DEV))
+    assert torch.count_nonzero(D2) == 0
+
+
+def test_empty_m_n_is_noop():
+    A = torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros((5, 64), dtype=torch.bfloat16, device=DEV)
+    assert binding.gemm_bf16(A, B).shape == (0, 5)
+    assert binding.gemm_bf16(B, A).shape == (5, 0)
+
+
+def test_strided_operands():
+    """Leading dimensions larger than the logical widths."""
+    p = workloads.random_problem(27, 150, 170, 136, dtype="bf16", values="quarter",
+                                 with_c=True, alpha=0.5, beta=-1.0)
+    ref, _, _ = oracle_full(p)
+    Abig = torch.zeros((150, 200), dtype=torch.bfloat16)
+    Abig[:, :136] = p.A
+    Bbig = torch.zeros((170, 144), dtype=torch.bfloat16)
+    Bbig[:, :136] = p.B
+    Cbig = torch.zeros((150, 180))
+    Cbig[:, :170] = p.C
+    Dbig = torch.full((150, 176), 7.0, device=DEV)
+    A, B, C = Abig.to(DEV)[:, :136], Bbig.to(DEV)[:, :136], Cbig.to(DEV)[:, :170]
+    D = Dbig[:, :170]
+    binding.gemm_bf16(A, B, C, D, alpha=0.5, beta=-1.0)
+    assert_bits(D, ref, OUT_F32, "strided")
+    assert torch.all(Dbig[:, 170:] == 7.0)
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    """A stage whose expected byte count is never met: the bounded wait runs out,
+    the kernel returns GEMM_ERR_TIMEOUT, and the next call works."""
+    p = workloads.random_problem(28, 256, 256, 256, dtype="bf16", values="quarter")
+    binding.gemm_set_wait_timeout(50_000_000)  # 50 ms
+    binding.gemm_debug_inject(1)
+    try:
+        run(p)
+        assert device_status() == binding.GEMM_ERR_TIMEOUT
+    finally:
+        binding.gemm_debug_inject(0)
+        binding.gemm_set_wait_timeout(0)
+    ref, _, _ = oracle_full(p)
+    assert_bits(run(p), ref, OUT_F32, "after timeout")
+
+
+def test_host_side_errors_with_device_tensors():
+    A = torch.zeros((64, 64), dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros((64, 64), dtype=torch.bfloat16, device=DEV)
+    D = torch.zeros((64, 64), device=DEV)
+    lib = binding.load_library()
+    s = binding._stream_ptr(None)
+    # misaligned A (offset by one element)
+    st = lib.gemm_bf16(64, 64, 64, A.data_ptr() + 2, 64, B.data_ptr(), 64, None, 0,
+                       D.data_ptr(), 64, 0, 1.0, 0.0, s)
+    assert st == 2
+    # D overlapping A
+    st = lib.gemm_bf16(32, 32, 64, A.data_ptr(), 64, B.data_ptr(), 64, None, 0,
+                       A.data_ptr(), 64, 0, 1.0, 0.0, s)
+    assert st == 4
