@@ -1,0 +1,449 @@
+"""Benchmark of the tcgen05 GEMM library on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--no-variants]
+
+Headline workload: bf16 GEMM M = N = K = 8192, A ~ N(0,1), B ~ N(0,0.02),
+no C, bf16 out (seeded synthetic inputs, tensor_core_gemm_02_gb300.workloads).
+One step = one gemm_bf16 call on inputs already in HBM.  The metric is
+TFLOP/s = 2 M N K / time.  The same line also carries:
+
+  e2e           the same metric through the C ABI with host buffers: each step
+                copies A and B from pinned host memory, runs the GEMM and reads
+                D back, all inside the timed region
+  roofline      the kernel's achieved TFLOP/s against the measured dense bf16
+                peak in MEASURED_PEAKS.json (tensor-bound), and the DRAM traffic
+                per launch from the committed ncu summary when it is current
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample of rows
+  variants      the other workloads (f16 1024^3 + C, 8192 x 28672 x 4096 with
+                C, the M = 16 skinny case, the gathered 16384-of-65536 rows
+                case), each timed per launch with an L2 flush in between, with
+                their own roofline (HBM-bound ones against the copy bandwidth)
+
+With --impl reference the oracle itself is timed as the comparison arm.
+Under torchrun every rank runs its own replica; rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tensor_core_gemm_02_gb300 import binding, workloads  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+HEADLINE = "bf16_8192"
+
+
+# ----------------------------------------------------------------- plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources; a stored ncu traffic figure is used only if it matches."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_core_gemm_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key):
+    """DRAM bytes per launch recorded from an ncu capture of the current sources, or None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    e = d.get("kernels", {}).get(kernel_key)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and os.path.getsize(self.out.name) == 0:
+                time.sleep(0.05)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.flush()
+
+    def summary(self):
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    rows.append({"sm": float(parts[2]), "max": float(parts[3]),
+                                 "power": float(parts[4]),
+                                 "hw_slowdown": parts[6] == "Active",
+                                 "hw_thermal_slowdown": parts[7] == "Active",
+                                 "sw_thermal_slowdown": parts[8] == "Active",
+                                 "sw_power_cap": parts[9] == "Active"})
+                except ValueError:
+                    continue
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        # samples under load: the upper half by power draw
+        pw = sorted(r["power"] for r in rows)
+        cut = pw[len(pw) // 2]
+        load = [r for r in rows if r["power"] >= cut] or rows
+        reasons = sorted({k for r in rows for k in ("hw_slowdown", "hw_thermal_slowdown",
+                                                     "sw_thermal_slowdown", "sw_power_cap")
+                          if r[k]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw)}
+
+
+def l2_flush(buf):
+    buf.zero_()
+
+
+def launch(p, dev_tensors):
+    A, B, C, idx, D = dev_tensors
+    if idx is not None:
+        return binding.gemm_gather_rows(A, idx, B, C, D, alpha=p.alpha, beta=p.beta, out=p.out)
+    if A.dtype == torch.bfloat16:
+        return binding.gemm_bf16(A, B, C, D, alpha=p.alpha, beta=p.beta, out=p.out)
+    return binding.gemm_f16(A, B, C, D, alpha=p.alpha, beta=p.beta, out=p.out)
+
+
+def to_device(p, dev):
+    A = p.A.to(dev)
+    B = p.B.to(dev)
+    C = p.C.to(dev) if p.C is not None else None
+    idx = p.idx.to(dev) if p.idx is not None else None
+    D = torch.empty((p.M, p.N), dtype=workloads.OUT_TORCH[p.out], device=dev)
+    return A, B, C, idx, D
+
+
+def algorithmic_bytes(p):
+    """Bytes the GEMM must move at least once: A (or the gathered rows), B, C, D, idx."""
+    esz = p.A.element_size()
+    a = p.M * p.K * esz
+    b = p.N * p.K * esz
+    c = p.M * p.N * 4 if (p.C is not None and p.beta != 0) else 0
+    d = p.M * p.N * workloads.OUT_TORCH[p.out].itemsize
+    i = p.M * 4 if p.idx is not None else 0
+    return a + b + c + d + i
+
+
+# ----------------------------------------------------------------- our arm
+
+def time_headline(p, dev, steps, warmup, rank, world):
+    tensors = to_device(p, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        launch(p, tensors)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            launch(p, tensors)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1)
+    status = binding.gemm_check_device_status()
+    if status != binding.GEMM_OK:
+        raise RuntimeError(f"device status after timing: {binding.gemm_status_string(status)}")
+    del tensors
+    return ms, clocks.summary()
+
+
+def time_e2e(p, dev, steps):
+    """Host buffers: H2D of A and B from pinned memory, the GEMM, D2H of D, per step."""
+    A_h = p.A.pin_memory()
+    B_h = p.B.pin_memory()
+    D_h = torch.empty((p.M, p.N), dtype=workloads.OUT_TORCH[p.out]).pin_memory()
+    A_d = torch.empty_like(A_h, device=dev)
+    B_d = torch.empty_like(B_h, device=dev)
+    D_d = torch.empty_like(D_h, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        A_d.copy_(A_h, non_blocking=True)
+        B_d.copy_(B_h, non_blocking=True)
+        binding.gemm_bf16(A_d, B_d, None, D_d, alpha=p.alpha, beta=p.beta, out=p.out)
+        D_h.copy_(D_d, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size()
+    d2h = D_h.numel() * D_h.element_size()
+    return ms, h2d, d2h
+
+
+def time_variant(name, dev, reps, flush):
+    p = workloads.WORKLOADS[name]()
+    tensors = to_device(p, dev)
+    for _ in range(3):
+        launch(p, tensors)
+    torch.cuda.synchronize()
+    times = []
+    stream = torch.cuda.current_stream()
+    for _ in range(reps):
+        l2_flush(flush)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch(p, tensors)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    status = binding.gemm_check_device_status()
+    if status != binding.GEMM_OK:
+        raise RuntimeError(f"{name}: device status {binding.gemm_status_string(status)}")
+    ms = statistics.median(times)
+    plan = binding.gemm_query_plan(p.M, p.N, p.K, gather=p.idx is not None,
+                                   sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
+    del tensors
+    return p, ms, plan
+
+
+def oracle_rows_rate(p, seconds, threads):
+    """Run the oracle on whole output rows for about `seconds`; returns (flops/s, rows)."""
+    import oracle
+
+    rows = threads  # calibration: one row per thread
+    t0 = time.time()
+    oracle.gemm(p.A, p.B, p.C, p.alpha, p.beta, idx=p.idx, threads=threads, rows=(0, rows))
+    dt = max(time.time() - t0, 1e-3)
+    rows = int(max(1, min(p.M, (seconds / dt) * rows)))
+    # whole multiples of the thread count keep every host core busy
+    rows = max(threads, (rows // threads) * threads) if p.M >= threads else rows
+    rows = min(rows, p.M)
+    t0 = time.time()
+    oracle.gemm(p.A, p.B, p.C, p.alpha, p.beta, idx=p.idx, threads=threads, rows=(0, rows))
+    dt = time.time() - t0
+    return 2.0 * rows * p.N * p.K / dt, rows, dt
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local % torch.cuda.device_count())
+    torch.cuda.set_device(dev)
+    binding.load_library()
+    peaks = measured_peaks()
+
+    p = workloads.WORKLOADS[HEADLINE]()
+    flops = p.flops
+    ms_total, clocks = time_headline(p, dev, args.steps, args.warmup, rank, world)
+    ms_step = ms_total / args.steps
+    # whole job: all ranks' work over the slowest rank's time
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    achieved = flops / (ms_step * 1e-3) / 1e12
+
+    e2e_steps = min(args.steps, 20)
+    e2e_ms, h2d, d2h = time_e2e(p, dev, e2e_steps)
+
+    result = {
+        "metric": "GEMM TFLOP/s (bf16 8192^3, bf16 out)",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) / N(0,0.02) bf16)",
+        "config": {"workload": "bf16 GEMM M=N=K=8192, A~N(0,1), B~N(0,0.02), C=0, bf16 out",
+                   "M": 8192, "N": 8192, "K": 8192, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": round(e2e_ms, 4)},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "peak_source": f"{peaks['source']} bf16_tflops (burst)",
+                     "traffic": stored_traffic("tile_gemm_kernel<256,4>@bf16_8192"),
+                     "algorithmic_flops_per_launch": flops},
+    }
+
+    if rank == 0 and args.variants:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        variants = {}
+        for name in ("f16_1024", "mlp_8192x28672x4096", "skinny_16x28672x4096",
+                     "gather_16384_of_65536"):
+            vp, ms, plan = time_variant(name, dev, args.variant_reps, flush)
+            tflops = vp.flops / (ms * 1e-3) / 1e12
+            gbs = algorithmic_bytes(vp) / (ms * 1e-3) / 1e9
+            hbm_bound = name in ("skinny_16x28672x4096",)
+            variants[name] = {
+                "ms": round(ms, 5), "TFLOP/s": round(tflops, 2), "GB/s": round(gbs, 1),
+                "algorithmic_bytes": algorithmic_bytes(vp),
+                "kernel": {1: "tile", 2: "skinny"}.get(plan.kernel, "?"),
+                "tile": f"{plan.bm}x{plan.bn}", "grid": plan.grid, "splits": plan.splits,
+                "roofline": ({"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                              "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
+                             if hbm_bound else
+                             {"bound": "tensor", "achieved": round(tflops, 2),
+                              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                              "frac": round(tflops / peaks["bf16_tflops"], 4)}),
+                "timing": "median of per-launch CUDA events, L2 flushed between launches",
+            }
+        result["variants"] = variants
+        del flush
+
+    if rank == 0:
+        threads = len(os.sched_getaffinity(0))
+        rate, rows, dt = oracle_rows_rate(p, args.cpu_seconds, threads)
+        result["cpu_baseline"] = {"value": round(rate / 1e12, 6), "unit": "TFLOP/s",
+                                  "cores": threads, "kind": "oracle",
+                                  "sample": f"{rows} full output rows of the 8192^3 bf16 GEMM "
+                                            f"(fp64 oracle, {dt:.1f} s)"}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle as the comparison arm: each step computes a bounded sample of rows."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    p = workloads.WORKLOADS[HEADLINE]()
+    threads = len(os.sched_getaffinity(0))
+    import oracle
+    oracle.load()
+    # size each step so that warm-up plus timed steps take about two minutes
+    t0 = time.time()
+    oracle.gemm(p.A, p.B, None, 1.0, 0.0, threads=threads, rows=(0, threads))
+    per_row = max(time.time() - t0, 1e-3) / threads
+    budget = 120.0 / (args.steps + args.warmup)
+    rows = int(max(1, min(p.M // 2, budget / per_row)))
+    for _ in range(args.warmup):
+        oracle.gemm(p.A, p.B, None, 1.0, 0.0, threads=threads, rows=(0, rows))
+    t0 = time.time()
+    for s in range(args.steps):
+        r0 = (s * rows) % (p.M - rows)
+        oracle.gemm(p.A, p.B, None, 1.0, 0.0, threads=threads, rows=(r0, r0 + rows))
+    dt = (time.time() - t0) / args.steps
+    value = 2.0 * rows * p.N * p.K / dt / 1e12
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "GEMM TFLOP/s (bf16 8192^3, bf16 out)",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "bf16 GEMM M=N=K=8192, A~N(0,1), B~N(0,0.02), C=0, bf16 out",
+                   "M": 8192, "N": 8192, "K": 8192},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{rows} full output rows per step (fp64 oracle)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-variants", dest="variants", action="store_false")
+    ap.add_argument("--variant-reps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -82,12 +82,17 @@ typedef enum {
  *              May be NULL only when K == 0.
  *  B, ldb      N x K f16, ldb >= K, ldb % 8 == 0, 16-byte aligned.
  *              May be NULL only when K == 0.
- *  C, ldc      M x N float32 or NULL (absent).  ldc >= N, ldc % 4 == 0,
- *              16-byte aligned.  Not read when beta == 0.
- *  D, ldd      M x N output of type `out`; ldd >= N, ldd * sizeof(out) a
- *              multiple of 16, 16-byte aligned.  D may be C exactly (same
- *              pointer, ldd == ldc, out == GEMM_OUT_F32); any other overlap
- *              of D with A, B or C is GEMM_ERR_ALIAS.
+ *  C, ldc      M x N float32 or NULL (absent); ldc >= N, 4-byte aligned.
+ *              Not read when beta == 0.
+ *  D, ldd      M x N output of type `out`; ldd >= N, aligned to its element
+ *              size.  Only columns j < N of each row are written.  D may be C
+ *              exactly (same pointer, ldd == ldc, out == GEMM_OUT_F32); any
+ *              other overlap of D with A, B or C is GEMM_ERR_ALIAS.
+ *              C and D move through TMA boxes when their base is 16-byte
+ *              aligned and their row pitch a multiple of 16 bytes; otherwise
+ *              (and for the 16-byte chunk that straddles column N when
+ *              N * sizeof(out) is not a multiple of 16) the epilogue uses
+ *              plain loads and stores, which is slower but exact.
  *  out         a gemm_out_t value.
  *  stream      cudaStream_t to run on.
  */
@@ -147,7 +152,7 @@ const char *gemm_status_string(int status);
  * anything and without touching the GPU (for diagnostics and tests).
  *
  *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles),
- *           2 = skinny swap-AB kernel (M <= 64), 3 = K == 0 epilogue only
+ *           2 = skinny swap-AB kernel (M <= 64)
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)

@@ -15,6 +15,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "launch.h"
 #include "tcgemm.h"
@@ -33,9 +34,24 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 struct DeviceInfo {
     bool ready = false;
+    int index = 0;
     int sm_count = 0;
     uint32_t *status = nullptr;
 };
+
+// Scratch of the skinny kernel: per-split partial tiles and per-tile arrival
+// counters.  One per (device, stream), so calls on different streams never
+// share it; calls on one stream are ordered by the stream.
+struct Workspace {
+    int device = -1;
+    cudaStream_t stream = nullptr;
+    float *partials = nullptr;
+    size_t partial_bytes = 0;
+    uint32_t *counters = nullptr;
+    size_t counter_count = 0;
+};
+std::mutex g_ws_mu;
+std::vector<Workspace> g_ws;
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
@@ -72,11 +88,67 @@ gemm_status device_info(DeviceInfo **out)
                 return GEMM_ERR_CUDA;
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
+        d.index = dev;
         d.sm_count = sms;
         d.status = static_cast<uint32_t *>(p);
         d.ready = true;
     }
     *out = &d;
+    return GEMM_OK;
+}
+
+// Workspace of (device, stream) with room for `bytes` of partials and `count`
+// counters; grows geometrically.  New counters start at zero; the kernel
+// returns every counter it uses to zero.
+gemm_status get_workspace(int device, cudaStream_t stream, size_t bytes, size_t count,
+                          Workspace *out)
+{
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    Workspace *w = nullptr;
+    for (Workspace &x : g_ws)
+        if (x.device == device && x.stream == stream)
+            w = &x;
+    if (!w) {
+        g_ws.push_back(Workspace{});
+        w = &g_ws.back();
+        w->device = device;
+        w->stream = stream;
+    }
+    if (w->partial_bytes < bytes || w->counter_count < count) {
+        if (w->partials || w->counters) {
+            // earlier kernels on this stream may still use the old buffers
+            if (cudaStreamSynchronize(stream) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            cudaFree(w->partials);
+            cudaFree(w->counters);
+            w->partials = nullptr;
+            w->counters = nullptr;
+        }
+        const size_t nb = bytes > 2 * w->partial_bytes ? bytes : 2 * w->partial_bytes;
+        const size_t nc = count > 2 * w->counter_count ? count : 2 * w->counter_count;
+        w->partial_bytes = 0;
+        w->counter_count = 0;
+        if (cudaMalloc(&w->partials, nb > 0 ? nb : 256) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaMalloc(&w->counters, nc * sizeof(uint32_t)) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaMemsetAsync(w->counters, 0, nc * sizeof(uint32_t), stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        w->partial_bytes = nb;
+        w->counter_count = nc;
+    }
+    *out = *w;
+    return GEMM_OK;
+}
+
+// After a kernel gave up half way, counters may be left non-zero: clear them.
+gemm_status reset_workspaces(int device)
+{
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    for (Workspace &x : g_ws)
+        if (x.device == device && x.counters &&
+            cudaMemset(x.counters, 0, x.counter_count * sizeof(uint32_t)) != cudaSuccess)
+            return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
 
@@ -221,9 +293,11 @@ gemm_status validate(const Problem &p, bool *empty)
     // alignment: 16-byte bases, row pitches that are multiples of 16 bytes
     if (p.K > 0 && (!aligned16(p.A) || !aligned16(p.B) || (p.lda * 2) % 16 || (p.ldb * 2) % 16))
         return GEMM_ERR_ALIGNMENT;
-    if (c_used && (!aligned16(p.C) || (p.ldc * 4) % 16))
+    // C and D only need their natural element alignment: when their base or
+    // row pitch is not 16-byte aligned the epilogue uses plain loads/stores
+    if (c_used && (reinterpret_cast<uintptr_t>(p.C) & 3u))
         return GEMM_ERR_ALIGNMENT;
-    if (!aligned16(p.D) || (p.ldd * out_size(p.out)) % 16)
+    if (reinterpret_cast<uintptr_t>(p.D) & static_cast<uintptr_t>(out_size(p.out) - 1))
         return GEMM_ERR_ALIGNMENT;
     if (p.gather && (reinterpret_cast<uintptr_t>(p.idx) & 3u))
         return GEMM_ERR_ALIGNMENT;
@@ -269,14 +343,30 @@ int choose_bn(int64_t M, int64_t N, int sm_count)
     return best;
 }
 
+int skinny_rows(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+
 gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, int sm_count)
 {
-    (void)K;
-    (void)gather;
     gemm_plan p;
     std::memset(&p, 0, sizeof(p));
     if (M == 0 || N == 0)
         return p;
+    if (!gather && M <= 64 && K > 0) {
+        // few rows: swap A and B so B streams through the MMA's M side
+        const int mp = skinny_rows(M);
+        const int64_t tiles = ceil_div(N, 128);
+        const int64_t nkb = ceil_div(K, 64);
+        const int64_t W = tiles * nkb;
+        const int64_t G = W < sm_count ? W : sm_count;
+        p.kernel = 2;
+        p.bm = mp;
+        p.bn = 128;
+        p.stages = tcg::skinny_stages(mp);
+        p.tiles = tiles;
+        p.splits = tcg::skinny_max_parts(tiles, nkb, G);
+        p.grid = static_cast<int32_t>(G);
+        return p;
+    }
     const int bn = choose_bn(M, N, sm_count);
     p.kernel = 1;
     p.bm = 128;
@@ -293,6 +383,58 @@ CUtensorMapDataType ab_type(bool bf16)
     return bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
+void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev)
+{
+    const bool c_used = p.C != nullptr && p.beta != 0.0f;
+    a.M = static_cast<int32_t>(p.M);
+    a.N = static_cast<int32_t>(p.N);
+    a.K = static_cast<int32_t>(p.K);
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.has_c = c_used ? 1 : 0;
+    a.out_kind = p.out;
+    a.ab_bf16 = p.bf16 ? 1 : 0;
+    a.C = p.C;
+    a.ldc = p.ldc;
+    a.D = p.D;
+    a.ldd = p.ldd;
+    a.extra_tx = g_inject.load() == 1 ? 16u : 0u;
+    a.status = dev->status;
+    a.timeout_ns = g_timeout_ns.load();
+}
+
+gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo *dev)
+{
+    const int mp = plan.bm;
+    GemmMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.M, p.lda * 2, 64,
+                   static_cast<uint32_t>(mp), CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&maps.b, ab_type(p.bf16), p.B, p.K, p.N, p.ldb * 2, 64, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return GEMM_ERR_CUDA;
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    fill_common(a, p, dev);
+    a.num_m_blocks = 1;
+    a.num_n_blocks = static_cast<int32_t>(plan.tiles);
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, 64));
+    a.num_tiles = static_cast<int32_t>(plan.tiles);
+    a.group_m = 1;
+    a.splits = plan.splits;
+    if (plan.splits > 1) {
+        Workspace w;
+        const size_t bytes = static_cast<size_t>(plan.tiles) * plan.splits * 128 * mp * sizeof(float);
+        gemm_status st = get_workspace(dev->index, p.stream, bytes, static_cast<size_t>(plan.tiles), &w);
+        if (st != GEMM_OK)
+            return st;
+        a.workspace = w.partials;
+        a.counters = w.counters;
+    }
+    const cudaError_t e = tcg::launch_skinny(mp, maps, a, plan.grid, p.stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 gemm_status run(const Problem &p)
 {
     bool empty = false;
@@ -307,6 +449,8 @@ gemm_status run(const Problem &p)
 
     GemmMaps maps;
     std::memset(&maps, 0, sizeof(maps));
+    if (plan.kernel == 2)
+        return run_skinny(p, plan, dev);
     const int bn = plan.bn;
     if (p.K > 0) {
         const bool ok_a =
@@ -319,10 +463,12 @@ gemm_status run(const Problem &p)
         if (!ok_a || !ok_b)
             return GEMM_ERR_CUDA;
     }
-    if (c_used && !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.C, p.N, p.M, p.ldc * 4,
-                             32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    const bool c_tma = c_used && aligned16(p.C) && (p.ldc * 4) % 16 == 0;
+    const bool d_tma = aligned16(p.D) && (p.ldd * out_size(p.out)) % 16 == 0;
+    if (c_tma && !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.C, p.N, p.M, p.ldc * 4,
+                            32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return GEMM_ERR_CUDA;
-    {
+    if (d_tma) {
         const CUtensorMapDataType dt = p.out == GEMM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                        : p.out == GEMM_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -334,9 +480,7 @@ gemm_status run(const Problem &p)
 
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    a.M = static_cast<int32_t>(p.M);
-    a.N = static_cast<int32_t>(p.N);
-    a.K = static_cast<int32_t>(p.K);
+    fill_common(a, p, dev);
     a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, 128));
     a.num_n_blocks = static_cast<int32_t>(ceil_div(p.N, bn));
     a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, 64));
@@ -344,17 +488,12 @@ gemm_status run(const Problem &p)
     a.group_m = a.num_m_blocks < 16 ? a.num_m_blocks : 16;
     a.splits = 1;
     a.kb_per_split = a.num_k_blocks;
-    a.alpha = p.alpha;
-    a.beta = p.beta;
-    a.has_c = c_used ? 1 : 0;
-    a.out_kind = p.out;
-    a.ab_bf16 = p.bf16 ? 1 : 0;
     a.gather = p.gather ? 1 : 0;
+    a.c_tma = c_tma ? 1 : 0;
+    a.d_tma = d_tma ? 1 : 0;
+    a.d_tail_direct = (p.N * out_size(p.out)) % 16 != 0 ? 1 : 0;
     a.idx = p.idx;
     a.table_rows = static_cast<int32_t>(p.a_rows);
-    a.extra_tx = g_inject.load() == 1 ? 16u : 0u;
-    a.status = dev->status;
-    a.timeout_ns = g_timeout_ns.load();
 
     const cudaError_t e = tcg::launch_tile(bn, maps, a, plan.grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -411,6 +550,8 @@ gemm_status gemm_check_device_status(void *stream)
     if (h[0] != 0) {
         if (cudaMemset(dev->status, 0, sizeof(h)) != cudaSuccess)
             return GEMM_ERR_CUDA;
+        if ((st = reset_workspaces(dev->index)) != GEMM_OK)
+            return st;
     }
     return static_cast<gemm_status>(h[0]);
 }

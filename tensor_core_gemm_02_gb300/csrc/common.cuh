@@ -34,12 +34,17 @@ struct GemmArgs {
     int32_t out_kind;       // kOutF32 / kOutBF16 / kOutF16
     int32_t ab_bf16;        // operand format: 1 bf16, 0 f16
     int32_t gather;         // A rows are table[idx[m]]
+    int32_t c_tma;          // C boxes come through TMA (aligned C); else plain loads
+    int32_t d_tma;          // D boxes go out through TMA stores (aligned D); else plain stores
+    int32_t d_tail_direct;  // N * sizeof(out) is not a multiple of 16: a TMA store would
+                            // write the whole 16-byte chunk that straddles column N, so the
+                            // chunk that crosses N is stored with plain stores instead
     const int32_t *idx;
     int32_t table_rows;
     uint32_t extra_tx;      // test hook: extra bytes expected on the first stage
     uint32_t *status;       // [0] first error code, [1] where a wait gave up
     uint64_t timeout_ns;    // limit of every bounded wait
-    // skinny kernel only
+    // plain-load / plain-store epilogue paths
     const float *C;
     int64_t ldc;
     void *D;

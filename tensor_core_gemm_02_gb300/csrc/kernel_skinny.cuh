@@ -1,0 +1,319 @@
+// kernel_skinny.cuh -- swap-AB stream-K tcgen05 GEMM for M <= 64.
+//
+// With few rows of A the product is bound by streaming B from HBM.  The
+// kernel computes D^T = B * A^T instead: 128 rows of B sit on the MMA's M
+// side and the (padded) MP <= 64 rows of A on its N side, so every B byte
+// feeds a 128 x MP x 16 MMA.  This relabels operands instead of moving data
+// ("mma.sync" page, section "Accumulation, transpose and alpha/beta": a
+// transpose is a change of view, not an exchange of values).
+//
+// Work split (stream-K): the (tile, k-block) pairs of all 128-row tiles of
+// B form one list; CTA g takes the contiguous share [W g / G, W (g+1) / G).
+// A tile touched by several CTAs gets one partial sum from each; each writes
+// its partial to the workspace, and the last to arrive (an atomic counter per
+// tile) adds them in a fixed order, applies the epilogue and resets the
+// counter.  No CTA waits for another.
+//
+//   warp 0     producer: TMA boxes of B (128 x 64) and A (MP x 64) per k-block
+//   warp 1     MMA issuer: tcgen05.mma M=128 N=MP K=16, two TMEM accumulators
+//   warps 2-5  epilogue: tcgen05.ld, partial or final fma.rn(alpha, acc, beta*C)
+//              with coalesced plain loads/stores (lanes walk along N)
+#pragma once
+
+#include "common.cuh"
+
+namespace tcg {
+
+template <int MP_, int STAGES_>
+struct SkinnyCfg {
+    static constexpr int MP = MP_;  // padded rows of A = MMA N
+    static constexpr int BN = 128;  // rows of B per tile = MMA M
+    static constexpr int BK = 64;
+    static constexpr int STAGES = STAGES_;
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t A_BYTES = MP * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t OFF_B = 0;
+    static constexpr uint32_t OFF_A = STAGES * B_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_A + STAGES * A_BYTES;
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+    static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
+    static constexpr uint32_t TMEM_COLS = (2 * MP < 32) ? 32 : 2 * MP;
+    static constexpr int THREADS = 192;
+    static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MMA N for M = 128 is a multiple of 16");
+    static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation is a power of two");
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage images stay 1024-aligned");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+};
+
+// The CTA that owns linear k-block x when W blocks are split over G CTAs as
+// [W g / G, W (g+1) / G).
+__device__ __forceinline__ int32_t skinny_owner(int64_t x, int64_t W, int64_t G)
+{
+    return static_cast<int32_t>(((x + 1) * G - 1) / W);
+}
+
+__device__ __forceinline__ void epi_bar_sync()
+{
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <int MP>
+__device__ __forceinline__ void skinny_store(const GemmArgs &a, int32_t n, const float (&v)[MP])
+{
+    if (n >= a.N)
+        return;
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+        if (m < a.M) {
+            float d;
+            if (a.has_c)
+                d = fma_rn(a.alpha, v[m], mul_rn(a.beta, a.C[static_cast<int64_t>(m) * a.ldc + n]));
+            else
+                d = mul_rn(a.alpha, v[m]);
+            const int64_t o = static_cast<int64_t>(m) * a.ldd + n;
+            if (a.out_kind == kOutF32)
+                static_cast<float *>(a.D)[o] = d;
+            else if (a.out_kind == kOutBF16)
+                static_cast<unsigned short *>(a.D)[o] = f32_to_bf16_rn(d);
+            else
+                static_cast<unsigned short *>(a.D)[o] = f32_to_f16_rn(d);
+        }
+    }
+}
+
+template <int MP, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, const GemmArgs args)
+{
+    using Cfg = SkinnyCfg<MP, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x / 32u, 0);
+    const uint32_t lane = threadIdx.x % 32u;
+
+    const uint32_t bar0 = base + Cfg::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
+    volatile uint32_t *arrival = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 8);
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int64_t nkb = args.num_k_blocks;
+    const int64_t W = static_cast<int64_t>(args.num_tiles) * nkb;
+    const int64_t G = gridDim.x;
+    const int64_t my_start = W * blockIdx.x / G;
+    const int64_t my_end = W * (blockIdx.x + 1) / G;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int s = 0;
+        uint32_t ph = 0;
+        int pending = 0;
+        bool first = true;
+        bool alive = true;
+        for (int64_t pos = my_start; pos < my_end && alive;) {
+            const int32_t t = static_cast<int32_t>(pos / nkb);
+            const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
+            const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + (my_end - pos) ? nkb : kb0 + (my_end - pos));
+            for (int32_t kb = kb0; kb < kb1; ++kb) {
+                if (!warp_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status,
+                                       args.timeout_ns, kWhereProducerEmpty)) {
+                    alive = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES + (first ? args.extra_tx : 0u));
+                    tma_load_2d(base + Cfg::OFF_B + s * Cfg::B_BYTES, &tmB, full_bar(s), kb * Cfg::BK,
+                                t * Cfg::BN);
+                    tma_load_2d(base + Cfg::OFF_A + s * Cfg::A_BYTES, &tmA, full_bar(s), kb * Cfg::BK, 0);
+                }
+                first = false;
+                __syncwarp();
+                pending = min(pending + 1, STAGES);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            pos += kb1 - kb0;
+        }
+        if (!alive && lane == 0) {
+            int ds = s;
+            uint32_t dph = ph;
+            for (int i = 0; i < pending; ++i) {
+                if (--ds < 0) {
+                    ds = STAGES - 1;
+                    dph ^= 1u;
+                }
+                wait_drain(full_bar(ds), dph, 10000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32acc(args.ab_bf16 != 0, Cfg::BN, MP);
+            int s = 0;
+            uint32_t ph = 0;
+            int ab = 0;
+            uint32_t aph = 0;
+            bool alive = true;
+            for (int64_t pos = my_start; pos < my_end && alive;) {
+                const int32_t t = static_cast<int32_t>(pos / nkb);
+                const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
+                const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + (my_end - pos) ? nkb : kb0 + (my_end - pos));
+                if (!wait_bounded(acce_bar(ab), aph ^ 1u, abort_flag, args.status, args.timeout_ns,
+                                  kWhereMmaAccEmpty))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * MP);
+                for (int32_t kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
+                                      kWhereMmaFull)) {
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES);
+                    const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < Cfg::BK / 16; ++k)
+                        tc_mma_f16(d_tmem, bd + 2u * k, ad + 2u * k, idesc,
+                                   (kb != kb0 || k != 0) ? 1u : 0u);
+                    tc_commit(empty_bar(s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!alive)
+                    break;
+                tc_commit(accf_bar(ab));
+                if (++ab == 2) {
+                    ab = 0;
+                    aph ^= 1u;
+                }
+                pos += kb1 - kb0;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t q = warp & 3u;
+        const bool leader = warp == 2 && lane == 0;
+        int ab = 0;
+        uint32_t aph = 0;
+        for (int64_t pos = my_start; pos < my_end;) {
+            const int32_t t = static_cast<int32_t>(pos / nkb);
+            const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
+            const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + (my_end - pos) ? nkb : kb0 + (my_end - pos));
+            pos += kb1 - kb0;
+            const bool ok = warp_wait_bounded(accf_bar(ab), aph, abort_flag, args.status,
+                                              args.timeout_ns, kWhereEpiAccFull);
+            // all four warps agree before the named barriers below
+            epi_bar_sync();
+            if (!ok || *abort_flag)
+                break;
+            tc_fence_after_sync();
+            float v[MP];
+#pragma unroll
+            for (int g = 0; g < MP / 16; ++g) {
+                uint32_t r[16];
+                tc_ld_32x32b_x16(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * MP + 16 * g), r);
+                tc_wait_ld(r);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[16 * g + i] = __uint_as_float(r[i]);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce_bar(ab));
+            if (++ab == 2) {
+                ab = 0;
+                aph ^= 1u;
+            }
+
+            const int32_t n_local = 32 * static_cast<int32_t>(q) + static_cast<int32_t>(lane);
+            const int32_t n = t * Cfg::BN + n_local;
+            const int32_t c_lo = skinny_owner(static_cast<int64_t>(t) * nkb, W, G);
+            const int32_t c_hi = skinny_owner(static_cast<int64_t>(t + 1) * nkb - 1, W, G);
+            const int32_t parts = c_hi - c_lo + 1;
+            if (parts == 1) {
+                skinny_store<MP>(args, n, v);
+                continue;
+            }
+            // partial sum of this CTA -> workspace slot (t, blockIdx.x - c_lo)
+            float *slot0 = args.workspace + static_cast<int64_t>(t) * args.splits * (Cfg::BN * MP);
+            float *mine = slot0 + static_cast<int64_t>(blockIdx.x - c_lo) * (Cfg::BN * MP);
+#pragma unroll
+            for (int m = 0; m < MP; ++m)
+                __stcg(mine + m * Cfg::BN + n_local, v[m]);
+            __threadfence();
+            epi_bar_sync();
+            if (leader)
+                *arrival = atomicAdd(args.counters + t, 1u);
+            epi_bar_sync();
+            const uint32_t before = *arrival;
+            if (before != static_cast<uint32_t>(parts - 1))
+                continue;  // another CTA still has to add its part
+            // last to arrive: add the parts in slot order, then finish the tile
+            __threadfence();
+            float sum[MP];
+#pragma unroll
+            for (int m = 0; m < MP; ++m)
+                sum[m] = 0.f;
+            for (int p = 0; p < parts; ++p) {
+                const float *src = slot0 + static_cast<int64_t>(p) * (Cfg::BN * MP);
+#pragma unroll
+                for (int m = 0; m < MP; ++m)
+                    sum[m] += __ldcg(src + m * Cfg::BN + n_local);
+            }
+            skinny_store<MP>(args, n, sum);
+            if (leader)
+                args.counters[t] = 0u;  // ready for the next call
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace tcg

@@ -105,9 +105,10 @@ __global__ void __launch_bounds__(192, 1)
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
         }
-        if (args.has_c)
+        if (args.has_c && args.c_tma)
             tma_prefetch_desc(&tmC);
-        tma_prefetch_desc(&tmD);
+        if (args.d_tma)
+            tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -240,6 +241,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may read
         const uint32_t buf0 = base + Cfg::OFF_EPI + q * 2u * Cfg::EPI_BUF;
         const bool has_c = args.has_c != 0;
+        const bool c_tma = has_c && args.c_tma != 0;
         const bool acc_zero = args.num_k_blocks == 0;
         const int out_kind = args.out_kind;
         int ab = 0;
@@ -253,11 +255,12 @@ __global__ void __launch_bounds__(192, 1)
             const int32_t row0 = m0 + 32 * (int32_t)q;
             const bool rows_ok = row0 < args.M;
             const int32_t nchunks = min(BN / 32, (args.N - n0 + 31) / 32);
+            const int32_t my_row = row0 + (int32_t)lane;
 
             if (lane == 0)
                 bulk_wait_group_read<0>();  // last tile's stores are done with the buffers
             __syncwarp();
-            if (has_c && rows_ok && lane == 0) {
+            if (c_tma && rows_ok && lane == 0) {
                 for (int j = 0; j < 2 && j < nchunks; ++j) {
                     mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
                     tma_load_2d(buf0 + j * Cfg::EPI_BUF, &tmC, c_bar(q, j), n0 + 32 * j, row0);
@@ -271,7 +274,6 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after_sync();
 
             bool zero_row = acc_zero;
-            const int32_t my_row = row0 + (int32_t)lane;
             if (args.gather && my_row < args.M) {
                 const int32_t v = args.idx[my_row];
                 zero_row = zero_row || v < 0 || v >= args.table_rows;
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int32_t c = 0; c < nchunks; ++c) {
                 const int j = c & 1;
                 const uint32_t buf = buf0 + j * Cfg::EPI_BUF;
+                const int32_t col0 = n0 + 32 * c;
                 uint32_t acc[32];
                 tc_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * BN + 32 * c),
                                  acc);
@@ -293,8 +296,9 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 if (!rows_ok)
                     continue;
+                const bool d_direct = !args.d_tma || (args.d_tail_direct && col0 + 32 > args.N);
                 float v[32];
-                if (has_c) {
+                if (c_tma) {
                     if (!warp_wait_bounded(c_bar(q, j), cph[j], abort_flag, args.status,
                                            args.timeout_ns, kWhereEpiC)) {
                         alive = false;
@@ -303,56 +307,79 @@ __global__ void __launch_bounds__(192, 1)
                     cph[j] ^= 1u;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        uint32_t x0, x1, x2, x3;
-                        ld_shared_v4(buf + swz_off(lane, i, 128u), x0, x1, x2, x3);
-                        const float a0 = zero_row ? 0.f : __uint_as_float(acc[4 * i + 0]);
-                        const float a1 = zero_row ? 0.f : __uint_as_float(acc[4 * i + 1]);
-                        const float a2 = zero_row ? 0.f : __uint_as_float(acc[4 * i + 2]);
-                        const float a3 = zero_row ? 0.f : __uint_as_float(acc[4 * i + 3]);
-                        v[4 * i + 0] = fma_rn(args.alpha, a0, mul_rn(args.beta, __uint_as_float(x0)));
-                        v[4 * i + 1] = fma_rn(args.alpha, a1, mul_rn(args.beta, __uint_as_float(x1)));
-                        v[4 * i + 2] = fma_rn(args.alpha, a2, mul_rn(args.beta, __uint_as_float(x2)));
-                        v[4 * i + 3] = fma_rn(args.alpha, a3, mul_rn(args.beta, __uint_as_float(x3)));
+                        uint32_t x[4];
+                        ld_shared_v4(buf + swz_off(lane, i, 128u), x[0], x[1], x[2], x[3]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float a = zero_row ? 0.f : __uint_as_float(acc[4 * i + e]);
+                            v[4 * i + e] = fma_rn(args.alpha, a, mul_rn(args.beta, __uint_as_float(x[e])));
+                        }
+                    }
+                } else if (has_c) {
+                    const float *crow = args.C + static_cast<int64_t>(my_row) * args.ldc;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float cv = (my_row < args.M && col0 + i < args.N) ? crow[col0 + i] : 0.f;
+                        const float a = zero_row ? 0.f : __uint_as_float(acc[i]);
+                        v[i] = fma_rn(args.alpha, a, mul_rn(args.beta, cv));
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = mul_rn(args.alpha, zero_row ? 0.f : __uint_as_float(acc[i]));
-                    if (lane == 0)
-                        bulk_wait_group_read<1>();  // the store two chunks back left buffer j
                 }
-                __syncwarp();  // all of C read (in-place D) and buffer j free
-                if (out_kind == kOutF32) {
+                if (d_direct) {
+                    // plain stores, column by column, nothing past column N
+                    if (my_row < args.M) {
+                        const int64_t o = static_cast<int64_t>(my_row) * args.ldd + col0;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        st_shared_v4(buf + swz_off(lane, i, 128u), __float_as_uint(v[4 * i]),
-                                     __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
-                                     __float_as_uint(v[4 * i + 3]));
-                } else if (out_kind == kOutBF16) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        st_shared_v4(buf + swz_off(lane, i, 64u), pack_bf16x2(v[8 * i], v[8 * i + 1]),
-                                     pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                     pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
-                                     pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        st_shared_v4(buf + swz_off(lane, i, 64u), pack_f16x2(v[8 * i], v[8 * i + 1]),
-                                     pack_f16x2(v[8 * i + 2], v[8 * i + 3]),
-                                     pack_f16x2(v[8 * i + 4], v[8 * i + 5]),
-                                     pack_f16x2(v[8 * i + 6], v[8 * i + 7]));
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmD, buf, n0 + 32 * c, row0);
-                    bulk_commit_group();
-                    if (has_c && c + 2 < nchunks) {
-                        bulk_wait_group_read<0>();  // this store is done with buffer j
-                        mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
-                        tma_load_2d(buf, &tmC, c_bar(q, j), n0 + 32 * (c + 2), row0);
+                        for (int i = 0; i < 32; ++i) {
+                            if (col0 + i < args.N) {
+                                if (out_kind == kOutF32)
+                                    static_cast<float *>(args.D)[o + i] = v[i];
+                                else if (out_kind == kOutBF16)
+                                    static_cast<unsigned short *>(args.D)[o + i] = f32_to_bf16_rn(v[i]);
+                                else
+                                    static_cast<unsigned short *>(args.D)[o + i] = f32_to_f16_rn(v[i]);
+                            }
+                        }
                     }
+                } else {
+                    if (!c_tma && lane == 0)
+                        bulk_wait_group_read<1>();  // the store two chunks back left buffer j
+                    __syncwarp();  // all of C read (in-place D) and buffer j free
+                    if (out_kind == kOutF32) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            st_shared_v4(buf + swz_off(lane, i, 128u), __float_as_uint(v[4 * i]),
+                                         __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                                         __float_as_uint(v[4 * i + 3]));
+                    } else if (out_kind == kOutBF16) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            st_shared_v4(buf + swz_off(lane, i, 64u), pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                         pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                         pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                         pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            st_shared_v4(buf + swz_off(lane, i, 64u), pack_f16x2(v[8 * i], v[8 * i + 1]),
+                                         pack_f16x2(v[8 * i + 2], v[8 * i + 3]),
+                                         pack_f16x2(v[8 * i + 4], v[8 * i + 5]),
+                                         pack_f16x2(v[8 * i + 6], v[8 * i + 7]));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmD, buf, col0, row0);
+                        bulk_commit_group();
+                    }
+                }
+                if (c_tma && c + 2 < nchunks && lane == 0) {
+                    bulk_wait_group_read<0>();  // the store of this chunk is done with buffer j
+                    mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
+                    tma_load_2d(buf, &tmC, c_bar(q, j), n0 + 32 * (c + 2), row0);
                 }
                 __syncwarp();
             }
@@ -361,7 +388,7 @@ __global__ void __launch_bounds__(192, 1)
                 aph ^= 1u;
             }
         }
-        if (!alive && has_c && lane == 0) {
+        if (!alive && c_tma && lane == 0) {
             // C loads issued for this tile may still be landing: let them finish
             for (int j = 0; j < 2; ++j)
                 wait_drain(c_bar(q, j), cph[j], 10000000ull);

@@ -20,4 +20,31 @@ int tile_stages(int bn);
 cudaError_t launch_tile(int bn, const GemmMaps &maps, const GemmArgs &args, int grid,
                         cudaStream_t stream);
 
+int skinny_stages(int mp);
+cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
+                          cudaStream_t stream);
+
+// Stream-K split of the skinny kernel: the CTA that owns linear k-block x
+// when W blocks are shared by G CTAs as [W g / G, W (g+1) / G).
+inline int64_t skinny_owner_host(int64_t x, int64_t W, int64_t G) { return ((x + 1) * G - 1) / W; }
+
+// Most CTAs that contribute to one tile (workspace slots per tile).
+inline int32_t skinny_max_parts(int64_t tiles, int64_t nkb, int64_t G)
+{
+    const int64_t W = tiles * nkb;
+    if (tiles > 65536) {
+        // shares are at least W / G blocks long, so a tile of nkb blocks holds at
+        // most (nkb - 1) / (W / G) + 1 share boundaries
+        const int64_t shortest = W / G;
+        return static_cast<int32_t>((nkb - 1) / shortest + 2);
+    }
+    int64_t most = 1;
+    for (int64_t t = 0; t < tiles; ++t) {
+        const int64_t parts = skinny_owner_host((t + 1) * nkb - 1, W, G) -
+                              skinny_owner_host(t * nkb, W, G) + 1;
+        most = parts > most ? parts : most;
+    }
+    return static_cast<int32_t>(most);
+}
+
 }  // namespace tcg

@@ -303,6 +303,20 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     return d;
 }
 
+__device__ __forceinline__ unsigned short f32_to_bf16_rn(float x)
+{
+    unsigned short d;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(d) : "f"(x));
+    return d;
+}
+
+__device__ __forceinline__ unsigned short f32_to_f16_rn(float x)
+{
+    unsigned short d;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(d) : "f"(x));
+    return d;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)
 {

@@ -254,3 +254,65 @@ def test_host_side_errors_with_device_tensors():
     st = lib.gemm_bf16(32, 32, 64, A.data_ptr(), 64, B.data_ptr(), 64, None, 0,
                        A.data_ptr(), 64, 0, 1.0, 0.0, s)
     assert st == 4
+
+
+SKINNY_SHAPES = [(1, 300, 64), (5, 1000, 520), (16, 4096, 1024), (17, 777, 264),
+                 (33, 2048, 4096), (64, 5000, 136), (64, 128, 64), (2, 28672, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", SKINNY_SHAPES)
+def test_skinny_quarter_bit_exact(M, N, K):
+    """M <= 64 goes through the swap-AB stream-K kernel; exact inputs stay exact
+    through its split partial sums."""
+    plan = binding.gemm_query_plan(M, N, K, sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan.kernel == 2
+    for out, with_c, alpha, beta in [(OUT_F32, True, 0.5, 2.0), (OUT_BF16, False, 1.0, 0.0)]:
+        p = workloads.random_problem(M + N + K, M, N, K, dtype="bf16", values="quarter",
+                                     with_c=with_c, alpha=alpha, beta=beta, out=out)
+        ref, _, _ = oracle_full(p)
+        assert_bits(run(p), ref, out, f"skinny {M}x{N}x{K} out={out}")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 28672, 4096), (40, 3000, 2056), (7, 513, 8192)])
+def test_skinny_normal_within_tolerance(M, N, K):
+    p = workloads.random_problem(M * N + K, M, N, K, dtype="f16", with_c=True, alpha=0.5,
+                                 beta=1.0, b_scale=0.02)
+    ref, absprod, _ = oracle_full(p)
+    assert_within(run(p), ref, absprod, OUT_F32, f"skinny {M}x{N}x{K}")
+
+
+def test_skinny_repeated_calls_are_deterministic():
+    """The stream-K partial sums are added in a fixed order: identical bits every call."""
+    p = workloads.random_problem(31, 16, 8192, 4096, dtype="bf16", with_c=True, alpha=0.5)
+    first = run(p)
+    for _ in range(3):
+        assert torch.equal(run(p), first)
+
+
+def test_skinny_timeout_is_reported():
+    p = workloads.random_problem(32, 16, 2048, 1024, dtype="bf16", values="quarter")
+    binding.gemm_set_wait_timeout(50_000_000)
+    binding.gemm_debug_inject(1)
+    try:
+        run(p)
+        assert device_status() == binding.GEMM_ERR_TIMEOUT
+    finally:
+        binding.gemm_debug_inject(0)
+        binding.gemm_set_wait_timeout(0)
+    ref, _, _ = oracle_full(p)
+    assert_bits(run(p), ref, OUT_F32, "skinny after timeout")
+
+
+@pytest.mark.parametrize("M", [16, 300])
+def test_k_tail_padding_is_not_read(M):
+    """K = 20 with a row pitch of 24: the 4 padding columns hold NaN and must not
+    reach the result (TMA zero-fills past the tensor's K extent)."""
+    K, ld, N = 20, 24, 200
+    p = workloads.random_problem(33, M, N, K, dtype="bf16", values="quarter")
+    Ap = torch.full((M, ld), float("nan"), dtype=torch.bfloat16)
+    Ap[:, :K] = p.A
+    Bp = torch.full((N, ld), float("nan"), dtype=torch.bfloat16)
+    Bp[:, :K] = p.B
+    ref, _, _ = oracle_full(p)
+    D = binding.gemm_bf16(Ap.to(DEV)[:, :K], Bp.to(DEV)[:, :K])
+    assert_bits(D, ref, OUT_F32, "K tail")

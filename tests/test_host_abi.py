@@ -1,0 +1,127 @@
+"""Host-side checks that need no GPU: the library loads, exports every symbol the
+header declares, rejects bad arguments before touching CUDA, and plans kernels."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tensor_core_gemm_02_gb300 import binding
+from tensor_core_gemm_02_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tcgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_check_device_status",
+              "gemm_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    names = ["GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_ALIGNMENT", "GEMM_ERR_UNSUPPORTED",
+             "GEMM_ERR_ALIAS", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT", "GEMM_ERR_INDEX"]
+    for code, name in enumerate(names):
+        assert binding.gemm_status_string(code) == name
+    assert binding.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+# Fake, never-dereferenced device addresses: validation runs before any CUDA call.
+A0, B0, C0, D0, I0 = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def call_bf16(lib, M=64, N=64, K=64, A=A0, lda=64, B=B0, ldb=64, C=None, ldc=0, D=D0, ldd=64,
+              out=0, alpha=1.0, beta=0.0):
+    return lib.gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, out, alpha, beta, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), 1), (dict(K=-5), 1), (dict(out=3), 1), (dict(D=None), 1),
+    (dict(A=None), 1), (dict(B=None), 1), (dict(lda=32), 1), (dict(ldb=8), 1),
+    (dict(ldd=63), 1), (dict(C=C0, ldc=10, beta=1.0), 1),
+    (dict(A=A0 + 8), 2), (dict(B=B0 + 2), 2), (dict(lda=68), 2), (dict(ldb=100), 2),
+    (dict(D=D0 + 2), 2), (dict(C=C0 + 2, ldc=64, beta=1.0), 2),
+    (dict(M=1 << 31), 3), (dict(K=1 << 32), 3),
+    (dict(D=A0 + 64), 4), (dict(D=B0), 4), (dict(C=D0 + 16, ldc=64, beta=1.0), 4),
+    (dict(C=D0, ldc=64, beta=1.0, out=1), 4), (dict(C=D0, ldc=72, ldd=64, beta=1.0), 4),
+])
+def test_invalid_arguments_rejected_without_gpu(lib, kw, code):
+    assert call_bf16(lib, **kw) == code
+
+
+def test_valid_shapes_that_need_no_launch(lib):
+    assert call_bf16(lib, M=0) == 0
+    assert call_bf16(lib, N=0) == 0
+    # C given but beta == 0: C is ignored entirely (even if misaligned / aliasing)
+    assert call_bf16(lib, M=0, C=D0 + 3, beta=0.0) == 0
+
+
+def test_gather_argument_checks(lib):
+    f = lib.gemm_gather_rows
+    ok = dict(M=64, N=64, K=64, bf=1, T=A0, rows=100, lda=64, idx=I0, B=B0, ldb=64, C=None,
+              ldc=0, D=D0, ldd=64, out=0, alpha=1.0, beta=0.0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["M"], a["N"], a["K"], a["bf"], a["T"], a["rows"], a["lda"], a["idx"], a["B"],
+                 a["ldb"], a["C"], a["ldc"], a["D"], a["ldd"], a["out"], a["alpha"], a["beta"],
+                 None)
+
+    assert call(idx=None) == 1
+    assert call(rows=0) == 1
+    assert call(bf=2) == 1
+    assert call(idx=I0 + 2) == 2
+    assert call(D=I0) == 4  # D overlaps idx
+    assert call(D=A0 + 99 * 128) == 4  # D overlaps the last table row
+
+
+def test_plan_matches_the_dispatch_rules(lib):
+    p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
+    assert (p.kernel, p.bm, p.bn, p.grid) == (1, 128, 256, 148)
+    assert p.tiles == 64 * 32
+    p = binding.gemm_query_plan(1024, 1024, 1024, sm_count=148)
+    assert (p.kernel, p.bn) == (1, 64) and p.tiles == 128 and p.grid == 128
+    p = binding.gemm_query_plan(16, 28672, 4096, sm_count=148)
+    assert (p.kernel, p.bm, p.bn, p.tiles, p.grid) == (2, 16, 128, 224, 148)
+    # stream-K shares of 224 * 64 k-blocks over 148 CTAs: at most 2 per tile
+    assert p.splits == 2
+    p = binding.gemm_query_plan(16384, 4096, 4096, gather=True, sm_count=148)
+    assert p.kernel == 1 and p.bn == 256
+    p = binding.gemm_query_plan(40, 1000, 64, sm_count=148)
+    assert p.kernel == 2 and p.bm == 64
+    assert binding.gemm_query_plan(0, 10, 10).kernel == 0
+
+
+def test_skinny_split_arithmetic_covers_every_block():
+    """The stream-K shares partition the k-block list and every tile's parts fit its slots."""
+    for tiles, nkb, G in [(224, 64, 148), (3, 5, 7), (1, 1, 1), (10, 3, 30), (1000, 7, 152)]:
+        W = tiles * nkb
+        G = min(G, W)
+        owner = lambda x: ((x + 1) * G - 1) // W
+        starts = [W * g // G for g in range(G)]
+        for g in range(G):
+            lo, hi = starts[g], W * (g + 1) // G
+            assert all(owner(x) == g for x in range(lo, hi))
+        most = max(owner((t + 1) * nkb - 1) - owner(t * nkb) + 1 for t in range(tiles))
+        p = binding.gemm_query_plan(16, tiles * 128, nkb * 64, sm_count=G)
+        assert p.splits == most
