@@ -427,6 +427,21 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_case(args):
+    """Run one workload's GEMM warmup + steps times and exit (a target for profilers)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    p = workloads.WORKLOADS[args.case]()
+    tensors = to_device(p, dev)
+    for _ in range(args.warmup + args.steps):
+        launch(p, tensors)
+    torch.cuda.synchronize()
+    status = binding.gemm_check_device_status()
+    if status != binding.GEMM_OK:
+        raise RuntimeError(f"device status {binding.gemm_status_string(status)}")
+    print(f"case {args.case}: {args.warmup} + {args.steps} launches ok", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -436,7 +451,12 @@ def main():
     ap.add_argument("--no-variants", dest="variants", action="store_false")
     ap.add_argument("--variant-reps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--case", choices=sorted(workloads.WORKLOADS), default=None,
+                    help="only launch this workload's GEMM warmup + steps times (profiling)")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

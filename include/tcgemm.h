@@ -136,6 +136,42 @@ gemm_status gemm_gather_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
                              int out, float alpha, float beta, void *stream);
 
 /*
+ * Allocation-free variant of the skinny (M <= 64) path.  The source pages have
+ * no counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc where they run the GEMM: code whose device memory is owned by
+ * another allocator (a framework's caching allocator, or a serving engine that
+ * reserves the whole GPU up front) and latency-critical sections where the
+ * implicit synchronisation of cudaMalloc/cudaFree is not allowed.
+ *
+ * It computes exactly what gemm_f16 / gemm_bf16 compute for M <= 64, with the
+ * same kernel, but its scratch (partial tiles and arrival counters) lives in
+ * one fixed device array inside the library: 16 MiB of partials plus 16384
+ * counters (16.06 MiB in all), held by every GPU that loads the library until
+ * the process exits.  The call itself allocates no device memory; the caller
+ * still owns A, B, C and D.
+ *
+ *  dtype_is_bf16  0: A and B are f16; 1: bf16.  Other arguments as gemm_f16.
+ *
+ * Returns GEMM_ERR_UNSUPPORTED when M > 64 or K == 0 (other kernels, which this
+ * entry point does not run) or when the problem needs more scratch than the
+ * array holds (more than 16384 tiles of 128 columns of N, or more than 16 MiB
+ * of partial tiles).  All other errors as gemm_f16.
+ *
+ * The first call on a device looks up the array's device address (and sets up
+ * the library's per-device state); make that first call before any stream
+ * capture.  Every call on a device shares the one array, which keeps what the
+ * last call left there: each call clears the counters it needs on `stream`
+ * before launching.  Calls whose executions overlap on the GPU (different
+ * streams, no ordering between them) race on the array and give wrong results.
+ */
+gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
+                                const void *A, int64_t lda,
+                                const void *B, int64_t ldb,
+                                const float *C, int64_t ldc,
+                                void *D, int64_t ldd,
+                                int out, float alpha, float beta, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the first error the device
  * recorded since the last call on the current device (GEMM_OK if none).
  * Returns GEMM_ERR_CUDA if the synchronisation itself failed.  After a

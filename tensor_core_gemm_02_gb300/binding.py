@@ -55,13 +55,16 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_bf16.argtypes = plain
     lib.gemm_gather_rows.argtypes = [i64, i64, i64, i32, vp, i64, i64, vp, vp, i64, vp, i64,
                                      vp, i64, i32, f32, f32, vp]
+    lib.gemm_skinny_noalloc.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
+                                        i32, f32, f32, vp]
     lib.gemm_check_device_status.argtypes = [vp]
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_query_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(Plan)]
     lib.gemm_set_wait_timeout.argtypes = [ctypes.c_uint64]
     lib.gemm_debug_inject.argtypes = [i32]
-    for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_check_device_status",
+    for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_skinny_noalloc",
+                 "gemm_check_device_status",
                  "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -148,6 +151,27 @@ def gemm_gather_rows(table, idx, B, C=None, D=None, *, alpha=1.0, beta=1.0, out=
         _ptr(idx), _ptr(B), _ld(B), _ptr(C), _ld(C) if C is not None else 0, _ptr(D), _ld(D),
         out, float(alpha), float(beta), _stream_ptr(stream))
     _check(st, "gemm_gather_rows")
+    return D
+
+
+def gemm_skinny_noalloc(A, B, C=None, D=None, *, alpha=1.0, beta=1.0, out=OUT_F32,
+                        stream=None):
+    """The M <= 64 path with the library's fixed scratch array: the call allocates
+    no device memory (D must then be given by the caller to avoid allocating here)."""
+    if A.dtype not in (torch.float16, torch.bfloat16) or B.dtype != A.dtype:
+        raise TypeError("A and B must both be f16 or both bf16")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    if C is not None and (C.dtype != torch.float32 or tuple(C.shape) != (M, N)):
+        raise ValueError("C must be float32 M x N")
+    D = _out_tensor(D, M, N, out, A.device)
+    st = load_library().gemm_skinny_noalloc(
+        M, N, K, 1 if A.dtype == torch.bfloat16 else 0, _ptr(A), _ld(A), _ptr(B), _ld(B),
+        _ptr(C), _ld(C) if C is not None else 0, _ptr(D), _ld(D), out, float(alpha),
+        float(beta), _stream_ptr(stream))
+    _check(st, "gemm_skinny_noalloc")
     return D
 
 

@@ -17,27 +17,18 @@
 #include <mutex>
 #include <vector>
 
-#include "launch.h"
-#include "tcgemm.h"
+#include "host_internal.h"
 
 // First device-side error code [0] and where it arose [1], one per device.
 static __device__ uint32_t g_device_status[4];
 
-namespace {
-
-using tcg::GemmArgs;
-using tcg::GemmMaps;
+namespace tcg {
+namespace host {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
-struct DeviceInfo {
-    bool ready = false;
-    int index = 0;
-    int sm_count = 0;
-    uint32_t *status = nullptr;
-};
 
 // Scratch of the skinny kernel: per-split partial tiles and per-tile arrival
 // counters.  One per (device, stream), so calls on different streams never
@@ -243,24 +234,6 @@ bool overlap(const void *a, uint64_t an, const void *b, uint64_t bn)
 
 int out_size(int out) { return out == GEMM_OUT_F32 ? 4 : 2; }
 
-struct Problem {
-    int64_t M, N, K;
-    bool bf16;
-    const void *A;
-    int64_t a_rows;  // rows of A, or of the gather table
-    int64_t lda;
-    const int32_t *idx;
-    const void *B;
-    int64_t ldb;
-    const float *C;
-    int64_t ldc;
-    void *D;
-    int64_t ldd;
-    int out;
-    float alpha, beta;
-    bool gather;
-    cudaStream_t stream;
-};
 
 gemm_status validate(const Problem &p, bool *empty)
 {
@@ -499,7 +472,10 @@ gemm_status run(const Problem &p)
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-}  // namespace
+}  // namespace host
+}  // namespace tcg
+
+using namespace tcg::host;
 
 // ------------------------------------------------------------- exported ABI
 

@@ -1,0 +1,61 @@
+// host_internal.h -- host-side helpers of the C ABI shared by the files that
+// implement entry points (validation, device state, TMA descriptors, plans).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+#include "tcgemm.h"
+
+namespace tcg {
+namespace host {
+
+struct DeviceInfo {
+    bool ready = false;
+    int index = 0;
+    int sm_count = 0;
+    uint32_t *status = nullptr;
+};
+
+struct Problem {
+    int64_t M, N, K;
+    bool bf16;
+    const void *A;
+    int64_t a_rows;  // rows of A, or of the gather table
+    int64_t lda;
+    const int32_t *idx;
+    const void *B;
+    int64_t ldb;
+    const float *C;
+    int64_t ldc;
+    void *D;
+    int64_t ldd;
+    int out;
+    float alpha, beta;
+    bool gather;
+    cudaStream_t stream;
+};
+
+// Per-device state (SM count, status word address); first call sets it up.
+gemm_status device_info(DeviceInfo **out);
+
+// Argument, alignment and aliasing checks; *empty is set for M == 0 or N == 0.
+gemm_status validate(const Problem &p, bool *empty);
+
+// Encode (or fetch from the cache) a 2-D tiled TMA descriptor.
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dtype, const void *ptr, uint64_t inner,
+               uint64_t outer, uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle);
+
+CUtensorMapDataType ab_type(bool bf16);
+int64_t ceil_div(int64_t a, int64_t b);
+gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, int sm_count);
+
+// Kernel arguments common to every kernel (sizes, epilogue, status, timeout).
+void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev);
+
+}  // namespace host
+}  // namespace tcg
