@@ -187,12 +187,14 @@ const char *gemm_status_string(int status);
  * The kernel choice the library makes for a problem, without launching
  * anything and without touching the GPU (for diagnostics and tests).
  *
- *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles),
- *           2 = skinny swap-AB kernel (M <= 64)
+ *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles, one
+ *           CTA each), 2 = skinny swap-AB kernel (M <= 64), 3 = tile kernel
+ *           on CTA pairs (256-row tiles, tcgen05 cta_group::2)
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)
- *  grid     CTAs launched for `sm_count` SMs
+ *  grid     CTAs launched for `sm_count` SMs (pairs: at most sm_count / 2
+ *           pairs; on a device, at most the pairs that can be resident)
  */
 typedef struct {
     int32_t kernel;
@@ -222,6 +224,15 @@ gemm_status gemm_set_wait_timeout(uint64_t ns);
  * mode 0 turns it off.
  */
 gemm_status gemm_debug_inject(int mode);
+
+/*
+ * Test hook.  Force the form of the tile kernel for later calls: kernel 1 =
+ * single CTAs with tile width bn in {64, 128, 256}, kernel 3 = CTA pairs with
+ * bn = 256, kernel 0 = automatic choice (the default).  Problems the forced
+ * form cannot run (the M <= 64 skinny path; K == 0 for pairs) keep the
+ * automatic choice.  Returns GEMM_ERR_INVALID_ARG for other values.
+ */
+gemm_status gemm_debug_force_tile(int kernel, int bn);
 
 #ifdef __cplusplus
 }

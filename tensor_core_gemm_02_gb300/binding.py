@@ -63,9 +63,11 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_query_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(Plan)]
     lib.gemm_set_wait_timeout.argtypes = [ctypes.c_uint64]
     lib.gemm_debug_inject.argtypes = [i32]
+    lib.gemm_debug_force_tile.argtypes = [i32, i32]
     for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_skinny_noalloc",
                  "gemm_check_device_status",
-                 "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject"):
+                 "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject",
+                 "gemm_debug_force_tile"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -200,3 +202,7 @@ def gemm_set_wait_timeout(ns: int) -> None:
 
 def gemm_debug_inject(mode: int) -> None:
     _check(load_library().gemm_debug_inject(int(mode)), "gemm_debug_inject")
+
+
+def gemm_debug_force_tile(kernel: int, bn: int = 0) -> None:
+    _check(load_library().gemm_debug_force_tile(int(kernel), int(bn)), "gemm_debug_force_tile")

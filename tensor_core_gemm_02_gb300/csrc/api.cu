@@ -49,6 +49,8 @@ DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_inject{0};
+std::atomic<int> g_force_kernel{0};  // test hook: 0 automatic, 1 single CTAs, 3 CTA pairs
+std::atomic<int> g_force_bn{0};
 
 gemm_status device_info(DeviceInfo **out)
 {
@@ -297,21 +299,34 @@ gemm_status validate(const Problem &p, bool *empty)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Tile width for the 128-row tile kernel: the fewest waves of persistent
-// CTAs, weighting each wave by the tile width plus a fixed per-tile cost.
-int choose_bn(int64_t M, int64_t N, int sm_count)
+// Tile shape for the tile kernel: single CTAs with 128 x {256, 128, 64} tiles,
+// or CTA pairs with 256 x 256 tiles.  Cost = waves of persistent CTA sets,
+// each weighted by the per-SM tile width plus a fixed per-tile cost; pairs
+// get a 10% credit because each SM moves 2/3 of the operand bytes.
+struct TileChoice {
+    bool pair;
+    int bn;
+};
+
+TileChoice choose_tile(int64_t M, int64_t N, int64_t K, int sm_count)
 {
     static const int widths[3] = {256, 128, 64};
-    int best = 256;
-    int64_t best_cost = -1;
+    TileChoice best{false, 256};
+    double best_cost = -1.0;
     for (int w : widths) {
         const int64_t tiles = ceil_div(M, 128) * ceil_div(N, w);
-        const int64_t waves = ceil_div(tiles, sm_count);
-        const int64_t cost = waves * (w + 32);
+        const double cost = static_cast<double>(ceil_div(tiles, sm_count) * (w + 32));
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
-            best = w;
+            best = TileChoice{false, w};
         }
+    }
+    const int pairs = sm_count / 2;
+    if (K > 0 && pairs > 0) {
+        const int64_t tiles = ceil_div(M, 256) * ceil_div(N, 256);
+        const double cost = 0.9 * static_cast<double>(ceil_div(tiles, pairs) * (256 + 32));
+        if (cost <= best_cost)
+            best = TileChoice{true, 256};
     }
     return best;
 }
@@ -340,14 +355,22 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, int sm_count)
         p.grid = static_cast<int32_t>(G);
         return p;
     }
-    const int bn = choose_bn(M, N, sm_count);
-    p.kernel = 1;
-    p.bm = 128;
-    p.bn = bn;
-    p.stages = tcg::tile_stages(bn);
-    p.tiles = ceil_div(M, 128) * ceil_div(N, bn);
+    const TileChoice c = choose_tile(M, N, K, sm_count);
     p.splits = 1;
-    p.grid = static_cast<int32_t>(p.tiles < sm_count ? p.tiles : sm_count);
+    p.bn = c.bn;
+    p.stages = tcg::tile_stages(c.bn, c.pair);
+    if (c.pair) {
+        const int64_t pairs = sm_count / 2;
+        p.kernel = 3;
+        p.bm = 256;
+        p.tiles = ceil_div(M, 256) * ceil_div(N, c.bn);
+        p.grid = static_cast<int32_t>(2 * (p.tiles < pairs ? p.tiles : pairs));
+    } else {
+        p.kernel = 1;
+        p.bm = 128;
+        p.tiles = ceil_div(M, 128) * ceil_div(N, c.bn);
+        p.grid = static_cast<int32_t>(p.tiles < sm_count ? p.tiles : sm_count);
+    }
     return p;
 }
 
@@ -408,6 +431,32 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Test hook: replace the automatic tile form by a forced one where it can run.
+gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
+{
+    const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
+    if (fk == 0 || (plan.kernel != 1 && plan.kernel != 3))
+        return plan;
+    if (fk == 3 && p.K == 0)
+        return plan;
+    plan.bn = fbn;
+    plan.stages = tcg::tile_stages(fbn, fk == 3);
+    plan.splits = 1;
+    if (fk == 3) {
+        const int64_t pairs = sm_count / 2;
+        plan.kernel = 3;
+        plan.bm = 256;
+        plan.tiles = ceil_div(p.M, 256) * ceil_div(p.N, fbn);
+        plan.grid = static_cast<int32_t>(2 * (plan.tiles < pairs ? plan.tiles : pairs));
+    } else {
+        plan.kernel = 1;
+        plan.bm = 128;
+        plan.tiles = ceil_div(p.M, 128) * ceil_div(p.N, fbn);
+        plan.grid = static_cast<int32_t>(plan.tiles < sm_count ? plan.tiles : sm_count);
+    }
+    return plan;
+}
+
 gemm_status run(const Problem &p)
 {
     bool empty = false;
@@ -417,7 +466,8 @@ gemm_status run(const Problem &p)
     DeviceInfo *dev = nullptr;
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
-    const gemm_plan plan = make_plan(p.M, p.N, p.K, p.gather, dev->sm_count);
+    const gemm_plan plan =
+        apply_forced_tile(make_plan(p.M, p.N, p.K, p.gather, dev->sm_count), p, dev->sm_count);
     const bool c_used = p.C != nullptr && p.beta != 0.0f;
 
     GemmMaps maps;
@@ -425,6 +475,16 @@ gemm_status run(const Problem &p)
     if (plan.kernel == 2)
         return run_skinny(p, plan, dev);
     const int bn = plan.bn;
+    const bool pair = plan.kernel == 3;
+    const int bn_local = pair ? bn / 2 : bn;  // rows of B each CTA loads
+    int grid = plan.grid;
+    if (pair) {
+        // never more pairs than can be resident together (unpaired SMs stay idle)
+        const int resident = tcg::tile_max_pairs(bn);
+        if (resident <= 0)
+            return GEMM_ERR_CUDA;
+        grid = static_cast<int>(2 * (plan.tiles < resident ? plan.tiles : resident));
+    }
     if (p.K > 0) {
         const bool ok_a =
             p.gather ? encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.a_rows, p.lda * 2, 64, 1,
@@ -432,7 +492,7 @@ gemm_status run(const Problem &p)
                      : encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.M, p.lda * 2, 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
         const bool ok_b = encode_2d(&maps.b, ab_type(p.bf16), p.B, p.K, p.N, p.ldb * 2, 64,
-                                    static_cast<uint32_t>(bn), CU_TENSOR_MAP_SWIZZLE_128B);
+                                    static_cast<uint32_t>(bn_local), CU_TENSOR_MAP_SWIZZLE_128B);
         if (!ok_a || !ok_b)
             return GEMM_ERR_CUDA;
     }
@@ -454,7 +514,7 @@ gemm_status run(const Problem &p)
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     fill_common(a, p, dev);
-    a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, 128));
+    a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, pair ? 256 : 128));
     a.num_n_blocks = static_cast<int32_t>(ceil_div(p.N, bn));
     a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, 64));
     a.num_tiles = static_cast<int32_t>(plan.tiles);
@@ -468,7 +528,7 @@ gemm_status run(const Problem &p)
     a.idx = p.idx;
     a.table_rows = static_cast<int32_t>(p.a_rows);
 
-    const cudaError_t e = tcg::launch_tile(bn, maps, a, plan.grid, p.stream);
+    const cudaError_t e = tcg::launch_tile(bn, pair, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -559,6 +619,17 @@ gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather, int sm_
 gemm_status gemm_set_wait_timeout(uint64_t ns)
 {
     g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
+    return GEMM_OK;
+}
+
+gemm_status gemm_debug_force_tile(int kernel, int bn)
+{
+    const bool ok = (kernel == 0) || (kernel == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
+                    (kernel == 3 && bn == 256);
+    if (!ok)
+        return GEMM_ERR_INVALID_ARG;
+    g_force_kernel.store(kernel);
+    g_force_bn.store(bn);
     return GEMM_OK;
 }
 

@@ -15,6 +15,13 @@
 //               swizzled shared image, TMA store ("cp.async.bulk.tensor"
 //               page, section "Stores, reductions, and completion").
 //
+// PAIR = true runs the same roles on a CTA pair (a cluster of two) sharing
+// one tcgen05.mma.cta_group::2 of M = 256: each CTA loads its own 128 rows of
+// A and its own half of the BN rows of B, both report their bytes to the
+// leader CTA's stage barrier, the leader's MMA thread issues for both, and
+// commits arrive in both CTAs.  Each CTA drains its own 128 accumulator rows.
+// Per SM this moves 2/3 of the operand bytes of the single-CTA form.
+//
 // Two accumulators let the epilogue of tile i overlap the mainloop of tile
 // i+1.  Every wait is bounded (common.cuh); on a timeout all roles leave
 // their loops, the copies in flight are drained, TMEM is freed and the
@@ -25,14 +32,17 @@
 
 namespace tcg {
 
-template <int BN_, int STAGES_>
+template <int BN_, int STAGES_, bool PAIR_ = false>
 struct TileCfg {
-    static constexpr int BM = 128;
+    static constexpr bool PAIR = PAIR_;
+    static constexpr int BM = 128;                  // rows of A (and D) per CTA
+    static constexpr int TILE_M = PAIR ? 256 : 128;  // rows per output tile
     static constexpr int BN = BN_;
+    static constexpr int BN_LOCAL = PAIR ? BN / 2 : BN;  // rows of B each CTA loads
     static constexpr int BK = 64;  // 64 x 16-bit = one 128-byte swizzle row
     static constexpr int STAGES = STAGES_;
     static constexpr uint32_t A_BYTES = BM * BK * 2;
-    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t B_BYTES = BN_LOCAL * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t EPI_BUF = 32 * 128;  // 32 rows x 128 B
     static constexpr uint32_t OFF_A = 0;
@@ -47,6 +57,7 @@ struct TileCfg {
     static constexpr int THREADS = 192;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+    static_assert(!PAIR || (BN % 32 == 0 && BN_LOCAL % 8 == 0), "pair splits B in 8-row groups");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
 };
@@ -61,14 +72,14 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t row, uint32_t chunk, uint32
     return lin ^ (((lin >> 7) & mask) << 4);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool PAIR>
 __global__ void __launch_bounds__(192, 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC,
                      const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
 {
-    using Cfg = TileCfg<BN, STAGES>;
+    using Cfg = TileCfg<BN, STAGES, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -86,6 +97,20 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
 
+    // pair bookkeeping (rank 0 leads; single-CTA form: rank 0, cluster of one)
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0u;
+    const int32_t cta_set = PAIR ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
+    const int32_t cta_sets = PAIR ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
+    // the leader's copy of a barrier, as a shared::cluster address
+    auto lead = [&](uint32_t bar) { return PAIR ? mapa_shared(bar, 0u) : bar; };
+    // raise the abort flag here and (pair) in the peer CTA
+    auto raise_abort = [&]() {
+        *abort_flag = 1u;
+        if (PAIR)
+            st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(abort_flag)), rank ^ 1u), 1u);
+    };
+
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -93,7 +118,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
+            mbar_init(acce_bar(b), PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
         }
         for (int q = 0; q < 4; ++q)
             for (int j = 0; j < 2; ++j)
@@ -111,11 +136,19 @@ __global__ void __launch_bounds__(192, 1)
             tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync_all();  // the peer's barriers exist before anything targets them
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -126,10 +159,11 @@ __global__ void __launch_bounds__(192, 1)
         int pending = 0;  // stages issued and not yet seen consumed (for teardown)
         bool first = true;
         bool alive = true;
-        for (int32_t t = blockIdx.x; t < args.num_tiles && alive; t += gridDim.x) {
+        for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
-            const int32_t m0 = mb * Cfg::BM, n0 = nb * BN;
+            const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * Cfg::BM;
+            const int32_t nb0 = nb * BN + static_cast<int32_t>(rank) * Cfg::BN_LOCAL;
             int32_t rows[4] = {0, 0, 0, 0};
             if (args.gather) {
                 // lane l fetches rows 4l .. 4l+3 of the tile, four per gather4
@@ -152,8 +186,9 @@ __global__ void __launch_bounds__(192, 1)
                     alive = false;
                     break;
                 }
-                if (lane == 0) {
-                    const uint32_t bytes = Cfg::STAGE_BYTES + (first ? args.extra_tx : 0u);
+                if (lane == 0 && leader) {
+                    // the leader's barrier counts the bytes of both CTAs of a pair
+                    const uint32_t bytes = (PAIR ? 2u : 1u) * Cfg::STAGE_BYTES + (first ? args.extra_tx : 0u);
                     mbar_arrive_expect_tx(full_bar(s), bytes);
                 }
                 first = false;
@@ -161,13 +196,24 @@ __global__ void __launch_bounds__(192, 1)
                 const int32_t k0 = kb * Cfg::BK;
                 const uint32_t sa = base + Cfg::OFF_A + s * Cfg::A_BYTES;
                 const uint32_t sb = base + Cfg::OFF_B + s * Cfg::B_BYTES;
-                if (args.gather)
-                    tma_gather4(sa + lane * 512u, &tmA, full_bar(s), k0, rows[0], rows[1], rows[2],
-                                rows[3]);
-                else if (lane == 0)
-                    tma_load_2d(sa, &tmA, full_bar(s), k0, m0);
-                if (lane == 0)
-                    tma_load_2d(sb, &tmB, full_bar(s), k0, n0);
+                if (PAIR) {
+                    const uint32_t fb = lead(full_bar(s));
+                    if (args.gather)
+                        tma_gather4_pair(sa + lane * 512u, &tmA, fb, k0, rows[0], rows[1], rows[2],
+                                         rows[3]);
+                    else if (lane == 0)
+                        tma_load_2d_pair(sa, &tmA, fb, k0, m0);
+                    if (lane == 0)
+                        tma_load_2d_pair(sb, &tmB, fb, k0, nb0);
+                } else {
+                    if (args.gather)
+                        tma_gather4(sa + lane * 512u, &tmA, full_bar(s), k0, rows[0], rows[1],
+                                    rows[2], rows[3]);
+                    else if (lane == 0)
+                        tma_load_2d(sa, &tmA, full_bar(s), k0, m0);
+                    if (lane == 0)
+                        tma_load_2d(sb, &tmB, full_bar(s), k0, nb0);
+                }
                 pending = min(pending + 1, STAGES);
                 if (++s == STAGES) {
                     s = 0;
@@ -175,10 +221,12 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
         }
-        if (!alive) {
+        if (!alive && leader) {
             // Drain: every issued stage's bytes land before shared memory is
-            // released.  The waits are bounded again; a stage whose expected
-            // count can never be met (the test hook) simply times out here.
+            // released (for a pair the leader's barriers count both CTAs' bytes,
+            // and the peer leaves only after the final cluster barrier).  The
+            // waits are bounded again; a stage whose expected count can never
+            // be met (the test hook) simply times out here.
             int ds = s;
             uint32_t dph = ph;
             for (int i = 0; i < pending; ++i) {
@@ -191,14 +239,14 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32acc(args.ab_bf16 != 0, Cfg::BM, BN);
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_f16_f32acc(args.ab_bf16 != 0, Cfg::TILE_M, BN);
             int s = 0;
             uint32_t ph = 0;
             int ab = 0;
             uint32_t aph = 0;
             bool alive = true;
-            for (int32_t t = blockIdx.x; t < args.num_tiles && alive; t += gridDim.x) {
+            for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
                 if (!wait_bounded(acce_bar(ab), aph ^ 1u, abort_flag, args.status,
                                   args.timeout_ns, kWhereMmaAccEmpty))
                     break;
@@ -214,10 +262,18 @@ __global__ void __launch_bounds__(192, 1)
                     const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES);
                     const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES);
 #pragma unroll
-                    for (int k = 0; k < Cfg::BK / 16; ++k)  // +32 B per K=16 step
-                        tc_mma_f16(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
-                                   (kb | k) != 0 ? 1u : 0u);
-                    tc_commit(empty_bar(s));
+                    for (int k = 0; k < Cfg::BK / 16; ++k) {  // +32 B per K=16 step
+                        if (PAIR)
+                            tc_mma_f16_pair(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
+                                            (kb | k) != 0 ? 1u : 0u);
+                        else
+                            tc_mma_f16(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
+                                       (kb | k) != 0 ? 1u : 0u);
+                    }
+                    if (PAIR)
+                        tc_commit_pair_multicast(empty_bar(s), 3);  // frees the stage in both CTAs
+                    else
+                        tc_commit(empty_bar(s));
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
@@ -225,7 +281,9 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 if (!alive)
                     break;
-                if (args.num_k_blocks == 0)
+                if (PAIR)
+                    tc_commit_pair_multicast(accf_bar(ab), 3);  // K > 0 always for pairs
+                else if (args.num_k_blocks == 0)
                     mbar_arrive(accf_bar(ab));  // nothing to multiply: acc reads as zero
                 else
                     tc_commit(accf_bar(ab));
@@ -248,10 +306,11 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t aph = 0;
         uint32_t cph[2] = {0u, 0u};
         bool alive = true;
-        for (int32_t t = blockIdx.x; t < args.num_tiles && alive; t += gridDim.x) {
+        for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
-            const int32_t m0 = mb * Cfg::BM, n0 = nb * BN;
+            const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * Cfg::BM;
+            const int32_t n0 = nb * BN;
             const int32_t row0 = m0 + 32 * (int32_t)q;
             const bool rows_ok = row0 < args.M;
             const int32_t nchunks = min(BN / 32, (args.N - n0 + 31) / 32);
@@ -291,8 +350,12 @@ __global__ void __launch_bounds__(192, 1)
                     // the accumulator is fully read: hand it back to the MMA warp
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(acce_bar(ab));
+                    if (lane == 0) {
+                        if (PAIR && !leader)
+                            mbar_arrive_cluster(lead(acce_bar(ab)));
+                        else
+                            mbar_arrive(acce_bar(ab));
+                    }
                 }
                 if (!rows_ok)
                     continue;
@@ -399,10 +462,26 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if (PAIR) {
+        if (threadIdx.x == 0 && *abort_flag)
+            raise_abort();  // the peer stops waiting instead of running out of time itself
+        if (*abort_flag && !leader) {
+            // copies this CTA issued report to the leader's barriers, which the
+            // leader drains; give any still in flight time to land as well
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < 100000ull) {
+            }
+        }
+        cluster_sync_all();  // the leader's MMAs read this CTA's shared memory until here
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
 }
 

@@ -16,8 +16,11 @@ struct GemmMaps {
     CUtensorMap d;  // D boxes
 };
 
-int tile_stages(int bn);
-cudaError_t launch_tile(int bn, const GemmMaps &maps, const GemmArgs &args, int grid,
+// Tile kernel: 128 x bn tiles on single CTAs, or (pair) 256 x bn tiles on CTA
+// pairs with tcgen05 cta_group::2.  grid counts CTAs (twice the pairs).
+int tile_stages(int bn, bool pair);
+int tile_max_pairs(int bn);  // co-resident CTA pairs on the current device (0: unknown)
+cudaError_t launch_tile(int bn, bool pair, const GemmMaps &maps, const GemmArgs &args, int grid,
                         cudaStream_t stream);
 
 int skinny_stages(int mp);

@@ -1,17 +1,22 @@
-// launch_tile.cu -- instantiations and launcher of the 128 x BN tile kernel.
+// launch_tile.cu -- instantiations and launcher of the tile kernel: 128 x BN
+// tiles on single CTAs, or 256 x BN tiles on CTA pairs (cluster of two).
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "kernel_tile.cuh"
 #include "launch.h"
 
 namespace tcg {
 
-template <int BN, int STAGES>
-static cudaError_t launch_tile_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
-                                    cudaStream_t stream)
+namespace {
+
+template <int BN, int STAGES, bool PAIR>
+cudaError_t launch_tile_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
+                             cudaStream_t stream)
 {
-    using Cfg = TileCfg<BN, STAGES>;
-    auto kfn = tile_gemm_kernel<BN, STAGES>;
+    using Cfg = TileCfg<BN, STAGES, PAIR>;
+    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_ALLOC));
     if (e != cudaSuccess)
@@ -21,11 +26,60 @@ static cudaError_t launch_tile_impl(const GemmMaps &maps, const GemmArgs &args, 
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, maps.d, args);
 }
 
-int tile_stages(int bn)
+// How many CTA pairs of the pair kernel can be resident at once on the current
+// device (SMs that cannot be paired within their GPC stay idle).
+template <int BN, int STAGES>
+int max_pairs_impl()
 {
+    using Cfg = TileCfg<BN, STAGES, true>;
+    static std::mutex mu;
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] > 0)
+        return cached[dev];
+    auto kfn = tile_gemm_kernel<BN, STAGES, true>;
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Cfg::SMEM_ALLOC)) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kfn, &cfg) != cudaSuccess)
+        return 0;
+    cached[dev] = clusters;
+    return clusters;
+}
+
+}  // namespace
+
+int tile_stages(int bn, bool pair)
+{
+    if (pair)
+        return bn == 256 ? 6 : 0;
     switch (bn) {
     case 256: return 4;
     case 128: return 6;
@@ -34,13 +88,21 @@ int tile_stages(int bn)
     }
 }
 
-cudaError_t launch_tile(int bn, const GemmMaps &maps, const GemmArgs &args, int grid,
+int tile_max_pairs(int bn)
+{
+    return bn == 256 ? max_pairs_impl<256, 6>() : 0;
+}
+
+cudaError_t launch_tile(int bn, bool pair, const GemmMaps &maps, const GemmArgs &args, int grid,
                         cudaStream_t stream)
 {
+    if (pair)
+        return bn == 256 ? launch_tile_impl<256, 6, true>(maps, args, grid, stream)
+                         : cudaErrorInvalidValue;
     switch (bn) {
-    case 256: return launch_tile_impl<256, 4>(maps, args, grid, stream);
-    case 128: return launch_tile_impl<128, 6>(maps, args, grid, stream);
-    case 64: return launch_tile_impl<64, 8>(maps, args, grid, stream);
+    case 256: return launch_tile_impl<256, 4, false>(maps, args, grid, stream);
+    case 128: return launch_tile_impl<128, 6, false>(maps, args, grid, stream);
+    case 64: return launch_tile_impl<64, 8, false>(maps, args, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

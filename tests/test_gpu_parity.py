@@ -19,9 +19,55 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 def _clean_status():
     binding.gemm_debug_inject(0)
     binding.gemm_set_wait_timeout(0)
+    binding.gemm_debug_force_tile(0, 0)
     assert device_status() == binding.GEMM_OK
     yield
+    binding.gemm_debug_force_tile(0, 0)
     assert device_status() == binding.GEMM_OK
+
+
+TILE_FORMS = [(1, 64), (1, 128), (1, 256), (3, 256)]
+FORM_IDS = ["single64", "single128", "single256", "pair256"]
+
+
+@pytest.mark.parametrize("form", TILE_FORMS, ids=FORM_IDS)
+@pytest.mark.parametrize("M,N,K", [(129, 257, 72), (300, 520, 264), (513, 700, 1000),
+                                   (256, 256, 64), (1000, 96, 136)])
+def test_every_tile_form_bit_exact(form, M, N, K):
+    """Each tile kernel form, forced, on ragged multi-tile shapes with exact inputs."""
+    binding.gemm_debug_force_tile(*form)
+    for dtype, out, with_c, alpha, beta in [("bf16", OUT_F32, True, 0.5, 2.0),
+                                            ("f16", OUT_BF16, False, 1.0, 0.0),
+                                            ("bf16", OUT_F16, True, -1.0, 1.0)]:
+        p = workloads.random_problem(M + 3 * N + K, M, N, K, dtype=dtype, values="quarter",
+                                     with_c=with_c, alpha=alpha, beta=beta, out=out)
+        ref, _, _ = oracle_full(p)
+        assert_bits(run(p), ref, out, f"form {form} {M}x{N}x{K} {dtype} out={out}")
+
+
+@pytest.mark.parametrize("form", TILE_FORMS, ids=FORM_IDS)
+def test_every_tile_form_gather(form):
+    binding.gemm_debug_force_tile(*form)
+    p = workloads.random_problem(42, 600, 400, 264, dtype="bf16", values="quarter",
+                                 with_c=True, alpha=0.5, gather_rows=333)
+    ref, _, _ = oracle_full(p)
+    assert_bits(run(p), ref, OUT_F32, f"gather form {form}")
+
+
+@pytest.mark.parametrize("form", TILE_FORMS, ids=FORM_IDS)
+def test_every_tile_form_timeout(form):
+    binding.gemm_debug_force_tile(*form)
+    p = workloads.random_problem(43, 512, 512, 256, dtype="bf16", values="quarter")
+    binding.gemm_set_wait_timeout(50_000_000)
+    binding.gemm_debug_inject(1)
+    try:
+        run(p)
+        assert device_status() == binding.GEMM_ERR_TIMEOUT
+    finally:
+        binding.gemm_debug_inject(0)
+        binding.gemm_set_wait_timeout(0)
+    ref, _, _ = oracle_full(p)
+    assert_bits(run(p), ref, OUT_F32, f"after timeout, form {form}")
 
 
 def test_worked_example_bit_exact():
