@@ -272,6 +272,7 @@ def time_variant(name, dev, reps, flush):
         raise RuntimeError(f"{name}: device status {binding.gemm_status_string(status)}")
     ms = statistics.median(times)
     plan = binding.gemm_query_plan(p.M, p.N, p.K, gather=p.idx is not None,
+                                   has_c=p.C is not None and p.beta != 0,
                                    sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
     del tensors
     return p, ms, plan
@@ -360,7 +361,8 @@ def run_ours(args):
             variants[name] = {
                 "ms": round(ms, 5), "TFLOP/s": round(tflops, 2), "GB/s": round(gbs, 1),
                 "algorithmic_bytes": algorithmic_bytes(vp),
-                "kernel": {1: "tile", 2: "skinny"}.get(plan.kernel, "?"),
+                "kernel": {1: "tile (single CTA)", 2: "skinny (swap-AB, stream-K)",
+                           3: "tile (CTA pair)", 4: "tile (CTA pair, two N halves)"}[plan.kernel],
                 "tile": f"{plan.bm}x{plan.bn}", "grid": plan.grid, "splits": plan.splits,
                 "roofline": ({"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                               "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}

@@ -186,10 +186,13 @@ const char *gemm_status_string(int status);
 /*
  * The kernel choice the library makes for a problem, without launching
  * anything and without touching the GPU (for diagnostics and tests).
+ * gather: the row-gathered form; has_c: C is given and beta != 0.
  *
  *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles, one
  *           CTA each), 2 = skinny swap-AB kernel (M <= 64), 3 = tile kernel
- *           on CTA pairs (256-row tiles, tcgen05 cta_group::2)
+ *           on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2), 4 = tile
+ *           kernel on CTA pairs with 256 x 512 tiles (two MMA halves, one
+ *           accumulator)
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)
@@ -206,7 +209,7 @@ typedef struct {
     int32_t grid;
 } gemm_plan;
 
-gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather,
+gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather, int has_c,
                             int sm_count, gemm_plan *plan);
 
 /*
@@ -228,9 +231,10 @@ gemm_status gemm_debug_inject(int mode);
 /*
  * Test hook.  Force the form of the tile kernel for later calls: kernel 1 =
  * single CTAs with tile width bn in {64, 128, 256}, kernel 3 = CTA pairs with
- * bn = 256, kernel 0 = automatic choice (the default).  Problems the forced
- * form cannot run (the M <= 64 skinny path; K == 0 for pairs) keep the
- * automatic choice.  Returns GEMM_ERR_INVALID_ARG for other values.
+ * bn = 256, kernel 4 = CTA pairs with bn = 512, kernel 0 = automatic choice
+ * (the default).  Problems the forced form cannot run (the M <= 64 skinny
+ * path; K == 0 for pairs) keep the automatic choice.  Returns
+ * GEMM_ERR_INVALID_ARG for other values.
  */
 gemm_status gemm_debug_force_tile(int kernel, int bn);
 

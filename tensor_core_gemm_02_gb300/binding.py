@@ -60,7 +60,7 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_check_device_status.argtypes = [vp]
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
-    lib.gemm_query_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(Plan)]
+    lib.gemm_query_plan.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Plan)]
     lib.gemm_set_wait_timeout.argtypes = [ctypes.c_uint64]
     lib.gemm_debug_inject.argtypes = [i32]
     lib.gemm_debug_force_tile.argtypes = [i32, i32]
@@ -189,10 +189,10 @@ def gemm_check_device_status(stream=None) -> int:
     return int(load_library().gemm_check_device_status(_stream_ptr(stream)))
 
 
-def gemm_query_plan(M, N, K, gather=False, sm_count=148) -> Plan:
+def gemm_query_plan(M, N, K, gather=False, has_c=False, sm_count=148) -> Plan:
     p = Plan()
-    _check(load_library().gemm_query_plan(M, N, K, int(bool(gather)), sm_count,
-                                          ctypes.byref(p)), "gemm_query_plan")
+    _check(load_library().gemm_query_plan(M, N, K, int(bool(gather)), int(bool(has_c)),
+                                          sm_count, ctypes.byref(p)), "gemm_query_plan")
     return p
 
 

@@ -19,6 +19,11 @@
 
 #include "host_internal.h"
 
+// Height, in block rows, of the groups the tile order walks through (L2 reuse).
+#ifndef TCG_GROUP_M
+#define TCG_GROUP_M 16
+#endif
+
 // First device-side error code [0] and where it arose [1], one per device.
 static __device__ uint32_t g_device_status[4];
 
@@ -299,41 +304,92 @@ gemm_status validate(const Problem &p, bool *empty)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Tile shape for the tile kernel: single CTAs with 128 x {256, 128, 64} tiles,
-// or CTA pairs with 256 x 256 tiles.  Cost = waves of persistent CTA sets,
-// each weighted by the per-SM tile width plus a fixed per-tile cost; pairs
-// get a 10% credit because each SM moves 2/3 of the operand bytes.
+// Tile shape for the tile kernel.  Candidates: single CTAs with 128 x {256,
+// 128, 64} tiles; CTA pairs with 256 x 256 tiles (two accumulators, so the
+// epilogue overlaps the next tile); CTA pairs with 256 x 512 tiles (each row
+// of A feeds twice the work, one accumulator).  Cost = waves of persistent
+// CTA sets x per-SM tile width plus a fixed per-tile cost.  Pairs get a 10%
+// credit (each SM moves 2/3 of the operand bytes); the 256 x 512 form gets a
+// further 5% when its epilogue is short relative to the tile (no C, K >= 2048)
+// and is always preferred for gathered rows, whose cost is the number of TMA
+// gather4 issues per flop.
 struct TileChoice {
-    bool pair;
+    int kernel;  // 1 single, 3 pair 256, 4 pair 512
     int bn;
 };
 
-TileChoice choose_tile(int64_t M, int64_t N, int64_t K, int sm_count)
+TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count)
 {
     static const int widths[3] = {256, 128, 64};
-    TileChoice best{false, 256};
+    TileChoice best{1, 256};
     double best_cost = -1.0;
     for (int w : widths) {
         const int64_t tiles = ceil_div(M, 128) * ceil_div(N, w);
         const double cost = static_cast<double>(ceil_div(tiles, sm_count) * (w + 32));
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
-            best = TileChoice{false, w};
+            best = TileChoice{1, w};
         }
     }
     const int pairs = sm_count / 2;
-    if (K > 0 && pairs > 0) {
-        const int64_t tiles = ceil_div(M, 256) * ceil_div(N, 256);
-        const double cost = 0.9 * static_cast<double>(ceil_div(tiles, pairs) * (256 + 32));
-        if (cost <= best_cost)
-            best = TileChoice{true, 256};
+    if (K == 0 || pairs == 0)
+        return best;
+    const int64_t tiles256 = ceil_div(M, 256) * ceil_div(N, 256);
+    const double cost256 = 0.9 * static_cast<double>(ceil_div(tiles256, pairs) * (256 + 32));
+    if (cost256 <= best_cost) {
+        best_cost = cost256;
+        best = TileChoice{3, 256};
+    }
+    if (N > 256) {
+        const int64_t tiles512 = ceil_div(M, 256) * ceil_div(N, 512);
+        double cost512 = 0.9 * static_cast<double>(ceil_div(tiles512, pairs) * (512 + 64));
+        if (!c_used && K >= 2048)
+            cost512 *= 0.95;
+        if (gather || cost512 < best_cost) {
+            best_cost = cost512;
+            best = TileChoice{4, 512};
+        }
     }
     return best;
 }
 
 int skinny_rows(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
-gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, int sm_count)
+// The tile kernel's form for plan.kernel 1 (single CTAs, 128 x bn tiles),
+// 3 (CTA pairs, 256 x 256) and 4 (CTA pairs, 256 x 512: two MMA halves).
+struct TileForm {
+    bool pair;
+    int mma_bn;
+    int nsub;
+    int tile_m;
+    int tile_n;
+};
+
+TileForm tile_form(const gemm_plan &p)
+{
+    if (p.kernel == 3)
+        return TileForm{true, 256, 1, 256, 256};
+    if (p.kernel == 4)
+        return TileForm{true, 256, 2, 256, 512};
+    return TileForm{false, p.bn, 1, 128, p.bn};
+}
+
+// Fill the tile-kernel fields of a plan for `kernel` (1, 3 or 4) and tile width bn.
+void set_tile_plan(gemm_plan &p, int kernel, int bn, int64_t M, int64_t N, int sm_count)
+{
+    p.kernel = kernel;
+    p.bn = bn;
+    p.splits = 1;
+    const TileForm f = tile_form(p);
+    p.bm = f.tile_m;
+    p.stages = tcg::tile_stages(f.mma_bn, f.pair, f.nsub);
+    p.tiles = ceil_div(M, f.tile_m) * ceil_div(N, f.tile_n);
+    const int64_t sets = f.pair ? sm_count / 2 : sm_count;
+    const int64_t used = p.tiles < sets ? p.tiles : sets;
+    p.grid = static_cast<int32_t>(f.pair ? 2 * used : used);
+}
+
+gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count)
 {
     gemm_plan p;
     std::memset(&p, 0, sizeof(p));
@@ -343,7 +399,7 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, int sm_count)
         // few rows: swap A and B so B streams through the MMA's M side
         const int mp = skinny_rows(M);
         const int64_t tiles = ceil_div(N, 128);
-        const int64_t nkb = ceil_div(K, 64);
+        const int64_t nkb = ceil_div(K, tcg::skinny_kstage());
         const int64_t W = tiles * nkb;
         const int64_t G = W < sm_count ? W : sm_count;
         p.kernel = 2;
@@ -355,22 +411,8 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, int sm_count)
         p.grid = static_cast<int32_t>(G);
         return p;
     }
-    const TileChoice c = choose_tile(M, N, K, sm_count);
-    p.splits = 1;
-    p.bn = c.bn;
-    p.stages = tcg::tile_stages(c.bn, c.pair);
-    if (c.pair) {
-        const int64_t pairs = sm_count / 2;
-        p.kernel = 3;
-        p.bm = 256;
-        p.tiles = ceil_div(M, 256) * ceil_div(N, c.bn);
-        p.grid = static_cast<int32_t>(2 * (p.tiles < pairs ? p.tiles : pairs));
-    } else {
-        p.kernel = 1;
-        p.bm = 128;
-        p.tiles = ceil_div(M, 128) * ceil_div(N, c.bn);
-        p.grid = static_cast<int32_t>(p.tiles < sm_count ? p.tiles : sm_count);
-    }
+    const TileChoice c = choose_tile(M, N, K, gather, c_used, sm_count);
+    set_tile_plan(p, c.kernel, c.bn, M, N, sm_count);
     return p;
 }
 
@@ -414,7 +456,7 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
     fill_common(a, p, dev);
     a.num_m_blocks = 1;
     a.num_n_blocks = static_cast<int32_t>(plan.tiles);
-    a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, 64));
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, tcg::skinny_kstage()));
     a.num_tiles = static_cast<int32_t>(plan.tiles);
     a.group_m = 1;
     a.splits = plan.splits;
@@ -435,25 +477,11 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || (plan.kernel != 1 && plan.kernel != 3))
+    if (fk == 0 || (plan.kernel != 1 && plan.kernel != 3 && plan.kernel != 4))
         return plan;
-    if (fk == 3 && p.K == 0)
-        return plan;
-    plan.bn = fbn;
-    plan.stages = tcg::tile_stages(fbn, fk == 3);
-    plan.splits = 1;
-    if (fk == 3) {
-        const int64_t pairs = sm_count / 2;
-        plan.kernel = 3;
-        plan.bm = 256;
-        plan.tiles = ceil_div(p.M, 256) * ceil_div(p.N, fbn);
-        plan.grid = static_cast<int32_t>(2 * (plan.tiles < pairs ? plan.tiles : pairs));
-    } else {
-        plan.kernel = 1;
-        plan.bm = 128;
-        plan.tiles = ceil_div(p.M, 128) * ceil_div(p.N, fbn);
-        plan.grid = static_cast<int32_t>(plan.tiles < sm_count ? plan.tiles : sm_count);
-    }
+    if (fk != 1 && p.K == 0)
+        return plan;  // pair forms need K > 0
+    set_tile_plan(plan, fk, fbn, p.M, p.N, sm_count);
     return plan;
 }
 
@@ -466,21 +494,22 @@ gemm_status run(const Problem &p)
     DeviceInfo *dev = nullptr;
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
-    const gemm_plan plan =
-        apply_forced_tile(make_plan(p.M, p.N, p.K, p.gather, dev->sm_count), p, dev->sm_count);
     const bool c_used = p.C != nullptr && p.beta != 0.0f;
+    const gemm_plan plan = apply_forced_tile(
+        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count), p, dev->sm_count);
 
     GemmMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (plan.kernel == 2)
         return run_skinny(p, plan, dev);
-    const int bn = plan.bn;
-    const bool pair = plan.kernel == 3;
-    const int bn_local = pair ? bn / 2 : bn;  // rows of B each CTA loads
+    const TileForm form = tile_form(plan);
+    const bool pair = form.pair;
+    const int bn = form.mma_bn;
+    const int bn_local = pair ? bn / 2 : bn;  // rows of B per MMA half each CTA loads
     int grid = plan.grid;
     if (pair) {
         // never more pairs than can be resident together (unpaired SMs stay idle)
-        const int resident = tcg::tile_max_pairs(bn);
+        const int resident = tcg::tile_max_pairs(bn, form.nsub);
         if (resident <= 0)
             return GEMM_ERR_CUDA;
         grid = static_cast<int>(2 * (plan.tiles < resident ? plan.tiles : resident));
@@ -514,11 +543,11 @@ gemm_status run(const Problem &p)
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     fill_common(a, p, dev);
-    a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, pair ? 256 : 128));
-    a.num_n_blocks = static_cast<int32_t>(ceil_div(p.N, bn));
+    a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, form.tile_m));
+    a.num_n_blocks = static_cast<int32_t>(ceil_div(p.N, form.tile_n));
     a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, 64));
     a.num_tiles = static_cast<int32_t>(plan.tiles);
-    a.group_m = a.num_m_blocks < 16 ? a.num_m_blocks : 16;
+    a.group_m = a.num_m_blocks < TCG_GROUP_M ? a.num_m_blocks : TCG_GROUP_M;
     a.splits = 1;
     a.kb_per_split = a.num_k_blocks;
     a.gather = p.gather ? 1 : 0;
@@ -528,7 +557,7 @@ gemm_status run(const Problem &p)
     a.idx = p.idx;
     a.table_rows = static_cast<int32_t>(p.a_rows);
 
-    const cudaError_t e = tcg::launch_tile(bn, pair, maps, a, grid, p.stream);
+    const cudaError_t e = tcg::launch_tile(bn, pair, form.nsub, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -607,12 +636,12 @@ const char *gemm_status_string(int status)
     }
 }
 
-gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather, int sm_count,
-                            gemm_plan *plan)
+gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather, int has_c,
+                            int sm_count, gemm_plan *plan)
 {
     if (!plan || sm_count < 1 || M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    *plan = make_plan(M, N, K, gather != 0, sm_count);
+    *plan = make_plan(M, N, K, gather != 0, has_c != 0, sm_count);
     return GEMM_OK;
 }
 
@@ -625,7 +654,7 @@ gemm_status gemm_set_wait_timeout(uint64_t ns)
 gemm_status gemm_debug_force_tile(int kernel, int bn)
 {
     const bool ok = (kernel == 0) || (kernel == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
-                    (kernel == 3 && bn == 256);
+                    (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512);
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

@@ -52,7 +52,7 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dtype, const void *ptr, uint6
 
 CUtensorMapDataType ab_type(bool bf16);
 int64_t ceil_div(int64_t a, int64_t b);
-gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, int sm_count);
+gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count);
 
 // Kernel arguments common to every kernel (sizes, epilogue, status, timeout).
 void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev);

@@ -14,7 +14,9 @@
 // tile) adds them in a fixed order, applies the epilogue and resets the
 // counter.  No CTA waits for another.
 //
-//   warp 0     producer: TMA boxes of B (128 x 64) and A (MP x 64) per k-block
+//   warp 0     producer: per stage, KBOX TMA boxes of B (128 x 64) and of A
+//              (MP x 64) at consecutive K, so each row of B is read in
+//              KBOX * 128-byte runs
 //   warp 1     MMA issuer: tcgen05.mma M=128 N=MP K=16, two TMEM accumulators
 //   warps 2-5  epilogue: tcgen05.ld, partial or final fma.rn(alpha, acc, beta*C)
 //              with coalesced plain loads/stores (lanes walk along N)
@@ -24,15 +26,20 @@
 
 namespace tcg {
 
-template <int MP_, int STAGES_>
+template <int MP_, int KBOX_>
 struct SkinnyCfg {
-    static constexpr int MP = MP_;  // padded rows of A = MMA N
-    static constexpr int BN = 128;  // rows of B per tile = MMA M
-    static constexpr int BK = 64;
-    static constexpr int STAGES = STAGES_;
-    static constexpr uint32_t B_BYTES = BN * BK * 2;
-    static constexpr uint32_t A_BYTES = MP * BK * 2;
+    static constexpr int MP = MP_;      // padded rows of A = MMA N
+    static constexpr int BN = 128;      // rows of B per tile = MMA M
+    static constexpr int BK = 64;       // K of one 128-byte swizzled box
+    static constexpr int KBOX = KBOX_;  // boxes per stage: each row of B is read KBOX*128 B at a time
+    static constexpr int KSTAGE = BK * KBOX;
+    static constexpr uint32_t B_BOX = BN * BK * 2;
+    static constexpr uint32_t A_BOX = MP * BK * 2;
+    static constexpr uint32_t B_BYTES = KBOX * B_BOX;
+    static constexpr uint32_t A_BYTES = KBOX * A_BOX;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    // as many stages as fit in about 200 KB of shared memory (at most 16)
+    static constexpr int STAGES = (204800 / STAGE_BYTES) < 16 ? (204800 / STAGE_BYTES) : 16;
     static constexpr uint32_t OFF_B = 0;
     static constexpr uint32_t OFF_A = STAGES * B_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_A + STAGES * A_BYTES;
@@ -44,7 +51,8 @@ struct SkinnyCfg {
     static constexpr int THREADS = 192;
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MMA N for M = 128 is a multiple of 16");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation is a power of two");
-    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage images stay 1024-aligned");
+    static_assert(A_BOX % 1024 == 0 && B_BOX % 1024 == 0, "box images stay 1024-aligned");
+    static_assert(STAGES >= 2, "at least double buffering");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
@@ -84,12 +92,13 @@ __device__ __forceinline__ void skinny_store(const GemmArgs &a, int32_t n, const
     }
 }
 
-template <int MP, int STAGES>
+template <int MP, int KBOX, int PF>
 __global__ void __launch_bounds__(192, 1)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args)
 {
-    using Cfg = SkinnyCfg<MP, STAGES>;
+    using Cfg = SkinnyCfg<MP, KBOX>;
+    constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -144,6 +153,18 @@ __global__ void __launch_bounds__(192, 1)
         int pending = 0;
         bool first = true;
         bool alive = true;
+        // PF > 0: keep L2 prefetches of B running PF stages ahead of the loads,
+        // so more of the stream is in flight than the shared ring holds
+        auto prefetch_stage = [&](int64_t q) {
+            if (PF > 0 && q < my_end && lane == 0) {
+                const int32_t tq = static_cast<int32_t>(q / nkb);
+                const int32_t kq = static_cast<int32_t>(q - tq * nkb);
+                for (int j = 0; j < KBOX; ++j)
+                    tma_prefetch_l2_2d(&tmB, kq * Cfg::KSTAGE + j * Cfg::BK, tq * Cfg::BN);
+            }
+        };
+        for (int64_t q = my_start; q < my_start + PF; ++q)
+            prefetch_stage(q);
         for (int64_t pos = my_start; pos < my_end && alive;) {
             const int32_t t = static_cast<int32_t>(pos / nkb);
             const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
@@ -154,11 +175,16 @@ __global__ void __launch_bounds__(192, 1)
                     alive = false;
                     break;
                 }
+                prefetch_stage(static_cast<int64_t>(t) * nkb + kb + PF);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES + (first ? args.extra_tx : 0u));
-                    tma_load_2d(base + Cfg::OFF_B + s * Cfg::B_BYTES, &tmB, full_bar(s), kb * Cfg::BK,
-                                t * Cfg::BN);
-                    tma_load_2d(base + Cfg::OFF_A + s * Cfg::A_BYTES, &tmA, full_bar(s), kb * Cfg::BK, 0);
+                    for (int j = 0; j < KBOX; ++j) {
+                        const int32_t k0 = kb * Cfg::KSTAGE + j * Cfg::BK;
+                        tma_load_2d(base + Cfg::OFF_B + s * Cfg::B_BYTES + j * Cfg::B_BOX, &tmB,
+                                    full_bar(s), k0, t * Cfg::BN);
+                        tma_load_2d(base + Cfg::OFF_A + s * Cfg::A_BYTES + j * Cfg::A_BOX, &tmA,
+                                    full_bar(s), k0, 0);
+                    }
                 }
                 first = false;
                 __syncwarp();
@@ -207,12 +233,17 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES);
-                    const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < Cfg::BK / 16; ++k)
-                        tc_mma_f16(d_tmem, bd + 2u * k, ad + 2u * k, idesc,
-                                   (kb != kb0 || k != 0) ? 1u : 0u);
+                    for (int j = 0; j < KBOX; ++j) {
+                        const uint64_t bd =
+                            sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES + j * Cfg::B_BOX);
+                        const uint64_t ad =
+                            sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES + j * Cfg::A_BOX);
+#pragma unroll
+                        for (int k = 0; k < Cfg::BK / 16; ++k)
+                            tc_mma_f16(d_tmem, bd + 2u * k, ad + 2u * k, idesc,
+                                       (kb != kb0 || j != 0 || k != 0) ? 1u : 0u);
+                    }
                     tc_commit(empty_bar(s));
                     if (++s == STAGES) {
                         s = 0;

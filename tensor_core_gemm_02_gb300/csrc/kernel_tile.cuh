@@ -32,17 +32,24 @@
 
 namespace tcg {
 
-template <int BN_, int STAGES_, bool PAIR_ = false>
+template <int BN_, int STAGES_, bool PAIR_ = false, int NSUB_ = 1>
 struct TileCfg {
     static constexpr bool PAIR = PAIR_;
+    // NSUB = 2: the tile is two BN-wide halves side by side (two MMAs per K
+    // step into one 2*BN-column accumulator), so each row of A feeds twice the
+    // work; without a second accumulator the epilogue no longer overlaps.
+    static constexpr int NSUB = NSUB_;
+    static constexpr int NUM_ACC = NSUB == 1 ? 2 : 1;
     static constexpr int BM = 128;                  // rows of A (and D) per CTA
     static constexpr int TILE_M = PAIR ? 256 : 128;  // rows per output tile
-    static constexpr int BN = BN_;
-    static constexpr int BN_LOCAL = PAIR ? BN / 2 : BN;  // rows of B each CTA loads
+    static constexpr int BN = BN_;       // N of one MMA
+    static constexpr int TILE_N = BN * NSUB;
+    static constexpr int BN_LOCAL = PAIR ? BN / 2 : BN;  // rows of B per half each CTA loads
     static constexpr int BK = 64;  // 64 x 16-bit = one 128-byte swizzle row
     static constexpr int STAGES = STAGES_;
     static constexpr uint32_t A_BYTES = BM * BK * 2;
-    static constexpr uint32_t B_BYTES = BN_LOCAL * BK * 2;
+    static constexpr uint32_t B_SUB_BYTES = BN_LOCAL * BK * 2;
+    static constexpr uint32_t B_BYTES = NSUB * B_SUB_BYTES;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t EPI_BUF = 32 * 128;  // 32 rows x 128 B
     static constexpr uint32_t OFF_A = 0;
@@ -53,10 +60,11 @@ struct TileCfg {
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base
-    static constexpr uint32_t TMEM_COLS = 2 * BN;               // two fp32 accumulators
+    static constexpr uint32_t TMEM_COLS = NUM_ACC * TILE_N;     // fp32 accumulators
     static constexpr int THREADS = 192;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+    static_assert(NSUB == 1 || NSUB == 2, "one or two halves");
     static_assert(!PAIR || (BN % 32 == 0 && BN_LOCAL % 8 == 0), "pair splits B in 8-row groups");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
@@ -72,14 +80,15 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t row, uint32_t chunk, uint32
     return lin ^ (((lin >> 7) & mask) << 4);
 }
 
-template <int BN, int STAGES, bool PAIR>
+template <int BN, int STAGES, bool PAIR, int NSUB>
 __global__ void __launch_bounds__(192, 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC,
                      const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
 {
-    using Cfg = TileCfg<BN, STAGES, PAIR>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB>;
+    constexpr int TILE_N = Cfg::TILE_N;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(192, 1)
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
             const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * Cfg::BM;
-            const int32_t nb0 = nb * BN + static_cast<int32_t>(rank) * Cfg::BN_LOCAL;
+            const int32_t nb0 = nb * TILE_N + static_cast<int32_t>(rank) * Cfg::BN_LOCAL;
             int32_t rows[4] = {0, 0, 0, 0};
             if (args.gather) {
                 // lane l fetches rows 4l .. 4l+3 of the tile, four per gather4
@@ -204,7 +213,8 @@ __global__ void __launch_bounds__(192, 1)
                     else if (lane == 0)
                         tma_load_2d_pair(sa, &tmA, fb, k0, m0);
                     if (lane == 0)
-                        tma_load_2d_pair(sb, &tmB, fb, k0, nb0);
+                        for (int j = 0; j < NSUB; ++j)
+                            tma_load_2d_pair(sb + j * Cfg::B_SUB_BYTES, &tmB, fb, k0, nb0 + j * BN);
                 } else {
                     if (args.gather)
                         tma_gather4(sa + lane * 512u, &tmA, full_bar(s), k0, rows[0], rows[1],
@@ -212,7 +222,8 @@ __global__ void __launch_bounds__(192, 1)
                     else if (lane == 0)
                         tma_load_2d(sa, &tmA, full_bar(s), k0, m0);
                     if (lane == 0)
-                        tma_load_2d(sb, &tmB, full_bar(s), k0, nb0);
+                        for (int j = 0; j < NSUB; ++j)
+                            tma_load_2d(sb + j * Cfg::B_SUB_BYTES, &tmB, full_bar(s), k0, nb0 + j * BN);
                 }
                 pending = min(pending + 1, STAGES);
                 if (++s == STAGES) {
@@ -251,7 +262,7 @@ __global__ void __launch_bounds__(192, 1)
                                   args.timeout_ns, kWhereMmaAccEmpty))
                     break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * TILE_N);
                 for (int32_t kb = 0; kb < args.num_k_blocks; ++kb) {
                     if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
                                       kWhereMmaFull)) {
@@ -260,15 +271,20 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     tc_fence_after_sync();
                     const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES);
-                    const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES);
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 16; ++k) {  // +32 B per K=16 step
-                        if (PAIR)
-                            tc_mma_f16_pair(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
-                                            (kb | k) != 0 ? 1u : 0u);
-                        else
-                            tc_mma_f16(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
-                                       (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int j = 0; j < NSUB; ++j) {
+                            const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES +
+                                                              j * Cfg::B_SUB_BYTES);
+                            const uint32_t dj = d_tmem + static_cast<uint32_t>(j * BN);
+                            if (PAIR)
+                                tc_mma_f16_pair(dj, ad + 2u * k, bd + 2u * k, idesc,
+                                                (kb | k) != 0 ? 1u : 0u);
+                            else
+                                tc_mma_f16(dj, ad + 2u * k, bd + 2u * k, idesc,
+                                           (kb | k) != 0 ? 1u : 0u);
+                        }
                     }
                     if (PAIR)
                         tc_commit_pair_multicast(empty_bar(s), 3);  // frees the stage in both CTAs
@@ -287,7 +303,7 @@ __global__ void __launch_bounds__(192, 1)
                     mbar_arrive(accf_bar(ab));  // nothing to multiply: acc reads as zero
                 else
                     tc_commit(accf_bar(ab));
-                if (++ab == 2) {
+                if (++ab == Cfg::NUM_ACC) {
                     ab = 0;
                     aph ^= 1u;
                 }
@@ -310,10 +326,10 @@ __global__ void __launch_bounds__(192, 1)
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
             const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * Cfg::BM;
-            const int32_t n0 = nb * BN;
+            const int32_t n0 = nb * TILE_N;
             const int32_t row0 = m0 + 32 * (int32_t)q;
             const bool rows_ok = row0 < args.M;
-            const int32_t nchunks = min(BN / 32, (args.N - n0 + 31) / 32);
+            const int32_t nchunks = min(TILE_N / 32, (args.N - n0 + 31) / 32);
             const int32_t my_row = row0 + (int32_t)lane;
 
             if (lane == 0)
@@ -343,7 +359,7 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t buf = buf0 + j * Cfg::EPI_BUF;
                 const int32_t col0 = n0 + 32 * c;
                 uint32_t acc[32];
-                tc_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * BN + 32 * c),
+                tc_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * TILE_N + 32 * c),
                                  acc);
                 tc_wait_ld(acc);
                 if (c == nchunks - 1) {
@@ -446,7 +462,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 __syncwarp();
             }
-            if (++ab == 2) {
+            if (++ab == Cfg::NUM_ACC) {
                 ab = 0;
                 aph ^= 1u;
             }

@@ -16,14 +16,16 @@ struct GemmMaps {
     CUtensorMap d;  // D boxes
 };
 
-// Tile kernel: 128 x bn tiles on single CTAs, or (pair) 256 x bn tiles on CTA
-// pairs with tcgen05 cta_group::2.  grid counts CTAs (twice the pairs).
-int tile_stages(int bn, bool pair);
-int tile_max_pairs(int bn);  // co-resident CTA pairs on the current device (0: unknown)
-cudaError_t launch_tile(int bn, bool pair, const GemmMaps &maps, const GemmArgs &args, int grid,
-                        cudaStream_t stream);
+// Tile kernel: 128 x bn tiles on single CTAs, or (pair) 256 x (nsub * bn)
+// tiles on CTA pairs with tcgen05 cta_group::2.  grid counts CTAs (twice the
+// pairs for pair forms).
+int tile_stages(int bn, bool pair, int nsub);
+int tile_max_pairs(int bn, int nsub);  // co-resident CTA pairs on the current device (0: unknown)
+cudaError_t launch_tile(int bn, bool pair, int nsub, const GemmMaps &maps, const GemmArgs &args,
+                        int grid, cudaStream_t stream);
 
 int skinny_stages(int mp);
+int skinny_kstage();  // K elements per pipeline stage (and per stream-K unit)
 cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
                           cudaStream_t stream);
 

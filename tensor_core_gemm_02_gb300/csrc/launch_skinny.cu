@@ -4,14 +4,25 @@
 #include "kernel_skinny.cuh"
 #include "launch.h"
 
+// K extent of one pipeline stage is 64 * TCG_SKINNY_KBOX elements.
+#ifndef TCG_SKINNY_KBOX
+#define TCG_SKINNY_KBOX 1
+#endif
+// L2 prefetch distance of the B stream, in stages (0: none).
+#ifndef TCG_SKINNY_PF
+#define TCG_SKINNY_PF 0
+#endif
+
 namespace tcg {
 
-template <int MP, int STAGES>
-static cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
-                                      cudaStream_t stream)
+namespace {
+
+template <int MP>
+cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
+                               cudaStream_t stream)
 {
-    using Cfg = SkinnyCfg<MP, STAGES>;
-    auto kfn = skinny_gemm_kernel<MP, STAGES>;
+    using Cfg = SkinnyCfg<MP, TCG_SKINNY_KBOX>;
+    auto kfn = skinny_gemm_kernel<MP, TCG_SKINNY_KBOX, TCG_SKINNY_PF>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_ALLOC));
     if (e != cudaSuccess)
@@ -24,12 +35,16 @@ static cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args
     return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, args);
 }
 
+}  // namespace
+
+int skinny_kstage() { return 64 * TCG_SKINNY_KBOX; }
+
 int skinny_stages(int mp)
 {
     switch (mp) {
-    case 16: return 11;
-    case 32: return 10;
-    case 64: return 8;
+    case 16: return SkinnyCfg<16, TCG_SKINNY_KBOX>::STAGES;
+    case 32: return SkinnyCfg<32, TCG_SKINNY_KBOX>::STAGES;
+    case 64: return SkinnyCfg<64, TCG_SKINNY_KBOX>::STAGES;
     default: return 0;
     }
 }
@@ -38,9 +53,9 @@ cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, in
                           cudaStream_t stream)
 {
     switch (mp) {
-    case 16: return launch_skinny_impl<16, 11>(maps, args, grid, stream);
-    case 32: return launch_skinny_impl<32, 10>(maps, args, grid, stream);
-    case 64: return launch_skinny_impl<64, 8>(maps, args, grid, stream);
+    case 16: return launch_skinny_impl<16>(maps, args, grid, stream);
+    case 32: return launch_skinny_impl<32>(maps, args, grid, stream);
+    case 64: return launch_skinny_impl<64>(maps, args, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -11,12 +11,12 @@ namespace tcg {
 
 namespace {
 
-template <int BN, int STAGES, bool PAIR>
+template <int BN, int STAGES, bool PAIR, int NSUB>
 cudaError_t launch_tile_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                              cudaStream_t stream)
 {
-    using Cfg = TileCfg<BN, STAGES, PAIR>;
-    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB>;
+    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_ALLOC));
     if (e != cudaSuccess)
@@ -40,10 +40,10 @@ cudaError_t launch_tile_impl(const GemmMaps &maps, const GemmArgs &args, int gri
 
 // How many CTA pairs of the pair kernel can be resident at once on the current
 // device (SMs that cannot be paired within their GPC stay idle).
-template <int BN, int STAGES>
+template <int BN, int STAGES, int NSUB>
 int max_pairs_impl()
 {
-    using Cfg = TileCfg<BN, STAGES, true>;
+    using Cfg = TileCfg<BN, STAGES, true, NSUB>;
     static std::mutex mu;
     static int cached[64] = {};
     int dev = 0;
@@ -52,7 +52,7 @@ int max_pairs_impl()
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev] > 0)
         return cached[dev];
-    auto kfn = tile_gemm_kernel<BN, STAGES, true>;
+    auto kfn = tile_gemm_kernel<BN, STAGES, true, NSUB>;
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::SMEM_ALLOC)) != cudaSuccess)
         return 0;
@@ -76,10 +76,12 @@ int max_pairs_impl()
 
 }  // namespace
 
-int tile_stages(int bn, bool pair)
+int tile_stages(int bn, bool pair, int nsub)
 {
     if (pair)
-        return bn == 256 ? 6 : 0;
+        return bn != 256 ? 0 : (nsub == 2 ? 4 : 6);
+    if (nsub != 1)
+        return 0;
     switch (bn) {
     case 256: return 4;
     case 128: return 6;
@@ -88,21 +90,28 @@ int tile_stages(int bn, bool pair)
     }
 }
 
-int tile_max_pairs(int bn)
+int tile_max_pairs(int bn, int nsub)
 {
-    return bn == 256 ? max_pairs_impl<256, 6>() : 0;
+    if (bn != 256)
+        return 0;
+    return nsub == 2 ? max_pairs_impl<256, 4, 2>() : max_pairs_impl<256, 6, 1>();
 }
 
-cudaError_t launch_tile(int bn, bool pair, const GemmMaps &maps, const GemmArgs &args, int grid,
-                        cudaStream_t stream)
+cudaError_t launch_tile(int bn, bool pair, int nsub, const GemmMaps &maps, const GemmArgs &args,
+                        int grid, cudaStream_t stream)
 {
-    if (pair)
-        return bn == 256 ? launch_tile_impl<256, 6, true>(maps, args, grid, stream)
-                         : cudaErrorInvalidValue;
+    if (pair) {
+        if (bn != 256)
+            return cudaErrorInvalidValue;
+        return nsub == 2 ? launch_tile_impl<256, 4, true, 2>(maps, args, grid, stream)
+                         : launch_tile_impl<256, 6, true, 1>(maps, args, grid, stream);
+    }
+    if (nsub != 1)
+        return cudaErrorInvalidValue;
     switch (bn) {
-    case 256: return launch_tile_impl<256, 4, false>(maps, args, grid, stream);
-    case 128: return launch_tile_impl<128, 6, false>(maps, args, grid, stream);
-    case 64: return launch_tile_impl<64, 8, false>(maps, args, grid, stream);
+    case 256: return launch_tile_impl<256, 4, false, 1>(maps, args, grid, stream);
+    case 128: return launch_tile_impl<128, 6, false, 1>(maps, args, grid, stream);
+    case 64: return launch_tile_impl<64, 8, false, 1>(maps, args, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -81,7 +81,8 @@ extern "C" gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int 
     DeviceInfo *dev = nullptr;
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
-    const gemm_plan plan = make_plan(p.M, p.N, p.K, false, dev->sm_count);
+    const gemm_plan plan =
+        make_plan(p.M, p.N, p.K, false, p.C != nullptr && p.beta != 0.0f, dev->sm_count);
     if (plan.kernel != 2)
         return GEMM_ERR_UNSUPPORTED;
     const int mp = plan.bm;
@@ -112,7 +113,7 @@ extern "C" gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int 
     fill_common(a, p, dev);
     a.num_m_blocks = 1;
     a.num_n_blocks = static_cast<int32_t>(plan.tiles);
-    a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, 64));
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, tcg::skinny_kstage()));
     a.num_tiles = static_cast<int32_t>(plan.tiles);
     a.group_m = 1;
     a.splits = plan.splits;

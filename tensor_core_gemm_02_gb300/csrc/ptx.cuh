@@ -157,6 +157,15 @@ __device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Hint: bring a box of a 2-D descriptor into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Shared image -> global box; completion through bulk groups.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t x,
                                              int32_t y)

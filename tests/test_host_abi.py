@@ -97,8 +97,10 @@ def test_gather_argument_checks(lib):
 
 def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
-    assert (p.kernel, p.bm, p.bn, p.grid) == (3, 256, 256, 148)
-    assert p.tiles == 32 * 32
+    assert (p.kernel, p.bm, p.bn, p.grid) == (4, 256, 512, 148)
+    assert p.tiles == 32 * 16
+    p = binding.gemm_query_plan(8192, 28672, 4096, has_c=True, sm_count=148)
+    assert (p.kernel, p.bm, p.bn) == (3, 256, 256) and p.tiles == 32 * 112
     p = binding.gemm_query_plan(8192, 8192, 0, sm_count=148)  # K == 0: single CTAs
     assert p.kernel == 1
     p = binding.gemm_query_plan(1024, 1024, 1024, sm_count=148)
@@ -108,7 +110,7 @@ def test_plan_matches_the_dispatch_rules(lib):
     # stream-K shares of 224 * 64 k-blocks over 148 CTAs: at most 2 per tile
     assert p.splits == 2
     p = binding.gemm_query_plan(16384, 4096, 4096, gather=True, sm_count=148)
-    assert p.kernel == 3 and p.bn == 256
+    assert p.kernel == 4 and p.bn == 512
     p = binding.gemm_query_plan(100, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bn) == (1, 64)
     p = binding.gemm_query_plan(40, 1000, 64, sm_count=148)
