@@ -23,7 +23,9 @@
 // Per SM this moves 2/3 of the operand bytes of the single-CTA form.
 //
 // Two accumulators let the epilogue of tile i overlap the mainloop of tile
-// i+1.  Every wait is bounded (common.cuh); on a timeout all roles leave
+// i+1.  NSUB = 2 (a 2*BN-wide tile made of two MMA halves) has room for one
+// accumulator only; its halves are handed over separately and the MMA order
+// at tile boundaries lets the drain of one half overlap MMAs of the other.  Every wait is bounded (common.cuh); on a timeout all roles leave
 // their loops, the copies in flight are drained, TMEM is freed and the
 // kernel returns with the error recorded.
 #pragma once
@@ -252,57 +254,131 @@ __global__ void __launch_bounds__(192, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && leader) {
             const uint32_t idesc = idesc_f16_f32acc(args.ab_bf16 != 0, Cfg::TILE_M, BN);
+            const int32_t nkb = args.num_k_blocks;
             int s = 0;
             uint32_t ph = 0;
             int ab = 0;
             uint32_t aph = 0;
             bool alive = true;
-            for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
-                if (!wait_bounded(acce_bar(ab), aph ^ 1u, abort_flag, args.status,
-                                  args.timeout_ns, kWhereMmaAccEmpty))
-                    break;
+            // K block kb of MMA half j on stage st into the accumulator at d_tmem
+            auto issue_half = [&](int st, int32_t kb, int j, uint32_t d_tmem) {
+                const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + st * Cfg::A_BYTES);
+                const uint64_t bd =
+                    sdesc_k_sw128(base + Cfg::OFF_B + st * Cfg::B_BYTES + j * Cfg::B_SUB_BYTES);
+                const uint32_t dj = d_tmem + static_cast<uint32_t>(j * BN);
+#pragma unroll
+                for (int k = 0; k < Cfg::BK / 16; ++k) {  // +32 B per K=16 step
+                    if (PAIR)
+                        tc_mma_f16_pair(dj, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    else
+                        tc_mma_f16(dj, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                }
+            };
+            // arrive on `bar` (both CTAs of a pair) once the MMAs issued so far finish
+            auto commit_to = [&](uint32_t bar) {
+                if (PAIR)
+                    tc_commit_pair_multicast(bar, 3);
+                else
+                    tc_commit(bar);
+            };
+            // wait until stage s holds K block data; false if the kernel is aborting
+            auto next_full = [&](int &st) {
+                if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
+                                  kWhereMmaFull))
+                    return false;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * TILE_N);
-                for (int32_t kb = 0; kb < args.num_k_blocks; ++kb) {
-                    if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
-                                      kWhereMmaFull)) {
-                        alive = false;
+                st = s;
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                return true;
+            };
+            auto wait_acc_free = [&](int b) {
+                if (!wait_bounded(acce_bar(b), aph ^ 1u, abort_flag, args.status, args.timeout_ns,
+                                  kWhereMmaAccEmpty))
+                    return false;
+                tc_fence_after_sync();
+                return true;
+            };
+            for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
+                if constexpr (NSUB == 1) {
+                    if (!wait_acc_free(ab))
                         break;
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * TILE_N);
+                    for (int32_t kb = 0; kb < nkb; ++kb) {
+                        int st;
+                        if (!next_full(st)) {
+                            alive = false;
+                            break;
+                        }
+                        issue_half(st, kb, 0, d_tmem);
+                        commit_to(empty_bar(st));  // frees the stage (in both CTAs of a pair)
                     }
-                    tc_fence_after_sync();
-                    const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES);
-#pragma unroll
-                    for (int k = 0; k < Cfg::BK / 16; ++k) {  // +32 B per K=16 step
-#pragma unroll
-                        for (int j = 0; j < NSUB; ++j) {
-                            const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES +
-                                                              j * Cfg::B_SUB_BYTES);
-                            const uint32_t dj = d_tmem + static_cast<uint32_t>(j * BN);
-                            if (PAIR)
-                                tc_mma_f16_pair(dj, ad + 2u * k, bd + 2u * k, idesc,
-                                                (kb | k) != 0 ? 1u : 0u);
-                            else
-                                tc_mma_f16(dj, ad + 2u * k, bd + 2u * k, idesc,
-                                           (kb | k) != 0 ? 1u : 0u);
+                    if (!alive)
+                        break;
+                    if (nkb == 0 && !PAIR)
+                        mbar_arrive(accf_bar(ab));  // nothing to multiply: acc reads as zero
+                    else
+                        commit_to(accf_bar(ab));
+                } else {
+                    // Two halves of one accumulator, handed to the epilogue and back
+                    // separately (barrier index = half).  At the start of a tile the
+                    // half-1 MMAs of the first kFirst K blocks wait until the epilogue
+                    // has drained half 1 of the previous tile; at the end, half 0 of
+                    // the last kLast K blocks goes first so half 0 can be drained
+                    // while half 1 finishes.  Both overlap drain time with MMA work.
+                    constexpr int kFirst = STAGES / 2, kLast = STAGES / 2;
+                    const uint32_t d_tmem = tmem_base;
+                    const int32_t f = nkb < kFirst ? nkb : kFirst;
+                    const int32_t l = (nkb - kLast) > f ? (nkb - kLast) : f;
+                    int held[kFirst > kLast ? kFirst : kLast];
+                    if (!wait_acc_free(0))
+                        break;
+                    for (int32_t kb = 0; kb < f && alive; ++kb) {
+                        alive = next_full(held[kb]);
+                        if (alive)
+                            issue_half(held[kb], kb, 0, d_tmem);
+                    }
+                    if (!alive)
+                        break;
+                    if (f == nkb)
+                        commit_to(accf_bar(0));  // all of half 0 is issued
+                    if (!wait_acc_free(1))
+                        break;
+                    for (int32_t kb = 0; kb < f; ++kb) {
+                        issue_half(held[kb], kb, 1, d_tmem);
+                        commit_to(empty_bar(held[kb]));
+                    }
+                    for (int32_t kb = f; kb < l && alive; ++kb) {
+                        int st;
+                        alive = next_full(st);
+                        if (alive) {
+                            issue_half(st, kb, 0, d_tmem);
+                            issue_half(st, kb, 1, d_tmem);
+                            commit_to(empty_bar(st));
                         }
                     }
-                    if (PAIR)
-                        tc_commit_pair_multicast(empty_bar(s), 3);  // frees the stage in both CTAs
-                    else
-                        tc_commit(empty_bar(s));
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
+                    if (!alive)
+                        break;
+                    if (l < nkb) {
+                        for (int32_t kb = l; kb < nkb && alive; ++kb) {
+                            alive = next_full(held[kb - l]);
+                            if (alive)
+                                issue_half(held[kb - l], kb, 0, d_tmem);
+                        }
+                        if (!alive)
+                            break;
+                        commit_to(accf_bar(0));
+                        for (int32_t kb = l; kb < nkb; ++kb) {
+                            issue_half(held[kb - l], kb, 1, d_tmem);
+                            commit_to(empty_bar(held[kb - l]));
+                        }
+                    } else if (f < nkb) {
+                        commit_to(accf_bar(0));
                     }
+                    commit_to(accf_bar(1));
                 }
-                if (!alive)
-                    break;
-                if (PAIR)
-                    tc_commit_pair_multicast(accf_bar(ab), 3);  // K > 0 always for pairs
-                else if (args.num_k_blocks == 0)
-                    mbar_arrive(accf_bar(ab));  // nothing to multiply: acc reads as zero
-                else
-                    tc_commit(accf_bar(ab));
                 if (++ab == Cfg::NUM_ACC) {
                     ab = 0;
                     aph ^= 1u;
@@ -341,40 +417,50 @@ __global__ void __launch_bounds__(192, 1)
                     tma_load_2d(buf0 + j * Cfg::EPI_BUF, &tmC, c_bar(q, j), n0 + 32 * j, row0);
                 }
             }
-            if (!warp_wait_bounded(accf_bar(ab), aph, abort_flag, args.status, args.timeout_ns,
-                                   kWhereEpiAccFull)) {
-                alive = false;
-                break;
-            }
-            tc_fence_after_sync();
-
             bool zero_row = acc_zero;
             if (args.gather && my_row < args.M) {
                 const int32_t v = args.idx[my_row];
                 zero_row = zero_row || v < 0 || v >= args.table_rows;
             }
 
-            for (int32_t c = 0; c < nchunks; ++c) {
-                const int j = c & 1;
-                const uint32_t buf = buf0 + j * Cfg::EPI_BUF;
-                const int32_t col0 = n0 + 32 * c;
+            // The accumulator comes and goes back in units: the whole tile
+            // (NSUB = 1, barrier index = ab) or each BN-wide half (NSUB = 2,
+            // barrier index = half), so the MMA can refill half 0 while half 1
+            // is still being drained.
+            constexpr int kUnitChunks = (NSUB == 2 ? BN : TILE_N) / 32;
+            for (int32_t c = 0; c < TILE_N / 32; ++c) {
+                const int unit = NSUB == 2 ? c / kUnitChunks : ab;
+                if (c % kUnitChunks == 0) {
+                    if (!warp_wait_bounded(accf_bar(unit), aph, abort_flag, args.status,
+                                           args.timeout_ns, kWhereEpiAccFull)) {
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                }
+                const bool have = c < nchunks;
                 uint32_t acc[32];
-                tc_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * TILE_N + 32 * c),
-                                 acc);
-                tc_wait_ld(acc);
-                if (c == nchunks - 1) {
-                    // the accumulator is fully read: hand it back to the MMA warp
+                if (have) {
+                    tc_ld_32x32b_x32(
+                        tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * TILE_N + 32 * c), acc);
+                    tc_wait_ld(acc);
+                }
+                if (c % kUnitChunks == kUnitChunks - 1) {
+                    // this unit of the accumulator is fully read: hand it back
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
                         if (PAIR && !leader)
-                            mbar_arrive_cluster(lead(acce_bar(ab)));
+                            mbar_arrive_cluster(lead(acce_bar(unit)));
                         else
-                            mbar_arrive(acce_bar(ab));
+                            mbar_arrive(acce_bar(unit));
                     }
                 }
-                if (!rows_ok)
+                if (!have || !rows_ok)
                     continue;
+                const int j = c & 1;
+                const uint32_t buf = buf0 + j * Cfg::EPI_BUF;
+                const int32_t col0 = n0 + 32 * c;
                 const bool d_direct = !args.d_tma || (args.d_tail_direct && col0 + 32 > args.N);
                 float v[32];
                 if (c_tma) {
@@ -462,6 +548,8 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 __syncwarp();
             }
+            if (!alive)
+                break;
             if (++ab == Cfg::NUM_ACC) {
                 ab = 0;
                 aph ^= 1u;
