@@ -26,6 +26,7 @@ Under torchrun every rank runs its own replica; rank 0 prints the JSON line.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -33,10 +34,8 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
-import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -103,11 +102,16 @@ class ClockSampler:
         self.proc = None
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
 
+    def mark(self, which):
+        """Host wall-clock bounds of the timed region (samples outside are dropped)."""
+        setattr(self, which, time.time())
+
     def __enter__(self):
+        self.t_start = self.t_end = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
             t0 = time.time()
             while time.time() - t0 < 3.0 and os.path.getsize(self.out.name) == 0:
@@ -133,8 +137,10 @@ class ClockSampler:
                 if len(parts) < 10:
                     continue
                 try:
-                    rows.append({"sm": float(parts[2]), "max": float(parts[3]),
-                                 "power": float(parts[4]),
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    mask = int(parts[5], 16) if parts[5].startswith("0x") else 0
+                    rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
+                                 "power": float(parts[4]), "mask": mask,
                                  "hw_slowdown": parts[6] == "Active",
                                  "hw_thermal_slowdown": parts[7] == "Active",
                                  "sw_thermal_slowdown": parts[8] == "Active",
@@ -142,18 +148,45 @@ class ClockSampler:
                 except ValueError:
                     continue
         os.unlink(self.out.name)
+        if self.t_start is not None and self.t_end is not None:
+            inside = [r for r in rows if self.t_start <= r["t"] <= self.t_end]
+            if not inside and rows:  # region shorter than the sampling period
+                mid = 0.5 * (self.t_start + self.t_end)
+                inside = sorted(rows, key=lambda r: abs(r["t"] - mid))[:2]
+            rows = inside
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        # samples under load: the upper half by power draw
         pw = sorted(r["power"] for r in rows)
-        cut = pw[len(pw) // 2]
-        load = [r for r in rows if r["power"] >= cut] or rows
+        load = rows
         reasons = sorted({k for r in rows for k in ("hw_slowdown", "hw_thermal_slowdown",
                                                      "sw_thermal_slowdown", "sw_power_cap")
                           if r[k]})
+        # every reason in the active bitmask (nvidia-smi's clocks_event_reasons bits)
+        names = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+                 0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+        active = sorted({n for r in rows for b, n in names.items() if r["mask"] & b})
         return {"sm_mhz": statistics.median(r["sm"] for r in load),
                 "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(pw)}
+                "active_reasons": active, "samples": len(rows), "power_w_max": max(pw),
+                "sm_mhz_samples": [r["sm"] for r in rows][:40]}
+
+
+def kernel_key(plan):
+    """The kernel instance a plan launches, as ncu names it (for profiles/traffic.json)."""
+    if plan.kernel == 2:
+        return f"skinny_gemm_kernel<{plan.bm}, 1, 0>"
+    if plan.kernel == 3:
+        return "tile_gemm_kernel<256, 6, 1, 1>"
+    if plan.kernel == 4:
+        return "tile_gemm_kernel<256, 4, 1, 2>"
+    return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1>"
+
+
+def plan_of(p, dev):
+    return binding.gemm_query_plan(p.M, p.N, p.K, gather=p.idx is not None,
+                                   has_c=p.C is not None and p.beta != 0,
+                                   sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
 
 
 def l2_flush(buf):
@@ -203,11 +236,13 @@ def time_headline(p, dev, steps, warmup, rank, world):
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
         torch.cuda.synchronize()
+        clocks.mark("t_start")
         e0.record(stream)
         for _ in range(steps):
             launch(p, tensors)
         e1.record(stream)
         torch.cuda.synchronize()
+        clocks.mark("t_end")
     if world > 1:
         torch.distributed.barrier()
     ms = e0.elapsed_time(e1)
@@ -271,9 +306,7 @@ def time_variant(name, dev, reps, flush):
     if status != binding.GEMM_OK:
         raise RuntimeError(f"{name}: device status {binding.gemm_status_string(status)}")
     ms = statistics.median(times)
-    plan = binding.gemm_query_plan(p.M, p.N, p.K, gather=p.idx is not None,
-                                   has_c=p.C is not None and p.beta != 0,
-                                   sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
+    plan = plan_of(p, dev)
     del tensors
     return p, ms, plan
 
@@ -345,7 +378,8 @@ def run_ours(args):
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4),
                      "peak_source": f"{peaks['source']} bf16_tflops (burst)",
-                     "traffic": stored_traffic("tile_gemm_kernel<256,4>@bf16_8192"),
+                     "traffic": stored_traffic(f"{kernel_key(plan_of(p, dev))}@{HEADLINE}"),
+                     "kernel": kernel_key(plan_of(p, dev)),
                      "algorithmic_flops_per_launch": flops},
     }
 
@@ -364,12 +398,14 @@ def run_ours(args):
                 "kernel": {1: "tile (single CTA)", 2: "skinny (swap-AB, stream-K)",
                            3: "tile (CTA pair)", 4: "tile (CTA pair, two N halves)"}[plan.kernel],
                 "tile": f"{plan.bm}x{plan.bn}", "grid": plan.grid, "splits": plan.splits,
-                "roofline": ({"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                              "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
-                             if hbm_bound else
-                             {"bound": "tensor", "achieved": round(tflops, 2),
-                              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                              "frac": round(tflops / peaks["bf16_tflops"], 4)}),
+                "roofline": dict(({"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
+                                  if hbm_bound else
+                                  {"bound": "tensor", "achieved": round(tflops, 2),
+                                   "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                   "frac": round(tflops / peaks["bf16_tflops"], 4)}),
+                                 traffic=stored_traffic(f"{kernel_key(plan)}@{name}"),
+                                 kernel=kernel_key(plan)),
                 "timing": "median of per-launch CUDA events, L2 flushed between launches",
             }
         result["variants"] = variants
@@ -447,7 +483,7 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-variants", dest="variants", action="store_false")
