@@ -177,10 +177,12 @@ def kernel_key(plan):
     if plan.kernel == 2:
         return f"skinny_gemm_kernel<{plan.bm}, 1, 0>"
     if plan.kernel == 3:
-        return "tile_gemm_kernel<256, 6, 1, 1>"
+        return "tile_gemm_kernel<256, 6, 1, 1, 1>"
     if plan.kernel == 4:
-        return "tile_gemm_kernel<256, 4, 1, 2>"
-    return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1>"
+        return "tile_gemm_kernel<256, 4, 1, 2, 1>"
+    if plan.kernel == 5:
+        return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1, 4>"
+    return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1, 1>"
 
 
 def plan_of(p, dev):
@@ -396,7 +398,8 @@ def run_ours(args):
                 "ms": round(ms, 5), "TFLOP/s": round(tflops, 2), "GB/s": round(gbs, 1),
                 "algorithmic_bytes": algorithmic_bytes(vp),
                 "kernel": {1: "tile (single CTA)", 2: "skinny (swap-AB, stream-K)",
-                           3: "tile (CTA pair)", 4: "tile (CTA pair, two N halves)"}[plan.kernel],
+                           3: "tile (CTA pair)", 4: "tile (CTA pair, two N halves)",
+                           5: "tile (4-CTA cluster, A multicast)"}[plan.kernel],
                 "tile": f"{plan.bm}x{plan.bn}", "grid": plan.grid, "splits": plan.splits,
                 "roofline": dict(({"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                                    "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}

@@ -307,7 +307,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Tile shape for the tile kernel.  Candidates: single CTAs with 128 x {256,
 // 128, 64} tiles; CTA pairs with 256 x 256 tiles (two accumulators, so the
 // epilogue overlaps the next tile); CTA pairs with 256 x 512 tiles (each row
-// of A feeds twice the work, one accumulator).  Cost = waves of persistent
+// of A feeds twice the work, one accumulator); clusters of four single CTAs
+// sharing A by multicast (gathered rows only).  Cost = waves of persistent
 // CTA sets x per-SM tile width plus a fixed per-tile cost.  Pairs get a 10%
 // credit (each SM moves 2/3 of the operand bytes); the 256 x 512 form gets a
 // further 5% when its epilogue is short relative to the tile (no C, K >= 2048)
@@ -350,17 +351,25 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used
             best = TileChoice{4, 512};
         }
     }
+    // Gathered rows with N >= 1024: clusters of four single CTAs that each
+    // issue a quarter of the gather4s and multicast the rows (measured 15%
+    // faster than the 256 x 512 pair form on 16384 rows, N = K = 4096).
+    if (gather && N >= 1024)
+        best = TileChoice{5, 256};
     return best;
 }
 
 int skinny_rows(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
 // The tile kernel's form for plan.kernel 1 (single CTAs, 128 x bn tiles),
-// 3 (CTA pairs, 256 x 256) and 4 (CTA pairs, 256 x 512: two MMA halves).
+// 3 (CTA pairs, 256 x 256), 4 (CTA pairs, 256 x 512: two MMA halves) and
+// 5 (single CTAs, 128 x bn tiles, in clusters of 4 along N sharing A).
 struct TileForm {
     bool pair;
     int mma_bn;
     int nsub;
+    int mc;       // CTAs sharing one A box by multicast
+    int cluster;  // CTAs per cluster (pairs: 2)
     int tile_m;
     int tile_n;
 };
@@ -368,13 +377,23 @@ struct TileForm {
 TileForm tile_form(const gemm_plan &p)
 {
     if (p.kernel == 3)
-        return TileForm{true, 256, 1, 256, 256};
+        return TileForm{true, 256, 1, 1, 2, 256, 256};
     if (p.kernel == 4)
-        return TileForm{true, 256, 2, 256, 512};
-    return TileForm{false, p.bn, 1, 128, p.bn};
+        return TileForm{true, 256, 2, 1, 2, 256, 512};
+    if (p.kernel == 5)
+        return TileForm{false, p.bn, 1, 4, 4, 128, p.bn};
+    return TileForm{false, p.bn, 1, 1, 1, 128, p.bn};
 }
 
-// Fill the tile-kernel fields of a plan for `kernel` (1, 3 or 4) and tile width bn.
+// Units the persistent loop walks: CTA tiles, or for A multicast the groups of
+// mc neighbouring tiles of a block row that one cluster computes together.
+int64_t loop_tiles(const TileForm &f, int64_t M, int64_t N)
+{
+    const int64_t n_units = f.mc > 1 ? ceil_div(ceil_div(N, f.tile_n), f.mc) : ceil_div(N, f.tile_n);
+    return ceil_div(M, f.tile_m) * n_units;
+}
+
+// Fill the tile-kernel fields of a plan for `kernel` (1, 3, 4 or 5) and tile width bn.
 void set_tile_plan(gemm_plan &p, int kernel, int bn, int64_t M, int64_t N, int sm_count)
 {
     p.kernel = kernel;
@@ -382,11 +401,12 @@ void set_tile_plan(gemm_plan &p, int kernel, int bn, int64_t M, int64_t N, int s
     p.splits = 1;
     const TileForm f = tile_form(p);
     p.bm = f.tile_m;
-    p.stages = tcg::tile_stages(f.mma_bn, f.pair, f.nsub);
+    p.stages = tcg::tile_stages(f.mma_bn, f.pair, f.nsub, f.mc);
     p.tiles = ceil_div(M, f.tile_m) * ceil_div(N, f.tile_n);
-    const int64_t sets = f.pair ? sm_count / 2 : sm_count;
-    const int64_t used = p.tiles < sets ? p.tiles : sets;
-    p.grid = static_cast<int32_t>(f.pair ? 2 * used : used);
+    const int64_t units = loop_tiles(f, M, N);
+    const int64_t sets = sm_count / f.cluster;
+    const int64_t used = units < sets ? units : sets;
+    p.grid = static_cast<int32_t>(f.cluster * used);
 }
 
 gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count)
@@ -477,10 +497,10 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || (plan.kernel != 1 && plan.kernel != 3 && plan.kernel != 4))
+    if (fk == 0 || (plan.kernel != 1 && plan.kernel != 3 && plan.kernel != 4 && plan.kernel != 5))
         return plan;
     if (fk != 1 && p.K == 0)
-        return plan;  // pair forms need K > 0
+        return plan;  // cluster forms need K > 0
     set_tile_plan(plan, fk, fbn, p.M, p.N, sm_count);
     return plan;
 }
@@ -506,20 +526,24 @@ gemm_status run(const Problem &p)
     const bool pair = form.pair;
     const int bn = form.mma_bn;
     const int bn_local = pair ? bn / 2 : bn;  // rows of B per MMA half each CTA loads
+    const int64_t units = loop_tiles(form, p.M, p.N);
     int grid = plan.grid;
-    if (pair) {
-        // never more pairs than can be resident together (unpaired SMs stay idle)
-        const int resident = tcg::tile_max_pairs(bn, form.nsub);
+    if (form.cluster > 1) {
+        // never more clusters than can be resident together (SMs left over
+        // within a GPC stay idle)
+        const int resident = tcg::tile_max_clusters(bn, pair, form.nsub, form.mc);
         if (resident <= 0)
             return GEMM_ERR_CUDA;
-        grid = static_cast<int>(2 * (plan.tiles < resident ? plan.tiles : resident));
+        grid = static_cast<int>(form.cluster * (units < resident ? units : resident));
     }
     if (p.K > 0) {
+        // dense A: each CTA loads its rows (A multicast: its 128 / mc rows for the cluster)
+        const uint32_t a_box_rows = static_cast<uint32_t>(128 / form.mc);
         const bool ok_a =
             p.gather ? encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.a_rows, p.lda * 2, 64, 1,
                                  CU_TENSOR_MAP_SWIZZLE_128B)
-                     : encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.M, p.lda * 2, 64, 128,
-                                 CU_TENSOR_MAP_SWIZZLE_128B);
+                     : encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.M, p.lda * 2, 64,
+                                 a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
         const bool ok_b = encode_2d(&maps.b, ab_type(p.bf16), p.B, p.K, p.N, p.ldb * 2, 64,
                                     static_cast<uint32_t>(bn_local), CU_TENSOR_MAP_SWIZZLE_128B);
         if (!ok_a || !ok_b)
@@ -544,9 +568,9 @@ gemm_status run(const Problem &p)
     std::memset(&a, 0, sizeof(a));
     fill_common(a, p, dev);
     a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, form.tile_m));
-    a.num_n_blocks = static_cast<int32_t>(ceil_div(p.N, form.tile_n));
+    a.num_n_blocks = static_cast<int32_t>(units / a.num_m_blocks);  // (clusters: groups of mc)
     a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, 64));
-    a.num_tiles = static_cast<int32_t>(plan.tiles);
+    a.num_tiles = static_cast<int32_t>(units);
     a.group_m = a.num_m_blocks < TCG_GROUP_M ? a.num_m_blocks : TCG_GROUP_M;
     a.splits = 1;
     a.kb_per_split = a.num_k_blocks;
@@ -557,7 +581,7 @@ gemm_status run(const Problem &p)
     a.idx = p.idx;
     a.table_rows = static_cast<int32_t>(p.a_rows);
 
-    const cudaError_t e = tcg::launch_tile(bn, pair, form.nsub, maps, a, grid, p.stream);
+    const cudaError_t e = tcg::launch_tile(bn, pair, form.nsub, form.mc, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -654,7 +678,8 @@ gemm_status gemm_set_wait_timeout(uint64_t ns)
 gemm_status gemm_debug_force_tile(int kernel, int bn)
 {
     const bool ok = (kernel == 0) || (kernel == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
-                    (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512);
+                    (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512) ||
+                    (kernel == 5 && (bn == 64 || bn == 256));
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

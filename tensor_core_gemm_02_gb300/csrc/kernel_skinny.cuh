@@ -68,19 +68,19 @@ __device__ __forceinline__ void epi_bar_sync()
     asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// Final values of column n: D[m][n] = fma.rn(alpha, v[m], cb[m]) with
+// cb[m] = mul.rn(beta, C[m][n]) loaded beforehand (or D = mul.rn(alpha, v[m])
+// without C).  No loads happen here, so nothing waits behind the stores.
 template <int MP>
-__device__ __forceinline__ void skinny_store(const GemmArgs &a, int32_t n, const float (&v)[MP])
+__device__ __forceinline__ void skinny_store(const GemmArgs &a, int32_t n, const float (&v)[MP],
+                                             const float (&cb)[MP])
 {
     if (n >= a.N)
         return;
 #pragma unroll
     for (int m = 0; m < MP; ++m) {
         if (m < a.M) {
-            float d;
-            if (a.has_c)
-                d = fma_rn(a.alpha, v[m], mul_rn(a.beta, a.C[static_cast<int64_t>(m) * a.ldc + n]));
-            else
-                d = mul_rn(a.alpha, v[m]);
+            const float d = a.has_c ? fma_rn(a.alpha, v[m], cb[m]) : mul_rn(a.alpha, v[m]);
             const int64_t o = static_cast<int64_t>(m) * a.ldd + n;
             if (a.out_kind == kOutF32)
                 static_cast<float *>(a.D)[o] = d;
@@ -92,7 +92,7 @@ __device__ __forceinline__ void skinny_store(const GemmArgs &a, int32_t n, const
     }
 }
 
-template <int MP, int KBOX, int PF>
+template <int MP, int KBOX>
 __global__ void __launch_bounds__(192, 1)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args)
@@ -116,6 +116,27 @@ __global__ void __launch_bounds__(192, 1)
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
     volatile uint32_t *arrival = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 8);
 
+    const int64_t nkb = args.num_k_blocks;
+    const int64_t W = static_cast<int64_t>(args.num_tiles) * nkb;
+    const int64_t G = gridDim.x;
+    const int64_t my_start = W * blockIdx.x / G;
+    const int64_t my_end = W * (blockIdx.x + 1) / G;
+
+    // stage st <- B and A boxes of linear K block q, counted on full_bar(st)
+    auto issue_stage = [&](int st, int64_t q, uint32_t extra) {
+        const int32_t t = static_cast<int32_t>(q / nkb);
+        const int32_t kb = static_cast<int32_t>(q - t * nkb);
+        mbar_arrive_expect_tx(full_bar(st), Cfg::STAGE_BYTES + extra);
+        for (int j = 0; j < KBOX; ++j) {
+            const int32_t k0 = kb * Cfg::KSTAGE + j * Cfg::BK;
+            tma_load_2d(base + Cfg::OFF_B + st * Cfg::B_BYTES + j * Cfg::B_BOX, &tmB, full_bar(st),
+                        k0, t * Cfg::BN);
+            tma_load_2d(base + Cfg::OFF_A + st * Cfg::A_BYTES + j * Cfg::A_BOX, &tmA, full_bar(st),
+                        k0, 0);
+        }
+    };
+
+    int pre = 0;  // stages the producer issued before the set-up barrier
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -130,6 +151,10 @@ __global__ void __launch_bounds__(192, 1)
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        // the ring is empty: start the B stream now instead of after the
+        // tensor-memory allocation and the set-up barrier
+        for (int64_t q = my_start; q < my_end && pre < STAGES; ++q, ++pre)
+            issue_stage(pre, q, pre == 0 ? args.extra_tx : 0u);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -140,61 +165,29 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int64_t nkb = args.num_k_blocks;
-    const int64_t W = static_cast<int64_t>(args.num_tiles) * nkb;
-    const int64_t G = gridDim.x;
-    const int64_t my_start = W * blockIdx.x / G;
-    const int64_t my_end = W * (blockIdx.x + 1) / G;
-
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        pre = __shfl_sync(0xffffffffu, pre, 0);
         int s = 0;
         uint32_t ph = 0;
         int pending = 0;
-        bool first = true;
         bool alive = true;
-        // PF > 0: keep L2 prefetches of B running PF stages ahead of the loads,
-        // so more of the stream is in flight than the shared ring holds
-        auto prefetch_stage = [&](int64_t q) {
-            if (PF > 0 && q < my_end && lane == 0) {
-                const int32_t tq = static_cast<int32_t>(q / nkb);
-                const int32_t kq = static_cast<int32_t>(q - tq * nkb);
-                for (int j = 0; j < KBOX; ++j)
-                    tma_prefetch_l2_2d(&tmB, kq * Cfg::KSTAGE + j * Cfg::BK, tq * Cfg::BN);
-            }
-        };
-        for (int64_t q = my_start; q < my_start + PF; ++q)
-            prefetch_stage(q);
-        for (int64_t pos = my_start; pos < my_end && alive;) {
-            const int32_t t = static_cast<int32_t>(pos / nkb);
-            const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
-            const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + (my_end - pos) ? nkb : kb0 + (my_end - pos));
-            for (int32_t kb = kb0; kb < kb1; ++kb) {
+        for (int64_t q = my_start; q < my_end; ++q) {
+            if (q - my_start >= pre) {
                 if (!warp_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status,
                                        args.timeout_ns, kWhereProducerEmpty)) {
                     alive = false;
                     break;
                 }
-                prefetch_stage(static_cast<int64_t>(t) * nkb + kb + PF);
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES + (first ? args.extra_tx : 0u));
-                    for (int j = 0; j < KBOX; ++j) {
-                        const int32_t k0 = kb * Cfg::KSTAGE + j * Cfg::BK;
-                        tma_load_2d(base + Cfg::OFF_B + s * Cfg::B_BYTES + j * Cfg::B_BOX, &tmB,
-                                    full_bar(s), k0, t * Cfg::BN);
-                        tma_load_2d(base + Cfg::OFF_A + s * Cfg::A_BYTES + j * Cfg::A_BOX, &tmA,
-                                    full_bar(s), k0, 0);
-                    }
-                }
-                first = false;
+                if (lane == 0)
+                    issue_stage(s, q, 0u);
                 __syncwarp();
-                pending = min(pending + 1, STAGES);
-                if (++s == STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
             }
-            pos += kb1 - kb0;
+            pending = min(pending + 1, STAGES);
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
         if (!alive && lane == 0) {
             int ds = s;
@@ -265,6 +258,7 @@ __global__ void __launch_bounds__(192, 1)
         // ------------------------------------------------------------ epilogue
         const uint32_t q = warp & 3u;
         const bool leader = warp == 2 && lane == 0;
+        const int32_t n_local = 32 * static_cast<int32_t>(q) + static_cast<int32_t>(lane);
         int ab = 0;
         uint32_t aph = 0;
         for (int64_t pos = my_start; pos < my_end;) {
@@ -272,6 +266,14 @@ __global__ void __launch_bounds__(192, 1)
             const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
             const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + (my_end - pos) ? nkb : kb0 + (my_end - pos));
             pos += kb1 - kb0;
+            const int32_t n = t * Cfg::BN + n_local;
+            // beta * C of this column, fetched while the MMAs still run
+            float cb[MP];
+#pragma unroll
+            for (int m = 0; m < MP; ++m)
+                cb[m] = (args.has_c && m < args.M && n < args.N)
+                            ? mul_rn(args.beta, args.C[static_cast<int64_t>(m) * args.ldc + n])
+                            : 0.f;
             const bool ok = warp_wait_bounded(accf_bar(ab), aph, abort_flag, args.status,
                                               args.timeout_ns, kWhereEpiAccFull);
             // all four warps agree before the named barriers below
@@ -298,42 +300,58 @@ __global__ void __launch_bounds__(192, 1)
                 aph ^= 1u;
             }
 
-            const int32_t n_local = 32 * static_cast<int32_t>(q) + static_cast<int32_t>(lane);
-            const int32_t n = t * Cfg::BN + n_local;
             const int32_t c_lo = skinny_owner(static_cast<int64_t>(t) * nkb, W, G);
             const int32_t c_hi = skinny_owner(static_cast<int64_t>(t + 1) * nkb - 1, W, G);
             const int32_t parts = c_hi - c_lo + 1;
             if (parts == 1) {
-                skinny_store<MP>(args, n, v);
+                skinny_store<MP>(args, n, v, cb);
                 continue;
             }
             // partial sum of this CTA -> workspace slot (t, blockIdx.x - c_lo)
+            const int32_t my_slot = static_cast<int32_t>(blockIdx.x) - c_lo;
             float *slot0 = args.workspace + static_cast<int64_t>(t) * args.splits * (Cfg::BN * MP);
-            float *mine = slot0 + static_cast<int64_t>(blockIdx.x - c_lo) * (Cfg::BN * MP);
+            float *mine = slot0 + static_cast<int64_t>(my_slot) * (Cfg::BN * MP);
 #pragma unroll
             for (int m = 0; m < MP; ++m)
                 __stcg(mine + m * Cfg::BN + n_local, v[m]);
-            __threadfence();
+            // The CTA barrier orders every thread's partial before the leader's
+            // device-scope fence and counter increment; for the last CTA to
+            // arrive, the leader's second fence orders the other CTAs' parts
+            // before the reads below (the barrier after it passes that on).
             epi_bar_sync();
-            if (leader)
-                *arrival = atomicAdd(args.counters + t, 1u);
+            if (leader) {
+                __threadfence();
+                const uint32_t before = atomicAdd(args.counters + t, 1u);
+                if (before == static_cast<uint32_t>(parts - 1))
+                    __threadfence();
+                *arrival = before;
+            }
             epi_bar_sync();
-            const uint32_t before = *arrival;
-            if (before != static_cast<uint32_t>(parts - 1))
+            if (*arrival != static_cast<uint32_t>(parts - 1))
                 continue;  // another CTA still has to add its part
-            // last to arrive: add the parts in slot order, then finish the tile
-            __threadfence();
+            // last to arrive: add the parts in slot order (this CTA's own part
+            // from registers: the same bits it wrote), then finish the tile
             float sum[MP];
 #pragma unroll
             for (int m = 0; m < MP; ++m)
                 sum[m] = 0.f;
             for (int p = 0; p < parts; ++p) {
-                const float *src = slot0 + static_cast<int64_t>(p) * (Cfg::BN * MP);
+                if (p == my_slot) {
 #pragma unroll
-                for (int m = 0; m < MP; ++m)
-                    sum[m] += __ldcg(src + m * Cfg::BN + n_local);
+                    for (int m = 0; m < MP; ++m)
+                        sum[m] += v[m];
+                } else {
+                    const float *src = slot0 + static_cast<int64_t>(p) * (Cfg::BN * MP);
+                    float part[MP];
+#pragma unroll
+                    for (int m = 0; m < MP; ++m)
+                        part[m] = __ldcg(src + m * Cfg::BN + n_local);
+#pragma unroll
+                    for (int m = 0; m < MP; ++m)
+                        sum[m] += part[m];
+                }
             }
-            skinny_store<MP>(args, n, sum);
+            skinny_store<MP>(args, n, sum, cb);
             if (leader)
                 args.counters[t] = 0u;  // ready for the next call
         }

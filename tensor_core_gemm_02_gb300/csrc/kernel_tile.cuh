@@ -34,9 +34,15 @@
 
 namespace tcg {
 
-template <int BN_, int STAGES_, bool PAIR_ = false, int NSUB_ = 1>
+template <int BN_, int STAGES_, bool PAIR_ = false, int NSUB_ = 1, int MC_ = 1>
 struct TileCfg {
     static constexpr bool PAIR = PAIR_;
+    // MC > 1 (single CTAs only): a cluster of MC CTAs works on MC neighbouring
+    // tiles of one block row; each loads 1/MC of the shared A box and
+    // multicasts it to all, so per CTA the A traffic (or the number of gather4
+    // issues) drops by MC.
+    static constexpr int MC = MC_;
+    static constexpr int CLUSTER = PAIR ? 2 : MC;
     // NSUB = 2: the tile is two BN-wide halves side by side (two MMAs per K
     // step into one 2*BN-column accumulator), so each row of A feeds twice the
     // work; without a second accumulator the epilogue no longer overlaps.
@@ -50,6 +56,8 @@ struct TileCfg {
     static constexpr int BK = 64;  // 64 x 16-bit = one 128-byte swizzle row
     static constexpr int STAGES = STAGES_;
     static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr int A_SLICE_ROWS = BM / MC;  // rows of A this CTA loads for the cluster
+    static constexpr uint32_t A_SLICE_BYTES = A_BYTES / MC;
     static constexpr uint32_t B_SUB_BYTES = BN_LOCAL * BK * 2;
     static constexpr uint32_t B_BYTES = NSUB * B_SUB_BYTES;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -67,6 +75,7 @@ struct TileCfg {
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(NSUB == 1 || NSUB == 2, "one or two halves");
+    static_assert(MC == 1 || (!PAIR && (MC == 2 || MC == 4)), "A multicast over 2 or 4 single CTAs");
     static_assert(!PAIR || (BN % 32 == 0 && BN_LOCAL % 8 == 0), "pair splits B in 8-row groups");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
@@ -82,14 +91,16 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t row, uint32_t chunk, uint32
     return lin ^ (((lin >> 7) & mask) << 4);
 }
 
-template <int BN, int STAGES, bool PAIR, int NSUB>
+template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
 __global__ void __launch_bounds__(192, 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC,
                      const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
 {
-    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
+    constexpr int CL = Cfg::CLUSTER;
+    constexpr uint16_t kAllCtas = static_cast<uint16_t>((1u << CL) - 1u);
     constexpr int TILE_N = Cfg::TILE_N;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -108,11 +119,11 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
 
-    // pair bookkeeping (rank 0 leads; single-CTA form: rank 0, cluster of one)
-    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-    const bool leader = rank == 0u;
-    const int32_t cta_set = PAIR ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
-    const int32_t cta_sets = PAIR ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
+    // cluster bookkeeping: a pair (rank 0 leads), MC CTAs sharing A, or one CTA
+    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+    const bool leader = !PAIR || rank == 0u;
+    const int32_t cta_set = static_cast<int32_t>(blockIdx.x) / CL;
+    const int32_t cta_sets = static_cast<int32_t>(gridDim.x) / CL;
     // the leader's copy of a barrier, as a shared::cluster address
     auto lead = [&](uint32_t bar) { return PAIR ? mapa_shared(bar, 0u) : bar; };
     // raise the abort flag here and (pair) in the peer CTA
@@ -125,7 +136,7 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), MC);  // MC > 1: every CTA's MMA frees the shared A slices
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
@@ -156,8 +167,8 @@ __global__ void __launch_bounds__(192, 1)
         }
     }
     tc_fence_before_sync();
-    if (PAIR)
-        cluster_sync_all();  // the peer's barriers exist before anything targets them
+    if (CL > 1)
+        cluster_sync_all();  // the peers' barriers exist before anything targets them
     else
         __syncthreads();
     tc_fence_after_sync();
@@ -173,13 +184,19 @@ __global__ void __launch_bounds__(192, 1)
         for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
-            const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * Cfg::BM;
-            const int32_t nb0 = nb * TILE_N + static_cast<int32_t>(rank) * Cfg::BN_LOCAL;
+            if (MC > 1)
+                nb = nb * MC + static_cast<int32_t>(rank);  // this CTA's tile of the cluster's row
+            const int32_t m0 = mb * Cfg::TILE_M + (PAIR ? static_cast<int32_t>(rank) * Cfg::BM : 0);
+            const int32_t nb0 = nb * TILE_N + (PAIR ? static_cast<int32_t>(rank) * Cfg::BN_LOCAL : 0);
+            // rows of A this CTA fetches: all 128, or (MC > 1) its slice for the cluster
+            const int32_t a_row0 = m0 + (MC > 1 ? static_cast<int32_t>(rank) * Cfg::A_SLICE_ROWS : 0);
+            const uint32_t a_off = MC > 1 ? rank * Cfg::A_SLICE_BYTES : 0u;
+            const bool gather_lane = static_cast<int>(lane) < Cfg::A_SLICE_ROWS / 4;
             int32_t rows[4] = {0, 0, 0, 0};
-            if (args.gather) {
-                // lane l fetches rows 4l .. 4l+3 of the tile, four per gather4
+            if (args.gather && gather_lane) {
+                // lane l fetches rows 4l .. 4l+3 of the slice, four per gather4
                 for (int r = 0; r < 4; ++r) {
-                    const int32_t m = m0 + 4 * (int32_t)lane + r;
+                    const int32_t m = a_row0 + 4 * (int32_t)lane + r;
                     int32_t v = 0;
                     if (m < args.M) {
                         v = args.idx[m];
@@ -217,6 +234,16 @@ __global__ void __launch_bounds__(192, 1)
                     if (lane == 0)
                         for (int j = 0; j < NSUB; ++j)
                             tma_load_2d_pair(sb + j * Cfg::B_SUB_BYTES, &tmB, fb, k0, nb0 + j * BN);
+                } else if (MC > 1) {
+                    if (args.gather) {
+                        if (gather_lane)
+                            tma_gather4_multicast(sa + a_off + lane * 512u, &tmA, full_bar(s), k0,
+                                                  rows[0], rows[1], rows[2], rows[3], kAllCtas);
+                    } else if (lane == 0) {
+                        tma_load_2d_multicast(sa + a_off, &tmA, full_bar(s), k0, a_row0, kAllCtas);
+                    }
+                    if (lane == 0)
+                        tma_load_2d(sb, &tmB, full_bar(s), k0, nb0);
                 } else {
                     if (args.gather)
                         tma_gather4(sa + lane * 512u, &tmA, full_bar(s), k0, rows[0], rows[1],
@@ -281,6 +308,14 @@ __global__ void __launch_bounds__(192, 1)
                 else
                     tc_commit(bar);
             };
+            // a stage whose A slices came from the whole cluster is free only
+            // once every CTA of the cluster has consumed it
+            auto free_stage = [&](int st) {
+                if (MC > 1)
+                    tc_commit_multicast(empty_bar(st), kAllCtas);
+                else
+                    commit_to(empty_bar(st));
+            };
             // wait until stage s holds K block data; false if the kernel is aborting
             auto next_full = [&](int &st) {
                 if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
@@ -313,7 +348,7 @@ __global__ void __launch_bounds__(192, 1)
                             break;
                         }
                         issue_half(st, kb, 0, d_tmem);
-                        commit_to(empty_bar(st));  // frees the stage (in both CTAs of a pair)
+                        free_stage(st);  // frees the stage (in both CTAs of a pair)
                     }
                     if (!alive)
                         break;
@@ -348,7 +383,7 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     for (int32_t kb = 0; kb < f; ++kb) {
                         issue_half(held[kb], kb, 1, d_tmem);
-                        commit_to(empty_bar(held[kb]));
+                        free_stage(held[kb]);
                     }
                     for (int32_t kb = f; kb < l && alive; ++kb) {
                         int st;
@@ -356,7 +391,7 @@ __global__ void __launch_bounds__(192, 1)
                         if (alive) {
                             issue_half(st, kb, 0, d_tmem);
                             issue_half(st, kb, 1, d_tmem);
-                            commit_to(empty_bar(st));
+                            free_stage(st);
                         }
                     }
                     if (!alive)
@@ -372,7 +407,7 @@ __global__ void __launch_bounds__(192, 1)
                         commit_to(accf_bar(0));
                         for (int32_t kb = l; kb < nkb; ++kb) {
                             issue_half(held[kb - l], kb, 1, d_tmem);
-                            commit_to(empty_bar(held[kb - l]));
+                            free_stage(held[kb - l]);
                         }
                     } else if (f < nkb) {
                         commit_to(accf_bar(0));
@@ -401,11 +436,15 @@ __global__ void __launch_bounds__(192, 1)
         for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
-            const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * Cfg::BM;
+            if (MC > 1)
+                nb = nb * MC + static_cast<int32_t>(rank);
+            const int32_t m0 = mb * Cfg::TILE_M + (PAIR ? static_cast<int32_t>(rank) * Cfg::BM : 0);
             const int32_t n0 = nb * TILE_N;
             const int32_t row0 = m0 + 32 * (int32_t)q;
             const bool rows_ok = row0 < args.M;
-            const int32_t nchunks = min(TILE_N / 32, (args.N - n0 + 31) / 32);
+            // (MC > 1: a CTA past the last column block still takes part in the
+            // cluster's loads and MMAs, and writes nothing)
+            const int32_t nchunks = max(0, min(TILE_N / 32, (args.N - n0 + 31) / 32));
             const int32_t my_row = row0 + (int32_t)lane;
 
             if (lane == 0)
@@ -566,7 +605,9 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     tc_fence_before_sync();
-    if (PAIR) {
+    if (MC > 1) {
+        cluster_sync_all();  // no CTA leaves while peers may still multicast into it
+    } else if (PAIR) {
         if (threadIdx.x == 0 && *abort_flag)
             raise_abort();  // the peer stops waiting instead of running out of time itself
         if (*abort_flag && !leader) {

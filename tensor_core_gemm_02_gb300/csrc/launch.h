@@ -16,13 +16,15 @@ struct GemmMaps {
     CUtensorMap d;  // D boxes
 };
 
-// Tile kernel: 128 x bn tiles on single CTAs, or (pair) 256 x (nsub * bn)
-// tiles on CTA pairs with tcgen05 cta_group::2.  grid counts CTAs (twice the
-// pairs for pair forms).
-int tile_stages(int bn, bool pair, int nsub);
-int tile_max_pairs(int bn, int nsub);  // co-resident CTA pairs on the current device (0: unknown)
-cudaError_t launch_tile(int bn, bool pair, int nsub, const GemmMaps &maps, const GemmArgs &args,
-                        int grid, cudaStream_t stream);
+// Tile kernel forms: 128 x bn tiles on single CTAs (mc = 1), or on clusters of
+// mc = 4 CTAs sharing each A box by multicast; 256 x (nsub * bn) tiles on CTA
+// pairs with tcgen05 cta_group::2.  grid counts CTAs.
+int tile_stages(int bn, bool pair, int nsub, int mc);
+// clusters (pairs, or groups of mc) of a form that can be resident at once on
+// the current device; 0 if unknown
+int tile_max_clusters(int bn, bool pair, int nsub, int mc);
+cudaError_t launch_tile(int bn, bool pair, int nsub, int mc, const GemmMaps &maps,
+                        const GemmArgs &args, int grid, cudaStream_t stream);
 
 int skinny_stages(int mp);
 int skinny_kstage();  // K elements per pipeline stage (and per stream-K unit)

@@ -8,10 +8,6 @@
 #ifndef TCG_SKINNY_KBOX
 #define TCG_SKINNY_KBOX 1
 #endif
-// L2 prefetch distance of the B stream, in stages (0: none).
-#ifndef TCG_SKINNY_PF
-#define TCG_SKINNY_PF 0
-#endif
 
 namespace tcg {
 
@@ -22,7 +18,7 @@ cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int g
                                cudaStream_t stream)
 {
     using Cfg = SkinnyCfg<MP, TCG_SKINNY_KBOX>;
-    auto kfn = skinny_gemm_kernel<MP, TCG_SKINNY_KBOX, TCG_SKINNY_PF>;
+    auto kfn = skinny_gemm_kernel<MP, TCG_SKINNY_KBOX>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_ALLOC));
     if (e != cudaSuccess)

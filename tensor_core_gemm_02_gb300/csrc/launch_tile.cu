@@ -1,5 +1,6 @@
 // launch_tile.cu -- instantiations and launcher of the tile kernel: 128 x BN
-// tiles on single CTAs, or 256 x BN tiles on CTA pairs (cluster of two).
+// tiles on single CTAs (alone, or in clusters of four sharing A by multicast),
+// or 256 x (NSUB * BN) tiles on CTA pairs (clusters of two).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -11,39 +12,46 @@ namespace tcg {
 
 namespace {
 
-template <int BN, int STAGES, bool PAIR, int NSUB>
-cudaError_t launch_tile_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
-                             cudaStream_t stream)
+template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
+void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid, cudaStream_t stream)
 {
-    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB>;
-    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB>;
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::SMEM_ALLOC));
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t cfg = {};
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
+    cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (PAIR) {
+    if (Cfg::CLUSTER > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = Cfg::CLUSTER;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
+}
+
+template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
+cudaError_t launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
+    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::SMEM_ALLOC));
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_config<BN, STAGES, PAIR, NSUB, MC>(cfg, attr, grid, stream);
     return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, maps.d, args);
 }
 
-// How many CTA pairs of the pair kernel can be resident at once on the current
-// device (SMs that cannot be paired within their GPC stay idle).
-template <int BN, int STAGES, int NSUB>
-int max_pairs_impl()
+// How many clusters of this form can be resident at once on the current device
+// (SMs that cannot be grouped within their GPC stay idle).  Cached per device.
+template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
+int max_clusters_impl()
 {
-    using Cfg = TileCfg<BN, STAGES, true, NSUB>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
     static std::mutex mu;
     static int cached[64] = {};
     int dev = 0;
@@ -52,21 +60,13 @@ int max_pairs_impl()
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev] > 0)
         return cached[dev];
-    auto kfn = tile_gemm_kernel<BN, STAGES, true, NSUB>;
+    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC>;
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::SMEM_ALLOC)) != cudaSuccess)
         return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
+    cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    fill_config<BN, STAGES, PAIR, NSUB, MC>(cfg, attr, Cfg::CLUSTER, nullptr);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kfn, &cfg) != cudaSuccess)
         return 0;
@@ -76,11 +76,15 @@ int max_pairs_impl()
 
 }  // namespace
 
-int tile_stages(int bn, bool pair, int nsub)
+int tile_stages(int bn, bool pair, int nsub, int mc)
 {
     if (pair)
-        return bn != 256 ? 0 : (nsub == 2 ? 4 : 6);
+        return (bn != 256 || mc != 1) ? 0 : (nsub == 2 ? 4 : 6);
     if (nsub != 1)
+        return 0;
+    if (mc == 4)
+        return bn == 256 ? 4 : (bn == 64 ? 8 : 0);
+    if (mc != 1)
         return 0;
     switch (bn) {
     case 256: return 4;
@@ -90,28 +94,44 @@ int tile_stages(int bn, bool pair, int nsub)
     }
 }
 
-int tile_max_pairs(int bn, int nsub)
+int tile_max_clusters(int bn, bool pair, int nsub, int mc)
 {
-    if (bn != 256)
-        return 0;
-    return nsub == 2 ? max_pairs_impl<256, 4, 2>() : max_pairs_impl<256, 6, 1>();
+    if (pair && bn == 256 && mc == 1)
+        return nsub == 2 ? max_clusters_impl<256, 4, true, 2, 1>()
+                         : max_clusters_impl<256, 6, true, 1, 1>();
+    if (!pair && nsub == 1 && mc == 4) {
+        if (bn == 256)
+            return max_clusters_impl<256, 4, false, 1, 4>();
+        if (bn == 64)
+            return max_clusters_impl<64, 8, false, 1, 4>();
+    }
+    return 0;
 }
 
-cudaError_t launch_tile(int bn, bool pair, int nsub, const GemmMaps &maps, const GemmArgs &args,
-                        int grid, cudaStream_t stream)
+cudaError_t launch_tile(int bn, bool pair, int nsub, int mc, const GemmMaps &maps,
+                        const GemmArgs &args, int grid, cudaStream_t stream)
 {
     if (pair) {
-        if (bn != 256)
+        if (bn != 256 || mc != 1)
             return cudaErrorInvalidValue;
-        return nsub == 2 ? launch_tile_impl<256, 4, true, 2>(maps, args, grid, stream)
-                         : launch_tile_impl<256, 6, true, 1>(maps, args, grid, stream);
+        return nsub == 2 ? launch_impl<256, 4, true, 2, 1>(maps, args, grid, stream)
+                         : launch_impl<256, 6, true, 1, 1>(maps, args, grid, stream);
     }
     if (nsub != 1)
         return cudaErrorInvalidValue;
+    if (mc == 4) {
+        if (bn == 256)
+            return launch_impl<256, 4, false, 1, 4>(maps, args, grid, stream);
+        if (bn == 64)
+            return launch_impl<64, 8, false, 1, 4>(maps, args, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (mc != 1)
+        return cudaErrorInvalidValue;
     switch (bn) {
-    case 256: return launch_tile_impl<256, 4, false, 1>(maps, args, grid, stream);
-    case 128: return launch_tile_impl<128, 6, false, 1>(maps, args, grid, stream);
-    case 64: return launch_tile_impl<64, 8, false, 1>(maps, args, grid, stream);
+    case 256: return launch_impl<256, 4, false, 1, 1>(maps, args, grid, stream);
+    case 128: return launch_impl<128, 6, false, 1, 1>(maps, args, grid, stream);
+    case 64: return launch_impl<64, 8, false, 1, 1>(maps, args, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

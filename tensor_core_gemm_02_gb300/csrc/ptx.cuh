@@ -157,13 +157,29 @@ __device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Hint: bring a box of a 2-D descriptor into L2 (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int32_t x, int32_t y)
+// Multicast forms: the same box lands at the same shared-memory offset of
+// every CTA in `mask` (a cluster of CTAs on this GPU), and each destination's
+// mbarrier at the offset of `bar` receives the byte count.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                                      int32_t x, int32_t y, uint16_t mask)
 {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(x), "r"(y)
-                 : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_gather4_multicast(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                                      int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                                      int32_t y3, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+        "h"(mask)
+        : "memory");
 }
 
 // Shared image -> global box; completion through bulk groups.
@@ -282,6 +298,16 @@ __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t 
 {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+// Single-CTA MMAs, arrival multicast to the mbarrier at the same offset in
+// every CTA of `mask` once this thread's earlier tcgen05 ops finish.
+__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
         "h"(mask)
         : "memory");
 }
