@@ -193,7 +193,8 @@ const char *gemm_status_string(int status);
  *           on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2), 4 = tile
  *           kernel on CTA pairs with 256 x 512 tiles (two MMA halves, one
  *           accumulator), 5 = tile kernel on single CTAs (128 x bn tiles) in
- *           clusters of 4 along N that share each A box by TMA multicast
+ *           clusters of 4 along N that share each A box by TMA multicast,
+ *           6 = the same in clusters of 8
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)
@@ -233,7 +234,8 @@ gemm_status gemm_debug_inject(int mode);
  * Test hook.  Force the form of the tile kernel for later calls: kernel 1 =
  * single CTAs with tile width bn in {64, 128, 256}, kernel 3 = CTA pairs with
  * bn = 256, kernel 4 = CTA pairs with bn = 512, kernel 5 = clusters of 4
- * single CTAs sharing A with bn in {64, 256}, kernel 0 = automatic choice
+ * single CTAs sharing A with bn in {64, 256}, kernel 6 = clusters of 8
+ * with bn = 256, kernel 0 = automatic choice
  * (the default).  Problems the forced form cannot run (the M <= 64 skinny
  * path; K == 0 for pairs) keep the automatic choice.  Returns
  * GEMM_ERR_INVALID_ARG for other values.

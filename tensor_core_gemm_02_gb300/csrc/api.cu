@@ -351,10 +351,14 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used
             best = TileChoice{4, 512};
         }
     }
-    // Gathered rows with N >= 1024: clusters of four single CTAs that each
-    // issue a quarter of the gather4s and multicast the rows (measured 15%
-    // faster than the 256 x 512 pair form on 16384 rows, N = K = 4096).
-    if (gather && N >= 1024)
+    // Gathered rows with N >= 2048: clusters of eight single CTAs that each
+    // issue an eighth of the gather4s and multicast the rows (16384 rows,
+    // N = K = 4096: 0.474 ms, against 0.489 for clusters of four and 0.563 for
+    // the 256 x 512 pair form, although only 15 clusters of eight, 120 SMs,
+    // fit at once); N >= 1024: clusters of four.
+    if (gather && N >= 2048)
+        best = TileChoice{6, 256};
+    else if (gather && N >= 1024)
         best = TileChoice{5, 256};
     return best;
 }
@@ -382,6 +386,8 @@ TileForm tile_form(const gemm_plan &p)
         return TileForm{true, 256, 2, 1, 2, 256, 512};
     if (p.kernel == 5)
         return TileForm{false, p.bn, 1, 4, 4, 128, p.bn};
+    if (p.kernel == 6)
+        return TileForm{false, p.bn, 1, 8, 8, 128, p.bn};
     return TileForm{false, p.bn, 1, 1, 1, 128, p.bn};
 }
 
@@ -497,7 +503,8 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || (plan.kernel != 1 && plan.kernel != 3 && plan.kernel != 4 && plan.kernel != 5))
+    if (fk == 0 || (plan.kernel != 1 && plan.kernel != 3 && plan.kernel != 4 && plan.kernel != 5 &&
+                    plan.kernel != 6))
         return plan;
     if (fk != 1 && p.K == 0)
         return plan;  // cluster forms need K > 0
@@ -679,7 +686,7 @@ gemm_status gemm_debug_force_tile(int kernel, int bn)
 {
     const bool ok = (kernel == 0) || (kernel == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
                     (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512) ||
-                    (kernel == 5 && (bn == 64 || bn == 256));
+                    (kernel == 5 && (bn == 64 || bn == 256)) || (kernel == 6 && bn == 256);
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

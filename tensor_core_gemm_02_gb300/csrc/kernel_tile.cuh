@@ -32,6 +32,12 @@
 
 #include "common.cuh"
 
+// Evict-first L2 policy on the epilogue's C loads and D stores (0 or 1;
+// measured 1-3% faster on the 8192^3 and 8192 x 28672 x 4096 workloads).
+#ifndef TCG_EPI_EVICT_FIRST
+#define TCG_EPI_EVICT_FIRST 1
+#endif
+
 namespace tcg {
 
 template <int BN_, int STAGES_, bool PAIR_ = false, int NSUB_ = 1, int MC_ = 1>
@@ -75,7 +81,8 @@ struct TileCfg {
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(NSUB == 1 || NSUB == 2, "one or two halves");
-    static_assert(MC == 1 || (!PAIR && (MC == 2 || MC == 4)), "A multicast over 2 or 4 single CTAs");
+    static_assert(MC == 1 || (!PAIR && (MC == 2 || MC == 4 || MC == 8)),
+                  "A multicast over 2, 4 or 8 single CTAs");
     static_assert(!PAIR || (BN % 32 == 0 && BN_LOCAL % 8 == 0), "pair splits B in 8-row groups");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
@@ -429,6 +436,9 @@ __global__ void __launch_bounds__(192, 1)
         const bool c_tma = has_c && args.c_tma != 0;
         const bool acc_zero = args.num_k_blocks == 0;
         const int out_kind = args.out_kind;
+        // C and D are touched once: their lines go first out of L2, so the A
+        // and B panels that neighbouring tiles share stay resident
+        const uint64_t epi_policy = l2_policy_evict_first();
         int ab = 0;
         uint32_t aph = 0;
         uint32_t cph[2] = {0u, 0u};
@@ -453,7 +463,11 @@ __global__ void __launch_bounds__(192, 1)
             if (c_tma && rows_ok && lane == 0) {
                 for (int j = 0; j < 2 && j < nchunks; ++j) {
                     mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
-                    tma_load_2d(buf0 + j * Cfg::EPI_BUF, &tmC, c_bar(q, j), n0 + 32 * j, row0);
+                    if (TCG_EPI_EVICT_FIRST)
+                        tma_load_2d_hint(buf0 + j * Cfg::EPI_BUF, &tmC, c_bar(q, j), n0 + 32 * j, row0,
+                                         epi_policy);
+                    else
+                        tma_load_2d(buf0 + j * Cfg::EPI_BUF, &tmC, c_bar(q, j), n0 + 32 * j, row0);
                 }
             }
             bool zero_row = acc_zero;
@@ -576,14 +590,20 @@ __global__ void __launch_bounds__(192, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmD, buf, col0, row0);
+                        if (TCG_EPI_EVICT_FIRST)
+                            tma_store_2d_hint(&tmD, buf, col0, row0, epi_policy);
+                        else
+                            tma_store_2d(&tmD, buf, col0, row0);
                         bulk_commit_group();
                     }
                 }
                 if (c_tma && c + 2 < nchunks && lane == 0) {
                     bulk_wait_group_read<0>();  // the store of this chunk is done with buffer j
                     mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
-                    tma_load_2d(buf, &tmC, c_bar(q, j), n0 + 32 * (c + 2), row0);
+                    if (TCG_EPI_EVICT_FIRST)
+                        tma_load_2d_hint(buf, &tmC, c_bar(q, j), n0 + 32 * (c + 2), row0, epi_policy);
+                    else
+                        tma_load_2d(buf, &tmC, c_bar(q, j), n0 + 32 * (c + 2), row0);
                 }
                 __syncwarp();
             }

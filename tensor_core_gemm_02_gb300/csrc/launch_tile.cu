@@ -84,6 +84,8 @@ int tile_stages(int bn, bool pair, int nsub, int mc)
         return 0;
     if (mc == 4)
         return bn == 256 ? 4 : (bn == 64 ? 8 : 0);
+    if (mc == 8)
+        return bn == 256 ? 4 : 0;
     if (mc != 1)
         return 0;
     switch (bn) {
@@ -105,6 +107,8 @@ int tile_max_clusters(int bn, bool pair, int nsub, int mc)
         if (bn == 64)
             return max_clusters_impl<64, 8, false, 1, 4>();
     }
+    if (!pair && nsub == 1 && mc == 8 && bn == 256)
+        return max_clusters_impl<256, 4, false, 1, 8>();
     return 0;
 }
 
@@ -126,6 +130,9 @@ cudaError_t launch_tile(int bn, bool pair, int nsub, int mc, const GemmMaps &map
             return launch_impl<64, 8, false, 1, 4>(maps, args, grid, stream);
         return cudaErrorInvalidValue;
     }
+    if (mc == 8)
+        return bn == 256 ? launch_impl<256, 4, false, 1, 8>(maps, args, grid, stream)
+                         : cudaErrorInvalidValue;
     if (mc != 1)
         return cudaErrorInvalidValue;
     switch (bn) {

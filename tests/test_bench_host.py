@@ -1,0 +1,78 @@
+"""Host-side logic of bench.py that needs no GPU: the whole-job aggregation over
+ranks (two gloo processes on the CPU), kernel naming and the traffic lookup."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from tensor_core_gemm_02_gb300 import binding  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local_ms = [2.0, 3.0][rank]  # rank 1 is the slow one
+    ms = bench.slowest_rank(local_ms, world, torch.device("cpu"))
+    value = bench.job_throughput(1e12, ms, world)
+    out[rank] = (ms, value)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_takes_the_slowest_rank():
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    for rank in (0, 1):
+        ms, value = res[rank]
+        assert ms == 3.0
+        # 2 ranks x 1 TFLOP each over 3 ms
+        assert abs(value - 2 * 1e12 / 3e-3 / 1e12) < 1e-9
+
+
+def test_single_rank_needs_no_process_group():
+    assert bench.slowest_rank(1.5, 1, torch.device("cpu")) == 1.5
+    assert bench.job_throughput(2e12, 2.0, 1) == pytest.approx(1000.0)
+
+
+def test_kernel_keys_name_the_launched_instance():
+    binding.load_library()
+    p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
+    assert bench.kernel_key(p) == "tile_gemm_kernel<256, 4, 1, 2, 1>"
+    p = binding.gemm_query_plan(8192, 28672, 4096, has_c=True, sm_count=148)
+    assert bench.kernel_key(p) == "tile_gemm_kernel<256, 6, 1, 1, 1>"
+    p = binding.gemm_query_plan(16, 28672, 4096, sm_count=148)
+    assert bench.kernel_key(p) == "skinny_gemm_kernel<16, 1>"
+    p = binding.gemm_query_plan(1024, 1024, 1024, sm_count=148)
+    assert bench.kernel_key(p) == "tile_gemm_kernel<64, 8, 0, 1, 1>"
+
+
+def test_traffic_is_reported_only_for_current_sources(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.json").write_text(json.dumps(
+        {"source_hash": "not-the-current-hash", "kernels": {"k@w": {"dram_bytes_per_launch": 5}}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "current")
+    assert bench.stored_traffic("k@w") is None
+    (prof / "traffic.json").write_text(json.dumps(
+        {"source_hash": "current", "kernels": {"k@w": {"dram_bytes_per_launch": 5}}}))
+    assert bench.stored_traffic("k@w") == 5
+    assert bench.stored_traffic("other@w") is None

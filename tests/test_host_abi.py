@@ -110,7 +110,9 @@ def test_plan_matches_the_dispatch_rules(lib):
     # stream-K shares of 224 * 64 k-blocks over 148 CTAs: at most 2 per tile
     assert p.splits == 2
     p = binding.gemm_query_plan(16384, 4096, 4096, gather=True, sm_count=148)
-    assert (p.kernel, p.bn, p.grid) == (5, 256, 148) and p.tiles == 128 * 16
+    assert (p.kernel, p.bn, p.grid) == (6, 256, 144) and p.tiles == 128 * 16
+    p = binding.gemm_query_plan(16384, 1024, 4096, gather=True, sm_count=148)
+    assert (p.kernel, p.bn) == (5, 256)
     p = binding.gemm_query_plan(16384, 512, 4096, gather=True, sm_count=148)
     assert p.kernel == 4 and p.bn == 512
     p = binding.gemm_query_plan(100, 8192, 8192, sm_count=148)
