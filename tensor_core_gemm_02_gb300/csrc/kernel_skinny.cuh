@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(192, 1)
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        // inputs are read only once the previous kernel in the stream is done
+        grid_dependency_wait();
         // the ring is empty: start the B stream now instead of after the
         // tensor-memory allocation and the set-up barrier
         for (int64_t q = my_start; q < my_end && pre < STAGES; ++q, ++pre)
@@ -160,10 +162,13 @@ __global__ void __launch_bounds__(192, 1)
         tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
         tmem_relinquish();
     }
+    grid_dependency_wait();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0)
+        grid_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer

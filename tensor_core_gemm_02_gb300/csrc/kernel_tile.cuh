@@ -173,6 +173,9 @@ __global__ void __launch_bounds__(192, 1)
             tmem_relinquish();
         }
     }
+    // set-up above touched only shared and tensor memory; inputs and outputs
+    // are used only after the previous kernel in the stream has finished
+    grid_dependency_wait();
     tc_fence_before_sync();
     if (CL > 1)
         cluster_sync_all();  // the peers' barriers exist before anything targets them
@@ -180,6 +183,8 @@ __global__ void __launch_bounds__(192, 1)
         __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0)
+        grid_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer

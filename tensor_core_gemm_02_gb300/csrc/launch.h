@@ -7,6 +7,12 @@
 
 #include "common.cuh"
 
+// Launch with programmatic dependent launch allowed (1) or not (0): a GEMM
+// may then start its set-up while the previous kernel in the stream ends.
+#ifndef TCG_PDL
+#define TCG_PDL 1
+#endif
+
 namespace tcg {
 
 struct GemmMaps {

@@ -28,6 +28,11 @@ cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int g
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = TCG_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, args);
 }
 

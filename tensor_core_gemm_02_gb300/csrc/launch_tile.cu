@@ -12,6 +12,7 @@ namespace tcg {
 
 namespace {
 
+// attr must hold two entries
 template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
 void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid, cudaStream_t stream)
 {
@@ -21,14 +22,19 @@ void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid, c
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
     cfg.stream = stream;
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = TCG_PDL;
+    ++n;
     if (Cfg::CLUSTER > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = Cfg::CLUSTER;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = Cfg::CLUSTER;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
 }
 
 template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
@@ -41,7 +47,7 @@ cudaError_t launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid, cu
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     fill_config<BN, STAGES, PAIR, NSUB, MC>(cfg, attr, grid, stream);
     return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, maps.d, args);
 }
@@ -65,8 +71,10 @@ int max_clusters_impl()
                              static_cast<int>(Cfg::SMEM_ALLOC)) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     fill_config<BN, STAGES, PAIR, NSUB, MC>(cfg, attr, Cfg::CLUSTER, nullptr);
+    cfg.attrs = attr + 1;  // the cluster shape only (the dependent-launch flag is not a query input)
+    cfg.numAttrs = 1;
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kfn, &cfg) != cudaSuccess)
         return 0;

@@ -54,6 +54,23 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// With programmatic dependent launch a kernel may start while the previous
+// one in the stream finishes.  wait: block until the grids this one depends
+// on have completed and their memory is visible (no-op without the launch
+// attribute); every access to inputs or outputs comes after it.
+// launch_dependents: let the next such launch begin its own set-up.
+
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 // Loads complete on an mbarrier that is initialised, armed with the expected
 // transaction bytes, and waited on by phase ("cp.async.bulk.tensor" page,
