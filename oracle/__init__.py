@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for D = alpha * A @ B.T + beta * C (plain and gathered forms).
+"""fp64 CPU oracle for D = alpha * A @ B.T + beta * C (plain, gathered and
+scattered forms).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product path
@@ -50,6 +51,9 @@ def _bind(lib):
     lib.oracle_gemm_entries.argtypes = [i64, vp, vp, i64, i32, vp, i64, vp, i64,
                                         vp, i64, vp, i64, dbl, dbl, vp, vp]
     lib.oracle_gemm_entries.restype = i32
+    lib.oracle_scatter_rows.argtypes = [i64, i64, i64, i64, i32, vp, i64, vp, i64,
+                                        vp, i64, vp, i64, dbl, dbl, vp, vp, i64]
+    lib.oracle_scatter_rows.restype = i32
     lib.oracle_init()
     return lib
 
@@ -198,6 +202,72 @@ def gemm_entries(A, B, ii, jj, C=None, alpha=1.0, beta=1.0, idx=None, dtype=None
     with ThreadPoolExecutor(max_workers=nthr) as ex:
         bad = list(ex.map(lambda p: run(*p), zip(bounds[:-1], bounds[1:])))
     return ref, absprod, bool(any(bad))
+
+
+def scatter_rows(A, B, idx, d_rows, C=None, alpha=1.0, beta=1.0, dtype=None, threads=None):
+    """Rows that a row-scattered GEMM sends: row i (M x N result) is
+    alpha * A[i] @ B.T + beta * C[idx[i]], bound for row idx[i] of D.
+
+    C (d_rows x N float32) is indexed by destination row, like D.  Returns
+    (rows, absprod, bad_index); a row with an index outside [0, d_rows) is NaN
+    and sets bad_index.
+    """
+    lib = load()
+    a, code_a = _as_bits(A, dtype)
+    b, code_b = _as_bits(B, dtype)
+    if code_a != code_b:
+        raise TypeError("A and B must have the same dtype")
+    c, ix = _f32(C), _i32(idx)
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    if ix is None or ix.shape[0] != M:
+        raise ValueError("idx must hold one destination row per row of A")
+    if c is not None and c.shape != (d_rows, N):
+        raise ValueError("C must be d_rows x N")
+    rows = np.empty((M, N), np.float64)
+    absprod = np.empty((M, N), np.float64)
+    nthr = threads or default_threads()
+    bounds = np.linspace(0, M, min(nthr, max(1, M)) + 1).astype(np.int64)
+
+    def run(lo, hi):
+        lo, hi = int(lo), int(hi)
+        if hi <= lo:
+            return 0
+        off = lo * N * 8
+        return lib.oracle_scatter_rows(lo, hi, N, K, code_a, _ptr(a), a.shape[1], _ptr(ix),
+                                       int(d_rows), _ptr(b), b.shape[1], _ptr(c), N,
+                                       float(alpha), float(beta), rows.ctypes.data + off,
+                                       absprod.ctypes.data + off, N)
+
+    with ThreadPoolExecutor(max_workers=nthr) as ex:
+        bad = list(ex.map(lambda p: run(*p), zip(bounds[:-1], bounds[1:])))
+    return rows, absprod, bool(any(bad))
+
+
+def scatter_place(D0, rows, idx):
+    """Place the rows a scattered GEMM sends into a copy of D0 (float64).
+
+    Rows of D named by no valid index keep D0.  A row named once holds the
+    row sent to it.  A row named more than once is left NaN in the result and
+    listed in the returned dict {row: [i, ...]}: every element of it must equal
+    the same element of one of the rows sent to it (which one is unspecified).
+    """
+    D = np.array(D0, np.float64, copy=True)
+    ix = np.asarray(idx, np.int64)
+    valid = (ix >= 0) & (ix < D.shape[0])
+    senders: dict[int, list[int]] = {}
+    for i in np.nonzero(valid)[0]:
+        senders.setdefault(int(ix[i]), []).append(int(i))
+    repeated = {}
+    for d, who in senders.items():
+        if len(who) == 1:
+            D[d] = rows[who[0]]
+        else:
+            D[d] = np.nan
+            repeated[d] = who
+    return D, repeated
 
 
 def decode(bits, dtype: str) -> np.ndarray:

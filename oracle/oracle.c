@@ -166,3 +166,61 @@ int oracle_gemm_entries(int64_t n, const int64_t *ii, const int64_t *jj,
                          C, ldc, alpha, beta, &ref[e], abs_out ? &abs_out[e] : NULL);
     return bad;
 }
+
+/*
+ * Row-scattered form ("cp.async.bulk.tensor" page, section "Gather4 and
+ * scatter4": scatter4 is the store-side dual of gather4 and writes four
+ * caller-chosen rows of the destination).  Row i of the product A * B^T goes
+ * to row d = idx[i] of D, and the C term comes from that same destination
+ * row, so C and D are indexed alike as in every other form:
+ *
+ *     D[d][j] = alpha * sum_k A[i][k] * B[j][k]  +  beta * C[d][j],  d = idx[i]
+ *
+ * For i in [i0, i1) this fills row (i - i0) of ref / abs_out (ldr apart) with
+ * the values that row i sends; where they land is the caller's business.  An
+ * index outside [0, d_rows) sends nothing: its row is set to NaN and the call
+ * returns 1.
+ */
+int oracle_scatter_rows(int64_t i0, int64_t i1, int64_t N, int64_t K, int dtype,
+                        const uint16_t *A, int64_t lda, const int32_t *idx,
+                        int64_t d_rows, const uint16_t *B, int64_t ldb,
+                        const float *C, int64_t ldc, double alpha, double beta,
+                        double *ref, double *abs_out, int64_t ldr)
+{
+    const double *val;
+    int bad = 0;
+    oracle_init();
+    val = g_value[dtype == ORACLE_BF16 ? ORACLE_BF16 : ORACLE_F16];
+    for (int64_t i = i0; i < i1; ++i) {
+        const int64_t d = idx[i];
+        const uint16_t *arow = A + i * lda;
+        double *out = ref + (i - i0) * ldr;
+        double *out_abs = abs_out ? abs_out + (i - i0) * ldr : NULL;
+        if (d < 0 || d >= d_rows) {
+            for (int64_t j = 0; j < N; ++j) {
+                out[j] = NAN;
+                if (out_abs)
+                    out_abs[j] = NAN;
+            }
+            bad = 1;
+            continue;
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            const uint16_t *brow = B + j * ldb;
+            double sum = 0.0, sum_abs = 0.0;
+            for (int64_t kk = 0; kk < K; ++kk) {
+                double a = val[arow[kk]];
+                double b = val[brow[kk]];
+                sum += a * b;
+                sum_abs += fabs(a) * fabs(b);
+            }
+            double r = alpha * sum;
+            if (C && beta != 0.0)
+                r += beta * (double)C[d * ldc + j];
+            out[j] = r;
+            if (out_abs)
+                out_abs[j] = sum_abs;
+        }
+    }
+    return bad;
+}

@@ -168,6 +168,55 @@ def pin_entries_match_rows():
     assert np.array_equal(part, full[4:11])
 
 
+def pin_scatter_rows():
+    """Row-scattered form: closed forms that tell the A row (source i) from
+    the C row (destination idx[i]), brute force on exact inputs, the identity
+    index, and the bad-index and placement rules."""
+    rng = np.random.default_rng(11)
+    M, K, d_rows = 5, 8, 7
+    perm = rng.permutation(d_rows)[:M].astype(np.int32)  # distinct, not the identity
+    assert not np.array_equal(perm, np.arange(M))
+    c = rng.standard_normal((d_rows, K)).astype(np.float32)
+    # A = 0: each row sent is beta * C[destination]
+    zeros = torch.zeros((M, K), dtype=torch.float16)
+    eye = torch.eye(K, dtype=torch.float16)
+    r0, _, bad0 = oracle.scatter_rows(zeros, eye, perm, d_rows, c, alpha=3.0, beta=0.5)
+    assert not bad0 and np.array_equal(r0, 0.5 * c[perm].astype(np.float64))
+    # B = I, no C: each row sent is alpha * A[source]
+    a = torch.from_numpy(rng.integers(-4, 5, (M, K)).astype(np.float32) / 4).to(torch.float16)
+    r1, _, _ = oracle.scatter_rows(a, eye, perm, d_rows, None, alpha=-2.0)
+    assert np.array_equal(r1, -2.0 * _f64(a))
+    # exact brute force against numpy on quarter-integer inputs
+    b = torch.from_numpy(rng.integers(-4, 5, (6, K)).astype(np.float32) / 4).to(torch.bfloat16)
+    ab = a.to(torch.bfloat16)
+    cq = (rng.integers(-4, 5, (d_rows, 6)) / 4).astype(np.float32)
+    r2, abs2, _ = oracle.scatter_rows(ab, b, perm, d_rows, cq, alpha=0.5, beta=-1.0)
+    assert np.array_equal(r2, 0.5 * (_f64(ab) @ _f64(b).T) - cq[perm].astype(np.float64))
+    assert np.array_equal(abs2, np.abs(_f64(ab)) @ np.abs(_f64(b)).T)
+    # identity index: the scattered rows are the plain GEMM's rows
+    ar = np.arange(M, dtype=np.int32)
+    r3, _, _ = oracle.scatter_rows(ab, b, ar, M, cq[:M].copy(), alpha=0.5, beta=-1.0)
+    plain, _, _ = oracle.gemm(ab, b, torch.from_numpy(cq[:M].copy()), 0.5, -1.0)
+    assert np.array_equal(r3, plain)
+    # an index outside [0, d_rows) sends nothing and is reported
+    badidx = np.array([2, d_rows, -1, 0, 6], np.int32)
+    r4, _, bad4 = oracle.scatter_rows(ab, b, badidx, d_rows, cq, alpha=0.5, beta=-1.0)
+    assert bad4 and np.isnan(r4[1]).all() and np.isnan(r4[2]).all()
+    want4 = 0.5 * (_f64(ab)[[0, 3, 4]] @ _f64(b).T) - cq[[2, 0, 6]].astype(np.float64)
+    assert np.array_equal(r4[[0, 3, 4]], want4)
+    # placement: rows named once take the row sent, unnamed rows keep D0,
+    # repeated rows are reported with their senders
+    d0 = rng.standard_normal((d_rows, 6))
+    dup = np.array([4, 1, 4, 9, 0], np.int32)
+    placed, rep = oracle.scatter_place(d0, r2, dup)
+    assert rep == {4: [0, 2]}
+    assert np.array_equal(placed[1], r2[1]) and np.array_equal(placed[0], r2[4])
+    for untouched in (2, 3, 5, 6):
+        assert np.array_equal(placed[untouched], d0[untouched])
+    assert np.isnan(placed[4]).all()
+
+
 ALL_PINS = [pin_decode_f16, pin_decode_bf16, pin_worked_example_exact,
             pin_matches_numpy_random_shapes, pin_two_a_plus_one, pin_fma_separation,
-            pin_alpha_beta_c_cases, pin_gather_invariants, pin_entries_match_rows]
+            pin_alpha_beta_c_cases, pin_gather_invariants, pin_entries_match_rows,
+            pin_scatter_rows]

@@ -35,6 +35,13 @@ MUTANTS = [
      "const double *val = g_value[ORACLE_F16];"),
     ("abs_not_absolute", "sum_abs += fabs(a) * fabs(b);", "sum_abs += a * b;"),
     ("beta_zero_reads_c", "if (C && beta != 0.0)", "if (C)"),
+    ("scatter_c_row_from_source", "r += beta * (double)C[d * ldc + j];",
+     "r += beta * (double)C[i * ldc + j];"),
+    ("scatter_a_row_from_destination", "const uint16_t *arow = A + i * lda;\n        double *out",
+     "const uint16_t *arow = A + d * lda;\n        double *out"),
+    ("scatter_no_range_check", "if (d < 0 || d >= d_rows)", "if (d < 0)"),
+    ("scatter_b_row_fixed", "const uint16_t *brow = B + j * ldb;\n            double sum",
+     "const uint16_t *brow = B;\n            double sum"),
     ("sign_bit_ignored_f16", "    return sign ? -v : v;\n}\n\n/* bfloat16", "    return v;\n}\n\n/* bfloat16"),
 ]
 
