@@ -201,7 +201,8 @@ def kernel_key(plan):
 
 
 def plan_of(p, dev):
-    return binding.gemm_query_plan(p.M, p.N, p.K, gather=p.idx is not None,
+    return binding.gemm_query_plan(p.M, p.N, p.K, gather=p.idx is not None and not p.scatter,
+                                   scatter=p.scatter,
                                    has_c=p.C is not None and p.beta != 0,
                                    sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
 
@@ -212,6 +213,8 @@ def l2_flush(buf):
 
 def launch(p, dev_tensors):
     A, B, C, idx, D = dev_tensors
+    if p.scatter:
+        return binding.gemm_scatter_rows(A, B, idx, D, C, alpha=p.alpha, beta=p.beta)
     if idx is not None:
         return binding.gemm_gather_rows(A, idx, B, C, D, alpha=p.alpha, beta=p.beta, out=p.out)
     if A.dtype == torch.bfloat16:
@@ -224,12 +227,17 @@ def to_device(p, dev):
     B = p.B.to(dev)
     C = p.C.to(dev) if p.C is not None else None
     idx = p.idx.to(dev) if p.idx is not None else None
-    D = torch.empty((p.M, p.N), dtype=workloads.OUT_TORCH[p.out], device=dev)
+    if p.scatter:
+        D = (p.D0.to(dev) if p.D0 is not None else
+             torch.zeros((p.d_rows, p.N), dtype=workloads.OUT_TORCH[p.out], device=dev))
+    else:
+        D = torch.empty((p.M, p.N), dtype=workloads.OUT_TORCH[p.out], device=dev)
     return A, B, C, idx, D
 
 
 def algorithmic_bytes(p):
-    """Bytes the GEMM must move at least once: A (or the gathered rows), B, C, D, idx."""
+    """Bytes the GEMM must move at least once: A (or the gathered rows), B, C, D, idx
+    (scattered form: the M rows of C read and of D written)."""
     esz = p.A.element_size()
     a = p.M * p.K * esz
     b = p.N * p.K * esz
@@ -328,7 +336,8 @@ def time_e2e(p, dev, steps):
 
 def input_bytes(p):
     """Bytes of input the GEMM reads (the gathered form: the rows it gathers)."""
-    a = (int(torch.unique(p.idx).numel()) if p.idx is not None else p.M) * p.K * p.A.element_size()
+    gathered = p.idx is not None and not p.scatter
+    a = (int(torch.unique(p.idx).numel()) if gathered else p.M) * p.K * p.A.element_size()
     b = p.N * p.K * p.B.element_size()
     c = p.M * p.N * 4 if (p.C is not None and p.beta != 0) else 0
     return a + b + c
@@ -443,7 +452,7 @@ def run_ours(args):
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
         variants = {}
         for name in ("f16_1024", "mlp_8192x28672x4096", "skinny_16x28672x4096",
-                     "gather_16384_of_65536"):
+                     "gather_16384_of_65536", "scatter_16384_into_65536"):
             vp, ms, plan, how = time_variant(name, dev, args.variant_reps, flush)
             tflops = vp.flops / (ms * 1e-3) / 1e12
             gbs = algorithmic_bytes(vp) / (ms * 1e-3) / 1e9

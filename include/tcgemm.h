@@ -136,6 +136,38 @@ gemm_status gemm_gather_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
                              int out, float alpha, float beta, void *stream);
 
 /*
+ * Row-scattered form, the dual of the gathered one: for i < M,
+ *     D[idx[i]][:] = fma.rn(alpha, A[i][:] * B^T, beta * C[idx[i]][:]).
+ * Row i of the product is written to row idx[i] of D with TMA tile::scatter4
+ * stores, four rows per issue ("cp.async.bulk.tensor" page, section "Gather4
+ * and scatter4": the store form takes the destination first and four runtime
+ * row coordinates; choosing them is the caller's logic).  C is read from the
+ * same destination row (by tile::gather4), so C == D is an in-place update of
+ * the rows named by idx.  Rows of D that idx does not name are not touched.
+ *
+ *  A, lda      M x K, lda >= K, lda % 8 == 0, 16-byte aligned (as gemm_f16).
+ *  idx         M int32 destination rows in device memory, 4-byte aligned.
+ *              An index outside [0, d_rows) writes nothing for that row and
+ *              records GEMM_ERR_INDEX in the device status word.  Indices may
+ *              repeat: every element of a row named more than once then holds
+ *              the value that one of those rows computed (which one is not
+ *              specified); with C == D such a row is not specified at all.
+ *  d_rows      rows of D (and of C), in [1, 2^31).
+ *  C, ldc      NULL or d_rows x N float32 (as gemm_f16).
+ *  D, ldd      d_rows x N; stores go through TMA for float32 output with a
+ *              16-byte aligned base and row pitch, otherwise (and for a last
+ *              column chunk narrower than 32) through plain stores.
+ *  Other arguments as in gemm_f16.  D must not overlap idx, A or B.
+ */
+gemm_status gemm_scatter_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
+                              const void *A, int64_t lda,
+                              const void *B, int64_t ldb,
+                              const int32_t *idx, int64_t d_rows,
+                              const float *C, int64_t ldc,
+                              void *D, int64_t ldd,
+                              int out, float alpha, float beta, void *stream);
+
+/*
  * Allocation-free variant of the skinny (M <= 64) path.  The source pages have
  * no counterpart to this entry point; it exists for callers that cannot call
  * cudaMalloc where they run the GEMM: code whose device memory is owned by
@@ -186,7 +218,9 @@ const char *gemm_status_string(int status);
 /*
  * The kernel choice the library makes for a problem, without launching
  * anything and without touching the GPU (for diagnostics and tests).
- * gather: the row-gathered form; has_c: C is given and beta != 0.
+ * form: 0 = plain, 1 = row-gathered (gemm_gather_rows), 2 = row-scattered
+ * (gemm_scatter_rows); any other value is GEMM_ERR_INVALID_ARG.  has_c: C
+ * is given and beta != 0.
  *
  *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles, one
  *           CTA each), 2 = skinny swap-AB kernel (M <= 64), 3 = tile kernel
@@ -211,7 +245,7 @@ typedef struct {
     int32_t grid;
 } gemm_plan;
 
-gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather, int has_c,
+gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int form, int has_c,
                             int sm_count, gemm_plan *plan);
 
 /*

@@ -55,6 +55,8 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_bf16.argtypes = plain
     lib.gemm_gather_rows.argtypes = [i64, i64, i64, i32, vp, i64, i64, vp, vp, i64, vp, i64,
                                      vp, i64, i32, f32, f32, vp]
+    lib.gemm_scatter_rows.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
+                                      vp, i64, i32, f32, f32, vp]
     lib.gemm_skinny_noalloc.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
                                         i32, f32, f32, vp]
     lib.gemm_check_device_status.argtypes = [vp]
@@ -64,7 +66,8 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_set_wait_timeout.argtypes = [ctypes.c_uint64]
     lib.gemm_debug_inject.argtypes = [i32]
     lib.gemm_debug_force_tile.argtypes = [i32, i32]
-    for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_skinny_noalloc",
+    for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows",
+                 "gemm_skinny_noalloc",
                  "gemm_check_device_status",
                  "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject",
                  "gemm_debug_force_tile"):
@@ -84,9 +87,12 @@ def _stream_ptr(stream) -> int:
 
 
 def _ld(t: torch.Tensor) -> int:
-    if t.dim() != 2 or t.stride(1) != 1:
+    rows, cols = (t.shape[0], t.shape[1]) if t.dim() == 2 else (0, 0)
+    if t.dim() != 2 or (cols > 1 and t.stride(1) != 1):
         raise ValueError("matrices must be 2-D with unit column stride")
-    return int(t.stride(0)) if t.shape[0] > 1 else max(int(t.stride(0)), int(t.shape[1]))
+    if cols == 0:
+        return 0  # no columns (K == 0): the leading dimension is never used
+    return int(t.stride(0)) if rows > 1 else max(int(t.stride(0)), int(cols))
 
 
 def _ptr(t) -> int | None:
@@ -156,6 +162,37 @@ def gemm_gather_rows(table, idx, B, C=None, D=None, *, alpha=1.0, beta=1.0, out=
     return D
 
 
+def gemm_scatter_rows(A, B, idx, D, C=None, *, alpha=1.0, beta=1.0, stream=None):
+    """D[idx[i]] = fma.rn(alpha, A[i] @ B.T, beta * C[idx[i]]) for every row i of A.
+
+    D (d_rows x N; its dtype picks the output type) is updated in place: rows
+    that idx does not name keep their contents.  C, if given, is float32 with
+    D's shape (C is D: in-place update of the named rows).  Returns D.
+    """
+    if A.dtype not in (torch.float16, torch.bfloat16) or B.dtype != A.dtype:
+        raise TypeError("A and B must both be f16 or both bf16")
+    if idx.dtype != torch.int32 or idx.dim() != 1 or idx.shape[0] != A.shape[0]:
+        raise TypeError("idx must be a 1-D int32 tensor with one entry per row of A")
+    if D is None or D.dim() != 2:
+        raise ValueError("D (the matrix the rows are scattered into) is required")
+    out = _OUT_OF_DTYPE.get(D.dtype)
+    if out is None:
+        raise TypeError("D must be float32, bfloat16 or float16")
+    M, K = A.shape
+    N = B.shape[0]
+    d_rows = int(D.shape[0])
+    if B.shape[1] != K or D.shape[1] != N:
+        raise ValueError("A, B and D disagree on K or N")
+    if C is not None and (C.dtype != torch.float32 or tuple(C.shape) != tuple(D.shape)):
+        raise ValueError("C must be float32 with D's shape")
+    st = load_library().gemm_scatter_rows(
+        M, N, K, 1 if A.dtype == torch.bfloat16 else 0, _ptr(A), _ld(A), _ptr(B), _ld(B),
+        _ptr(idx), d_rows, _ptr(C), _ld(C) if C is not None else 0, _ptr(D), _ld(D), out,
+        float(alpha), float(beta), _stream_ptr(stream))
+    _check(st, "gemm_scatter_rows")
+    return D
+
+
 def gemm_skinny_noalloc(A, B, C=None, D=None, *, alpha=1.0, beta=1.0, out=OUT_F32,
                         stream=None):
     """The M <= 64 path with the library's fixed scratch array: the call allocates
@@ -189,9 +226,10 @@ def gemm_check_device_status(stream=None) -> int:
     return int(load_library().gemm_check_device_status(_stream_ptr(stream)))
 
 
-def gemm_query_plan(M, N, K, gather=False, has_c=False, sm_count=148) -> Plan:
+def gemm_query_plan(M, N, K, gather=False, has_c=False, sm_count=148, scatter=False) -> Plan:
     p = Plan()
-    _check(load_library().gemm_query_plan(M, N, K, int(bool(gather)), int(bool(has_c)),
+    form = 1 if gather else (2 if scatter else 0)
+    _check(load_library().gemm_query_plan(M, N, K, form, int(bool(has_c)),
                                           sm_count, ctypes.byref(p)), "gemm_query_plan")
     return p
 

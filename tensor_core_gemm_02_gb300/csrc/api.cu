@@ -245,7 +245,7 @@ int out_size(int out) { return out == GEMM_OUT_F32 ? 4 : 2; }
 gemm_status validate(const Problem &p, bool *empty)
 {
     *empty = false;
-    if (p.M < 0 || p.N < 0 || p.K < 0 || p.a_rows < 0)
+    if (p.M < 0 || p.N < 0 || p.K < 0 || p.a_rows < 0 || p.d_rows < 0)
         return GEMM_ERR_INVALID_ARG;
     if (p.out != GEMM_OUT_F32 && p.out != GEMM_OUT_BF16 && p.out != GEMM_OUT_F16)
         return GEMM_ERR_INVALID_ARG;
@@ -262,6 +262,12 @@ gemm_status validate(const Problem &p, bool *empty)
         return GEMM_ERR_INVALID_ARG;
     if (p.gather && (!p.idx || p.a_rows < 1))
         return GEMM_ERR_INVALID_ARG;
+    if (p.scatter && (!p.idx || p.d_rows < 1 || p.gather))
+        return GEMM_ERR_INVALID_ARG;
+    if (p.d_rows > kMaxDim)
+        return GEMM_ERR_UNSUPPORTED;
+    // rows of C and D: M, or the rows of the matrix the result is scattered into
+    const int64_t out_rows = p.scatter ? p.d_rows : p.M;
     if (p.ldd < p.N)
         return GEMM_ERR_INVALID_ARG;
     if (c_used && p.ldc < p.N)
@@ -279,19 +285,19 @@ gemm_status validate(const Problem &p, bool *empty)
         return GEMM_ERR_ALIGNMENT;
     if (reinterpret_cast<uintptr_t>(p.D) & static_cast<uintptr_t>(out_size(p.out) - 1))
         return GEMM_ERR_ALIGNMENT;
-    if (p.gather && (reinterpret_cast<uintptr_t>(p.idx) & 3u))
+    if ((p.gather || p.scatter) && (reinterpret_cast<uintptr_t>(p.idx) & 3u))
         return GEMM_ERR_ALIGNMENT;
     // aliasing: D may only coincide exactly with C (fp32 in-place update)
-    const uint64_t d_span = span_bytes(p.M, p.N, p.ldd, out_size(p.out));
+    const uint64_t d_span = span_bytes(out_rows, p.N, p.ldd, out_size(p.out));
     if (p.K > 0) {
         if (overlap(p.D, d_span, p.A, span_bytes(p.a_rows, p.K, p.lda, 2)))
             return GEMM_ERR_ALIAS;
         if (overlap(p.D, d_span, p.B, span_bytes(p.N, p.K, p.ldb, 2)))
             return GEMM_ERR_ALIAS;
     }
-    if (p.gather && overlap(p.D, d_span, p.idx, static_cast<uint64_t>(p.M) * 4))
+    if ((p.gather || p.scatter) && overlap(p.D, d_span, p.idx, static_cast<uint64_t>(p.M) * 4))
         return GEMM_ERR_ALIAS;
-    if (c_used && overlap(p.D, d_span, p.C, span_bytes(p.M, p.N, p.ldc, 4))) {
+    if (c_used && overlap(p.D, d_span, p.C, span_bytes(out_rows, p.N, p.ldc, 4))) {
         const bool exact_in_place = static_cast<const void *>(p.C) == p.D &&
                                     p.out == GEMM_OUT_F32 && p.ldc == p.ldd;
         if (!exact_in_place)
@@ -311,15 +317,19 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // sharing A by multicast (gathered rows only).  Cost = waves of persistent
 // CTA sets x per-SM tile width plus a fixed per-tile cost.  Pairs get a 10%
 // credit (each SM moves 2/3 of the operand bytes); the 256 x 512 form gets a
-// further 5% when its epilogue is short relative to the tile (no C, K >= 2048)
-// and is always preferred for gathered rows, whose cost is the number of TMA
-// gather4 issues per flop.
+// further 5% when its epilogue is short relative to the tile (no C, not
+// scattered, K >= 2048) and is always preferred for gathered rows, whose cost
+// is the number of TMA gather4 issues per flop.  (Scattered rows: 16384 rows,
+// N = K = 4096, f32 out: 256 x 256 pairs 0.326 ms, 256 x 512 pairs 0.355 ms --
+// eight scatter4 issues per 32-column chunk make the epilogue long enough that
+// it must overlap the next tile's mainloop, which needs two accumulators.)
 struct TileChoice {
     int kernel;  // 1 single, 3 pair 256, 4 pair 512
     int bn;
 };
 
-TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count)
+TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, bool scatter,
+                       int sm_count)
 {
     static const int widths[3] = {256, 128, 64};
     TileChoice best{1, 256};
@@ -344,7 +354,7 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used
     if (N > 256) {
         const int64_t tiles512 = ceil_div(M, 256) * ceil_div(N, 512);
         double cost512 = 0.9 * static_cast<double>(ceil_div(tiles512, pairs) * (512 + 64));
-        if (!c_used && K >= 2048)
+        if (!c_used && !scatter && K >= 2048)
             cost512 *= 0.95;
         if (gather || cost512 < best_cost) {
             best_cost = cost512;
@@ -415,7 +425,8 @@ void set_tile_plan(gemm_plan &p, int kernel, int bn, int64_t M, int64_t N, int s
     p.grid = static_cast<int32_t>(f.cluster * used);
 }
 
-gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count)
+gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count,
+                    bool scatter)
 {
     gemm_plan p;
     std::memset(&p, 0, sizeof(p));
@@ -437,7 +448,7 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, i
         p.grid = static_cast<int32_t>(G);
         return p;
     }
-    const TileChoice c = choose_tile(M, N, K, gather, c_used, sm_count);
+    const TileChoice c = choose_tile(M, N, K, gather, c_used, scatter, sm_count);
     set_tile_plan(p, c.kernel, c.bn, M, N, sm_count);
     return p;
 }
@@ -486,6 +497,9 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
     a.num_tiles = static_cast<int32_t>(plan.tiles);
     a.group_m = 1;
     a.splits = plan.splits;
+    a.scatter = p.scatter ? 1 : 0;
+    a.idx = p.idx;
+    a.d_rows = static_cast<int32_t>(p.d_rows);
     if (plan.splits > 1) {
         Workspace w;
         const size_t bytes = static_cast<size_t>(plan.tiles) * plan.splits * 128 * mp * sizeof(float);
@@ -523,7 +537,7 @@ gemm_status run(const Problem &p)
         return st;
     const bool c_used = p.C != nullptr && p.beta != 0.0f;
     const gemm_plan plan = apply_forced_tile(
-        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count), p, dev->sm_count);
+        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count, p.scatter), p, dev->sm_count);
 
     GemmMaps maps;
     std::memset(&maps, 0, sizeof(maps));
@@ -556,10 +570,16 @@ gemm_status run(const Problem &p)
         if (!ok_a || !ok_b)
             return GEMM_ERR_CUDA;
     }
+    // C and D boxes: 32 x 32, or for scattered rows boxes one row high that
+    // tile::gather4 / tile::scatter4 move four rows at a time (D by TMA only
+    // for float32 output, whose 32-column rows fill the 128-byte swizzle span)
+    const int64_t out_rows = p.scatter ? p.d_rows : p.M;
+    const uint32_t box_rows = p.scatter ? 1u : 32u;
     const bool c_tma = c_used && aligned16(p.C) && (p.ldc * 4) % 16 == 0;
-    const bool d_tma = aligned16(p.D) && (p.ldd * out_size(p.out)) % 16 == 0;
-    if (c_tma && !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.C, p.N, p.M, p.ldc * 4,
-                            32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    const bool d_tma = aligned16(p.D) && (p.ldd * out_size(p.out)) % 16 == 0 &&
+                       (!p.scatter || p.out == GEMM_OUT_F32);
+    if (c_tma && !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.C, p.N, out_rows,
+                            p.ldc * 4, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
         return GEMM_ERR_CUDA;
     if (d_tma) {
         const CUtensorMapDataType dt = p.out == GEMM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -567,7 +587,8 @@ gemm_status run(const Problem &p)
                                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         const CUtensorMapSwizzle sw =
             p.out == GEMM_OUT_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        if (!encode_2d(&maps.d, dt, p.D, p.N, p.M, p.ldd * out_size(p.out), 32, 32, sw))
+        if (!encode_2d(&maps.d, dt, p.D, p.N, out_rows, p.ldd * out_size(p.out), 32, box_rows,
+                       sw))
             return GEMM_ERR_CUDA;
     }
 
@@ -587,6 +608,8 @@ gemm_status run(const Problem &p)
     a.d_tail_direct = (p.N * out_size(p.out)) % 16 != 0 ? 1 : 0;
     a.idx = p.idx;
     a.table_rows = static_cast<int32_t>(p.a_rows);
+    a.scatter = p.scatter ? 1 : 0;
+    a.d_rows = static_cast<int32_t>(p.d_rows);
 
     const cudaError_t e = tcg::launch_tile(bn, pair, form.nsub, form.mc, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -632,6 +655,20 @@ gemm_status gemm_gather_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
     return run(p);
 }
 
+gemm_status gemm_scatter_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16, const void *A,
+                              int64_t lda, const void *B, int64_t ldb, const int32_t *idx,
+                              int64_t d_rows, const float *C, int64_t ldc, void *D, int64_t ldd,
+                              int out, float alpha, float beta, void *stream)
+{
+    if (dtype_is_bf16 != 0 && dtype_is_bf16 != 1)
+        return GEMM_ERR_INVALID_ARG;
+    Problem p{M, N, K, dtype_is_bf16 == 1, A, M, lda, idx, B, ldb, C, ldc, D, ldd,
+              out, alpha, beta, false, static_cast<cudaStream_t>(stream)};
+    p.scatter = true;
+    p.d_rows = d_rows;
+    return run(p);
+}
+
 gemm_status gemm_check_device_status(void *stream)
 {
     DeviceInfo *dev = nullptr;
@@ -667,12 +704,14 @@ const char *gemm_status_string(int status)
     }
 }
 
-gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int gather, int has_c,
+gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int form, int has_c,
                             int sm_count, gemm_plan *plan)
 {
     if (!plan || sm_count < 1 || M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    *plan = make_plan(M, N, K, gather != 0, has_c != 0, sm_count);
+    if (form < 0 || form > 2)
+        return GEMM_ERR_INVALID_ARG;
+    *plan = make_plan(M, N, K, form == 1, has_c != 0, sm_count, form == 2);
     return GEMM_OK;
 }
 

@@ -39,8 +39,10 @@ struct GemmArgs {
     int32_t d_tail_direct;  // N * sizeof(out) is not a multiple of 16: a TMA store would
                             // write the whole 16-byte chunk that straddles column N, so the
                             // chunk that crosses N is stored with plain stores instead
-    const int32_t *idx;
-    int32_t table_rows;
+    const int32_t *idx;     // gathered A rows, or scattered C/D rows
+    int32_t table_rows;     // rows of the gather table
+    int32_t scatter;        // row m of the result goes to row idx[m] of D (and reads C there)
+    int32_t d_rows;         // rows of C and D when scattering
     uint32_t extra_tx;      // test hook: extra bytes expected on the first stage
     uint32_t *status;       // [0] first error code, [1] where a wait gave up
     uint64_t timeout_ns;    // limit of every bounded wait

@@ -37,6 +37,8 @@ struct Problem {
     float alpha, beta;
     bool gather;
     cudaStream_t stream;
+    bool scatter = false;  // row m of the result goes to row idx[m] of D (C read there too)
+    int64_t d_rows = 0;    // rows of C and D when scattering
 };
 
 // Per-device state (SM count, status word address); first call sets it up.
@@ -52,7 +54,8 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dtype, const void *ptr, uint6
 
 CUtensorMapDataType ab_type(bool bf16);
 int64_t ceil_div(int64_t a, int64_t b);
-gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count);
+gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count,
+                    bool scatter = false);
 
 // Kernel arguments common to every kernel (sizes, epilogue, status, timeout).
 void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev);

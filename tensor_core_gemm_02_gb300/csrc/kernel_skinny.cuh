@@ -19,7 +19,8 @@
 //              KBOX * 128-byte runs
 //   warp 1     MMA issuer: tcgen05.mma M=128 N=MP K=16, two TMEM accumulators
 //   warps 2-5  epilogue: tcgen05.ld, partial or final fma.rn(alpha, acc, beta*C)
-//              with coalesced plain loads/stores (lanes walk along N)
+//              with coalesced plain loads/stores (lanes walk along N); with
+//              scattered rows, row m of the result lands in row idx[m] of D
 #pragma once
 
 #include "common.cuh"
@@ -45,7 +46,8 @@ struct SkinnyCfg {
     static constexpr uint32_t OFF_BAR = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t NUM_BARS = 2 * STAGES + 4;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+    static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;  // MP destination rows (scattered rows)
+    static constexpr uint32_t SMEM_BYTES = OFF_ROWS + MP * 4;
     static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = (2 * MP < 32) ? 32 : 2 * MP;
     static constexpr int THREADS = 192;
@@ -68,20 +70,32 @@ __device__ __forceinline__ void epi_bar_sync()
     asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-// Final values of column n: D[m][n] = fma.rn(alpha, v[m], cb[m]) with
-// cb[m] = mul.rn(beta, C[m][n]) loaded beforehand (or D = mul.rn(alpha, v[m])
-// without C).  No loads happen here, so nothing waits behind the stores.
+// Row of C and D for row m of A: m itself, or (scattered rows) the entry
+// that the epilogue staged in shared memory; -1 when nothing is written.
 template <int MP>
-__device__ __forceinline__ void skinny_store(const GemmArgs &a, int32_t n, const float (&v)[MP],
-                                             const float (&cb)[MP])
+__device__ __forceinline__ int32_t skinny_row(const GemmArgs &a, const int32_t *drow, int m)
+{
+    if (a.scatter)
+        return drow[m];
+    return m < a.M ? m : -1;
+}
+
+// Final values of column n: D[r][n] = fma.rn(alpha, v[m], cb[m]) with
+// r = skinny_row(m) and cb[m] = mul.rn(beta, C[r][n]) loaded beforehand (or
+// D = mul.rn(alpha, v[m]) without C).  No loads of C or D happen here, so
+// nothing waits behind the stores.
+template <int MP>
+__device__ __forceinline__ void skinny_store(const GemmArgs &a, const int32_t *drow, int32_t n,
+                                             const float (&v)[MP], const float (&cb)[MP])
 {
     if (n >= a.N)
         return;
 #pragma unroll
     for (int m = 0; m < MP; ++m) {
-        if (m < a.M) {
+        const int32_t r = skinny_row<MP>(a, drow, m);
+        if (r >= 0) {
             const float d = a.has_c ? fma_rn(a.alpha, v[m], cb[m]) : mul_rn(a.alpha, v[m]);
-            const int64_t o = static_cast<int64_t>(m) * a.ldd + n;
+            const int64_t o = static_cast<int64_t>(r) * a.ldd + n;
             if (a.out_kind == kOutF32)
                 static_cast<float *>(a.D)[o] = d;
             else if (a.out_kind == kOutBF16)
@@ -264,6 +278,24 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t q = warp & 3u;
         const bool leader = warp == 2 && lane == 0;
         const int32_t n_local = 32 * static_cast<int32_t>(q) + static_cast<int32_t>(lane);
+        // scattered rows: D row of each row of A, read once (after the set-up
+        // barrier, so after the previous kernel in the stream has finished)
+        int32_t *drow = reinterpret_cast<int32_t *>(gbase + Cfg::OFF_ROWS);
+        if (args.scatter) {
+            const int32_t e = static_cast<int32_t>(threadIdx.x) - 64;  // 0 .. 127
+            if (e < MP) {
+                int32_t r = -1;
+                if (e < args.M) {
+                    r = args.idx[e];
+                    if (r < 0 || r >= args.d_rows) {
+                        record_error(args.status, kStatusIndex, 0);
+                        r = -1;
+                    }
+                }
+                drow[e] = r;
+            }
+            epi_bar_sync();
+        }
         int ab = 0;
         uint32_t aph = 0;
         for (int64_t pos = my_start; pos < my_end;) {
@@ -275,10 +307,12 @@ __global__ void __launch_bounds__(192, 1)
             // beta * C of this column, fetched while the MMAs still run
             float cb[MP];
 #pragma unroll
-            for (int m = 0; m < MP; ++m)
-                cb[m] = (args.has_c && m < args.M && n < args.N)
-                            ? mul_rn(args.beta, args.C[static_cast<int64_t>(m) * args.ldc + n])
+            for (int m = 0; m < MP; ++m) {
+                const int32_t r = skinny_row<MP>(args, drow, m);
+                cb[m] = (args.has_c && r >= 0 && n < args.N)
+                            ? mul_rn(args.beta, args.C[static_cast<int64_t>(r) * args.ldc + n])
                             : 0.f;
+            }
             const bool ok = warp_wait_bounded(accf_bar(ab), aph, abort_flag, args.status,
                                               args.timeout_ns, kWhereEpiAccFull);
             // all four warps agree before the named barriers below
@@ -309,7 +343,7 @@ __global__ void __launch_bounds__(192, 1)
             const int32_t c_hi = skinny_owner(static_cast<int64_t>(t + 1) * nkb - 1, W, G);
             const int32_t parts = c_hi - c_lo + 1;
             if (parts == 1) {
-                skinny_store<MP>(args, n, v, cb);
+                skinny_store<MP>(args, drow, n, v, cb);
                 continue;
             }
             // partial sum of this CTA -> workspace slot (t, blockIdx.x - c_lo)
@@ -356,7 +390,7 @@ __global__ void __launch_bounds__(192, 1)
                         sum[m] += part[m];
                 }
             }
-            skinny_store<MP>(args, n, sum, cb);
+            skinny_store<MP>(args, drow, n, sum, cb);
             if (leader)
                 args.counters[t] = 0u;  // ready for the next call
         }

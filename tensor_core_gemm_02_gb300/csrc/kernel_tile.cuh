@@ -13,7 +13,10 @@
 //   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), optional C box via
 //               TMA, D = fma.rn(alpha, acc, beta*C) ("fma" page), convert,
 //               swizzled shared image, TMA store ("cp.async.bulk.tensor"
-//               page, section "Stores, reductions, and completion").
+//               page, section "Stores, reductions, and completion").  With
+//               scattered rows, C comes in by tile::gather4 and D goes out by
+//               tile::scatter4 at the rows idx[m] (section "Gather4 and
+//               scatter4").
 //
 // PAIR = true runs the same roles on a CTA pair (a cluster of two) sharing
 // one tcgen05.mma.cta_group::2 of M = 256: each CTA loads its own 128 rows of
@@ -439,8 +442,13 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t buf0 = base + Cfg::OFF_EPI + q * 2u * Cfg::EPI_BUF;
         const bool has_c = args.has_c != 0;
         const bool c_tma = has_c && args.c_tma != 0;
+        const bool scatter = args.scatter != 0;
         const bool acc_zero = args.num_k_blocks == 0;
         const int out_kind = args.out_kind;
+        // A 32 x 32 box goes out from lane 0; scattered rows go out as eight
+        // tile::scatter4 copies of four rows, lane g moving rows 4g .. 4g+3
+        // (bulk groups belong to the issuing thread, so each waits for its own).
+        const bool bulk_lane = lane < (scatter ? 8u : 1u);
         // C and D are touched once: their lines go first out of L2, so the A
         // and B panels that neighbouring tiles share stay resident
         const uint64_t epi_policy = l2_policy_evict_first();
@@ -462,18 +470,76 @@ __global__ void __launch_bounds__(192, 1)
             const int32_t nchunks = max(0, min(TILE_N / 32, (args.N - n0 + 31) / 32));
             const int32_t my_row = row0 + (int32_t)lane;
 
-            if (lane == 0)
+            // Row of C and D for this lane: my_row, or idx[my_row] when the
+            // rows are scattered; -1 where nothing is written (past M, or an
+            // index outside D).
+            int32_t d_row = my_row < args.M ? my_row : -1;
+            int32_t grp_rows[4] = {0, 0, 0, 0};  // the four rows lane g < 8 moves
+            bool own_group_whole = true, issue_group_whole = true;
+            if (scatter && rows_ok) {
+                if (d_row >= 0) {
+                    const int32_t v = args.idx[d_row];
+                    if (v < 0 || v >= args.d_rows) {
+                        record_error(args.status, kStatusIndex, 0);
+                        d_row = -1;
+                    } else {
+                        d_row = v;
+                    }
+                }
+                // a group of four rows goes out by one scatter4 only when all
+                // four are written; otherwise its lanes store their own rows
+                const uint32_t written = __ballot_sync(0xffffffffu, d_row >= 0);
+                own_group_whole = ((written >> (lane & ~3u)) & 0xFu) == 0xFu;
+                issue_group_whole = ((written >> (4u * (lane & 7u))) & 0xFu) == 0xFu;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)  // (rows not written read row 0 of C, unused)
+                    grp_rows[r] = __shfl_sync(0xffffffffu, d_row < 0 ? 0 : d_row,
+                                              4 * static_cast<int>(lane & 7u) + r);
+            }
+
+            // the C box of columns [col, col + 32) into buffer j (warp-wide call)
+            auto load_c = [&](int j, int32_t col) {
+                const uint32_t dst = buf0 + j * Cfg::EPI_BUF;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
+                if (!scatter) {
+                    if (lane == 0) {
+                        if (TCG_EPI_EVICT_FIRST)
+                            tma_load_2d_hint(dst, &tmC, c_bar(q, j), col, row0, epi_policy);
+                        else
+                            tma_load_2d(dst, &tmC, c_bar(q, j), col, row0);
+                    }
+                } else {
+                    __syncwarp();
+                    if (lane < 8)
+                        tma_gather4_hint(dst + 512u * lane, &tmC, c_bar(q, j), col, grp_rows[0],
+                                         grp_rows[1], grp_rows[2], grp_rows[3], epi_policy);
+                }
+            };
+            // plain stores of this lane's row, column by column, nothing past column N
+            auto store_direct = [&](const float(&v)[32], int32_t col0) {
+                if (d_row < 0)
+                    return;
+                const int64_t o = static_cast<int64_t>(d_row) * args.ldd + col0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if (col0 + i < args.N) {
+                        if (out_kind == kOutF32)
+                            static_cast<float *>(args.D)[o + i] = v[i];
+                        else if (out_kind == kOutBF16)
+                            static_cast<unsigned short *>(args.D)[o + i] = f32_to_bf16_rn(v[i]);
+                        else
+                            static_cast<unsigned short *>(args.D)[o + i] = f32_to_f16_rn(v[i]);
+                    }
+                }
+            };
+
+            if (bulk_lane)
                 bulk_wait_group_read<0>();  // last tile's stores are done with the buffers
             __syncwarp();
-            if (c_tma && rows_ok && lane == 0) {
-                for (int j = 0; j < 2 && j < nchunks; ++j) {
-                    mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
-                    if (TCG_EPI_EVICT_FIRST)
-                        tma_load_2d_hint(buf0 + j * Cfg::EPI_BUF, &tmC, c_bar(q, j), n0 + 32 * j, row0,
-                                         epi_policy);
-                    else
-                        tma_load_2d(buf0 + j * Cfg::EPI_BUF, &tmC, c_bar(q, j), n0 + 32 * j, row0);
-                }
+            if (c_tma && rows_ok) {
+                for (int j = 0; j < 2 && j < nchunks; ++j)
+                    load_c(j, n0 + 32 * j);
             }
             bool zero_row = acc_zero;
             if (args.gather && my_row < args.M) {
@@ -519,7 +585,10 @@ __global__ void __launch_bounds__(192, 1)
                 const int j = c & 1;
                 const uint32_t buf = buf0 + j * Cfg::EPI_BUF;
                 const int32_t col0 = n0 + 32 * c;
-                const bool d_direct = !args.d_tma || (args.d_tail_direct && col0 + 32 > args.N);
+                // plain stores: D not TMA-aligned, the 16-byte chunk that
+                // straddles column N, or (scattered rows) any partial chunk
+                const bool d_direct = !args.d_tma ||
+                                      ((args.d_tail_direct || scatter) && col0 + 32 > args.N);
                 float v[32];
                 if (c_tma) {
                     if (!warp_wait_bounded(c_bar(q, j), cph[j], abort_flag, args.status,
@@ -539,10 +608,10 @@ __global__ void __launch_bounds__(192, 1)
                         }
                     }
                 } else if (has_c) {
-                    const float *crow = args.C + static_cast<int64_t>(my_row) * args.ldc;
+                    const float *crow = args.C + static_cast<int64_t>(d_row < 0 ? 0 : d_row) * args.ldc;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float cv = (my_row < args.M && col0 + i < args.N) ? crow[col0 + i] : 0.f;
+                        const float cv = (d_row >= 0 && col0 + i < args.N) ? crow[col0 + i] : 0.f;
                         const float a = zero_row ? 0.f : __uint_as_float(acc[i]);
                         v[i] = fma_rn(args.alpha, a, mul_rn(args.beta, cv));
                     }
@@ -552,23 +621,9 @@ __global__ void __launch_bounds__(192, 1)
                         v[i] = mul_rn(args.alpha, zero_row ? 0.f : __uint_as_float(acc[i]));
                 }
                 if (d_direct) {
-                    // plain stores, column by column, nothing past column N
-                    if (my_row < args.M) {
-                        const int64_t o = static_cast<int64_t>(my_row) * args.ldd + col0;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (col0 + i < args.N) {
-                                if (out_kind == kOutF32)
-                                    static_cast<float *>(args.D)[o + i] = v[i];
-                                else if (out_kind == kOutBF16)
-                                    static_cast<unsigned short *>(args.D)[o + i] = f32_to_bf16_rn(v[i]);
-                                else
-                                    static_cast<unsigned short *>(args.D)[o + i] = f32_to_f16_rn(v[i]);
-                            }
-                        }
-                    }
+                    store_direct(v, col0);
                 } else {
-                    if (!c_tma && lane == 0)
+                    if (!c_tma && bulk_lane)
                         bulk_wait_group_read<1>();  // the store two chunks back left buffer j
                     __syncwarp();  // all of C read (in-place D) and buffer j free
                     if (out_kind == kOutF32) {
@@ -594,21 +649,32 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) {
-                        if (TCG_EPI_EVICT_FIRST)
-                            tma_store_2d_hint(&tmD, buf, col0, row0, epi_policy);
-                        else
-                            tma_store_2d(&tmD, buf, col0, row0);
-                        bulk_commit_group();
+                    if (!scatter) {
+                        if (lane == 0) {
+                            if (TCG_EPI_EVICT_FIRST)
+                                tma_store_2d_hint(&tmD, buf, col0, row0, epi_policy);
+                            else
+                                tma_store_2d(&tmD, buf, col0, row0);
+                            bulk_commit_group();
+                        }
+                    } else {
+                        // (scattered rows use TMA stores only for 128-byte rows:
+                        // float32 output, 128-byte swizzled image)
+                        if (lane < 8) {
+                            if (issue_group_whole)
+                                tma_scatter4_hint(&tmD, buf + 512u * lane, col0, grp_rows[0],
+                                                  grp_rows[1], grp_rows[2], grp_rows[3], epi_policy);
+                            bulk_commit_group();
+                        }
+                        if (!own_group_whole)
+                            store_direct(v, col0);
                     }
                 }
-                if (c_tma && c + 2 < nchunks && lane == 0) {
-                    bulk_wait_group_read<0>();  // the store of this chunk is done with buffer j
-                    mbar_arrive_expect_tx(c_bar(q, j), Cfg::EPI_BUF);
-                    if (TCG_EPI_EVICT_FIRST)
-                        tma_load_2d_hint(buf, &tmC, c_bar(q, j), n0 + 32 * (c + 2), row0, epi_policy);
-                    else
-                        tma_load_2d(buf, &tmC, c_bar(q, j), n0 + 32 * (c + 2), row0);
+                if (c_tma && c + 2 < nchunks) {
+                    if (bulk_lane)
+                        bulk_wait_group_read<0>();  // the store of this chunk is done with buffer j
+                    __syncwarp();
+                    load_c(j, n0 + 32 * (c + 2));
                 }
                 __syncwarp();
             }
@@ -624,7 +690,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int j = 0; j < 2; ++j)
                 wait_drain(c_bar(q, j), cph[j], 10000000ull);
         }
-        if (lane == 0)
+        if (bulk_lane)
             bulk_wait_group_all();
         __syncwarp();
     }

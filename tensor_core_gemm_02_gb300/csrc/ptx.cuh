@@ -229,6 +229,33 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *m, uint32_t
         : "memory");
 }
 
+// tma_gather4 with an L2 cache policy
+__device__ __forceinline__ void tma_gather4_hint(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                                 int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                                 int32_t y3, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+        "l"(policy)
+        : "memory");
+}
+
+// Four rows of a shared image (box one row high) -> rows y0..y3 of a 2-D
+// tensor, starting at column x; the dual of tile::gather4 ("cp.async.bulk.tensor"
+// page, section "Gather4 and scatter4").  Completion through bulk groups.
+__device__ __forceinline__ void tma_scatter4_hint(const CUtensorMap *m, uint32_t src, int32_t x,
+                                                  int32_t y0, int32_t y1, int32_t y2, int32_t y3,
+                                                  uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile::scatter4.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3, %4, %5, %6}], [%1], %7;" ::"l"(reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "l"(policy)
+        : "memory");
+}
+
 // Shared image -> global box; completion through bulk groups.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t x,
                                              int32_t y)

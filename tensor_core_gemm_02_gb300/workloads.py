@@ -28,6 +28,12 @@ torch ``.to(torch.bfloat16)``, both round-to-nearest-even):
                    seed 4: table (65536, 4096) N(0,1) -> bf16, idx =
                    integers(0, 65536, 16384) int32 (repeats allowed),
                    B (4096, 4096) 0.02 * N(0,1) -> bf16; no C; fp32 out.
+  scatter_16384_into_65536
+                   seed 5: A (16384, 4096) N(0,1) -> bf16, idx =
+                   permutation(65536)[:16384] int32 (distinct destination
+                   rows), B (4096, 4096) 0.02 * N(0,1) -> bf16; no C; fp32 out
+                   into D (65536, 4096), whose other rows are left as they were.
+                   The row-scattered dual of the gathered workload.
 """
 from __future__ import annotations
 
@@ -42,16 +48,21 @@ OUT_TORCH = {OUT_F32: torch.float32, OUT_BF16: torch.bfloat16, OUT_F16: torch.fl
 
 @dataclass
 class Problem:
-    """One GEMM problem: D = alpha * A @ B.T + beta * C, or the gathered form."""
+    """One GEMM problem: D = alpha * A @ B.T + beta * C, or the gathered form,
+    or (scatter = True) the scattered form D[idx[i]] = alpha * A[i] @ B.T +
+    beta * C[idx[i]] into a D of d_rows rows."""
     name: str
     A: torch.Tensor                 # M x K operand, or the gather table
     B: torch.Tensor                 # N x K
-    C: torch.Tensor | None = None   # M x N float32
-    idx: torch.Tensor | None = None  # int32 row indices into A (gathered form)
+    C: torch.Tensor | None = None   # M x N float32 (scattered: d_rows x N)
+    idx: torch.Tensor | None = None  # int32 rows into A (gathered) or into D (scattered)
     alpha: float = 1.0
     beta: float = 1.0
     out: int = OUT_F32
     meta: dict = field(default_factory=dict)
+    scatter: bool = False
+    d_rows: int = 0
+    D0: torch.Tensor | None = None  # scattered form: D's contents before the call (None: zeros)
 
     @property
     def M(self) -> int:
@@ -133,6 +144,15 @@ def gather_16384_of_65536() -> Problem:
                    beta=0.0, out=OUT_F32)
 
 
+def scatter_16384_into_65536() -> Problem:
+    rng = np.random.default_rng(5)
+    A = _bf16(rng.standard_normal((16384, 4096), dtype=np.float32))
+    idx = torch.from_numpy(rng.permutation(65536)[:16384].astype(np.int32))
+    B = _bf16(0.02 * rng.standard_normal((4096, 4096), dtype=np.float32))
+    return Problem("scatter_16384_into_65536", A, B, None, idx=idx, alpha=1.0, beta=0.0,
+                   out=OUT_F32, scatter=True, d_rows=65536)
+
+
 WORKLOADS = {
     "worked_16x8x32": worked_16x8x32,
     "f16_1024": f16_1024,
@@ -140,13 +160,15 @@ WORKLOADS = {
     "mlp_8192x28672x4096": mlp_8192x28672x4096,
     "skinny_16x28672x4096": skinny_16x28672x4096,
     "gather_16384_of_65536": gather_16384_of_65536,
+    "scatter_16384_into_65536": scatter_16384_into_65536,
 }
 
 
 def random_problem(seed: int, M: int, N: int, K: int, dtype: str = "bf16",
                    values: str = "normal", with_c: bool = False, alpha: float = 1.0,
                    beta: float = 1.0, out: int = OUT_F32, gather_rows: int | None = None,
-                   b_scale: float = 1.0) -> Problem:
+                   b_scale: float = 1.0, scatter_rows: int | None = None,
+                   repeats: bool = False) -> Problem:
     """A seeded problem of any size.
 
     values="quarter": entries are integers in [-4, 4] divided by 4 (the worked
@@ -154,6 +176,10 @@ def random_problem(seed: int, M: int, N: int, K: int, dtype: str = "bf16",
     values="normal": N(0,1) entries (B scaled by b_scale, C N(0,1)).
     gather_rows: if set, A is a table of that many rows and M random indices
     (with repeats) are drawn into it.
+    scatter_rows: if set, the scattered form into a D of that many rows: after
+    the draws above, idx = M distinct rows (permutation(scatter_rows)[:M]; with
+    repeats=True, integers(0, scatter_rows, M)), then C (scatter_rows x N, if
+    with_c) and D0 (scatter_rows x N, rounded to the output type).
     """
     rng = np.random.default_rng(seed)
     a_rows = gather_rows if gather_rows is not None else M
@@ -168,6 +194,17 @@ def random_problem(seed: int, M: int, N: int, K: int, dtype: str = "bf16",
     if gather_rows is not None:
         idx = torch.from_numpy(rng.integers(0, gather_rows, M).astype(np.int32))
     B = _cast(draw((N, K), b_scale), dtype)
+    if scatter_rows is not None:
+        if repeats:
+            ix = rng.integers(0, scatter_rows, M)
+        else:
+            ix = rng.permutation(scatter_rows)[:M]
+        idx = torch.from_numpy(ix.astype(np.int32))
+        C = torch.from_numpy(draw((scatter_rows, N))) if with_c else None
+        D0 = torch.from_numpy(draw((scatter_rows, N))).to(OUT_TORCH[out])
+        return Problem(f"random_scatter_{values}_{M}x{N}x{K}_{dtype}_into_{scatter_rows}", A,
+                       B, C, idx=idx, alpha=alpha, beta=beta, out=out, scatter=True,
+                       d_rows=scatter_rows, D0=D0)
     C = torch.from_numpy(draw((M, N))) if with_c else None
     return Problem(f"random_{values}_{M}x{N}x{K}_{dtype}", A, B, C, idx=idx,
                    alpha=alpha, beta=beta, out=out)

@@ -27,8 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_check_device_status",
-              "gemm_status_string"):
+    for n in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows",
+              "gemm_check_device_status", "gemm_status_string"):
         assert n in names
 
 
@@ -95,6 +95,30 @@ def test_gather_argument_checks(lib):
     assert call(D=A0 + 99 * 128) == 4  # D overlaps the last table row
 
 
+def test_scatter_argument_checks(lib):
+    f = lib.gemm_scatter_rows
+    ok = dict(M=64, N=64, K=64, bf=1, A=A0, lda=64, B=B0, ldb=64, idx=I0, d_rows=100, C=None,
+              ldc=0, D=D0, ldd=64, out=0, alpha=1.0, beta=0.0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["M"], a["N"], a["K"], a["bf"], a["A"], a["lda"], a["B"], a["ldb"], a["idx"],
+                 a["d_rows"], a["C"], a["ldc"], a["D"], a["ldd"], a["out"], a["alpha"],
+                 a["beta"], None)
+
+    assert call(idx=None) == 1
+    assert call(d_rows=0) == 1
+    assert call(d_rows=-3) == 1
+    assert call(bf=2) == 1
+    assert call(d_rows=1 << 31) == 3
+    assert call(idx=I0 + 2) == 2
+    assert call(D=I0 - 64 * 4 * 99) == 4  # the last of D's 100 rows overlaps idx
+    assert call(D=A0 + 63 * 128) == 4  # D overlaps the last row of A
+    # C spans d_rows rows like D: the exact in-place form is allowed, a shifted C is not
+    assert call(C=D0 + 64 * 4 * 99, ldc=64, beta=1.0) == 4
+    assert call(M=0, idx=None) == 0  # nothing to do
+
+
 def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bm, p.bn, p.grid) == (4, 256, 512, 148)
@@ -115,6 +139,15 @@ def test_plan_matches_the_dispatch_rules(lib):
     assert (p.kernel, p.bn) == (5, 256)
     p = binding.gemm_query_plan(16384, 512, 4096, gather=True, sm_count=148)
     assert p.kernel == 4 and p.bn == 512
+    # scattered rows: the same shape takes 256 x 256 pairs (the epilogue must overlap)
+    p = binding.gemm_query_plan(16384, 4096, 4096, scatter=True, sm_count=148)
+    assert (p.kernel, p.bn) == (3, 256)
+    p = binding.gemm_query_plan(16384, 4096, 4096, sm_count=148)
+    assert (p.kernel, p.bn) == (4, 512)
+    p = binding.gemm_query_plan(16, 28672, 4096, scatter=True, sm_count=148)
+    assert p.kernel == 2
+    plan = binding.Plan()
+    assert lib.gemm_query_plan(64, 64, 64, 3, 0, 148, ctypes.byref(plan)) == 1
     p = binding.gemm_query_plan(100, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bn) == (1, 64)
     p = binding.gemm_query_plan(40, 1000, 64, sm_count=148)
