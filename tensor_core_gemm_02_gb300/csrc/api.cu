@@ -361,12 +361,16 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used
             best = TileChoice{4, 512};
         }
     }
-    // Gathered rows with N >= 2048: clusters of eight single CTAs that each
-    // issue an eighth of the gather4s and multicast the rows (16384 rows,
-    // N = K = 4096: 0.474 ms, against 0.489 for clusters of four and 0.563 for
-    // the 256 x 512 pair form, although only 15 clusters of eight, 120 SMs,
-    // fit at once); N >= 1024: clusters of four.
-    if (gather && N >= 2048)
+    // Gathered rows, N >= 1024, K >= 2048: two CTA pairs of 256 x 512 tiles,
+    // each CTA issuing half of its rows' gather4s and multicasting them to its
+    // counterpart in the other pair (16384 of 65536 rows, K = 4096: N = 4096
+    // 0.431 ms against 0.469 for clusters of eight single CTAs and 0.564 for
+    // one pair; N = 1024 0.113 ms against 0.136 for clusters of four).  With
+    // shorter K the single accumulator's drain weighs more: clusters of eight
+    // (N >= 2048; N = 4096, K = 1024: 0.145 against 0.158 ms) or of four.
+    if (gather && N >= 1024 && K >= 2048)
+        best = TileChoice{7, 512};
+    else if (gather && N >= 2048)
         best = TileChoice{6, 256};
     else if (gather && N >= 1024)
         best = TileChoice{5, 256};
@@ -376,14 +380,15 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used
 int skinny_rows(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
 // The tile kernel's form for plan.kernel 1 (single CTAs, 128 x bn tiles),
-// 3 (CTA pairs, 256 x 256), 4 (CTA pairs, 256 x 512: two MMA halves) and
-// 5 (single CTAs, 128 x bn tiles, in clusters of 4 along N sharing A).
+// 3 (CTA pairs, 256 x 256), 4 (CTA pairs, 256 x 512: two MMA halves),
+// 5 / 6 (single CTAs, 128 x bn tiles, in clusters of 4 / 8 along N sharing A)
+// and 7 / 8 (two CTA pairs, 256 x 512 / 256 x 256 tiles, sharing A).
 struct TileForm {
     bool pair;
     int mma_bn;
     int nsub;
-    int mc;       // CTAs sharing one A box by multicast
-    int cluster;  // CTAs per cluster (pairs: 2)
+    int mc;       // CTAs (pairs) sharing one A box by multicast
+    int cluster;  // CTAs per cluster
     int tile_m;
     int tile_n;
 };
@@ -398,6 +403,10 @@ TileForm tile_form(const gemm_plan &p)
         return TileForm{false, p.bn, 1, 4, 4, 128, p.bn};
     if (p.kernel == 6)
         return TileForm{false, p.bn, 1, 8, 8, 128, p.bn};
+    if (p.kernel == 7)
+        return TileForm{true, 256, 2, 2, 4, 256, 512};
+    if (p.kernel == 8)
+        return TileForm{true, 256, 1, 2, 4, 256, 256};
     return TileForm{false, p.bn, 1, 1, 1, 128, p.bn};
 }
 
@@ -517,8 +526,7 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || (plan.kernel != 1 && plan.kernel != 3 && plan.kernel != 4 && plan.kernel != 5 &&
-                    plan.kernel != 6))
+    if (fk == 0 || plan.kernel == 0 || plan.kernel == 2)
         return plan;
     if (fk != 1 && p.K == 0)
         return plan;  // cluster forms need K > 0
@@ -725,7 +733,8 @@ gemm_status gemm_debug_force_tile(int kernel, int bn)
 {
     const bool ok = (kernel == 0) || (kernel == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
                     (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512) ||
-                    (kernel == 5 && (bn == 64 || bn == 256)) || (kernel == 6 && bn == 256);
+                    (kernel == 5 && (bn == 64 || bn == 256)) || (kernel == 6 && bn == 256) ||
+                    (kernel == 7 && bn == 512) || (kernel == 8 && bn == 256);
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

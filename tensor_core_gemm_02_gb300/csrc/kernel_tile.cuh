@@ -18,12 +18,16 @@
 //               tile::scatter4 at the rows idx[m] (section "Gather4 and
 //               scatter4").
 //
-// PAIR = true runs the same roles on a CTA pair (a cluster of two) sharing
+// PAIR = true runs the same roles on a CTA pair (ranks 2p, 2p+1 of a cluster) sharing
 // one tcgen05.mma.cta_group::2 of M = 256: each CTA loads its own 128 rows of
 // A and its own half of the BN rows of B, both report their bytes to the
 // leader CTA's stage barrier, the leader's MMA thread issues for both, and
 // commits arrive in both CTAs.  Each CTA drains its own 128 accumulator rows.
-// Per SM this moves 2/3 of the operand bytes of the single-CTA form.
+// Per SM this moves 2/3 of the operand bytes of the single-CTA form.  With
+// MC = 2 as well, two pairs (a cluster of four) compute neighbouring tiles of
+// one block row and each CTA loads half of its A rows, multicasting them to the
+// CTA with the same role in the other pair: half the A loads (or gather4
+// issues) per CTA at the pair form's bytes per flop.
 //
 // Two accumulators let the epilogue of tile i overlap the mainloop of tile
 // i+1.  NSUB = 2 (a 2*BN-wide tile made of two MMA halves) has room for one
@@ -46,12 +50,12 @@ namespace tcg {
 template <int BN_, int STAGES_, bool PAIR_ = false, int NSUB_ = 1, int MC_ = 1>
 struct TileCfg {
     static constexpr bool PAIR = PAIR_;
-    // MC > 1 (single CTAs only): a cluster of MC CTAs works on MC neighbouring
-    // tiles of one block row; each loads 1/MC of the shared A box and
-    // multicasts it to all, so per CTA the A traffic (or the number of gather4
-    // issues) drops by MC.
+    // MC > 1: MC CTAs (or MC pairs) work on MC neighbouring tiles of one
+    // block row; each loads 1/MC of the shared A box and multicasts it to the
+    // others, so per CTA the A traffic (or the number of gather4 issues) drops
+    // by MC.
     static constexpr int MC = MC_;
-    static constexpr int CLUSTER = PAIR ? 2 : MC;
+    static constexpr int CLUSTER = (PAIR ? 2 : 1) * MC;
     // NSUB = 2: the tile is two BN-wide halves side by side (two MMAs per K
     // step into one 2*BN-column accumulator), so each row of A feeds twice the
     // work; without a second accumulator the epilogue no longer overlaps.
@@ -84,8 +88,8 @@ struct TileCfg {
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(NSUB == 1 || NSUB == 2, "one or two halves");
-    static_assert(MC == 1 || (!PAIR && (MC == 2 || MC == 4 || MC == 8)),
-                  "A multicast over 2, 4 or 8 single CTAs");
+    static_assert(MC == 1 || (!PAIR && (MC == 2 || MC == 4 || MC == 8)) || (PAIR && MC == 2),
+                  "A multicast over 2, 4 or 8 single CTAs, or over two pairs");
     static_assert(!PAIR || (BN % 32 == 0 && BN_LOCAL % 8 == 0), "pair splits B in 8-row groups");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
@@ -129,13 +133,23 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
 
-    // cluster bookkeeping: a pair (rank 0 leads), MC CTAs sharing A, or one CTA
+    // cluster bookkeeping: pairs (ranks 2p, 2p+1; the even rank leads), MC
+    // CTAs or pairs sharing A, or one CTA
     const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
-    const bool leader = !PAIR || rank == 0u;
+    const uint32_t role = PAIR ? (rank & 1u) : 0u;        // place within the pair
+    const uint32_t share = PAIR ? (rank >> 1) : rank;     // which of the MC sharers of A
+    const uint32_t pair_base = rank & ~1u;
+    const bool leader = !PAIR || role == 0u;
     const int32_t cta_set = static_cast<int32_t>(blockIdx.x) / CL;
     const int32_t cta_sets = static_cast<int32_t>(gridDim.x) / CL;
+    // CTAs that receive this CTA's slice of A: all of the cluster, or (pairs)
+    // the CTAs with the same role in every pair
+    constexpr uint16_t kSameRole = PAIR ? static_cast<uint16_t>(0x5555u & kAllCtas) : kAllCtas;
+    const uint16_t a_mask = static_cast<uint16_t>(kSameRole << role);
+    // this pair's two CTAs, as a multicast mask
+    const uint16_t pair_mask = static_cast<uint16_t>(3u << pair_base);
     // the leader's copy of a barrier, as a shared::cluster address
-    auto lead = [&](uint32_t bar) { return PAIR ? mapa_shared(bar, 0u) : bar; };
+    auto lead = [&](uint32_t bar) { return PAIR ? mapa_shared(bar, pair_base) : bar; };
     // raise the abort flag here and (pair) in the peer CTA
     auto raise_abort = [&]() {
         *abort_flag = 1u;
@@ -200,12 +214,12 @@ __global__ void __launch_bounds__(192, 1)
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
             if (MC > 1)
-                nb = nb * MC + static_cast<int32_t>(rank);  // this CTA's tile of the cluster's row
-            const int32_t m0 = mb * Cfg::TILE_M + (PAIR ? static_cast<int32_t>(rank) * Cfg::BM : 0);
-            const int32_t nb0 = nb * TILE_N + (PAIR ? static_cast<int32_t>(rank) * Cfg::BN_LOCAL : 0);
-            // rows of A this CTA fetches: all 128, or (MC > 1) its slice for the cluster
-            const int32_t a_row0 = m0 + (MC > 1 ? static_cast<int32_t>(rank) * Cfg::A_SLICE_ROWS : 0);
-            const uint32_t a_off = MC > 1 ? rank * Cfg::A_SLICE_BYTES : 0u;
+                nb = nb * MC + static_cast<int32_t>(share);  // this CTA's tile of the cluster's row
+            const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(role) * Cfg::BM;
+            const int32_t nb0 = nb * TILE_N + static_cast<int32_t>(role) * Cfg::BN_LOCAL;
+            // rows of A this CTA fetches: all 128, or (MC > 1) its slice for the sharers
+            const int32_t a_row0 = m0 + (MC > 1 ? static_cast<int32_t>(share) * Cfg::A_SLICE_ROWS : 0);
+            const uint32_t a_off = MC > 1 ? share * Cfg::A_SLICE_BYTES : 0u;
             const bool gather_lane = static_cast<int>(lane) < Cfg::A_SLICE_ROWS / 4;
             int32_t rows[4] = {0, 0, 0, 0};
             if (args.gather && gather_lane) {
@@ -241,11 +255,20 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t sb = base + Cfg::OFF_B + s * Cfg::B_BYTES;
                 if (PAIR) {
                     const uint32_t fb = lead(full_bar(s));
-                    if (args.gather)
+                    if (MC > 1) {
+                        if (args.gather) {
+                            if (gather_lane)
+                                tma_gather4_pair_multicast(sa + a_off + lane * 512u, &tmA, fb, k0,
+                                                           rows[0], rows[1], rows[2], rows[3], a_mask);
+                        } else if (lane == 0) {
+                            tma_load_2d_pair_multicast(sa + a_off, &tmA, fb, k0, a_row0, a_mask);
+                        }
+                    } else if (args.gather) {
                         tma_gather4_pair(sa + lane * 512u, &tmA, fb, k0, rows[0], rows[1], rows[2],
                                          rows[3]);
-                    else if (lane == 0)
+                    } else if (lane == 0) {
                         tma_load_2d_pair(sa, &tmA, fb, k0, m0);
+                    }
                     if (lane == 0)
                         for (int j = 0; j < NSUB; ++j)
                             tma_load_2d_pair(sb + j * Cfg::B_SUB_BYTES, &tmB, fb, k0, nb0 + j * BN);
@@ -253,9 +276,9 @@ __global__ void __launch_bounds__(192, 1)
                     if (args.gather) {
                         if (gather_lane)
                             tma_gather4_multicast(sa + a_off + lane * 512u, &tmA, full_bar(s), k0,
-                                                  rows[0], rows[1], rows[2], rows[3], kAllCtas);
+                                                  rows[0], rows[1], rows[2], rows[3], a_mask);
                     } else if (lane == 0) {
-                        tma_load_2d_multicast(sa + a_off, &tmA, full_bar(s), k0, a_row0, kAllCtas);
+                        tma_load_2d_multicast(sa + a_off, &tmA, full_bar(s), k0, a_row0, a_mask);
                     }
                     if (lane == 0)
                         tma_load_2d(sb, &tmB, full_bar(s), k0, nb0);
@@ -319,14 +342,16 @@ __global__ void __launch_bounds__(192, 1)
             // arrive on `bar` (both CTAs of a pair) once the MMAs issued so far finish
             auto commit_to = [&](uint32_t bar) {
                 if (PAIR)
-                    tc_commit_pair_multicast(bar, 3);
+                    tc_commit_pair_multicast(bar, pair_mask);
                 else
                     tc_commit(bar);
             };
             // a stage whose A slices came from the whole cluster is free only
-            // once every CTA of the cluster has consumed it
+            // once every CTA (every pair) of the cluster has consumed it
             auto free_stage = [&](int st) {
-                if (MC > 1)
+                if (MC > 1 && PAIR)
+                    tc_commit_pair_multicast(empty_bar(st), kAllCtas);
+                else if (MC > 1)
                     tc_commit_multicast(empty_bar(st), kAllCtas);
                 else
                     commit_to(empty_bar(st));
@@ -460,8 +485,8 @@ __global__ void __launch_bounds__(192, 1)
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
             if (MC > 1)
-                nb = nb * MC + static_cast<int32_t>(rank);
-            const int32_t m0 = mb * Cfg::TILE_M + (PAIR ? static_cast<int32_t>(rank) * Cfg::BM : 0);
+                nb = nb * MC + static_cast<int32_t>(share);
+            const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(role) * Cfg::BM;
             const int32_t n0 = nb * TILE_N;
             const int32_t row0 = m0 + 32 * (int32_t)q;
             const bool rows_ok = row0 < args.M;
@@ -696,9 +721,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     tc_fence_before_sync();
-    if (MC > 1) {
-        cluster_sync_all();  // no CTA leaves while peers may still multicast into it
-    } else if (PAIR) {
+    if (PAIR) {
         if (threadIdx.x == 0 && *abort_flag)
             raise_abort();  // the peer stops waiting instead of running out of time itself
         if (*abort_flag && !leader) {
@@ -708,10 +731,12 @@ __global__ void __launch_bounds__(192, 1)
             while (global_timer_ns() - t0 < 100000ull) {
             }
         }
-        cluster_sync_all();  // the leader's MMAs read this CTA's shared memory until here
-    } else {
-        __syncthreads();
     }
+    if (CL > 1)
+        cluster_sync_all();  // the leader's MMAs read this CTA's shared memory, and peers
+                             // may multicast into it, until here
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
         if (PAIR)

@@ -1,6 +1,7 @@
 // launch_tile.cu -- instantiations and launcher of the tile kernel: 128 x BN
-// tiles on single CTAs (alone, or in clusters of four sharing A by multicast),
-// or 256 x (NSUB * BN) tiles on CTA pairs (clusters of two).
+// tiles on single CTAs (alone, or in clusters of 4 or 8 sharing A by
+// multicast), or 256 x (NSUB * BN) tiles on CTA pairs (clusters of two, or of
+// four: two pairs sharing A by multicast).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -87,7 +88,7 @@ int max_clusters_impl()
 int tile_stages(int bn, bool pair, int nsub, int mc)
 {
     if (pair)
-        return (bn != 256 || mc != 1) ? 0 : (nsub == 2 ? 4 : 6);
+        return (bn != 256 || (mc != 1 && mc != 2)) ? 0 : (nsub == 2 ? 4 : 6);
     if (nsub != 1)
         return 0;
     if (mc == 4)
@@ -109,6 +110,9 @@ int tile_max_clusters(int bn, bool pair, int nsub, int mc)
     if (pair && bn == 256 && mc == 1)
         return nsub == 2 ? max_clusters_impl<256, 4, true, 2, 1>()
                          : max_clusters_impl<256, 6, true, 1, 1>();
+    if (pair && bn == 256 && mc == 2)
+        return nsub == 2 ? max_clusters_impl<256, 4, true, 2, 2>()
+                         : max_clusters_impl<256, 6, true, 1, 2>();
     if (!pair && nsub == 1 && mc == 4) {
         if (bn == 256)
             return max_clusters_impl<256, 4, false, 1, 4>();
@@ -124,8 +128,11 @@ cudaError_t launch_tile(int bn, bool pair, int nsub, int mc, const GemmMaps &map
                         const GemmArgs &args, int grid, cudaStream_t stream)
 {
     if (pair) {
-        if (bn != 256 || mc != 1)
+        if (bn != 256 || (mc != 1 && mc != 2))
             return cudaErrorInvalidValue;
+        if (mc == 2)
+            return nsub == 2 ? launch_impl<256, 4, true, 2, 2>(maps, args, grid, stream)
+                             : launch_impl<256, 6, true, 1, 2>(maps, args, grid, stream);
         return nsub == 2 ? launch_impl<256, 4, true, 2, 1>(maps, args, grid, stream)
                          : launch_impl<256, 6, true, 1, 1>(maps, args, grid, stream);
     }

@@ -174,6 +174,35 @@ __device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Pair + multicast forms: the box lands at the same offset in every CTA of
+// `mask`, and each destination reports its bytes to its own pair's leader:
+// `bar` is the issuing CTA's pair-leader barrier, and the destinations all
+// play the same role in their pairs as the issuing CTA (same rank parity).
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap *m,
+                                                           uint32_t bar, int32_t x, int32_t y,
+                                                           uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_gather4_pair_multicast(uint32_t dst, const CUtensorMap *m,
+                                                           uint32_t bar, int32_t x, int32_t y0,
+                                                           int32_t y1, int32_t y2, int32_t y3,
+                                                           uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+        ".mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+        "h"(mask)
+        : "memory");
+}
+
 // Multicast forms: the same box lands at the same shared-memory offset of
 // every CTA in `mask` (a cluster of CTAs on this GPU), and each destination's
 // mbarrier at the offset of `bar` receives the byte count.
