@@ -199,6 +199,8 @@ def kernel_key(plan):
         return "tile_gemm_kernel<256, 4, 1, 2, 2>"
     if plan.kernel == 8:
         return "tile_gemm_kernel<256, 6, 1, 1, 2>"
+    if plan.kernel == 9:
+        return "tile_gemm_kernel<256, 4, 1, 2, 4>"
     if plan.kernel in (5, 6):
         return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1, {4 if plan.kernel == 5 else 8}>"
     return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1, 1>"
@@ -469,7 +471,8 @@ def run_ours(args):
                            5: "tile (4-CTA cluster, A multicast)",
                            6: "tile (8-CTA cluster, A multicast)",
                            7: "tile (two CTA pairs, 256 x 512, A multicast)",
-                           8: "tile (two CTA pairs, 256 x 256, A multicast)"}[plan.kernel],
+                           8: "tile (two CTA pairs, 256 x 256, A multicast)",
+                           9: "tile (four CTA pairs, 256 x 512, A multicast)"}[plan.kernel],
                 "tile": f"{plan.bm}x{plan.bn}", "grid": plan.grid, "splits": plan.splits,
                 "roofline": dict(({"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                                    "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}

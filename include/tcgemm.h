@@ -231,7 +231,9 @@ const char *gemm_status_string(int status);
  *           6 = the same in clusters of 8, 7 = two CTA pairs (a cluster of
  *           4) with 256 x 512 tiles side by side along N, each CTA loading
  *           half of its A rows and multicasting them to the CTA in the same
- *           place of the other pair, 8 = the same with 256 x 256 tiles
+ *           place of the other pair, 8 = the same with 256 x 256 tiles,
+ *           9 = four CTA pairs (a cluster of 8) with 256 x 512 tiles, each
+ *           CTA loading a quarter of its A rows for the four
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)
@@ -273,7 +275,8 @@ gemm_status gemm_debug_inject(int mode);
  * bn = 256, kernel 4 = CTA pairs with bn = 512, kernel 5 = clusters of 4
  * single CTAs sharing A with bn in {64, 256}, kernel 6 = clusters of 8
  * with bn = 256, kernel 7 = two CTA pairs sharing A with bn = 512,
- * kernel 8 = two CTA pairs sharing A with bn = 256, kernel 0 = automatic
+ * kernel 8 = two CTA pairs sharing A with bn = 256, kernel 9 = four CTA pairs
+ * sharing A with bn = 512, kernel 0 = automatic
  * choice (the default).  Problems the forced form cannot run (the M <= 64 skinny
  * path; K == 0 for pairs) keep the automatic choice.  Returns
  * GEMM_ERR_INVALID_ARG for other values.

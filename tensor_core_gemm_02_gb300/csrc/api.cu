@@ -361,14 +361,19 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used
             best = TileChoice{4, 512};
         }
     }
-    // Gathered rows, N >= 1024, K >= 2048: two CTA pairs of 256 x 512 tiles,
-    // each CTA issuing half of its rows' gather4s and multicasting them to its
-    // counterpart in the other pair (16384 of 65536 rows, K = 4096: N = 4096
-    // 0.431 ms against 0.469 for clusters of eight single CTAs and 0.564 for
-    // one pair; N = 1024 0.113 ms against 0.136 for clusters of four).  With
-    // shorter K the single accumulator's drain weighs more: clusters of eight
-    // (N >= 2048; N = 4096, K = 1024: 0.145 against 0.158 ms) or of four.
-    if (gather && N >= 1024 && K >= 2048)
+    // Gathered rows, K >= 2048: CTA pairs of 256 x 512 tiles side by side
+    // along N, each CTA issuing its share of its rows' gather4s and
+    // multicasting them to the CTAs in the same place of the other pairs --
+    // four pairs for N >= 2048, two for N >= 1024 (16384 of 65536 rows,
+    // K = 4096, N = 4096: four pairs 0.391 ms, two 0.431, clusters of eight
+    // single CTAs 0.469, one pair 0.564; N = 1024: two pairs 0.113 ms,
+    // clusters of four single CTAs 0.136).  With shorter K the single
+    // accumulator's drain weighs more: clusters of eight single CTAs
+    // (N >= 2048; N = 4096, K = 1024: 0.145 against 0.158 ms for two pairs)
+    // or of four.
+    if (gather && N >= 2048 && K >= 2048)
+        best = TileChoice{9, 512};
+    else if (gather && N >= 1024 && K >= 2048)
         best = TileChoice{7, 512};
     else if (gather && N >= 2048)
         best = TileChoice{6, 256};
@@ -407,6 +412,8 @@ TileForm tile_form(const gemm_plan &p)
         return TileForm{true, 256, 2, 2, 4, 256, 512};
     if (p.kernel == 8)
         return TileForm{true, 256, 1, 2, 4, 256, 256};
+    if (p.kernel == 9)
+        return TileForm{true, 256, 2, 4, 8, 256, 512};
     return TileForm{false, p.bn, 1, 1, 1, 128, p.bn};
 }
 
@@ -734,7 +741,8 @@ gemm_status gemm_debug_force_tile(int kernel, int bn)
     const bool ok = (kernel == 0) || (kernel == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
                     (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512) ||
                     (kernel == 5 && (bn == 64 || bn == 256)) || (kernel == 6 && bn == 256) ||
-                    (kernel == 7 && bn == 512) || (kernel == 8 && bn == 256);
+                    (kernel == 7 && bn == 512) || (kernel == 8 && bn == 256) ||
+                    (kernel == 9 && bn == 512);
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

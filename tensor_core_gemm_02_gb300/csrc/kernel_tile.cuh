@@ -88,8 +88,9 @@ struct TileCfg {
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(NSUB == 1 || NSUB == 2, "one or two halves");
-    static_assert(MC == 1 || (!PAIR && (MC == 2 || MC == 4 || MC == 8)) || (PAIR && MC == 2),
-                  "A multicast over 2, 4 or 8 single CTAs, or over two pairs");
+    static_assert(MC == 1 || (!PAIR && (MC == 2 || MC == 4 || MC == 8)) ||
+                      (PAIR && (MC == 2 || MC == 4)),
+                  "A multicast over 2, 4 or 8 single CTAs, or over two or four pairs");
     static_assert(!PAIR || (BN % 32 == 0 && BN_LOCAL % 8 == 0), "pair splits B in 8-row groups");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");

@@ -88,7 +88,8 @@ int max_clusters_impl()
 int tile_stages(int bn, bool pair, int nsub, int mc)
 {
     if (pair)
-        return (bn != 256 || (mc != 1 && mc != 2)) ? 0 : (nsub == 2 ? 4 : 6);
+        return (bn != 256 || (mc != 1 && mc != 2 && mc != 4) || (mc == 4 && nsub != 2))
+                   ? 0 : (nsub == 2 ? 4 : 6);
     if (nsub != 1)
         return 0;
     if (mc == 4)
@@ -113,6 +114,8 @@ int tile_max_clusters(int bn, bool pair, int nsub, int mc)
     if (pair && bn == 256 && mc == 2)
         return nsub == 2 ? max_clusters_impl<256, 4, true, 2, 2>()
                          : max_clusters_impl<256, 6, true, 1, 2>();
+    if (pair && bn == 256 && mc == 4 && nsub == 2)
+        return max_clusters_impl<256, 4, true, 2, 4>();
     if (!pair && nsub == 1 && mc == 4) {
         if (bn == 256)
             return max_clusters_impl<256, 4, false, 1, 4>();
@@ -128,8 +131,10 @@ cudaError_t launch_tile(int bn, bool pair, int nsub, int mc, const GemmMaps &map
                         const GemmArgs &args, int grid, cudaStream_t stream)
 {
     if (pair) {
-        if (bn != 256 || (mc != 1 && mc != 2))
+        if (bn != 256 || (mc != 1 && mc != 2 && mc != 4) || (mc == 4 && nsub != 2))
             return cudaErrorInvalidValue;
+        if (mc == 4)
+            return launch_impl<256, 4, true, 2, 4>(maps, args, grid, stream);
         if (mc == 2)
             return nsub == 2 ? launch_impl<256, 4, true, 2, 2>(maps, args, grid, stream)
                              : launch_impl<256, 6, true, 1, 2>(maps, args, grid, stream);

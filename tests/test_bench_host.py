@@ -63,6 +63,8 @@ def test_kernel_keys_name_the_launched_instance():
     p = binding.gemm_query_plan(1024, 1024, 1024, sm_count=148)
     assert bench.kernel_key(p) == "tile_gemm_kernel<64, 8, 0, 1, 1>"
     p = binding.gemm_query_plan(16384, 4096, 4096, gather=True, sm_count=148)
+    assert bench.kernel_key(p) == "tile_gemm_kernel<256, 4, 1, 2, 4>"
+    p = binding.gemm_query_plan(16384, 1024, 4096, gather=True, sm_count=148)
     assert bench.kernel_key(p) == "tile_gemm_kernel<256, 4, 1, 2, 2>"
     p = binding.gemm_query_plan(16384, 1024, 1024, gather=True, sm_count=148)
     assert bench.kernel_key(p) == "tile_gemm_kernel<256, 4, 0, 1, 4>"

@@ -134,7 +134,7 @@ def test_plan_matches_the_dispatch_rules(lib):
     # stream-K shares of 224 * 64 k-blocks over 148 CTAs: at most 2 per tile
     assert p.splits == 2
     p = binding.gemm_query_plan(16384, 4096, 4096, gather=True, sm_count=148)
-    assert (p.kernel, p.bm, p.bn, p.grid) == (7, 256, 512, 148) and p.tiles == 64 * 8
+    assert (p.kernel, p.bm, p.bn, p.grid) == (9, 256, 512, 144) and p.tiles == 64 * 8
     p = binding.gemm_query_plan(16384, 1024, 4096, gather=True, sm_count=148)
     assert (p.kernel, p.bn) == (7, 512)
     p = binding.gemm_query_plan(16384, 4096, 1024, gather=True, sm_count=148)
