@@ -219,6 +219,8 @@ def l2_flush(buf):
 
 def launch(p, dev_tensors):
     A, B, C, idx, D = dev_tensors
+    if p.accumulate:
+        return binding.gemm_accumulate(A, B, D, alpha=p.alpha)
     if p.scatter:
         return binding.gemm_scatter_rows(A, B, idx, D, C, alpha=p.alpha, beta=p.beta)
     if idx is not None:
@@ -233,7 +235,9 @@ def to_device(p, dev):
     B = p.B.to(dev)
     C = p.C.to(dev) if p.C is not None else None
     idx = p.idx.to(dev) if p.idx is not None else None
-    if p.scatter:
+    if p.accumulate:
+        D = p.D0.to(dev).contiguous()
+    elif p.scatter:
         D = (p.D0.to(dev) if p.D0 is not None else
              torch.zeros((p.d_rows, p.N), dtype=workloads.OUT_TORCH[p.out], device=dev))
     else:
@@ -243,12 +247,13 @@ def to_device(p, dev):
 
 def algorithmic_bytes(p):
     """Bytes the GEMM must move at least once: A (or the gathered rows), B, C, D, idx
-    (scattered form: the M rows of C read and of D written)."""
+    (scattered form: the M rows of C read and of D written; accumulating form: D
+    read and written)."""
     esz = p.A.element_size()
     a = p.M * p.K * esz
     b = p.N * p.K * esz
     c = p.M * p.N * 4 if (p.C is not None and p.beta != 0) else 0
-    d = p.M * p.N * workloads.OUT_TORCH[p.out].itemsize
+    d = p.M * p.N * workloads.OUT_TORCH[p.out].itemsize * (2 if p.accumulate else 1)
     i = p.M * 4 if p.idx is not None else 0
     return a + b + c + d + i
 
@@ -458,11 +463,12 @@ def run_ours(args):
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
         variants = {}
         for name in ("f16_1024", "mlp_8192x28672x4096", "skinny_16x28672x4096",
-                     "gather_16384_of_65536", "scatter_16384_into_65536"):
+                     "gather_16384_of_65536", "scatter_16384_into_65536",
+                     "skinny_accumulate_16x28672x4096"):
             vp, ms, plan, how = time_variant(name, dev, args.variant_reps, flush)
             tflops = vp.flops / (ms * 1e-3) / 1e12
             gbs = algorithmic_bytes(vp) / (ms * 1e-3) / 1e9
-            hbm_bound = name in ("skinny_16x28672x4096",)
+            hbm_bound = name in ("skinny_16x28672x4096", "skinny_accumulate_16x28672x4096")
             variants[name] = {
                 "ms": round(ms, 5), "TFLOP/s": round(tflops, 2), "GB/s": round(gbs, 1),
                 "algorithmic_bytes": algorithmic_bytes(vp),

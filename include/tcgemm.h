@@ -168,6 +168,33 @@ gemm_status gemm_scatter_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16
                               int out, float alpha, float beta, void *stream);
 
 /*
+ * Accumulating form: D[i][j] += alpha * sum_k A[i][k] * B[j][k] for float32 D.
+ * The result is added into D by TMA reduce-add stores ("cp.async.bulk.tensor"
+ * page, section "Stores, reductions, and completion": the reduction form adds
+ * the shared image into the global box, whose contents are the starting
+ * value, so the caller initialises D).  Rounding: each element receives
+ * D + mul.rn(alpha, acc) with one float32 add per part of the K sum; for
+ * M > 64 there is one part, so the result is deterministic; for M <= 64 the
+ * K sum of a tile may be split over several CTAs, each adding its part (in an
+ * order that is not specified, so the last bits may differ from call to call
+ * unless every partial sum is exact).  Unlike fma.rn(alpha, acc, beta * C)
+ * this is two roundings (the product, then the add).
+ *
+ *  A, lda, B, ldb  as in gemm_f16; dtype_is_bf16 as in gemm_gather_rows.
+ *  D, ldd          M x N float32, 4-byte aligned; added into through TMA when
+ *                  16-byte aligned with a pitch that is a multiple of 16 bytes,
+ *                  otherwise (and for the last column chunk when N * 4 is not
+ *                  a multiple of 16) with float32 atomic adds.
+ *  K == 0          adds nothing (GEMM_OK, no launch).
+ *  Errors as gemm_f16; D must not overlap A or B.
+ */
+gemm_status gemm_accumulate(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
+                            const void *A, int64_t lda,
+                            const void *B, int64_t ldb,
+                            float *D, int64_t ldd,
+                            float alpha, void *stream);
+
+/*
  * Allocation-free variant of the skinny (M <= 64) path.  The source pages have
  * no counterpart to this entry point; it exists for callers that cannot call
  * cudaMalloc where they run the GEMM: code whose device memory is owned by

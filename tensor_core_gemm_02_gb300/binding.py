@@ -55,6 +55,7 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_bf16.argtypes = plain
     lib.gemm_gather_rows.argtypes = [i64, i64, i64, i32, vp, i64, i64, vp, vp, i64, vp, i64,
                                      vp, i64, i32, f32, f32, vp]
+    lib.gemm_accumulate.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, f32, vp]
     lib.gemm_scatter_rows.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
                                       vp, i64, i32, f32, f32, vp]
     lib.gemm_skinny_noalloc.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
@@ -66,7 +67,7 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_set_wait_timeout.argtypes = [ctypes.c_uint64]
     lib.gemm_debug_inject.argtypes = [i32]
     lib.gemm_debug_force_tile.argtypes = [i32, i32]
-    for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows",
+    for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows", "gemm_accumulate",
                  "gemm_skinny_noalloc",
                  "gemm_check_device_status",
                  "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject",
@@ -190,6 +191,23 @@ def gemm_scatter_rows(A, B, idx, D, C=None, *, alpha=1.0, beta=1.0, stream=None)
         _ptr(idx), d_rows, _ptr(C), _ld(C) if C is not None else 0, _ptr(D), _ld(D), out,
         float(alpha), float(beta), _stream_ptr(stream))
     _check(st, "gemm_scatter_rows")
+    return D
+
+
+def gemm_accumulate(A, B, D, *, alpha=1.0, stream=None):
+    """D += alpha * A @ B.T, added into float32 D (M x N) in place.  Returns D."""
+    if A.dtype not in (torch.float16, torch.bfloat16) or B.dtype != A.dtype:
+        raise TypeError("A and B must both be f16 or both bf16")
+    if D is None or D.dtype != torch.float32 or D.dim() != 2:
+        raise TypeError("D must be a 2-D float32 tensor")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("A, B and D disagree on M, N or K")
+    st = load_library().gemm_accumulate(
+        M, N, K, 1 if A.dtype == torch.bfloat16 else 0, _ptr(A), _ld(A), _ptr(B), _ld(B),
+        _ptr(D), _ld(D), float(alpha), _stream_ptr(stream))
+    _check(st, "gemm_accumulate")
     return D
 
 

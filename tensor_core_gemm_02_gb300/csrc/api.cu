@@ -264,6 +264,8 @@ gemm_status validate(const Problem &p, bool *empty)
         return GEMM_ERR_INVALID_ARG;
     if (p.scatter && (!p.idx || p.d_rows < 1 || p.gather))
         return GEMM_ERR_INVALID_ARG;
+    if (p.reduce && (p.out != GEMM_OUT_F32 || p.gather || p.scatter))
+        return GEMM_ERR_INVALID_ARG;
     if (p.d_rows > kMaxDim)
         return GEMM_ERR_UNSUPPORTED;
     // rows of C and D: M, or the rows of the matrix the result is scattered into
@@ -516,7 +518,8 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
     a.scatter = p.scatter ? 1 : 0;
     a.idx = p.idx;
     a.d_rows = static_cast<int32_t>(p.d_rows);
-    if (plan.splits > 1) {
+    a.reduce = p.reduce ? 1 : 0;
+    if (plan.splits > 1 && !p.reduce) {  // (the accumulating form adds every part into D)
         Workspace w;
         const size_t bytes = static_cast<size_t>(plan.tiles) * plan.splits * 128 * mp * sizeof(float);
         gemm_status st = get_workspace(dev->index, p.stream, bytes, static_cast<size_t>(plan.tiles), &w);
@@ -547,6 +550,8 @@ gemm_status run(const Problem &p)
     gemm_status st = validate(p, &empty);
     if (st != GEMM_OK || empty)
         return st;
+    if (p.reduce && p.K == 0)
+        return GEMM_OK;  // adding zero
     DeviceInfo *dev = nullptr;
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
@@ -625,6 +630,7 @@ gemm_status run(const Problem &p)
     a.table_rows = static_cast<int32_t>(p.a_rows);
     a.scatter = p.scatter ? 1 : 0;
     a.d_rows = static_cast<int32_t>(p.d_rows);
+    a.reduce = p.reduce ? 1 : 0;
 
     const cudaError_t e = tcg::launch_tile(bn, pair, form.nsub, form.mc, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -681,6 +687,18 @@ gemm_status gemm_scatter_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16
               out, alpha, beta, false, static_cast<cudaStream_t>(stream)};
     p.scatter = true;
     p.d_rows = d_rows;
+    return run(p);
+}
+
+gemm_status gemm_accumulate(int64_t M, int64_t N, int64_t K, int dtype_is_bf16, const void *A,
+                            int64_t lda, const void *B, int64_t ldb, float *D, int64_t ldd,
+                            float alpha, void *stream)
+{
+    if (dtype_is_bf16 != 0 && dtype_is_bf16 != 1)
+        return GEMM_ERR_INVALID_ARG;
+    Problem p{M, N, K, dtype_is_bf16 == 1, A, M, lda, nullptr, B, ldb, nullptr, 0, D, ldd,
+              GEMM_OUT_F32, alpha, 0.0f, false, static_cast<cudaStream_t>(stream)};
+    p.reduce = true;
     return run(p);
 }
 

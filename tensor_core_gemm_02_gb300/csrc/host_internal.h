@@ -39,6 +39,7 @@ struct Problem {
     cudaStream_t stream;
     bool scatter = false;  // row m of the result goes to row idx[m] of D (C read there too)
     int64_t d_rows = 0;    // rows of C and D when scattering
+    bool reduce = false;   // D += alpha * A * B^T into float32 D (no C)
 };
 
 // Per-device state (SM count, status word address); first call sets it up.

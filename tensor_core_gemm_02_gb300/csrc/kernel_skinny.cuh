@@ -20,7 +20,9 @@
 //   warp 1     MMA issuer: tcgen05.mma M=128 N=MP K=16, two TMEM accumulators
 //   warps 2-5  epilogue: tcgen05.ld, partial or final fma.rn(alpha, acc, beta*C)
 //              with coalesced plain loads/stores (lanes walk along N); with
-//              scattered rows, row m of the result lands in row idx[m] of D
+//              scattered rows, row m of the result lands in row idx[m] of D;
+//              in the accumulating form every part is added into D with
+//              float32 atomic adds instead (no workspace, no last arriver)
 #pragma once
 
 #include "common.cuh"
@@ -103,6 +105,23 @@ __device__ __forceinline__ void skinny_store(const GemmArgs &a, const int32_t *d
             else
                 static_cast<unsigned short *>(a.D)[o] = f32_to_f16_rn(d);
         }
+    }
+}
+
+// Accumulating form: add mul.rn(alpha, v[m]) into D[r][n] (float32 atomic
+// adds, so the parts of a split tile need no workspace and no ordering).
+template <int MP>
+__device__ __forceinline__ void skinny_add(const GemmArgs &a, const int32_t *drow, int32_t n,
+                                           const float (&v)[MP])
+{
+    if (n >= a.N)
+        return;
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+        const int32_t r = skinny_row<MP>(a, drow, m);
+        if (r >= 0)
+            atomicAdd(static_cast<float *>(a.D) + static_cast<int64_t>(r) * a.ldd + n,
+                      mul_rn(a.alpha, v[m]));
     }
 }
 
@@ -339,6 +358,10 @@ __global__ void __launch_bounds__(192, 1)
                 aph ^= 1u;
             }
 
+            if (args.reduce) {
+                skinny_add<MP>(args, drow, n, v);  // every part adds itself into D
+                continue;
+            }
             const int32_t c_lo = skinny_owner(static_cast<int64_t>(t) * nkb, W, G);
             const int32_t c_hi = skinny_owner(static_cast<int64_t>(t + 1) * nkb - 1, W, G);
             const int32_t parts = c_hi - c_lo + 1;

@@ -16,7 +16,8 @@
 //               page, section "Stores, reductions, and completion").  With
 //               scattered rows, C comes in by tile::gather4 and D goes out by
 //               tile::scatter4 at the rows idx[m] (section "Gather4 and
-//               scatter4").
+//               scatter4").  In the accumulating form the box is added into
+//               D by a TMA reduce-add instead of stored.
 //
 // PAIR = true runs the same roles on a CTA pair (ranks 2p, 2p+1 of a cluster) sharing
 // one tcgen05.mma.cta_group::2 of M = 256: each CTA loads its own 128 rows of
@@ -469,6 +470,7 @@ __global__ void __launch_bounds__(192, 1)
         const bool has_c = args.has_c != 0;
         const bool c_tma = has_c && args.c_tma != 0;
         const bool scatter = args.scatter != 0;
+        const bool reduce = args.reduce != 0;  // D += alpha * acc (float32 D, no C)
         const bool acc_zero = args.num_k_blocks == 0;
         const int out_kind = args.out_kind;
         // A 32 x 32 box goes out from lane 0; scattered rows go out as eight
@@ -542,7 +544,8 @@ __global__ void __launch_bounds__(192, 1)
                                          grp_rows[1], grp_rows[2], grp_rows[3], epi_policy);
                 }
             };
-            // plain stores of this lane's row, column by column, nothing past column N
+            // plain stores (reduce: float32 atomic adds) of this lane's row,
+            // column by column, nothing past column N
             auto store_direct = [&](const float(&v)[32], int32_t col0) {
                 if (d_row < 0)
                     return;
@@ -550,7 +553,9 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     if (col0 + i < args.N) {
-                        if (out_kind == kOutF32)
+                        if (reduce)
+                            atomicAdd(static_cast<float *>(args.D) + o + i, v[i]);
+                        else if (out_kind == kOutF32)
                             static_cast<float *>(args.D)[o + i] = v[i];
                         else if (out_kind == kOutBF16)
                             static_cast<unsigned short *>(args.D)[o + i] = f32_to_bf16_rn(v[i]);
@@ -677,7 +682,9 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (!scatter) {
                         if (lane == 0) {
-                            if (TCG_EPI_EVICT_FIRST)
+                            if (reduce)
+                                tma_reduce_add_2d_hint(&tmD, buf, col0, row0, epi_policy);
+                            else if (TCG_EPI_EVICT_FIRST)
                                 tma_store_2d_hint(&tmD, buf, col0, row0, epi_policy);
                             else
                                 tma_store_2d(&tmD, buf, col0, row0);

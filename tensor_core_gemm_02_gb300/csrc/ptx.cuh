@@ -285,6 +285,19 @@ __device__ __forceinline__ void tma_scatter4_hint(const CUtensorMap *m, uint32_t
         : "memory");
 }
 
+// Shared image added element by element into the global box (float32 add at
+// L2); the destination holds the starting value ("cp.async.bulk.tensor" page,
+// section "Stores, reductions, and completion").  Completion through bulk groups.
+__device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap *m, uint32_t src, int32_t x,
+                                                       int32_t y, uint64_t policy)
+{
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
 // Shared image -> global box; completion through bulk groups.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t x,
                                              int32_t y)

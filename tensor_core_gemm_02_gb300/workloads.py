@@ -34,6 +34,9 @@ torch ``.to(torch.bfloat16)``, both round-to-nearest-even):
                    rows), B (4096, 4096) 0.02 * N(0,1) -> bf16; no C; fp32 out
                    into D (65536, 4096), whose other rows are left as they were.
                    The row-scattered dual of the gathered workload.
+  skinny_accumulate_16x28672x4096
+                   the skinny draws; D starts as C[:16] and receives
+                   D += 0.5 * A @ B.T (the accumulating form, no C operand).
 """
 from __future__ import annotations
 
@@ -62,7 +65,8 @@ class Problem:
     meta: dict = field(default_factory=dict)
     scatter: bool = False
     d_rows: int = 0
-    D0: torch.Tensor | None = None  # scattered form: D's contents before the call (None: zeros)
+    D0: torch.Tensor | None = None  # scattered / accumulating forms: D before the call
+    accumulate: bool = False        # D += alpha * A @ B.T into float32 D = D0
 
     @property
     def M(self) -> int:
@@ -144,6 +148,12 @@ def gather_16384_of_65536() -> Problem:
                    beta=0.0, out=OUT_F32)
 
 
+def skinny_accumulate_16x28672x4096() -> Problem:
+    A, B, C = _mlp_draws(16)
+    return Problem("skinny_accumulate_16x28672x4096", A[:16].contiguous(), B, None, alpha=0.5,
+                   beta=0.0, out=OUT_F32, D0=C, accumulate=True)
+
+
 def scatter_16384_into_65536() -> Problem:
     rng = np.random.default_rng(5)
     A = _bf16(rng.standard_normal((16384, 4096), dtype=np.float32))
@@ -161,6 +171,7 @@ WORKLOADS = {
     "skinny_16x28672x4096": skinny_16x28672x4096,
     "gather_16384_of_65536": gather_16384_of_65536,
     "scatter_16384_into_65536": scatter_16384_into_65536,
+    "skinny_accumulate_16x28672x4096": skinny_accumulate_16x28672x4096,
 }
 
 

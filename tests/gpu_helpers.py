@@ -21,6 +21,10 @@ def run(p, D=None, stream=None):
     """Launch the problem on the GPU through the library; returns D (device)."""
     A, B = p.A.to(DEV), p.B.to(DEV)
     C = p.C.to(DEV) if p.C is not None else None
+    if p.accumulate:
+        if D is None:
+            D = p.D0.to(DEV).contiguous()
+        return binding.gemm_accumulate(A, B, D, alpha=p.alpha, stream=stream)
     if p.scatter:
         if D is None:
             D = (p.D0.to(DEV) if p.D0 is not None else

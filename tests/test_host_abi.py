@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows",
-              "gemm_check_device_status", "gemm_status_string"):
+              "gemm_accumulate", "gemm_check_device_status", "gemm_status_string"):
         assert n in names
 
 
@@ -117,6 +117,22 @@ def test_scatter_argument_checks(lib):
     # C spans d_rows rows like D: the exact in-place form is allowed, a shifted C is not
     assert call(C=D0 + 64 * 4 * 99, ldc=64, beta=1.0) == 4
     assert call(M=0, idx=None) == 0  # nothing to do
+
+
+def test_accumulate_argument_checks(lib):
+    f = lib.gemm_accumulate
+
+    def call(M=64, N=64, K=64, bf=1, A=A0, lda=64, B=B0, ldb=64, D=D0, ldd=64, alpha=1.0):
+        return f(M, N, K, bf, A, lda, B, ldb, D, ldd, alpha, None)
+
+    assert call(D=None) == 1
+    assert call(bf=2) == 1
+    assert call(ldd=63) == 1
+    assert call(D=D0 + 2) == 2
+    assert call(D=A0 + 64) == 4
+    assert call(D=B0) == 4
+    assert call(M=0) == 0
+    assert call(K=0) == 0  # adds nothing, launches nothing
 
 
 def test_plan_matches_the_dispatch_rules(lib):
