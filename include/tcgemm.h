@@ -260,7 +260,9 @@ const char *gemm_status_string(int status);
  *           half of its A rows and multicasting them to the CTA in the same
  *           place of the other pair, 8 = the same with 256 x 256 tiles,
  *           9 = four CTA pairs (a cluster of 8) with 256 x 512 tiles, each
- *           CTA loading a quarter of its A rows for the four
+ *           CTA loading a quarter of its A rows for the four, 10 = the
+ *           warp-level kernel (mma.sync.m16n8k16, one 16 x 8 block of D per
+ *           warp; problems of at most 2^20 multiply-adds)
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)
@@ -303,7 +305,8 @@ gemm_status gemm_debug_inject(int mode);
  * single CTAs sharing A with bn in {64, 256}, kernel 6 = clusters of 8
  * with bn = 256, kernel 7 = two CTA pairs sharing A with bn = 512,
  * kernel 8 = two CTA pairs sharing A with bn = 256, kernel 9 = four CTA pairs
- * sharing A with bn = 512, kernel 0 = automatic
+ * sharing A with bn = 512, kernel 10 = the warp-level kernel with bn = 8 (it
+ * then runs every problem, the skinny ones too), kernel 0 = automatic
  * choice (the default).  Problems the forced form cannot run (the M <= 64 skinny
  * path; K == 0 for pairs) keep the automatic choice.  Returns
  * GEMM_ERR_INVALID_ARG for other values.

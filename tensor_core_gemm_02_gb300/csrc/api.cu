@@ -19,6 +19,15 @@
 
 #include "host_internal.h"
 
+// Fewest K blocks a CTA of the skinny kernel is given (when there are fewer
+// than SMs x this many blocks, fewer CTAs run).  Measured per launch from a
+// replayed CUDA graph: 1 -> 8 takes 64 x 512 x 512 from 16.4 to 11.1 us and
+// 32 x 8192 x 1024 from 13.3 to 10.2 us; 4 and 16 were each worse on some
+// shapes; 16 x 28672 x 4096 is unchanged.
+#ifndef TCG_SKINNY_MIN_KB
+#define TCG_SKINNY_MIN_KB 8
+#endif
+
 // Height, in block rows, of the groups the tile order walks through (L2 reuse).
 #ifndef TCG_GROUP_M
 #define TCG_GROUP_M 16
@@ -386,6 +395,9 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used
 
 int skinny_rows(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
+// Problems with at most this many multiply-adds run on the warp-level kernel.
+constexpr int64_t kTinyWork = int64_t(1) << 20;
+
 // The tile kernel's form for plan.kernel 1 (single CTAs, 128 x bn tiles),
 // 3 (CTA pairs, 256 x 256), 4 (CTA pairs, 256 x 512: two MMA halves),
 // 5 / 6 (single CTAs, 128 x bn tiles, in clusters of 4 / 8 along N sharing A)
@@ -443,6 +455,18 @@ void set_tile_plan(gemm_plan &p, int kernel, int bn, int64_t M, int64_t N, int s
     p.grid = static_cast<int32_t>(f.cluster * used);
 }
 
+// The warp-level kernel: 16 x 8 blocks, four per CTA.
+void set_tiny_plan(gemm_plan &p, int64_t M, int64_t N)
+{
+    p.kernel = 10;
+    p.bm = 16;
+    p.bn = 8;
+    p.stages = 0;
+    p.tiles = ceil_div(M, 16) * ceil_div(N, 8);
+    p.splits = 1;
+    p.grid = static_cast<int32_t>(ceil_div(p.tiles, tcg::tiny_warps_per_cta()));
+}
+
 gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count,
                     bool scatter)
 {
@@ -450,13 +474,22 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, i
     std::memset(&p, 0, sizeof(p));
     if (M == 0 || N == 0)
         return p;
+    // (sizes are at most 2^31 each: bound the factors before multiplying)
+    if (M <= kTinyWork && N <= kTinyWork && M * N <= kTinyWork &&
+        M * N * (K > 0 ? K : 1) <= kTinyWork) {
+        set_tiny_plan(p, M, N);
+        return p;
+    }
     if (!gather && M <= 64 && K > 0) {
         // few rows: swap A and B so B streams through the MMA's M side
         const int mp = skinny_rows(M);
         const int64_t tiles = ceil_div(N, 128);
         const int64_t nkb = ceil_div(K, tcg::skinny_kstage());
         const int64_t W = tiles * nkb;
-        const int64_t G = W < sm_count ? W : sm_count;
+        // at least TCG_SKINNY_MIN_KB K blocks per CTA, so small problems are
+        // not cut into many parts whose reduction costs more than it saves
+        const int64_t want = ceil_div(W, TCG_SKINNY_MIN_KB);
+        const int64_t G = want < sm_count ? want : sm_count;
         p.kernel = 2;
         p.bm = mp;
         p.bn = 128;
@@ -532,11 +565,33 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+gemm_status run_tiny(const Problem &p, const gemm_plan &plan, const DeviceInfo *dev)
+{
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    fill_common(a, p, dev);
+    a.num_tiles = static_cast<int32_t>(plan.tiles);
+    a.gather = p.gather ? 1 : 0;
+    a.scatter = p.scatter ? 1 : 0;
+    a.reduce = p.reduce ? 1 : 0;
+    a.idx = p.idx;
+    a.table_rows = static_cast<int32_t>(p.a_rows);
+    a.d_rows = static_cast<int32_t>(p.d_rows);
+    const cudaError_t e = tcg::launch_tiny(p.A, p.lda, p.B, p.ldb, a, plan.grid, p.stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 // Test hook: replace the automatic tile form by a forced one where it can run.
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || plan.kernel == 0 || plan.kernel == 2)
+    if (fk == 0 || plan.kernel == 0)
+        return plan;
+    if (fk == 10) {
+        set_tiny_plan(plan, p.M, p.N);  // the warp-level kernel runs every problem
+        return plan;
+    }
+    if (plan.kernel == 2)
         return plan;
     if (fk != 1 && p.K == 0)
         return plan;  // cluster forms need K > 0
@@ -563,6 +618,8 @@ gemm_status run(const Problem &p)
     std::memset(&maps, 0, sizeof(maps));
     if (plan.kernel == 2)
         return run_skinny(p, plan, dev);
+    if (plan.kernel == 10)
+        return run_tiny(p, plan, dev);
     const TileForm form = tile_form(plan);
     const bool pair = form.pair;
     const int bn = form.mma_bn;
@@ -760,7 +817,7 @@ gemm_status gemm_debug_force_tile(int kernel, int bn)
                     (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512) ||
                     (kernel == 5 && (bn == 64 || bn == 256)) || (kernel == 6 && bn == 256) ||
                     (kernel == 7 && bn == 512) || (kernel == 8 && bn == 256) ||
-                    (kernel == 9 && bn == 512);
+                    (kernel == 9 && bn == 512) || (kernel == 10 && bn == 8);
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

@@ -58,6 +58,9 @@ int64_t ceil_div(int64_t a, int64_t b);
 gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count,
                     bool scatter = false);
 
+// Launch the warp-level kernel for a validated problem with a plan of kernel 10.
+gemm_status run_tiny(const Problem &p, const gemm_plan &plan, const DeviceInfo *dev);
+
 // Kernel arguments common to every kernel (sizes, epilogue, status, timeout).
 void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev);
 

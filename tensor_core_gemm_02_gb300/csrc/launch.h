@@ -32,6 +32,11 @@ int tile_max_clusters(int bn, bool pair, int nsub, int mc);
 cudaError_t launch_tile(int bn, bool pair, int nsub, int mc, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream);
 
+// Warp-level tiny-GEMM kernel: one 16 x 8 block of D per warp.
+int tiny_warps_per_cta();
+cudaError_t launch_tiny(const void *A, int64_t lda, const void *B, int64_t ldb,
+                        const GemmArgs &args, int grid, cudaStream_t stream);
+
 int skinny_stages(int mp);
 int skinny_kstage();  // K elements per pipeline stage (and per stream-K unit)
 cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,

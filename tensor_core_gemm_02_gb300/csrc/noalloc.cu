@@ -83,6 +83,8 @@ extern "C" gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int 
         return st;
     const gemm_plan plan =
         make_plan(p.M, p.N, p.K, false, p.C != nullptr && p.beta != 0.0f, dev->sm_count);
+    if (plan.kernel == 10)
+        return run_tiny(p, plan, dev);  // the warp-level kernel needs no scratch at all
     if (plan.kernel != 2)
         return GEMM_ERR_UNSUPPORTED;
     const int mp = plan.bm;

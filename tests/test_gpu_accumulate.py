@@ -19,9 +19,9 @@ from tensor_core_gemm_02_gb300.workloads import OUT_F32
 pytestmark = pytest.mark.gpu
 
 TILE_FORMS = [(1, 64), (1, 128), (1, 256), (3, 256), (4, 512), (5, 64), (5, 256), (6, 256),
-              (7, 512), (8, 256), (9, 512)]
+              (7, 512), (8, 256), (9, 512), (10, 8)]
 FORM_IDS = ["single64", "single128", "single256", "pair256", "pair512", "mcast64", "mcast256",
-            "mcast8x256", "pairs2x512", "pairs2x256", "pairs4x512"]
+            "mcast8x256", "pairs2x512", "pairs2x256", "pairs4x512", "tiny"]
 
 
 @pytest.fixture(autouse=True)

@@ -173,13 +173,23 @@ def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(40, 1000, 64, sm_count=148)
     assert p.kernel == 2 and p.bm == 64
     assert binding.gemm_query_plan(0, 10, 10).kernel == 0
+    # at most 2^20 multiply-adds: the warp-level kernel, one 16 x 8 block per warp
+    p = binding.gemm_query_plan(16, 8, 32, sm_count=148)
+    assert (p.kernel, p.bm, p.bn, p.tiles, p.grid) == (10, 16, 8, 1, 1)
+    p = binding.gemm_query_plan(64, 128, 128, sm_count=148)
+    assert (p.kernel, p.tiles, p.grid) == (10, 4 * 16, 16)
+    assert binding.gemm_query_plan(128, 128, 128, sm_count=148).kernel == 1
+    assert binding.gemm_query_plan(16, 1024, 1024, sm_count=148).kernel == 2
+    assert binding.gemm_query_plan(300, 200, 0, sm_count=148).kernel == 10  # K = 0: beta * C
+    assert binding.gemm_query_plan(3000, 2000, 0, sm_count=148).kernel == 1
 
 
 def test_skinny_split_arithmetic_covers_every_block():
     """The stream-K shares partition the k-block list and every tile's parts fit its slots."""
-    for tiles, nkb, G in [(224, 64, 148), (3, 5, 7), (1, 1, 1), (10, 3, 30), (1000, 7, 152)]:
+    for tiles, nkb, G in [(224, 64, 148), (3, 5, 7), (1, 1, 1), (10, 3, 30), (1000, 7, 152),
+                          (4, 8, 148), (8, 16, 148), (64, 16, 148)]:
         W = tiles * nkb
-        G = min(G, W)
+        G = min(G, -(-W // 8))  # at least 8 K blocks per CTA
         owner = lambda x: ((x + 1) * G - 1) // W
         starts = [W * g // G for g in range(G)]
         for g in range(G):
