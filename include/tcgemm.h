@@ -168,6 +168,32 @@ gemm_status gemm_scatter_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16
                               int out, float alpha, float beta, void *stream);
 
 /*
+ * Seeded form, the pages' recurrence taken literally: D = C + A * B^T where C
+ * is the accumulator's starting value.  The first K issue reads C and every
+ * later one reads the running fp32 sum ("mma.sync" page, section
+ * "Accumulation, transpose and alpha/beta": only the first K issue reads the
+ * start value, later ones read D).  C (M x N float32, required) is written
+ * into the tensor-memory accumulator (tcgen05.st) before the first MMA of
+ * each tile, and the result is converted to `out` without a further
+ * operation (alpha = beta = 1).  The sum is therefore rounded to fp32 after
+ * every K step of 16 with C already in it: for |C| much larger than the
+ * products the result can differ from gemm_f16/gemm_bf16's
+ * fma.rn(1, acc, C) (where C is added once, at the end) by up to one fp32
+ * ulp of the running sum per K step.
+ *
+ *  Arguments as gemm_f16 without alpha and beta; C must not be NULL (when
+ *  M, N > 0).  C == D (float32 out, ldc == ldd) is an in-place update.  M <= 64
+ *  runs on the tile kernel (or on the warp-level kernel for tiny problems),
+ *  not the skinny one.
+ */
+gemm_status gemm_seeded(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
+                        const void *A, int64_t lda,
+                        const void *B, int64_t ldb,
+                        const float *C, int64_t ldc,
+                        void *D, int64_t ldd,
+                        int out, void *stream);
+
+/*
  * Accumulating form: D[i][j] += alpha * sum_k A[i][k] * B[j][k] for float32 D.
  * The result is added into D by TMA reduce-add stores ("cp.async.bulk.tensor"
  * page, section "Stores, reductions, and completion": the reduction form adds
@@ -246,7 +272,8 @@ const char *gemm_status_string(int status);
  * The kernel choice the library makes for a problem, without launching
  * anything and without touching the GPU (for diagnostics and tests).
  * form: 0 = plain, 1 = row-gathered (gemm_gather_rows), 2 = row-scattered
- * (gemm_scatter_rows); any other value is GEMM_ERR_INVALID_ARG.  has_c: C
+ * (gemm_scatter_rows), 3 = seeded (gemm_seeded); any other value is
+ * GEMM_ERR_INVALID_ARG.  has_c: C
  * is given and beta != 0.
  *
  *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles, one

@@ -55,6 +55,7 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_bf16.argtypes = plain
     lib.gemm_gather_rows.argtypes = [i64, i64, i64, i32, vp, i64, i64, vp, vp, i64, vp, i64,
                                      vp, i64, i32, f32, f32, vp]
+    lib.gemm_seeded.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, i32, vp]
     lib.gemm_accumulate.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, f32, vp]
     lib.gemm_scatter_rows.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
                                       vp, i64, i32, f32, f32, vp]
@@ -68,6 +69,7 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_debug_inject.argtypes = [i32]
     lib.gemm_debug_force_tile.argtypes = [i32, i32]
     for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows", "gemm_accumulate",
+                 "gemm_seeded",
                  "gemm_skinny_noalloc",
                  "gemm_check_device_status",
                  "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject",
@@ -194,6 +196,25 @@ def gemm_scatter_rows(A, B, idx, D, C=None, *, alpha=1.0, beta=1.0, stream=None)
     return D
 
 
+def gemm_seeded(A, B, C, D=None, *, out=OUT_F32, stream=None):
+    """D = C + A @ B.T with C (float32 M x N) as the accumulator's starting value:
+    every K step of the tensor-core sum accumulates onto it."""
+    if A.dtype not in (torch.float16, torch.bfloat16) or B.dtype != A.dtype:
+        raise TypeError("A and B must both be f16 or both bf16")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    if C is None or C.dtype != torch.float32 or tuple(C.shape) != (M, N):
+        raise ValueError("C must be float32 M x N")
+    D = _out_tensor(D, M, N, out, A.device)
+    st = load_library().gemm_seeded(
+        M, N, K, 1 if A.dtype == torch.bfloat16 else 0, _ptr(A), _ld(A), _ptr(B), _ld(B),
+        _ptr(C), _ld(C), _ptr(D), _ld(D), out, _stream_ptr(stream))
+    _check(st, "gemm_seeded")
+    return D
+
+
 def gemm_accumulate(A, B, D, *, alpha=1.0, stream=None):
     """D += alpha * A @ B.T, added into float32 D (M x N) in place.  Returns D."""
     if A.dtype not in (torch.float16, torch.bfloat16) or B.dtype != A.dtype:
@@ -244,9 +265,10 @@ def gemm_check_device_status(stream=None) -> int:
     return int(load_library().gemm_check_device_status(_stream_ptr(stream)))
 
 
-def gemm_query_plan(M, N, K, gather=False, has_c=False, sm_count=148, scatter=False) -> Plan:
+def gemm_query_plan(M, N, K, gather=False, has_c=False, sm_count=148, scatter=False,
+                    seeded=False) -> Plan:
     p = Plan()
-    form = 1 if gather else (2 if scatter else 0)
+    form = 1 if gather else (2 if scatter else (3 if seeded else 0))
     _check(load_library().gemm_query_plan(M, N, K, form, int(bool(has_c)),
                                           sm_count, ctypes.byref(p)), "gemm_query_plan")
     return p

@@ -275,6 +275,8 @@ gemm_status validate(const Problem &p, bool *empty)
         return GEMM_ERR_INVALID_ARG;
     if (p.reduce && (p.out != GEMM_OUT_F32 || p.gather || p.scatter))
         return GEMM_ERR_INVALID_ARG;
+    if (p.seed && (!p.C || p.gather || p.scatter || p.reduce))
+        return GEMM_ERR_INVALID_ARG;
     if (p.d_rows > kMaxDim)
         return GEMM_ERR_UNSUPPORTED;
     // rows of C and D: M, or the rows of the matrix the result is scattered into
@@ -468,7 +470,7 @@ void set_tiny_plan(gemm_plan &p, int64_t M, int64_t N)
 }
 
 gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count,
-                    bool scatter)
+                    bool scatter, bool seeded)
 {
     gemm_plan p;
     std::memset(&p, 0, sizeof(p));
@@ -480,7 +482,7 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, i
         set_tiny_plan(p, M, N);
         return p;
     }
-    if (!gather && M <= 64 && K > 0) {
+    if (!gather && !seeded && M <= 64 && K > 0) {  // (seeded accumulators: tile kernel)
         // few rows: swap A and B so B streams through the MMA's M side
         const int mp = skinny_rows(M);
         const int64_t tiles = ceil_div(N, 128);
@@ -577,6 +579,10 @@ gemm_status run_tiny(const Problem &p, const gemm_plan &plan, const DeviceInfo *
     a.idx = p.idx;
     a.table_rows = static_cast<int32_t>(p.a_rows);
     a.d_rows = static_cast<int32_t>(p.d_rows);
+    if (p.seed) {
+        a.seed = 1;
+        a.has_c = 0;
+    }
     const cudaError_t e = tcg::launch_tiny(p.A, p.lda, p.B, p.ldb, a, plan.grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -612,7 +618,8 @@ gemm_status run(const Problem &p)
         return st;
     const bool c_used = p.C != nullptr && p.beta != 0.0f;
     const gemm_plan plan = apply_forced_tile(
-        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count, p.scatter), p, dev->sm_count);
+        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count, p.scatter, p.seed), p,
+        dev->sm_count);
 
     GemmMaps maps;
     std::memset(&maps, 0, sizeof(maps));
@@ -652,7 +659,8 @@ gemm_status run(const Problem &p)
     // for float32 output, whose 32-column rows fill the 128-byte swizzle span)
     const int64_t out_rows = p.scatter ? p.d_rows : p.M;
     const uint32_t box_rows = p.scatter ? 1u : 32u;
-    const bool c_tma = c_used && aligned16(p.C) && (p.ldc * 4) % 16 == 0;
+    // (seeded accumulators read C with plain loads, once, into tensor memory)
+    const bool c_tma = c_used && !p.seed && aligned16(p.C) && (p.ldc * 4) % 16 == 0;
     const bool d_tma = aligned16(p.D) && (p.ldd * out_size(p.out)) % 16 == 0 &&
                        (!p.scatter || p.out == GEMM_OUT_F32);
     if (c_tma && !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.C, p.N, out_rows,
@@ -688,6 +696,10 @@ gemm_status run(const Problem &p)
     a.scatter = p.scatter ? 1 : 0;
     a.d_rows = static_cast<int32_t>(p.d_rows);
     a.reduce = p.reduce ? 1 : 0;
+    if (p.seed) {
+        a.seed = 1;
+        a.has_c = 0;  // C went into the accumulator; the epilogue writes D = acc
+    }
 
     const cudaError_t e = tcg::launch_tile(bn, pair, form.nsub, form.mc, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -759,6 +771,20 @@ gemm_status gemm_accumulate(int64_t M, int64_t N, int64_t K, int dtype_is_bf16, 
     return run(p);
 }
 
+gemm_status gemm_seeded(int64_t M, int64_t N, int64_t K, int dtype_is_bf16, const void *A,
+                        int64_t lda, const void *B, int64_t ldb, const float *C, int64_t ldc,
+                        void *D, int64_t ldd, int out, void *stream)
+{
+    if (dtype_is_bf16 != 0 && dtype_is_bf16 != 1)
+        return GEMM_ERR_INVALID_ARG;
+    Problem p{M, N, K, dtype_is_bf16 == 1, A, M, lda, nullptr, B, ldb, C, ldc, D, ldd,
+              out, 1.0f, 1.0f, false, static_cast<cudaStream_t>(stream)};
+    p.seed = true;
+    if (M > 0 && N > 0 && !C)
+        return GEMM_ERR_INVALID_ARG;
+    return run(p);
+}
+
 gemm_status gemm_check_device_status(void *stream)
 {
     DeviceInfo *dev = nullptr;
@@ -799,9 +825,9 @@ gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int form, int has_c
 {
     if (!plan || sm_count < 1 || M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (form < 0 || form > 2)
+    if (form < 0 || form > 3)
         return GEMM_ERR_INVALID_ARG;
-    *plan = make_plan(M, N, K, form == 1, has_c != 0, sm_count, form == 2);
+    *plan = make_plan(M, N, K, form == 1, has_c != 0 || form == 3, sm_count, form == 2, form == 3);
     return GEMM_OK;
 }
 

@@ -44,6 +44,8 @@ struct GemmArgs {
     int32_t scatter;        // row m of the result goes to row idx[m] of D (and reads C there)
     int32_t d_rows;         // rows of C and D when scattering
     int32_t reduce;         // D += alpha * acc (float32 adds into D; no C)
+    int32_t seed;           // the accumulator starts from C (written to TMEM before the
+                            // first MMA, which then accumulates); D = acc, C not read after
     uint32_t extra_tx;      // test hook: extra bytes expected on the first stage
     uint32_t *status;       // [0] first error code, [1] where a wait gave up
     uint64_t timeout_ns;    // limit of every bounded wait

@@ -328,6 +328,9 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t aph = 0;
             bool alive = true;
             // K block kb of MMA half j on stage st into the accumulator at d_tmem
+            // seeded accumulators (C written to TMEM by the epilogue) are
+            // accumulated onto from the first K step on
+            const bool seeded = args.seed != 0;
             auto issue_half = [&](int st, int32_t kb, int j, uint32_t d_tmem) {
                 const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + st * Cfg::A_BYTES);
                 const uint64_t bd =
@@ -336,9 +339,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int k = 0; k < Cfg::BK / 16; ++k) {  // +32 B per K=16 step
                     if (PAIR)
-                        tc_mma_f16_pair(dj, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                        tc_mma_f16_pair(dj, ad + 2u * k, bd + 2u * k, idesc,
+                                        (seeded || (kb | k) != 0) ? 1u : 0u);
                     else
-                        tc_mma_f16(dj, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                        tc_mma_f16(dj, ad + 2u * k, bd + 2u * k, idesc,
+                                   (seeded || (kb | k) != 0) ? 1u : 0u);
                 }
             };
             // arrive on `bar` (both CTAs of a pair) once the MMAs issued so far finish
@@ -372,7 +377,10 @@ __global__ void __launch_bounds__(192, 1)
                 return true;
             };
             auto wait_acc_free = [&](int b) {
-                if (!wait_bounded(acce_bar(b), aph ^ 1u, abort_flag, args.status, args.timeout_ns,
+                // (seeded: the epilogue's first arrival is the seed, so the first
+                // use waits for it instead of passing on a fresh barrier)
+                if (!wait_bounded(acce_bar(b), seeded ? aph : aph ^ 1u, abort_flag, args.status,
+                                  args.timeout_ns,
                                   kWhereMmaAccEmpty))
                     return false;
                 tc_fence_after_sync();
@@ -471,7 +479,8 @@ __global__ void __launch_bounds__(192, 1)
         const bool c_tma = has_c && args.c_tma != 0;
         const bool scatter = args.scatter != 0;
         const bool reduce = args.reduce != 0;  // D += alpha * acc (float32 D, no C)
-        const bool acc_zero = args.num_k_blocks == 0;
+        const bool seed = args.seed != 0;  // accumulators start from C
+        const bool acc_zero = !seed && args.num_k_blocks == 0;
         const int out_kind = args.out_kind;
         // A 32 x 32 box goes out from lane 0; scattered rows go out as eight
         // tile::scatter4 copies of four rows, lane g moving rows 4g .. 4g+3
@@ -480,6 +489,66 @@ __global__ void __launch_bounds__(192, 1)
         // C and D are touched once: their lines go first out of L2, so the A
         // and B panels that neighbouring tiles share stay resident
         const uint64_t epi_policy = l2_policy_evict_first();
+        // The accumulator comes and goes back in units: the whole tile
+        // (NSUB = 1, barrier index = ab) or each BN-wide half (NSUB = 2,
+        // barrier index = half), so the MMA can refill half 0 while half 1
+        // is still being drained.
+        constexpr int kUnitChunks = (NSUB == 2 ? BN : TILE_N) / 32;
+        // hand accumulator unit `unit` back to the MMA warp (of the leader CTA)
+        auto release_unit = [&](int unit) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR && !leader)
+                    mbar_arrive_cluster(lead(acce_bar(unit)));
+                else
+                    mbar_arrive(acce_bar(unit));
+            }
+        };
+        // Seeded accumulators: write C of tile t (this warp's 32 rows, columns
+        // 32c .. 32c+31 of the tile) into accumulator columns `col`, zero past
+        // M and N, for the MMAs to accumulate onto.
+        const bool c_vec = (reinterpret_cast<uintptr_t>(args.C) & 15u) == 0 && (args.ldc & 3) == 0;
+        auto seed_chunk = [&](int32_t ts, int32_t c, uint32_t col) {
+            int32_t smb, snb;
+            tile_coords(ts, args, smb, snb);
+            if (MC > 1)
+                snb = snb * MC + static_cast<int32_t>(share);
+            const int32_t row = smb * Cfg::TILE_M + static_cast<int32_t>(role) * Cfg::BM +
+                                32 * static_cast<int32_t>(q) + static_cast<int32_t>(lane);
+            const int32_t col0 = snb * TILE_N + 32 * c;
+            uint32_t r[32];
+            const float *crow = args.C + static_cast<int64_t>(row < args.M ? row : 0) * args.ldc + col0;
+            if (row < args.M && col0 + 32 <= args.N && c_vec) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 x = *reinterpret_cast<const float4 *>(crow + 4 * i);
+                    r[4 * i] = __float_as_uint(x.x);
+                    r[4 * i + 1] = __float_as_uint(x.y);
+                    r[4 * i + 2] = __float_as_uint(x.z);
+                    r[4 * i + 3] = __float_as_uint(x.w);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    r[i] = __float_as_uint((row < args.M && col0 + i < args.N) ? crow[i] : 0.f);
+            }
+            tc_st_32x32b_x32(tmem_base + ((32u * q) << 16) + col, r);
+        };
+        if (seed) {
+            // the first tiles on each accumulator start from C as well
+            for (int b = 0; b < Cfg::NUM_ACC; ++b) {
+                const int32_t tb = cta_set + b * cta_sets;
+                for (int32_t c = 0; c < TILE_N / 32; ++c) {
+                    if (tb < args.num_tiles)
+                        seed_chunk(tb, c, static_cast<uint32_t>(b * TILE_N + 32 * c));
+                    if (c % kUnitChunks == kUnitChunks - 1) {
+                        tc_wait_st();
+                        release_unit(NSUB == 2 ? c / kUnitChunks : b);
+                    }
+                }
+            }
+        }
         int ab = 0;
         uint32_t aph = 0;
         uint32_t cph[2] = {0u, 0u};
@@ -578,11 +647,8 @@ __global__ void __launch_bounds__(192, 1)
                 zero_row = zero_row || v < 0 || v >= args.table_rows;
             }
 
-            // The accumulator comes and goes back in units: the whole tile
-            // (NSUB = 1, barrier index = ab) or each BN-wide half (NSUB = 2,
-            // barrier index = half), so the MMA can refill half 0 while half 1
-            // is still being drained.
-            constexpr int kUnitChunks = (NSUB == 2 ? BN : TILE_N) / 32;
+            // the next tile on this accumulator (seeded mode)
+            const int32_t t_next = t + Cfg::NUM_ACC * cta_sets;
             for (int32_t c = 0; c < TILE_N / 32; ++c) {
                 const int unit = NSUB == 2 ? c / kUnitChunks : ab;
                 if (c % kUnitChunks == 0) {
@@ -600,16 +666,15 @@ __global__ void __launch_bounds__(192, 1)
                         tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * TILE_N + 32 * c), acc);
                     tc_wait_ld(acc);
                 }
+                // seeded mode: these columns are read, so the next tile's C can
+                // take their place
+                if (seed && t_next < args.num_tiles)
+                    seed_chunk(t_next, c, static_cast<uint32_t>(ab * TILE_N + 32 * c));
                 if (c % kUnitChunks == kUnitChunks - 1) {
                     // this unit of the accumulator is fully read: hand it back
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (PAIR && !leader)
-                            mbar_arrive_cluster(lead(acce_bar(unit)));
-                        else
-                            mbar_arrive(acce_bar(unit));
-                    }
+                    if (seed)
+                        tc_wait_st();
+                    release_unit(unit);
                 }
                 if (!have || !rows_ok)
                     continue;

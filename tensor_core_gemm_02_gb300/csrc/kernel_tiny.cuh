@@ -5,8 +5,9 @@
 // more than the arithmetic.  Here each warp computes one 16 x 8 block of D
 // with mma.sync.m16n8k16 (fp32 accumulate), walking K in steps of 16: the
 // instruction the "mma.sync" page is about, with the first K step starting
-// from zero and the later ones accumulating (section "Accumulation, transpose
-// and alpha/beta"); its worked example is one such block with two K steps.
+// from zero (or, seeded, from C) and the later ones accumulating (section
+// "Accumulation, transpose and alpha/beta"); its worked example is one such
+// block with two K steps.
 // Operands come straight from global memory into the fragment registers, the
 // epilogue is the same fma.rn(alpha, acc, mul.rn(beta, C)) as everywhere else.
 //
@@ -95,6 +96,15 @@ __global__ void __launch_bounds__(32 * kTinyWarps)
                                                               : nullptr;
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (args.seed) {
+        // the accumulator starts from C: the first K step accumulates onto it
+        for (int h = 0; h < 2; ++h)
+            for (int e = 0; e < 2; ++e) {
+                const int32_t m = m0 + g + 8 * h, n = n0 + 2 * t + e;
+                if (m < args.M && n < args.N)
+                    acc[2 * h + e] = args.C[static_cast<int64_t>(m) * args.ldc + n];
+            }
+    }
     const bool bf16 = args.ab_bf16 != 0;
     for (int32_t k0 = 0; k0 < args.K; k0 += 16) {
         const uint32_t a[4] = {tiny_pair(arow[0], k0 + 2 * t, args.K),

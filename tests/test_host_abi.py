@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows",
-              "gemm_accumulate", "gemm_check_device_status", "gemm_status_string"):
+              "gemm_accumulate", "gemm_seeded", "gemm_check_device_status",
+              "gemm_status_string"):
         assert n in names
 
 
@@ -135,6 +136,24 @@ def test_accumulate_argument_checks(lib):
     assert call(K=0) == 0  # adds nothing, launches nothing
 
 
+def test_seeded_argument_checks(lib):
+    f = lib.gemm_seeded
+
+    def call(M=64, N=64, K=64, bf=1, A=A0, lda=64, B=B0, ldb=64, C=C0, ldc=64, D=D0, ldd=64,
+             out=0):
+        return f(M, N, K, bf, A, lda, B, ldb, C, ldc, D, ldd, out, None)
+
+    assert call(C=None) == 1
+    assert call(bf=2) == 1
+    assert call(ldc=10) == 1
+    assert call(C=C0 + 2) == 2
+    assert call(C=D0 + 16) == 4
+    assert call(M=0, C=None) == 0
+    # M <= 64 takes the tile kernel (the skinny kernel has no seeded form)
+    assert binding.gemm_query_plan(16, 28672, 4096, seeded=True, sm_count=148).kernel == 1
+    assert binding.gemm_query_plan(16, 8, 32, seeded=True, sm_count=148).kernel == 10
+
+
 def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bm, p.bn, p.grid) == (4, 256, 512, 148)
@@ -167,7 +186,7 @@ def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(16, 28672, 4096, scatter=True, sm_count=148)
     assert p.kernel == 2
     plan = binding.Plan()
-    assert lib.gemm_query_plan(64, 64, 64, 3, 0, 148, ctypes.byref(plan)) == 1
+    assert lib.gemm_query_plan(64, 64, 64, 4, 0, 148, ctypes.byref(plan)) == 1
     p = binding.gemm_query_plan(100, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bn) == (1, 64)
     p = binding.gemm_query_plan(40, 1000, 64, sm_count=148)
