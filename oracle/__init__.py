@@ -1,5 +1,5 @@
 """fp64 CPU oracle for D = alpha * A @ B.T + beta * C (plain, gathered and
-scattered forms).
+scattered forms, and FP4 block-scaled weights).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product path
@@ -54,6 +54,13 @@ def _bind(lib):
     lib.oracle_scatter_rows.argtypes = [i64, i64, i64, i64, i32, vp, i64, vp, i64,
                                         vp, i64, vp, i64, dbl, dbl, vp, vp, i64]
     lib.oracle_scatter_rows.restype = i32
+    lib.oracle_decode_e2m1.argtypes = [i32]
+    lib.oracle_decode_e2m1.restype = dbl
+    lib.oracle_decode_ue8m0.argtypes = [i32]
+    lib.oracle_decode_ue8m0.restype = dbl
+    lib.oracle_w4_rows.argtypes = [i64, i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
+                                   dbl, dbl, vp, vp, i64]
+    lib.oracle_w4_rows.restype = None
     lib.oracle_init()
     return lib
 
@@ -268,6 +275,51 @@ def scatter_place(D0, rows, idx):
             D[d] = np.nan
             repeated[d] = who
     return D, repeated
+
+
+def decode_e2m1(codes) -> np.ndarray:
+    """Value of each FP4 E2M1 code (0..15)."""
+    lib = load()
+    flat = np.asarray(codes, np.int64).ravel()
+    return np.array([lib.oracle_decode_e2m1(int(c)) for c in flat]).reshape(np.shape(codes))
+
+
+def decode_ue8m0(scales) -> np.ndarray:
+    """Value 2^(s - 127) of each UE8M0 scale byte (255: NaN)."""
+    lib = load()
+    flat = np.asarray(scales, np.int64).ravel()
+    return np.array([lib.oracle_decode_ue8m0(int(c)) for c in flat]).reshape(np.shape(scales))
+
+
+def w4(A, Wq, Ws, C=None, alpha=1.0, beta=1.0, dtype=None, threads=None):
+    """alpha * A @ W.T + beta * C with FP4 weights W (N x K) given as packed codes
+    Wq (N x K/2 uint8, element k in the low nibble of byte k/2 for even k) and
+    UE8M0 scales Ws (K/32 x N uint8).  Returns (ref, absprod) as float64 M x N."""
+    lib = load()
+    a, code_a = _as_bits(A, dtype)
+    wq = np.ascontiguousarray(np.asarray(Wq, np.uint8))
+    ws = np.ascontiguousarray(np.asarray(Ws, np.uint8))
+    c = _f32(C)
+    M, K = a.shape
+    N = wq.shape[0]
+    if K % 32 or wq.shape[1] != K // 2 or ws.shape != (K // 32, N):
+        raise ValueError("Wq must be N x K/2 and Ws K/32 x N, K a multiple of 32")
+    ref = np.empty((M, N), np.float64)
+    absprod = np.empty((M, N), np.float64)
+    nthr = threads or default_threads()
+    bounds = np.linspace(0, M, min(nthr, max(1, M)) + 1).astype(np.int64)
+
+    def run(lo, hi):
+        lo, hi = int(lo), int(hi)
+        if hi > lo:
+            off = lo * N * 8
+            lib.oracle_w4_rows(lo, hi, N, K, code_a, _ptr(a), a.shape[1], _ptr(wq), wq.shape[1],
+                               _ptr(ws), N, _ptr(c), N, float(alpha), float(beta),
+                               ref.ctypes.data + off, absprod.ctypes.data + off, N)
+
+    with ThreadPoolExecutor(max_workers=nthr) as ex:
+        list(ex.map(lambda p: run(*p), zip(bounds[:-1], bounds[1:])))
+    return ref, absprod
 
 
 def decode(bits, dtype: str) -> np.ndarray:

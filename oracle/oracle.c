@@ -224,3 +224,66 @@ int oracle_scatter_rows(int64_t i0, int64_t i1, int64_t N, int64_t K, int dtype,
     }
     return bad;
 }
+
+/*
+ * FP4 weights with block scales.  The "cp.async.bulk.tensor" page (section
+ * "Interleave and packed FP4") gives the float4_e2m1fn operand format; it does
+ * not give the numbers the codes stand for or how blocks are scaled.  Those
+ * come from the OCP Microscaling (MX) formats definition that the e2m1 name
+ * refers to: an E2M1 element has 1 sign bit, 2 exponent bits with bias 1 and
+ * 1 mantissa bit, exponent 0 being subnormal (mantissa * 0.5), no infinity or
+ * NaN; a UE8M0 block scale s stands for 2^(s - 127), s = 255 being NaN; one
+ * scale covers 32 consecutive elements along K.
+ */
+double oracle_decode_e2m1(int code)
+{
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+double oracle_decode_ue8m0(int s)
+{
+    return s == 255 ? NAN : ldexp(1.0, s - 127);
+}
+
+/*
+ * Rows [i0, i1) of D = alpha * A * W^T + beta * C with
+ *   W[j][k] = e2m1(code of element k in row j of Wq) * ue8m0(Ws[k / 32][j]).
+ * Row j of Wq holds K / 2 bytes; element k is the low nibble of byte k / 2 when
+ * k is even and the high nibble when k is odd.  Ws holds K / 32 rows of N
+ * scale bytes, lds bytes apart.  A is f16 or bf16 (dtype), as in
+ * oracle_gemm_rows; ref and abs_out likewise.
+ */
+void oracle_w4_rows(int64_t i0, int64_t i1, int64_t N, int64_t K, int dtype,
+                    const uint16_t *A, int64_t lda, const uint8_t *Wq, int64_t ldq,
+                    const uint8_t *Ws, int64_t lds, const float *C, int64_t ldc,
+                    double alpha, double beta, double *ref, double *abs_out, int64_t ldr)
+{
+    const double *val;
+    oracle_init();
+    val = g_value[dtype == ORACLE_BF16 ? ORACLE_BF16 : ORACLE_F16];
+    for (int64_t i = i0; i < i1; ++i) {
+        const uint16_t *arow = A + i * lda;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint8_t *wrow = Wq + j * ldq;
+            double sum = 0.0, sum_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                int byte = wrow[k / 2];
+                int code = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
+                double w = oracle_decode_e2m1(code) * oracle_decode_ue8m0(Ws[(k / 32) * lds + j]);
+                double a = val[arow[k]];
+                sum += a * w;
+                sum_abs += fabs(a) * fabs(w);
+            }
+            double r = alpha * sum;
+            if (C && beta != 0.0)
+                r += beta * (double)C[i * ldc + j];
+            ref[(i - i0) * ldr + j] = r;
+            if (abs_out)
+                abs_out[(i - i0) * ldr + j] = sum_abs;
+        }
+    }
+}

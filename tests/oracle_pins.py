@@ -216,7 +216,66 @@ def pin_scatter_rows():
     assert np.isnan(placed[4]).all()
 
 
+# FP4 E2M1 magnitudes as the OCP MX definition tabulates them (codes 0..7).
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _unpack_codes(wq):
+    """N x K codes from N x K/2 bytes: even k in the low nibble (numpy, not the oracle)."""
+    lo, hi = wq & 15, wq >> 4
+    return np.stack([lo, hi], axis=-1).reshape(wq.shape[0], -1)
+
+
+def _dequant_numpy(wq, ws):
+    codes = _unpack_codes(wq).astype(np.int64)
+    mag = np.array(E2M1_TABLE)[codes & 7]
+    sign = np.where(codes & 8, -1.0, 1.0)
+    scale = np.repeat(np.ldexp(1.0, ws.astype(np.int64) - 127), 32, axis=0).T  # N x K
+    return sign * mag * scale
+
+
+def pin_fp4_decode():
+    got = oracle.decode_e2m1(np.arange(16))
+    want = np.array(E2M1_TABLE + [-v for v in E2M1_TABLE])
+    assert np.array_equal(got, want) and np.signbit(got[8]) and not np.signbit(got[0])
+    s = np.array([0, 1, 100, 126, 127, 128, 200, 254])
+    want_s = np.array([float(Fraction(2) ** (int(v) - 127)) for v in s])
+    assert np.array_equal(oracle.decode_ue8m0(s), want_s)
+    assert np.isnan(oracle.decode_ue8m0([255])[0])
+
+
+def pin_w4_matches_numpy():
+    rng = np.random.default_rng(13)
+    M, N, K = 9, 11, 96
+    a = torch.from_numpy(rng.integers(-4, 5, (M, K)).astype(np.float32) / 4).to(torch.bfloat16)
+    wq = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    ws = rng.integers(118, 137, (K // 32, N)).astype(np.uint8)
+    c = (rng.integers(-4, 5, (M, N)) / 4).astype(np.float32)
+    ref, absprod = oracle.w4(a, wq, ws, c, alpha=0.5, beta=-2.0)
+    w = _dequant_numpy(wq, ws)
+    assert np.array_equal(ref, 0.5 * (_f64(a) @ w.T) - 2.0 * c.astype(np.float64))
+    assert np.array_equal(absprod, np.abs(_f64(a)) @ np.abs(w).T)
+
+
+def pin_w4_nibble_order_and_blocks():
+    """A = I picks single weights: W[j][k] lands in D[k][j]."""
+    K, N = 64, 3
+    a = torch.eye(K, dtype=torch.float16)
+    wq = np.zeros((N, K // 2), np.uint8)
+    wq[0, 0] = 0x72            # k = 0: code 2 (1.0); k = 1: code 7 (6.0)
+    wq[1, 16] = 0x0B           # k = 32: code 11 (-1.5)
+    wq[2, 31] = 0x50           # k = 63: code 5 (3.0)
+    ws = np.full((K // 32, N), 127, np.uint8)
+    ws[1, 1] = 130             # block 1 of row 1: x 8
+    ws[1, 2] = 126             # block 1 of row 2: x 0.5
+    ref, _ = oracle.w4(a, wq, ws)
+    want = np.zeros((K, N))
+    want[0, 0], want[1, 0], want[32, 1], want[63, 2] = 1.0, 6.0, -12.0, 1.5
+    assert np.array_equal(ref, want)
+
+
 ALL_PINS = [pin_decode_f16, pin_decode_bf16, pin_worked_example_exact,
             pin_matches_numpy_random_shapes, pin_two_a_plus_one, pin_fma_separation,
             pin_alpha_beta_c_cases, pin_gather_invariants, pin_entries_match_rows,
-            pin_scatter_rows]
+            pin_scatter_rows, pin_fp4_decode, pin_w4_matches_numpy,
+            pin_w4_nibble_order_and_blocks]

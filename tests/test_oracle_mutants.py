@@ -42,6 +42,15 @@ MUTANTS = [
     ("scatter_no_range_check", "if (d < 0 || d >= d_rows)", "if (d < 0)"),
     ("scatter_b_row_fixed", "const uint16_t *brow = B + j * ldb;\n            double sum",
      "const uint16_t *brow = B;\n            double sum"),
+    ("fp4_nibble_order_swapped", "int code = (k % 2 == 0) ? (byte & 15) : (byte >> 4);",
+     "int code = (k % 2 == 0) ? (byte >> 4) : (byte & 15);"),
+    ("fp4_scale_block_16", "Ws[(k / 32) * lds + j]", "Ws[(k / 16) * lds + j]"),
+    ("fp4_exponent_bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)"),
+    ("fp4_subnormal_value", "e == 0 ? 0.5 * m :", "e == 0 ? 1.0 * m :"),
+    ("fp4_sign_ignored", "    return sign ? -v : v;\n}\n\ndouble oracle_decode_ue8m0",
+     "    return v;\n}\n\ndouble oracle_decode_ue8m0"),
+    ("ue8m0_bias", "ldexp(1.0, s - 127)", "ldexp(1.0, s - 128)"),
+    ("fp4_scale_transposed", "Ws[(k / 32) * lds + j]", "Ws[j * lds + (k / 32)]"),
     ("sign_bit_ignored_f16", "    return sign ? -v : v;\n}\n\n/* bfloat16", "    return v;\n}\n\n/* bfloat16"),
 ]
 
