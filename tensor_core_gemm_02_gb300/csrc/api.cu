@@ -701,7 +701,9 @@ gemm_status run(const Problem &p)
         a.has_c = 0;  // C went into the accumulator; the epilogue writes D = acc
     }
 
-    const cudaError_t e = tcg::launch_tile(bn, pair, form.nsub, form.mc, maps, a, grid, p.stream);
+    const int mode = p.scatter ? 1 : (p.reduce ? 2 : (p.seed ? 3 : 0));  // epilogue mode
+    const cudaError_t e =
+        tcg::launch_tile(mode, bn, pair, form.nsub, form.mc, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

@@ -107,7 +107,12 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t row, uint32_t chunk, uint32
     return lin ^ (((lin >> 7) & mask) << 4);
 }
 
-template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
+// Epilogue modes, a template parameter so that each kernel carries only its own:
+// the fma.rn epilogue with optional C, rows scattered through idx, reduce-add
+// into D, and accumulators seeded with C.
+enum : int { kModePlain = 0, kModeScatter = 1, kModeReduce = 2, kModeSeed = 3 };
+
+template <int BN, int STAGES, bool PAIR, int NSUB, int MC, int MODE>
 __global__ void __launch_bounds__(192, 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
@@ -330,7 +335,7 @@ __global__ void __launch_bounds__(192, 1)
             // K block kb of MMA half j on stage st into the accumulator at d_tmem
             // seeded accumulators (C written to TMEM by the epilogue) are
             // accumulated onto from the first K step on
-            const bool seeded = args.seed != 0;
+            constexpr bool seeded = MODE == kModeSeed;
             auto issue_half = [&](int st, int32_t kb, int j, uint32_t d_tmem) {
                 const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + st * Cfg::A_BYTES);
                 const uint64_t bd =
@@ -477,9 +482,9 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t buf0 = base + Cfg::OFF_EPI + q * 2u * Cfg::EPI_BUF;
         const bool has_c = args.has_c != 0;
         const bool c_tma = has_c && args.c_tma != 0;
-        const bool scatter = args.scatter != 0;
-        const bool reduce = args.reduce != 0;  // D += alpha * acc (float32 D, no C)
-        const bool seed = args.seed != 0;  // accumulators start from C
+        constexpr bool scatter = MODE == kModeScatter;
+        constexpr bool reduce = MODE == kModeReduce;  // D += alpha * acc (float32 D, no C)
+        constexpr bool seed = MODE == kModeSeed;      // accumulators start from C
         const bool acc_zero = !seed && args.num_k_blocks == 0;
         const int out_kind = args.out_kind;
         // A 32 x 32 box goes out from lane 0; scattered rows go out as eight

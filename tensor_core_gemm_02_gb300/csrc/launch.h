@@ -29,7 +29,9 @@ int tile_stages(int bn, bool pair, int nsub, int mc);
 // clusters (pairs, or groups of mc) of a form that can be resident at once on
 // the current device; 0 if unknown
 int tile_max_clusters(int bn, bool pair, int nsub, int mc);
-cudaError_t launch_tile(int bn, bool pair, int nsub, int mc, const GemmMaps &maps,
+// mode: 0 plain epilogue, 1 scattered rows, 2 reduce-add into D, 3 seeded
+// accumulators (kModePlain ... kModeSeed)
+cudaError_t launch_tile(int mode, int bn, bool pair, int nsub, int mc, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream);
 
 // Warp-level tiny-GEMM kernel: one 16 x 8 block of D per warp.
@@ -38,6 +40,16 @@ cudaError_t launch_tiny(const void *A, int64_t lda, const void *B, int64_t ldb,
                         const GemmArgs &args, int grid, cudaStream_t stream);
 
 int skinny_stages(int mp);
+// The same kernel with FP4 B: maps.b = the codes (uint8, 32-byte boxes of 128
+// rows), maps.c = the block scales (uint8, 128 x 2 boxes); bf16 A.
+int skinny_w4_stages(int mp);
+// FP4 codes (N rows of K/2 bytes, ldq apart) and scales (K/32 rows of N bytes,
+// lds apart) -> bf16 N x K rows, ldo elements apart; K a multiple of 32.
+cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldq, const uint8_t *scales,
+                               int64_t lds, int32_t N, int32_t K, uint16_t *out, int64_t ldo,
+                               cudaStream_t stream);
+cudaError_t launch_skinny_w4(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
+                             cudaStream_t stream);
 int skinny_kstage();  // K elements per pipeline stage (and per stream-K unit)
 cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
                           cudaStream_t stream);

@@ -1,57 +1,16 @@
-// launch_tile.cu -- instantiations and launcher of the tile kernel: 128 x BN
-// tiles on single CTAs (alone, or in clusters of 4 or 8 sharing A by
-// multicast), or 256 x (NSUB * BN) tiles on CTA pairs (clusters of two, or of
-// four: two pairs sharing A by multicast).
+// launch_tile.cu -- the tile kernel's plain-epilogue instantiations, its
+// per-form ring depths and co-residency, and the launch dispatch over
+// epilogue modes (the other modes' kernels live in launch_tile_{scatter,
+// reduce,seed}.cu).
 #include <cuda_runtime.h>
 
 #include <mutex>
 
-#include "kernel_tile.cuh"
-#include "launch.h"
+#include "launch_tile_impl.cuh"
 
 namespace tcg {
 
 namespace {
-
-// attr must hold two entries
-template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
-void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid, cudaStream_t stream)
-{
-    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
-    cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
-    cfg.stream = stream;
-    int n = 0;
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = TCG_PDL;
-    ++n;
-    if (Cfg::CLUSTER > 1) {
-        attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = Cfg::CLUSTER;
-        attr[n].val.clusterDim.y = 1;
-        attr[n].val.clusterDim.z = 1;
-        ++n;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = n;
-}
-
-template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
-cudaError_t launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid, cudaStream_t stream)
-{
-    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
-    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC>;
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::SMEM_ALLOC));
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
-    fill_config<BN, STAGES, PAIR, NSUB, MC>(cfg, attr, grid, stream);
-    return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, maps.d, args);
-}
 
 // How many clusters of this form can be resident at once on the current device
 // (SMs that cannot be grouped within their GPC stay idle).  Cached per device.
@@ -67,13 +26,13 @@ int max_clusters_impl()
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev] > 0)
         return cached[dev];
-    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC>;
+    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, kModePlain>;
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::SMEM_ALLOC)) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    fill_config<BN, STAGES, PAIR, NSUB, MC>(cfg, attr, Cfg::CLUSTER, nullptr);
+    tile_fill_config<BN, STAGES, PAIR, NSUB, MC>(cfg, attr, Cfg::CLUSTER, nullptr);
     cfg.attrs = attr + 1;  // the cluster shape only (the dependent-launch flag is not a query input)
     cfg.numAttrs = 1;
     int clusters = 0;
@@ -127,38 +86,16 @@ int tile_max_clusters(int bn, bool pair, int nsub, int mc)
     return 0;
 }
 
-cudaError_t launch_tile(int bn, bool pair, int nsub, int mc, const GemmMaps &maps,
+cudaError_t launch_tile(int mode, int bn, bool pair, int nsub, int mc, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream)
 {
-    if (pair) {
-        if (bn != 256 || (mc != 1 && mc != 2 && mc != 4) || (mc == 4 && nsub != 2))
-            return cudaErrorInvalidValue;
-        if (mc == 4)
-            return launch_impl<256, 4, true, 2, 4>(maps, args, grid, stream);
-        if (mc == 2)
-            return nsub == 2 ? launch_impl<256, 4, true, 2, 2>(maps, args, grid, stream)
-                             : launch_impl<256, 6, true, 1, 2>(maps, args, grid, stream);
-        return nsub == 2 ? launch_impl<256, 4, true, 2, 1>(maps, args, grid, stream)
-                         : launch_impl<256, 6, true, 1, 1>(maps, args, grid, stream);
-    }
-    if (nsub != 1)
-        return cudaErrorInvalidValue;
-    if (mc == 4) {
-        if (bn == 256)
-            return launch_impl<256, 4, false, 1, 4>(maps, args, grid, stream);
-        if (bn == 64)
-            return launch_impl<64, 8, false, 1, 4>(maps, args, grid, stream);
-        return cudaErrorInvalidValue;
-    }
-    if (mc == 8)
-        return bn == 256 ? launch_impl<256, 4, false, 1, 8>(maps, args, grid, stream)
-                         : cudaErrorInvalidValue;
-    if (mc != 1)
-        return cudaErrorInvalidValue;
-    switch (bn) {
-    case 256: return launch_impl<256, 4, false, 1, 1>(maps, args, grid, stream);
-    case 128: return launch_impl<128, 6, false, 1, 1>(maps, args, grid, stream);
-    case 64: return launch_impl<64, 8, false, 1, 1>(maps, args, grid, stream);
+    switch (mode) {
+    case kModePlain: return launch_tile_mode<kModePlain>(bn, pair, nsub, mc, maps, args, grid, stream);
+    case kModeScatter:
+        return launch_tile_mode<kModeScatter>(bn, pair, nsub, mc, maps, args, grid, stream);
+    case kModeReduce:
+        return launch_tile_mode<kModeReduce>(bn, pair, nsub, mc, maps, args, grid, stream);
+    case kModeSeed: return launch_tile_mode<kModeSeed>(bn, pair, nsub, mc, maps, args, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }
