@@ -187,28 +187,26 @@ class ClockSampler:
                 "sm_mhz_samples": [r["sm"] for r in rows][:40]}
 
 
-def kernel_key(plan):
-    """The kernel instance a plan launches, as ncu names it (for profiles/traffic.json)."""
+def kernel_key(plan, p=None):
+    """The kernel instance a plan launches for problem p, as ncu names it (for
+    profiles/traffic.json): tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, MODE>,
+    MODE 0 plain, 1 scattered rows, 2 reduce-add; skinny_gemm_kernel<MP, 1, W4>."""
+    mode = 0 if p is None else (1 if p.scatter else (2 if p.accumulate else 0))
     if plan.kernel == 2:
-        return f"skinny_gemm_kernel<{plan.bm}, 1>"
-    if plan.kernel == 3:
-        return "tile_gemm_kernel<256, 6, 1, 1, 1>"
-    if plan.kernel == 4:
-        return "tile_gemm_kernel<256, 4, 1, 2, 1>"
-    if plan.kernel == 7:
-        return "tile_gemm_kernel<256, 4, 1, 2, 2>"
-    if plan.kernel == 8:
-        return "tile_gemm_kernel<256, 6, 1, 1, 2>"
-    if plan.kernel == 9:
-        return "tile_gemm_kernel<256, 4, 1, 2, 4>"
-    if plan.kernel in (5, 6):
-        return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1, {4 if plan.kernel == 5 else 8}>"
-    return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1, 1>"
+        return f"skinny_gemm_kernel<{plan.bm}, 1, {1 if p is not None and p.fp4 else 0}>"
+    if plan.kernel == 10:
+        return "tiny_gemm_kernel"
+    form = {3: "256, 6, 1, 1, 1", 4: "256, 4, 1, 2, 1", 7: "256, 4, 1, 2, 2",
+            8: "256, 6, 1, 1, 2", 9: "256, 4, 1, 2, 4"}.get(plan.kernel)
+    if form is None:
+        mc = {5: 4, 6: 8}.get(plan.kernel, 1)
+        form = f"{plan.bn}, {plan.stages}, 0, 1, {mc}"
+    return f"tile_gemm_kernel<{form}, {mode}>"
 
 
 def plan_of(p, dev):
     return binding.gemm_query_plan(p.M, p.N, p.K, gather=p.idx is not None and not p.scatter,
-                                   scatter=p.scatter,
+                                   scatter=p.scatter, fp4=p.fp4,
                                    has_c=p.C is not None and p.beta != 0,
                                    sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
 
@@ -219,6 +217,8 @@ def l2_flush(buf):
 
 def launch(p, dev_tensors):
     A, B, C, idx, D = dev_tensors
+    if p.fp4:
+        return binding.gemm_bf16_e2m1(A, B, idx, C, D, alpha=p.alpha, beta=p.beta, out=p.out)
     if p.accumulate:
         return binding.gemm_accumulate(A, B, D, alpha=p.alpha)
     if p.scatter:
@@ -235,6 +235,8 @@ def to_device(p, dev):
     B = p.B.to(dev)
     C = p.C.to(dev) if p.C is not None else None
     idx = p.idx.to(dev) if p.idx is not None else None
+    if p.fp4:
+        idx = p.Bs.to(dev)  # (the scales ride in the index slot)
     if p.accumulate:
         D = p.D0.to(dev).contiguous()
     elif p.scatter:
@@ -251,7 +253,7 @@ def algorithmic_bytes(p):
     read and written)."""
     esz = p.A.element_size()
     a = p.M * p.K * esz
-    b = p.N * p.K * esz
+    b = p.N * p.K * esz if not p.fp4 else p.N * p.K // 2 + p.Bs.numel()  # FP4: codes + scales
     c = p.M * p.N * 4 if (p.C is not None and p.beta != 0) else 0
     d = p.M * p.N * workloads.OUT_TORCH[p.out].itemsize * (2 if p.accumulate else 1)
     i = p.M * 4 if p.idx is not None else 0
@@ -349,7 +351,7 @@ def input_bytes(p):
     """Bytes of input the GEMM reads (the gathered form: the rows it gathers)."""
     gathered = p.idx is not None and not p.scatter
     a = (int(torch.unique(p.idx).numel()) if gathered else p.M) * p.K * p.A.element_size()
-    b = p.N * p.K * p.B.element_size()
+    b = p.N * p.K * p.B.element_size() if not p.fp4 else p.N * p.K // 2 + p.Bs.numel()
     c = p.M * p.N * 4 if (p.C is not None and p.beta != 0) else 0
     return a + b + c
 
@@ -454,8 +456,8 @@ def run_ours(args):
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4),
                      "peak_source": f"{peaks['source']} bf16_tflops (burst)",
-                     "traffic": stored_traffic(f"{kernel_key(plan_of(p, dev))}@{HEADLINE}"),
-                     "kernel": kernel_key(plan_of(p, dev)),
+                     "traffic": stored_traffic(f"{kernel_key(plan_of(p, dev), p)}@{HEADLINE}"),
+                     "kernel": kernel_key(plan_of(p, dev), p),
                      "algorithmic_flops_per_launch": flops},
     }
 
@@ -464,11 +466,12 @@ def run_ours(args):
         variants = {}
         for name in ("f16_1024", "mlp_8192x28672x4096", "skinny_16x28672x4096",
                      "gather_16384_of_65536", "scatter_16384_into_65536",
-                     "skinny_accumulate_16x28672x4096"):
+                     "skinny_accumulate_16x28672x4096", "fp4_skinny_16x28672x4096"):
             vp, ms, plan, how = time_variant(name, dev, args.variant_reps, flush)
             tflops = vp.flops / (ms * 1e-3) / 1e12
             gbs = algorithmic_bytes(vp) / (ms * 1e-3) / 1e9
-            hbm_bound = name in ("skinny_16x28672x4096", "skinny_accumulate_16x28672x4096")
+            hbm_bound = name in ("skinny_16x28672x4096", "skinny_accumulate_16x28672x4096",
+                                 "fp4_skinny_16x28672x4096")
             variants[name] = {
                 "ms": round(ms, 5), "TFLOP/s": round(tflops, 2), "GB/s": round(gbs, 1),
                 "algorithmic_bytes": algorithmic_bytes(vp),
@@ -486,8 +489,8 @@ def run_ours(args):
                                   {"bound": "tensor", "achieved": round(tflops, 2),
                                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                    "frac": round(tflops / peaks["bf16_tflops"], 4)}),
-                                 traffic=stored_traffic(f"{kernel_key(plan)}@{name}"),
-                                 kernel=kernel_key(plan)),
+                                 traffic=stored_traffic(f"{kernel_key(plan, vp)}@{name}"),
+                                 kernel=kernel_key(plan, vp)),
                 "timing": f"median of per-launch CUDA events; {how}",
             }
         result["variants"] = variants

@@ -168,6 +168,40 @@ gemm_status gemm_scatter_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16
                               int out, float alpha, float beta, void *stream);
 
 /*
+ * FP4 weights: D = fma.rn(alpha, A * W^T, beta * C) with bf16 A (M x K) and
+ *     W[n][k] = e2m1(code of element k of row n) * 2^(Bs[k / 32][n] - 127).
+ * The "cp.async.bulk.tensor" page (section "Interleave and packed FP4") gives
+ * float4_e2m1fn as an operand format; the code values and the block scaling
+ * are those of the OCP Microscaling definition that name refers to (E2M1: sign,
+ * 2 exponent bits with bias 1, 1 mantissa bit, codes 0..7 = 0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6; UE8M0 scale s = 2^(s - 127), 255 = NaN; 32 elements per scale).
+ * M <= 64 streams the codes and scales with TMA and converts them to bf16 in
+ * shared memory next to the tensor-core pipeline (a quarter of the bytes of a
+ * bf16 B); larger M converts W to bf16 once (a per-stream buffer the library
+ * allocates) and runs the bf16 GEMM.  W's values are exact in bf16 for scales
+ * up to 252; 253-254 can overflow to infinity.
+ *
+ *  A, lda      M x K bf16, as in gemm_bf16.
+ *  Bq, ldbq    N rows of K/2 bytes, ldbq bytes apart: element k of a row is
+ *              the low nibble of byte k/2 when k is even, the high nibble when
+ *              odd.  16-byte aligned, ldbq >= K/2 and a multiple of 16.
+ *  Bs, ldbs    K/32 rows of N scale bytes, ldbs bytes apart (row b holds the
+ *              scales of elements 32b .. 32b+31 of every row of W), ldbs >= N.
+ *              With a 16-byte aligned base and a pitch that is a multiple of
+ *              16 the kernel reads them in place; otherwise (M <= 64) the
+ *              library first copies them to a padded buffer of its own.
+ *  K           a multiple of 32 (GEMM_ERR_UNSUPPORTED otherwise).
+ *  Other arguments as in gemm_bf16.  D must not overlap A, Bq or Bs.
+ */
+gemm_status gemm_bf16_e2m1(int64_t M, int64_t N, int64_t K,
+                           const void *A, int64_t lda,
+                           const uint8_t *Bq, int64_t ldbq,
+                           const uint8_t *Bs, int64_t ldbs,
+                           const float *C, int64_t ldc,
+                           void *D, int64_t ldd,
+                           int out, float alpha, float beta, void *stream);
+
+/*
  * Seeded form, the pages' recurrence taken literally: D = C + A * B^T where C
  * is the accumulator's starting value.  The first K issue reads C and every
  * later one reads the running fp32 sum ("mma.sync" page, section
@@ -272,8 +306,8 @@ const char *gemm_status_string(int status);
  * The kernel choice the library makes for a problem, without launching
  * anything and without touching the GPU (for diagnostics and tests).
  * form: 0 = plain, 1 = row-gathered (gemm_gather_rows), 2 = row-scattered
- * (gemm_scatter_rows), 3 = seeded (gemm_seeded); any other value is
- * GEMM_ERR_INVALID_ARG.  has_c: C
+ * (gemm_scatter_rows), 3 = seeded (gemm_seeded), 4 = FP4 weights
+ * (gemm_bf16_e2m1); any other value is GEMM_ERR_INVALID_ARG.  has_c: C
  * is given and beta != 0.
  *
  *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles, one

@@ -55,6 +55,8 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_bf16.argtypes = plain
     lib.gemm_gather_rows.argtypes = [i64, i64, i64, i32, vp, i64, i64, vp, vp, i64, vp, i64,
                                      vp, i64, i32, f32, f32, vp]
+    lib.gemm_bf16_e2m1.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                   i32, f32, f32, vp]
     lib.gemm_seeded.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, i32, vp]
     lib.gemm_accumulate.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, f32, vp]
     lib.gemm_scatter_rows.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
@@ -69,7 +71,7 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_debug_inject.argtypes = [i32]
     lib.gemm_debug_force_tile.argtypes = [i32, i32]
     for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows", "gemm_accumulate",
-                 "gemm_seeded",
+                 "gemm_seeded", "gemm_bf16_e2m1",
                  "gemm_skinny_noalloc",
                  "gemm_check_device_status",
                  "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject",
@@ -196,6 +198,29 @@ def gemm_scatter_rows(A, B, idx, D, C=None, *, alpha=1.0, beta=1.0, stream=None)
     return D
 
 
+def gemm_bf16_e2m1(A, Bq, Bs, C=None, D=None, *, alpha=1.0, beta=1.0, out=OUT_F32, stream=None):
+    """D = fma.rn(alpha, A @ W.T, beta * C) with bf16 A (M x K) and FP4 weights W
+    given as packed E2M1 codes Bq (N x K/2 uint8, even k in the low nibble) and
+    UE8M0 block scales Bs (K/32 x N uint8)."""
+    if A.dtype != torch.bfloat16:
+        raise TypeError("A must be bf16")
+    if Bq.dtype != torch.uint8 or Bs.dtype != torch.uint8:
+        raise TypeError("Bq and Bs must be uint8")
+    M, K = A.shape
+    N = Bq.shape[0]
+    if Bq.shape[1] * 2 != K or tuple(Bs.shape) != (K // 32, N):
+        raise ValueError("Bq must be N x K/2 and Bs K/32 x N")
+    if C is not None and (C.dtype != torch.float32 or tuple(C.shape) != (M, N)):
+        raise ValueError("C must be float32 M x N")
+    D = _out_tensor(D, M, N, out, A.device)
+    st = load_library().gemm_bf16_e2m1(
+        M, N, K, _ptr(A), _ld(A), _ptr(Bq), _ld(Bq), _ptr(Bs), _ld(Bs), _ptr(C),
+        _ld(C) if C is not None else 0, _ptr(D), _ld(D), out, float(alpha), float(beta),
+        _stream_ptr(stream))
+    _check(st, "gemm_bf16_e2m1")
+    return D
+
+
 def gemm_seeded(A, B, C, D=None, *, out=OUT_F32, stream=None):
     """D = C + A @ B.T with C (float32 M x N) as the accumulator's starting value:
     every K step of the tensor-core sum accumulates onto it."""
@@ -266,9 +291,9 @@ def gemm_check_device_status(stream=None) -> int:
 
 
 def gemm_query_plan(M, N, K, gather=False, has_c=False, sm_count=148, scatter=False,
-                    seeded=False) -> Plan:
+                    seeded=False, fp4=False) -> Plan:
     p = Plan()
-    form = 1 if gather else (2 if scatter else (3 if seeded else 0))
+    form = 1 if gather else (2 if scatter else (3 if seeded else (4 if fp4 else 0)))
     _check(load_library().gemm_query_plan(M, N, K, form, int(bool(has_c)),
                                           sm_count, ctypes.byref(p)), "gemm_query_plan")
     return p

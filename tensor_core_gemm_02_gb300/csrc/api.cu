@@ -277,6 +277,19 @@ gemm_status validate(const Problem &p, bool *empty)
         return GEMM_ERR_INVALID_ARG;
     if (p.seed && (!p.C || p.gather || p.scatter || p.reduce))
         return GEMM_ERR_INVALID_ARG;
+    if (p.w4) {
+        if (!p.bf16 || p.gather || p.scatter || p.reduce || p.seed)
+            return GEMM_ERR_INVALID_ARG;
+        if (p.K % 32 != 0)
+            return GEMM_ERR_UNSUPPORTED;  // whole scale blocks only
+        if (p.K > 0 && (!p.bscale || p.ldbs < p.N))
+            return GEMM_ERR_INVALID_ARG;
+        if (p.ldbs > kMaxDim)
+            return GEMM_ERR_UNSUPPORTED;
+    }
+    // B: N rows of K 16-bit elements, or (FP4) of K / 2 bytes
+    const int64_t b_cols = p.w4 ? p.K / 2 : p.K;
+    const int64_t b_esize = p.w4 ? 1 : 2;
     if (p.d_rows > kMaxDim)
         return GEMM_ERR_UNSUPPORTED;
     // rows of C and D: M, or the rows of the matrix the result is scattered into
@@ -285,12 +298,13 @@ gemm_status validate(const Problem &p, bool *empty)
         return GEMM_ERR_INVALID_ARG;
     if (c_used && p.ldc < p.N)
         return GEMM_ERR_INVALID_ARG;
-    if (p.K > 0 && (p.lda < p.K || p.ldb < p.K))
+    if (p.K > 0 && (p.lda < p.K || p.ldb < b_cols))
         return GEMM_ERR_INVALID_ARG;
     if (p.lda > kMaxDim || p.ldb > kMaxDim || p.ldc > kMaxDim || p.ldd > kMaxDim)
         return GEMM_ERR_UNSUPPORTED;
     // alignment: 16-byte bases, row pitches that are multiples of 16 bytes
-    if (p.K > 0 && (!aligned16(p.A) || !aligned16(p.B) || (p.lda * 2) % 16 || (p.ldb * 2) % 16))
+    if (p.K > 0 &&
+        (!aligned16(p.A) || !aligned16(p.B) || (p.lda * 2) % 16 || (p.ldb * b_esize) % 16))
         return GEMM_ERR_ALIGNMENT;
     // C and D only need their natural element alignment: when their base or
     // row pitch is not 16-byte aligned the epilogue uses plain loads/stores
@@ -305,7 +319,9 @@ gemm_status validate(const Problem &p, bool *empty)
     if (p.K > 0) {
         if (overlap(p.D, d_span, p.A, span_bytes(p.a_rows, p.K, p.lda, 2)))
             return GEMM_ERR_ALIAS;
-        if (overlap(p.D, d_span, p.B, span_bytes(p.N, p.K, p.ldb, 2)))
+        if (overlap(p.D, d_span, p.B, span_bytes(p.N, b_cols, p.ldb, b_esize)))
+            return GEMM_ERR_ALIAS;
+        if (p.w4 && overlap(p.D, d_span, p.bscale, span_bytes(p.K / 32, p.N, p.ldbs, 1)))
             return GEMM_ERR_ALIAS;
     }
     if ((p.gather || p.scatter) && overlap(p.D, d_span, p.idx, static_cast<uint64_t>(p.M) * 4))
@@ -470,14 +486,14 @@ void set_tiny_plan(gemm_plan &p, int64_t M, int64_t N)
 }
 
 gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count,
-                    bool scatter, bool seeded)
+                    bool scatter, bool seeded, bool w4)
 {
     gemm_plan p;
     std::memset(&p, 0, sizeof(p));
     if (M == 0 || N == 0)
         return p;
     // (sizes are at most 2^31 each: bound the factors before multiplying)
-    if (M <= kTinyWork && N <= kTinyWork && M * N <= kTinyWork &&
+    if (!(w4 && K > 0) && M <= kTinyWork && N <= kTinyWork && M * N <= kTinyWork &&
         M * N * (K > 0 ? K : 1) <= kTinyWork) {
         set_tiny_plan(p, M, N);
         return p;
@@ -495,7 +511,7 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, i
         p.kernel = 2;
         p.bm = mp;
         p.bn = 128;
-        p.stages = tcg::skinny_stages(mp);
+        p.stages = w4 ? tcg::skinny_w4_stages(mp) : tcg::skinny_stages(mp);
         p.tiles = tiles;
         p.splits = tcg::skinny_max_parts(tiles, nkb, G);
         p.grid = static_cast<int32_t>(G);
@@ -531,16 +547,89 @@ void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev)
     a.timeout_ns = g_timeout_ns.load();
 }
 
+// Buffers of the FP4 paths, one per (device, stream, use), grown
+// geometrically: kBufWeights holds the bf16 copy of the weights for M > 64,
+// kBufScales a copy of the scales with a 16-byte row pitch for the TMA loads
+// of the M <= 64 path when the caller's pitch or base is not 16-byte aligned.
+enum { kBufWeights = 0, kBufScales = 1 };
+struct DequantBuffer {
+    int device = -1;
+    cudaStream_t stream = nullptr;
+    int use = 0;
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_dq_mu;
+std::vector<DequantBuffer> g_dq;
+
+gemm_status get_dequant_buffer(int device, cudaStream_t stream, int use, size_t bytes,
+                               void **out)
+{
+    std::lock_guard<std::mutex> lock(g_dq_mu);
+    DequantBuffer *b = nullptr;
+    for (DequantBuffer &x : g_dq)
+        if (x.device == device && x.stream == stream && x.use == use)
+            b = &x;
+    if (!b) {
+        g_dq.push_back(DequantBuffer{});
+        b = &g_dq.back();
+        b->device = device;
+        b->stream = stream;
+        b->use = use;
+    }
+    if (b->bytes < bytes) {
+        if (b->ptr) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess)  // earlier calls may still read it
+                return GEMM_ERR_CUDA;
+            cudaFree(b->ptr);
+            b->ptr = nullptr;
+        }
+        const size_t nb = bytes > 2 * b->bytes ? bytes : 2 * b->bytes;
+        b->bytes = 0;
+        if (cudaMalloc(&b->ptr, nb) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        b->bytes = nb;
+    }
+    *out = b->ptr;
+    return GEMM_OK;
+}
+
 gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo *dev)
 {
     const int mp = plan.bm;
     GemmMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (!encode_2d(&maps.a, ab_type(p.bf16), p.A, p.K, p.M, p.lda * 2, 64,
-                   static_cast<uint32_t>(mp), CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&maps.b, ab_type(p.bf16), p.B, p.K, p.N, p.ldb * 2, 64, 128,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+                   static_cast<uint32_t>(mp), CU_TENSOR_MAP_SWIZZLE_128B))
         return GEMM_ERR_CUDA;
+    if (p.w4) {
+        // codes: 32-byte boxes (64 elements) of 128 rows; scales: the block's
+        // two rows of 128 columns (rows 16-byte aligned for TMA: copy them if
+        // the caller's are not)
+        const void *scales = p.bscale;
+        int64_t lds = p.ldbs;
+        if (!aligned16(scales) || lds % 16) {
+            const int64_t pitch = (p.N + 15) / 16 * 16;
+            void *buf = nullptr;
+            gemm_status st = get_dequant_buffer(dev->index, p.stream, kBufScales,
+                                                static_cast<size_t>(pitch) * (p.K / 32), &buf);
+            if (st != GEMM_OK)
+                return st;
+            if (cudaMemcpy2DAsync(buf, pitch, p.bscale, p.ldbs, p.N, p.K / 32,
+                                  cudaMemcpyDeviceToDevice, p.stream) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            scales = buf;
+            lds = pitch;
+        }
+        if (!encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K / 2, p.N, p.ldb, 32, 128,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, p.N, p.K / 32, lds, 128, 2,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GEMM_ERR_CUDA;
+    } else if (!encode_2d(&maps.b, ab_type(p.bf16), p.B, p.K, p.N, p.ldb * 2, 64, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) {
+        return GEMM_ERR_CUDA;
+    }
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     fill_common(a, p, dev);
@@ -563,7 +652,8 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
         a.workspace = w.partials;
         a.counters = w.counters;
     }
-    const cudaError_t e = tcg::launch_skinny(mp, maps, a, plan.grid, p.stream);
+    const cudaError_t e = p.w4 ? tcg::launch_skinny_w4(mp, maps, a, plan.grid, p.stream)
+                               : tcg::launch_skinny(mp, maps, a, plan.grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -591,8 +681,8 @@ gemm_status run_tiny(const Problem &p, const gemm_plan &plan, const DeviceInfo *
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || plan.kernel == 0)
-        return plan;
+    if (fk == 0 || plan.kernel == 0 || p.w4)
+        return plan;  // (FP4 weights run only on their own paths)
     if (fk == 10) {
         set_tiny_plan(plan, p.M, p.N);  // the warp-level kernel runs every problem
         return plan;
@@ -616,10 +706,29 @@ gemm_status run(const Problem &p)
     DeviceInfo *dev = nullptr;
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
+    if (p.w4 && p.K > 0 && p.M > 64) {
+        // many rows: turn the weights into bf16 once (exact: every code times a
+        // power of two fits bf16 unless it leaves its range) and run the bf16 GEMM
+        void *wb = nullptr;
+        if ((st = get_dequant_buffer(dev->index, p.stream, kBufWeights,
+                                     static_cast<size_t>(p.N) * p.K * 2, &wb)) != GEMM_OK)
+            return st;
+        if (tcg::launch_dequant_fp4(static_cast<const uint8_t *>(p.B), p.ldb, p.bscale, p.ldbs,
+                                    static_cast<int32_t>(p.N), static_cast<int32_t>(p.K),
+                                    static_cast<uint16_t *>(wb), p.K, p.stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        Problem q = p;
+        q.w4 = false;
+        q.B = wb;
+        q.ldb = p.K;
+        q.bscale = nullptr;
+        return run(q);
+    }
     const bool c_used = p.C != nullptr && p.beta != 0.0f;
     const gemm_plan plan = apply_forced_tile(
-        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count, p.scatter, p.seed), p,
-        dev->sm_count);
+        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count, p.scatter, p.seed,
+                  p.w4 && p.K > 0),
+        p, dev->sm_count);
 
     GemmMaps maps;
     std::memset(&maps, 0, sizeof(maps));
@@ -787,6 +896,19 @@ gemm_status gemm_seeded(int64_t M, int64_t N, int64_t K, int dtype_is_bf16, cons
     return run(p);
 }
 
+gemm_status gemm_bf16_e2m1(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                           const uint8_t *Bq, int64_t ldbq, const uint8_t *Bs, int64_t ldbs,
+                           const float *C, int64_t ldc, void *D, int64_t ldd, int out,
+                           float alpha, float beta, void *stream)
+{
+    Problem p{M, N, K, true, A, M, lda, nullptr, Bq, ldbq, C, ldc, D, ldd,
+              out, alpha, beta, false, static_cast<cudaStream_t>(stream)};
+    p.w4 = true;
+    p.bscale = Bs;
+    p.ldbs = ldbs;
+    return run(p);
+}
+
 gemm_status gemm_check_device_status(void *stream)
 {
     DeviceInfo *dev = nullptr;
@@ -827,9 +949,10 @@ gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int form, int has_c
 {
     if (!plan || sm_count < 1 || M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (form < 0 || form > 3)
+    if (form < 0 || form > 4)
         return GEMM_ERR_INVALID_ARG;
-    *plan = make_plan(M, N, K, form == 1, has_c != 0 || form == 3, sm_count, form == 2, form == 3);
+    *plan = make_plan(M, N, K, form == 1, has_c != 0 || form == 3, sm_count, form == 2, form == 3,
+                      form == 4 && K > 0);
     return GEMM_OK;
 }
 

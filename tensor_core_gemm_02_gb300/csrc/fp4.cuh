@@ -1,0 +1,41 @@
+// fp4.cuh -- FP4 E2M1 codes and UE8M0 block scales to bf16.
+//
+// Code values follow the OCP Microscaling definition that the "cp.async.bulk.
+// tensor" page's float4_e2m1fn format name refers to (section "Interleave and
+// packed FP4"): sign, two exponent bits with bias 1, one mantissa bit, the zero
+// exponent subnormal; a UE8M0 scale s stands for 2^(s - 127), 255 for NaN.
+#pragma once
+
+#include <stdint.h>
+
+namespace tcg {
+
+// The low and the high byte of the bf16 value of codes 0..7 (0, 0.5, 1, 1.5,
+// 2, 3, 4, 6): codes 0-3 in the first word of each pair, 4-7 in the second.
+constexpr uint32_t kE2m1LoA = 0xC0800000u, kE2m1LoB = 0xC0804000u;
+constexpr uint32_t kE2m1HiA = 0x3F3F3F00u, kE2m1HiB = 0x40404040u;
+
+// Four codes (element i in nibble i of w) -> two bf16x2 words (elements 0,1 and
+// 2,3), multiplied by the block scale `sc2` (bf16x2, both halves the same power
+// of two, so the products are exact unless they leave bf16's range).
+__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t w, uint32_t sc2, uint32_t &p01,
+                                               uint32_t &p23)
+{
+    const uint32_t sel = w & 0x7777u;  // magnitudes (sign bits cleared)
+    const uint32_t lo = __byte_perm(kE2m1LoA, kE2m1LoB, sel);
+    const uint32_t hi = __byte_perm(kE2m1HiA, kE2m1HiB, sel);
+    p01 = __byte_perm(lo, hi, 0x5140u) | ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
+    p23 = __byte_perm(lo, hi, 0x7362u) | ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(p01) : "r"(sc2));
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(p23) : "r"(sc2));
+}
+
+// UE8M0 scale byte -> bf16x2 with 2^(s - 127) in both halves (0 is the
+// subnormal 2^-127, 255 NaN).
+__device__ __forceinline__ uint32_t ue8m0_to_bf16x2(uint32_t s)
+{
+    const uint32_t h = s == 255u ? 0x7FC0u : (s == 0u ? 0x0040u : (s << 7));
+    return h | (h << 16);
+}
+
+}  // namespace tcg

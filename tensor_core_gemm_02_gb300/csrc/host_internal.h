@@ -41,6 +41,11 @@ struct Problem {
     int64_t d_rows = 0;    // rows of C and D when scattering
     bool reduce = false;   // D += alpha * A * B^T into float32 D (no C)
     bool seed = false;     // D = C + A * B^T with C as the accumulator's starting value
+    // FP4 B: B holds E2M1 codes (N rows of K/2 bytes, ldb bytes apart), bscale
+    // the UE8M0 block scales (K/32 rows of N bytes, ldbs bytes apart)
+    bool w4 = false;
+    const uint8_t *bscale = nullptr;
+    int64_t ldbs = 0;
 };
 
 // Per-device state (SM count, status word address); first call sets it up.
@@ -57,7 +62,7 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dtype, const void *ptr, uint6
 CUtensorMapDataType ab_type(bool bf16);
 int64_t ceil_div(int64_t a, int64_t b);
 gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count,
-                    bool scatter = false, bool seeded = false);
+                    bool scatter = false, bool seeded = false, bool w4 = false);
 
 // Launch the warp-level kernel for a validated problem with a plan of kernel 10.
 gemm_status run_tiny(const Problem &p, const gemm_plan &plan, const DeviceInfo *dev);

@@ -1,4 +1,5 @@
-// launch_skinny.cu -- instantiations and launcher of the swap-AB stream-K kernel.
+// launch_skinny.cu -- instantiations and launcher of the swap-AB stream-K kernel
+// (bf16/f16 B, or FP4 B with block scales converted in shared memory).
 #include <cuda_runtime.h>
 
 #include "kernel_skinny.cuh"
@@ -13,12 +14,13 @@ namespace tcg {
 
 namespace {
 
-template <int MP>
+template <int MP, bool W4>
 cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                                cudaStream_t stream)
 {
-    using Cfg = SkinnyCfg<MP, TCG_SKINNY_KBOX>;
-    auto kfn = skinny_gemm_kernel<MP, TCG_SKINNY_KBOX>;
+    constexpr int KBOX = W4 ? 1 : TCG_SKINNY_KBOX;
+    using Cfg = SkinnyCfg<MP, KBOX, W4>;
+    auto kfn = skinny_gemm_kernel<MP, KBOX, W4>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_ALLOC));
     if (e != cudaSuccess)
@@ -33,7 +35,7 @@ cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int g
     attr[0].val.programmaticStreamSerializationAllowed = TCG_PDL;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, args);
+    return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, args);
 }
 
 }  // namespace
@@ -54,9 +56,30 @@ cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, in
                           cudaStream_t stream)
 {
     switch (mp) {
-    case 16: return launch_skinny_impl<16>(maps, args, grid, stream);
-    case 32: return launch_skinny_impl<32>(maps, args, grid, stream);
-    case 64: return launch_skinny_impl<64>(maps, args, grid, stream);
+    case 16: return launch_skinny_impl<16, false>(maps, args, grid, stream);
+    case 32: return launch_skinny_impl<32, false>(maps, args, grid, stream);
+    case 64: return launch_skinny_impl<64, false>(maps, args, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int skinny_w4_stages(int mp)
+{
+    switch (mp) {
+    case 16: return SkinnyCfg<16, 1, true>::STAGES;
+    case 32: return SkinnyCfg<32, 1, true>::STAGES;
+    case 64: return SkinnyCfg<64, 1, true>::STAGES;
+    default: return 0;
+    }
+}
+
+cudaError_t launch_skinny_w4(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
+                             cudaStream_t stream)
+{
+    switch (mp) {
+    case 16: return launch_skinny_impl<16, true>(maps, args, grid, stream);
+    case 32: return launch_skinny_impl<32, true>(maps, args, grid, stream);
+    case 64: return launch_skinny_impl<64, true>(maps, args, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -488,6 +488,13 @@ __device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[16])
                  : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Registers -> TMEM, the dual of tc_ld_32x32b_x32: thread t of the warp writes
 // lane (taddr lane + t), columns col .. col+31.  Followed by tc_wait_st before
 // the values may be read by an MMA (with a fence and barrier in between).

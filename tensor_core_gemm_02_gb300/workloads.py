@@ -37,6 +37,12 @@ torch ``.to(torch.bfloat16)``, both round-to-nearest-even):
   skinny_accumulate_16x28672x4096
                    the skinny draws; D starts as C[:16] and receives
                    D += 0.5 * A @ B.T (the accumulating form, no C operand).
+  fp4_skinny_16x28672x4096
+                   seed 6: A (16, 4096) N(0,1) -> bf16; FP4 weights as codes
+                   integers(0, 256, (28672, 2048)) uint8 (two E2M1 codes per
+                   byte) and scales integers(118, 121, (128, 28672)) uint8
+                   (2^-9 .. 2^-7: weights of the size of 0.02 * N(0,1));
+                   C (16, 28672) N(0,1) float32; alpha = 0.5, beta = 1; fp32 out.
 """
 from __future__ import annotations
 
@@ -67,6 +73,12 @@ class Problem:
     d_rows: int = 0
     D0: torch.Tensor | None = None  # scattered / accumulating forms: D before the call
     accumulate: bool = False        # D += alpha * A @ B.T into float32 D = D0
+    Bs: torch.Tensor | None = None  # FP4 weights: B holds codes (N x K/2 uint8), Bs the
+                                    # UE8M0 scales (K/32 x N uint8)
+
+    @property
+    def fp4(self) -> bool:
+        return self.Bs is not None
 
     @property
     def M(self) -> int:
@@ -154,6 +166,15 @@ def skinny_accumulate_16x28672x4096() -> Problem:
                    beta=0.0, out=OUT_F32, D0=C, accumulate=True)
 
 
+def fp4_skinny_16x28672x4096() -> Problem:
+    rng = np.random.default_rng(6)
+    A = _bf16(rng.standard_normal((16, 4096), dtype=np.float32))
+    Bq = torch.from_numpy(rng.integers(0, 256, (28672, 2048)).astype(np.uint8))
+    Bs = torch.from_numpy(rng.integers(118, 121, (128, 28672)).astype(np.uint8))
+    C = torch.from_numpy(rng.standard_normal((16, 28672), dtype=np.float32))
+    return Problem("fp4_skinny_16x28672x4096", A, Bq, C, alpha=0.5, beta=1.0, out=OUT_F32, Bs=Bs)
+
+
 def scatter_16384_into_65536() -> Problem:
     rng = np.random.default_rng(5)
     A = _bf16(rng.standard_normal((16384, 4096), dtype=np.float32))
@@ -172,6 +193,7 @@ WORKLOADS = {
     "gather_16384_of_65536": gather_16384_of_65536,
     "scatter_16384_into_65536": scatter_16384_into_65536,
     "skinny_accumulate_16x28672x4096": skinny_accumulate_16x28672x4096,
+    "fp4_skinny_16x28672x4096": fp4_skinny_16x28672x4096,
 }
 
 

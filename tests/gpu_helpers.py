@@ -21,6 +21,9 @@ def run(p, D=None, stream=None):
     """Launch the problem on the GPU through the library; returns D (device)."""
     A, B = p.A.to(DEV), p.B.to(DEV)
     C = p.C.to(DEV) if p.C is not None else None
+    if p.fp4:
+        return binding.gemm_bf16_e2m1(A, B, p.Bs.to(DEV), C, D, alpha=p.alpha, beta=p.beta,
+                                      out=p.out, stream=stream)
     if p.accumulate:
         if D is None:
             D = p.D0.to(DEV).contiguous()

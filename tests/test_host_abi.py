@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows",
-              "gemm_accumulate", "gemm_seeded", "gemm_check_device_status",
+              "gemm_accumulate", "gemm_seeded", "gemm_bf16_e2m1", "gemm_check_device_status",
               "gemm_status_string"):
         assert n in names
 
@@ -154,6 +154,30 @@ def test_seeded_argument_checks(lib):
     assert binding.gemm_query_plan(16, 8, 32, seeded=True, sm_count=148).kernel == 10
 
 
+def test_fp4_argument_checks(lib):
+    f = lib.gemm_bf16_e2m1
+    S0 = 0x60000000
+
+    def call(M=16, N=256, K=128, A=A0, lda=128, Bq=B0, ldq=64, Bs=S0, lds=256, C=None, ldc=0,
+             D=D0, ldd=256, out=0):
+        return f(M, N, K, A, lda, Bq, ldq, Bs, lds, C, ldc, D, ldd, out, 1.0, 0.0, None)
+
+    assert call(Bs=None) == 1
+    assert call(ldq=32) == 1            # < K / 2
+    assert call(lds=128) == 1           # < N
+    assert call(K=48, lda=64) == 3      # not a multiple of 32
+    assert call(ldq=72) == 2            # not a multiple of 16 bytes
+    # (an unaligned scale base or pitch is fine: the library copies the scales)
+    assert call(D=B0 + 64) == 4         # D overlaps the codes
+    assert call(D=S0 + 16) == 4         # D overlaps the scales
+    assert call(M=0) == 0
+    # M <= 64: the skinny kernel with converter warps; more rows: the bf16 plan
+    p = binding.gemm_query_plan(16, 28672, 4096, fp4=True, sm_count=148)
+    assert (p.kernel, p.bm) == (2, 16) and p.stages > 0
+    assert binding.gemm_query_plan(16, 8, 64, fp4=True, sm_count=148).kernel == 2  # never tiny
+    assert binding.gemm_query_plan(4096, 4096, 4096, fp4=True, sm_count=148).kernel == 4
+
+
 def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bm, p.bn, p.grid) == (4, 256, 512, 148)
@@ -186,7 +210,7 @@ def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(16, 28672, 4096, scatter=True, sm_count=148)
     assert p.kernel == 2
     plan = binding.Plan()
-    assert lib.gemm_query_plan(64, 64, 64, 4, 0, 148, ctypes.byref(plan)) == 1
+    assert lib.gemm_query_plan(64, 64, 64, 5, 0, 148, ctypes.byref(plan)) == 1
     p = binding.gemm_query_plan(100, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bn) == (1, 64)
     p = binding.gemm_query_plan(40, 1000, 64, sm_count=148)
