@@ -502,7 +502,7 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, i
         // few rows: swap A and B so B streams through the MMA's M side
         const int mp = skinny_rows(M);
         const int64_t tiles = ceil_div(N, 128);
-        const int64_t nkb = ceil_div(K, tcg::skinny_kstage());
+        const int64_t nkb = ceil_div(K, w4 ? tcg::skinny_w4_kstage() : tcg::skinny_kstage());
         const int64_t W = tiles * nkb;
         // at least TCG_SKINNY_MIN_KB K blocks per CTA, so small problems are
         // not cut into many parts whose reduction costs more than it saves
@@ -621,9 +621,9 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
             scales = buf;
             lds = pitch;
         }
-        if (!encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K / 2, p.N, p.ldb, 32, 128,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, p.N, p.K / 32, lds, 128, 2,
+        if (!encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K / 2, p.N, p.ldb, 128, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, p.N, p.K / 32, lds, 128, 8,
                        CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_ERR_CUDA;
     } else if (!encode_2d(&maps.b, ab_type(p.bf16), p.B, p.K, p.N, p.ldb * 2, 64, 128,
@@ -635,7 +635,8 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
     fill_common(a, p, dev);
     a.num_m_blocks = 1;
     a.num_n_blocks = static_cast<int32_t>(plan.tiles);
-    a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, tcg::skinny_kstage()));
+    a.num_k_blocks =
+        static_cast<int32_t>(ceil_div(p.K, p.w4 ? tcg::skinny_w4_kstage() : tcg::skinny_kstage()));
     a.num_tiles = static_cast<int32_t>(plan.tiles);
     a.group_m = 1;
     a.splits = plan.splits;

@@ -30,6 +30,39 @@ __device__ __forceinline__ void e2m1x4_to_bf16(uint32_t w, uint32_t sc2, uint32_
     asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(p23) : "r"(sc2));
 }
 
+// prmt.b32 in its default mode: byte n of the result is byte (s >> 4n) & 7 of
+// {b, a}, or, when bit 3 of that selector nibble is set, the top bit of that
+// byte copied into all eight bits (PTX ISA, prmt).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(s));
+    return r;
+}
+
+// Eight codes (element i in nibble i of w) -> four bf16x2 words (elements 2j,
+// 2j+1 in word j), times the block scale sc2.  The magnitudes go through the
+// byte tables four codes per permute; the signs through the permute's
+// sign-replicating mode, which copies the top bit of a source byte: the sign of
+// code 2j+1 is the top bit of byte j of w, that of code 2j the top bit of byte
+// j of w << 4.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t sc2, uint32_t (&p)[4])
+{
+    const uint32_t m = w & 0x77777777u;
+    const uint32_t lo0 = prmt(kE2m1LoA, kE2m1LoB, m);
+    const uint32_t hi0 = prmt(kE2m1HiA, kE2m1HiB, m);
+    const uint32_t lo1 = prmt(kE2m1LoA, kE2m1LoB, m >> 16);
+    const uint32_t hi1 = prmt(kE2m1HiA, kE2m1HiB, m >> 16);
+    const uint32_t se = w << 4;
+    p[0] = prmt(lo0, hi0, 0x5140u) | (prmt(se, w, 0xC080u) & 0x80008000u);
+    p[1] = prmt(lo0, hi0, 0x7362u) | (prmt(se, w, 0xD090u) & 0x80008000u);
+    p[2] = prmt(lo1, hi1, 0x5140u) | (prmt(se, w, 0xE0A0u) & 0x80008000u);
+    p[3] = prmt(lo1, hi1, 0x7362u) | (prmt(se, w, 0xF0B0u) & 0x80008000u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(p[j]) : "r"(sc2));
+}
+
 // UE8M0 scale byte -> bf16x2 with 2^(s - 127) in both halves (0 is the
 // subnormal 2^-127, 255 NaN).
 __device__ __forceinline__ uint32_t ue8m0_to_bf16x2(uint32_t s)

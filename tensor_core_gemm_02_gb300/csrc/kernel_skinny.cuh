@@ -38,20 +38,27 @@ struct SkinnyCfg {
     static constexpr int KBOX = KBOX_;  // boxes per stage: each row of B is read KBOX*128 B at a time
     static constexpr int KSTAGE = BK * KBOX;
     // W4: B arrives as FP4 codes (two per byte) with one UE8M0 scale per 32
-    // elements, and converter warps turn each stage into the bf16 image the MMA
-    // reads, in a ring of CSLOTS slots of their own
+    // elements, KBOX = 4 blocks of 64 per stage so each row of codes is read
+    // in 128-byte runs (32-byte runs leave HBM mostly idle); converter warps
+    // turn each 64-wide block into the bf16 image the MMA reads, in a ring of
+    // CSLOTS slots of their own
     static constexpr bool W4 = W4_;
-    static constexpr uint32_t RAW_B = W4 ? BN * BK / 2 : 0;   // 128 rows x 32 bytes of codes
-    static constexpr uint32_t SCALE_B = W4 ? 2 * BN : 0;      // 2 scale rows x 128 columns
-    static constexpr int CSLOTS = W4 ? 4 : 0;
+    static constexpr uint32_t RAW_B = W4 ? BN * BK / 2 * KBOX : 0;  // 128 rows x 128 bytes of codes
+    static constexpr uint32_t SCALE_B = W4 ? 2 * KBOX * BN : 0;     // 8 scale rows x 128 columns
+    // converted slots, handed to the MMA a stage (KBOX slots) at a time: one
+    // barrier handshake per stage instead of per block (the single MMA-issuing
+    // thread's waits and commits, not the conversion, had set the rate)
+    static constexpr int CSETS = W4 ? (MP >= 64 ? 1 : 2) : 0;
+    static constexpr int CSLOTS = CSETS * KBOX;
     static constexpr uint32_t B_BOX = BN * BK * 2;
     static constexpr uint32_t A_BOX = MP * BK * 2;
     static constexpr uint32_t B_BYTES = W4 ? 0 : KBOX * B_BOX;
     static constexpr uint32_t A_BYTES = KBOX * A_BOX;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + RAW_B + SCALE_B;
     static constexpr uint32_t CB_BYTES = CSLOTS * B_BOX;  // converted ring (W4)
-    // as many stages as fit in about 200 KB of shared memory (at most 16)
-    static constexpr uint32_t RING_BUDGET = 204800 - CB_BYTES;
+    // as many stages as fit in about 200 KB of shared memory (at most 16); W4
+    // takes up to 220 KB for its two rings
+    static constexpr uint32_t RING_BUDGET = (W4 ? 225280u : 204800u) - CB_BYTES;
     static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) < 16 ? (RING_BUDGET / STAGE_BYTES) : 16;
     static constexpr uint32_t OFF_CB = 0;
     static constexpr uint32_t OFF_B = CB_BYTES;
@@ -59,17 +66,19 @@ struct SkinnyCfg {
     static constexpr uint32_t OFF_RAW = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_SC = OFF_RAW + STAGES * RAW_B;
     static constexpr uint32_t OFF_BAR = (OFF_SC + STAGES * SCALE_B + 7u) & ~7u;
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 2 * CSLOTS;
-    // converter warps: 8 (two threads per row of B), or 4 for MP = 64, whose
-    // epilogue needs the registers that more threads would take
-    static constexpr int CONV_WARPS = W4 ? (MP >= 64 ? 4 : 8) : 0;
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 2 * CSETS;
+    // converter warps: one group of four per converted set, taking alternate
+    // stages (one thread per row of B); MP = 64's epilogue needs the registers
+    // that more threads would take
+    static constexpr int CONV_GROUPS = CSETS;
+    static constexpr int CONV_WARPS = 4 * CONV_GROUPS;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;  // MP destination rows (scattered rows)
     static constexpr uint32_t SMEM_BYTES = OFF_ROWS + MP * 4;
     static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = (2 * MP < 32) ? 32 : 2 * MP;
     static constexpr int THREADS = 192 + 32 * CONV_WARPS;
-    static_assert(!W4 || KBOX == 1, "W4 stages are one 64-wide K block");
+    static_assert(!W4 || KBOX == 4, "W4 stages hold 128-byte runs of codes");
     static_assert(OFF_RAW % 1024 == 0 && RAW_B % 128 == 0, "TMA destinations stay aligned");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MMA N for M = 128 is a multiple of 16");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation is a power of two");
@@ -164,8 +173,8 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 4 + c); };
-    auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 4 + Cfg::CSLOTS + c); };
+    auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 4 + c); };  // per converted set
+    auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 4 + Cfg::CSETS + c); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
     volatile uint32_t *arrival = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 8);
@@ -182,12 +191,15 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         const int32_t kb = static_cast<int32_t>(q - t * nkb);
         mbar_arrive_expect_tx(full_bar(st), Cfg::STAGE_BYTES + extra);
         if constexpr (W4) {
-            // 128 rows x 32 bytes of codes, the block's two scale rows, A
-            tma_load_2d(base + Cfg::OFF_RAW + st * Cfg::RAW_B, &tmB, full_bar(st), kb * (Cfg::BK / 2),
-                        t * Cfg::BN);
+            // 128 rows x 128 bytes of codes (128-byte swizzle), the stage's
+            // eight scale rows, and KBOX boxes of A
+            tma_load_2d(base + Cfg::OFF_RAW + st * Cfg::RAW_B, &tmB, full_bar(st),
+                        kb * (Cfg::KSTAGE / 2), t * Cfg::BN);
             tma_load_2d(base + Cfg::OFF_SC + st * Cfg::SCALE_B, &tmS, full_bar(st), t * Cfg::BN,
-                        kb * 2);
-            tma_load_2d(base + Cfg::OFF_A + st * Cfg::A_BYTES, &tmA, full_bar(st), kb * Cfg::BK, 0);
+                        kb * (Cfg::KSTAGE / 32));
+            for (int j = 0; j < KBOX; ++j)
+                tma_load_2d(base + Cfg::OFF_A + st * Cfg::A_BYTES + j * Cfg::A_BOX, &tmA,
+                            full_bar(st), kb * Cfg::KSTAGE + j * Cfg::BK, 0);
         } else {
             for (int j = 0; j < KBOX; ++j) {
                 const int32_t k0 = kb * Cfg::KSTAGE + j * Cfg::BK;
@@ -203,10 +215,11 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1 + Cfg::CONV_WARPS);  // the MMA, and each converter warp (W4)
+            // the MMA, and (W4) each warp of the converter group that takes the stage
+            mbar_init(empty_bar(s), W4 ? 5 : 1);
         }
-        for (int c = 0; c < Cfg::CSLOTS; ++c) {
-            mbar_init(cfull_bar(c), Cfg::CONV_WARPS);
+        for (int c = 0; c < Cfg::CSETS; ++c) {
+            mbar_init(cfull_bar(c), 4);
             mbar_init(cempty_bar(c), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -283,7 +296,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             uint32_t ph = 0;
             int ab = 0;
             uint32_t aph = 0;
-            int cs = 0;  // converted slot (W4)
+            int cset = 0;  // converted set (W4)
             uint32_t cph = 0;
             bool alive = true;
             for (int64_t pos = my_start; pos < my_end && alive;) {
@@ -301,16 +314,16 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                         alive = false;
                         break;
                     }
-                    if (W4 && !wait_bounded(cfull_bar(cs), cph, abort_flag, args.status,
+                    if (W4 && !wait_bounded(cfull_bar(cset), cph, abort_flag, args.status,
                                             args.timeout_ns, kWhereMmaFull)) {
-                        alive = false;
+                        alive = false;  // (the stage's blocks, as bf16 in converted set cset)
                         break;
                     }
                     tc_fence_after_sync();
 #pragma unroll
                     for (int j = 0; j < KBOX; ++j) {
                         const uint64_t bd =
-                            W4 ? sdesc_k_sw128(base + Cfg::OFF_CB + cs * Cfg::B_BOX)
+                            W4 ? sdesc_k_sw128(base + Cfg::OFF_CB + (cset * KBOX + j) * Cfg::B_BOX)
                                : sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES + j * Cfg::B_BOX);
                         const uint64_t ad =
                             sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES + j * Cfg::A_BOX);
@@ -325,9 +338,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                         ph ^= 1u;
                     }
                     if (W4) {
-                        tc_commit(cempty_bar(cs));
-                        if (++cs == Cfg::CSLOTS) {
-                            cs = 0;
+                        tc_commit(cempty_bar(cset));
+                        if (++cset == Cfg::CSETS) {
+                            cset = 0;
                             cph ^= 1u;
                         }
                     }
@@ -470,53 +483,49 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         }
     } else if constexpr (W4) {
         // ------------------------------------------------------------ converters
-        // Unit u = 2 * row + half of a stage is 32 elements of one row of B
-        // (16 bytes of codes, one scale); thread ct converts units ct, ct +
-        // CONV_THREADS, ... into bf16 in the swizzled image the MMA reads as B.
-        constexpr uint32_t kConvThreads = 32u * Cfg::CONV_WARPS;
+        // Group g of four warps takes the stages g, g + G, ... of this CTA's
+        // share (G groups, one converted set each); thread i of the group turns
+        // row i of the stage's codes (KBOX blocks of 32 bytes, two scales each)
+        // into bf16 in the set's swizzled images, which the MMA reads as B.
         const uint32_t ct = threadIdx.x - 192u;
-        int s = 0, cs = 0;
-        uint32_t ph = 0, cph = 0;
-        for (int64_t qb = my_start; qb < my_end; ++qb) {
+        const int32_t group = static_cast<int32_t>(ct / 128u);
+        const uint32_t row = ct % 128u;
+        for (int64_t qs = group; qs < my_end - my_start; qs += Cfg::CONV_GROUPS) {
+            const int s = static_cast<int>(qs % STAGES);
+            const uint32_t ph = static_cast<uint32_t>((qs / STAGES) & 1);
+            const int cset = static_cast<int>(qs % Cfg::CSETS);
+            const uint32_t cph = static_cast<uint32_t>((qs / Cfg::CSETS) & 1);
             if (!warp_wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
                                    kWhereMmaFull))
                 break;
-            if (!warp_wait_bounded(cempty_bar(cs), cph ^ 1u, abort_flag, args.status,
+            if (!warp_wait_bounded(cempty_bar(cset), cph ^ 1u, abort_flag, args.status,
                                    args.timeout_ns, kWhereProducerEmpty))
                 break;
-            const uint32_t dst = base + Cfg::OFF_CB + cs * Cfg::B_BOX;
+            const uint32_t src = base + Cfg::OFF_RAW + s * Cfg::RAW_B + row * 128u;
+            const uint32_t sc = base + Cfg::OFF_SC + s * Cfg::SCALE_B + row;
+#pragma unroll 1
+            for (uint32_t j = 0; j < static_cast<uint32_t>(KBOX); ++j) {
+                // block j: the row's 16-byte chunks 2j, 2j+1 of the 128-byte swizzled image
+                uint32_t w[8];
+                ld_shared_v4(src + (((2u * j) ^ (row & 7u)) << 4), w[0], w[1], w[2], w[3]);
+                ld_shared_v4(src + (((2u * j + 1u) ^ (row & 7u)) << 4), w[4], w[5], w[6], w[7]);
+                const uint32_t sc_lo = ue8m0_to_bf16x2(ld_shared_u8(sc + 2u * j * 128u));
+                const uint32_t sc_hi = ue8m0_to_bf16x2(ld_shared_u8(sc + (2u * j + 1u) * 128u));
+                const uint32_t dst =
+                    base + Cfg::OFF_CB + (static_cast<uint32_t>(cset) * KBOX + j) * Cfg::B_BOX + row * 128u;
 #pragma unroll
-            for (uint32_t u = ct; u < 2u * Cfg::BN; u += kConvThreads) {
-                const uint32_t row = u >> 1, half = u & 1u;
-                uint32_t w[4];
-                ld_shared_v4(base + Cfg::OFF_RAW + s * Cfg::RAW_B + row * 32u + half * 16u, w[0],
-                             w[1], w[2], w[3]);
-                const uint32_t sc2 = ue8m0_to_bf16x2(
-                    ld_shared_u8(base + Cfg::OFF_SC + s * Cfg::SCALE_B + half * 128u + row));
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // 8 codes -> 16-byte chunk half * 4 + j of the 128-byte row (128-byte swizzle)
-                    uint32_t p0, p1, p2, p3;
-                    e2m1x4_to_bf16(w[j] & 0xFFFFu, sc2, p0, p1);
-                    e2m1x4_to_bf16(w[j] >> 16, sc2, p2, p3);
-                    const uint32_t chunk = half * 4u + static_cast<uint32_t>(j);
-                    st_shared_v4(dst + ((row * 128u + chunk * 16u) ^ ((row & 7u) << 4)), p0, p1,
-                                 p2, p3);
+                for (uint32_t k = 0; k < 8; ++k) {
+                    // word k: elements 8k .. 8k+7 -> 16-byte chunk k (128-byte swizzle)
+                    uint32_t p[4];
+                    e2m1x8_to_bf16(w[k], k < 4 ? sc_lo : sc_hi, p);
+                    st_shared_v4(dst + ((k ^ (row & 7u)) << 4), p[0], p[1], p[2], p[3]);
                 }
             }
-            fence_proxy_async_smem();  // the MMA reads the image through the async proxy
+            fence_proxy_async_smem();  // the MMA reads the images through the async proxy
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(cfull_bar(cs));
+                mbar_arrive(cfull_bar(cset));
                 mbar_arrive(empty_bar(s));
-            }
-            if (++s == STAGES) {
-                s = 0;
-                ph ^= 1u;
-            }
-            if (++cs == Cfg::CSLOTS) {
-                cs = 0;
-                cph ^= 1u;
             }
         }
     }

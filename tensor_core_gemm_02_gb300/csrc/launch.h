@@ -40,9 +40,11 @@ cudaError_t launch_tiny(const void *A, int64_t lda, const void *B, int64_t ldb,
                         const GemmArgs &args, int grid, cudaStream_t stream);
 
 int skinny_stages(int mp);
-// The same kernel with FP4 B: maps.b = the codes (uint8, 32-byte boxes of 128
-// rows), maps.c = the block scales (uint8, 128 x 2 boxes); bf16 A.
+// The same kernel with FP4 B: maps.b = the codes (uint8, 128-byte boxes of
+// 128 rows, 128-byte swizzle), maps.c = the block scales (uint8, 128 x 8
+// boxes); bf16 A.
 int skinny_w4_stages(int mp);
+int skinny_w4_kstage();  // K elements per stage (and per stream-K unit) of the FP4 form
 // FP4 codes (N rows of K/2 bytes, ldq apart) and scales (K/32 rows of N bytes,
 // lds apart) -> bf16 N x K rows, ldo elements apart; K a multiple of 32.
 cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldq, const uint8_t *scales,

@@ -18,7 +18,7 @@ template <int MP, bool W4>
 cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                                cudaStream_t stream)
 {
-    constexpr int KBOX = W4 ? 1 : TCG_SKINNY_KBOX;
+    constexpr int KBOX = W4 ? 4 : TCG_SKINNY_KBOX;
     using Cfg = SkinnyCfg<MP, KBOX, W4>;
     auto kfn = skinny_gemm_kernel<MP, KBOX, W4>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -41,6 +41,7 @@ cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int g
 }  // namespace
 
 int skinny_kstage() { return 64 * TCG_SKINNY_KBOX; }
+int skinny_w4_kstage() { return SkinnyCfg<16, 4, true>::KSTAGE; }
 
 int skinny_stages(int mp)
 {
@@ -66,9 +67,9 @@ cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, in
 int skinny_w4_stages(int mp)
 {
     switch (mp) {
-    case 16: return SkinnyCfg<16, 1, true>::STAGES;
-    case 32: return SkinnyCfg<32, 1, true>::STAGES;
-    case 64: return SkinnyCfg<64, 1, true>::STAGES;
+    case 16: return SkinnyCfg<16, 4, true>::STAGES;
+    case 32: return SkinnyCfg<32, 4, true>::STAGES;
+    case 64: return SkinnyCfg<64, 4, true>::STAGES;
     default: return 0;
     }
 }
