@@ -190,10 +190,11 @@ class ClockSampler:
 def kernel_key(plan, p=None):
     """The kernel instance a plan launches for problem p, as ncu names it (for
     profiles/traffic.json): tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, MODE>,
-    MODE 0 plain, 1 scattered rows, 2 reduce-add; skinny_gemm_kernel<MP, 1, W4>."""
+    MODE 0 plain, 1 scattered rows, 2 reduce-add; skinny_gemm_kernel<MP, KBOX, W4>."""
     mode = 0 if p is None else (1 if p.scatter else (2 if p.accumulate else 0))
-    if plan.kernel == 2:
-        return f"skinny_gemm_kernel<{plan.bm}, 1, {1 if p is not None and p.fp4 else 0}>"
+    if plan.kernel == 2:  # (FP4 stages hold four 64-wide K blocks)
+        return ("skinny_gemm_kernel<{}, 4, 1>" if p is not None and p.fp4
+                else "skinny_gemm_kernel<{}, 1, 0>").format(plan.bm)
     if plan.kernel == 10:
         return "tiny_gemm_kernel"
     form = {3: "256, 6, 1, 1, 1", 4: "256, 4, 1, 2, 1", 7: "256, 4, 1, 2, 2",

@@ -75,7 +75,7 @@ def test_kernel_keys_name_the_launched_instance():
     assert bench.kernel_key(p, sc) == "tile_gemm_kernel<256, 6, 1, 1, 1, 1>"
     fp = workloads.Problem("f", torch.zeros(1, 1), torch.zeros(1, 1), Bs=torch.zeros(1, 1))
     p = binding.gemm_query_plan(16, 28672, 4096, fp4=True, sm_count=148)
-    assert bench.kernel_key(p, fp) == "skinny_gemm_kernel<16, 1, 1>"
+    assert bench.kernel_key(p, fp) == "skinny_gemm_kernel<16, 4, 1>"
 
 
 def test_traffic_is_reported_only_for_current_sources(tmp_path, monkeypatch):
