@@ -184,6 +184,27 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
     const int64_t G = gridDim.x;
     const int64_t my_start = W * blockIdx.x / G;
     const int64_t my_end = W * (blockIdx.x + 1) / G;
+    // The share [my_start, my_end) is the tail of one tile, whole tiles, and the
+    // head of another.  The two partial pieces go first: the tiles they belong
+    // to are finished by a neighbour CTA too, so doing them early moves the
+    // last-arriver reductions off the end of the kernel.  Step i of the share
+    // (0 <= i < my_end - my_start) is K block order(i); pieces stay contiguous.
+    const int64_t b1 = (my_start + nkb - 1) / nkb * nkb;  // first tile boundary
+    const int64_t b2 = my_end / nkb * nkb;                 // last tile boundary
+    const bool crosses = b1 < my_end;
+    const int64_t len_a = crosses ? b1 - my_start : my_end - my_start;  // tail piece
+    const int64_t len_b = crosses ? my_end - b2 : 0;                      // head piece
+    auto order = [&](int64_t i) -> int64_t {
+        if (i < len_a)
+            return my_start + i;
+        if (i < len_a + len_b)
+            return b2 + (i - len_a);
+        return b1 + (i - len_a - len_b);
+    };
+    // end, in steps, of the piece that step i belongs to
+    auto piece_end = [&](int64_t i) -> int64_t {
+        return i < len_a ? len_a : (i < len_a + len_b ? len_a + len_b : my_end - my_start);
+    };
 
     // stage st <- B and A boxes of linear K block q, counted on full_bar(st)
     auto issue_stage = [&](int st, int64_t q, uint32_t extra) {
@@ -237,8 +258,8 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         grid_dependency_wait();
         // the ring is empty: start the B stream now instead of after the
         // tensor-memory allocation and the set-up barrier
-        for (int64_t q = my_start; q < my_end && pre < STAGES; ++q, ++pre)
-            issue_stage(pre, q, pre == 0 ? args.extra_tx : 0u);
+        for (int64_t i = 0; i < my_end - my_start && pre < STAGES; ++i, ++pre)
+            issue_stage(pre, order(i), pre == 0 ? args.extra_tx : 0u);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -259,8 +280,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         uint32_t ph = 0;
         int pending = 0;
         bool alive = true;
-        for (int64_t q = my_start; q < my_end; ++q) {
-            if (q - my_start >= pre) {
+        for (int64_t i = 0; i < my_end - my_start; ++i) {
+            const int64_t q = order(i);
+            if (i >= pre) {
                 if (!warp_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status,
                                        args.timeout_ns, kWhereProducerEmpty)) {
                     alive = false;
@@ -299,10 +321,12 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             int cset = 0;  // converted set (W4)
             uint32_t cph = 0;
             bool alive = true;
-            for (int64_t pos = my_start; pos < my_end && alive;) {
+            for (int64_t i = 0; i < my_end - my_start && alive;) {
+                const int64_t pos = order(i);
                 const int32_t t = static_cast<int32_t>(pos / nkb);
                 const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
-                const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + (my_end - pos) ? nkb : kb0 + (my_end - pos));
+                const int64_t left = piece_end(i) - i;
+                const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + left ? nkb : kb0 + left);
                 if (!wait_bounded(acce_bar(ab), aph ^ 1u, abort_flag, args.status, args.timeout_ns,
                                   kWhereMmaAccEmpty))
                     break;
@@ -352,7 +376,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                     ab = 0;
                     aph ^= 1u;
                 }
-                pos += kb1 - kb0;
+                i += kb1 - kb0;
             }
         }
         __syncwarp();
@@ -381,11 +405,13 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         }
         int ab = 0;
         uint32_t aph = 0;
-        for (int64_t pos = my_start; pos < my_end;) {
+        for (int64_t i = 0; i < my_end - my_start;) {
+            const int64_t pos = order(i);
             const int32_t t = static_cast<int32_t>(pos / nkb);
             const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
-            const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + (my_end - pos) ? nkb : kb0 + (my_end - pos));
-            pos += kb1 - kb0;
+            const int64_t left = piece_end(i) - i;
+            const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + left ? nkb : kb0 + left);
+            i += kb1 - kb0;
             const int32_t n = t * Cfg::BN + n_local;
             // beta * C of this column, fetched while the MMAs still run
             float cb[MP];
