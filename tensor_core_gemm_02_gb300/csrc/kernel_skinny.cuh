@@ -28,6 +28,14 @@
 #include "common.cuh"
 #include "fp4.cuh"
 
+// FP4 converters: threads per row of B (1 or 2) and the unroll of their block loop
+#ifndef TCG_CONV_SPLIT
+#define TCG_CONV_SPLIT 1
+#endif
+#ifndef TCG_CONV_UNROLL
+#define TCG_CONV_UNROLL 1
+#endif
+
 namespace tcg {
 
 template <int MP_, int KBOX_, bool W4_ = false>
@@ -40,28 +48,27 @@ struct SkinnyCfg {
     // W4: B arrives as FP4 codes (two per byte) with one UE8M0 scale per 32
     // elements, KBOX = 4 blocks of 64 per stage so each row of codes is read
     // in 128-byte runs (32-byte runs leave HBM mostly idle); converter warps
-    // turn each 64-wide block into the bf16 image the MMA reads, in a ring of
-    // CSLOTS slots of their own
+    // turn a stage into bf16 in tensor memory, where the MMA takes its A
+    // operand from (row r of B in TMEM lane r, two elements per column)
     static constexpr bool W4 = W4_;
     static constexpr uint32_t RAW_B = W4 ? BN * BK / 2 * KBOX : 0;  // 128 rows x 128 bytes of codes
     static constexpr uint32_t SCALE_B = W4 ? 2 * KBOX * BN : 0;     // 8 scale rows x 128 columns
-    // converted slots, handed to the MMA a stage (KBOX slots) at a time: one
-    // barrier handshake per stage instead of per block (the single MMA-issuing
-    // thread's waits and commits, not the conversion, had set the rate)
-    static constexpr int CSETS = W4 ? (MP >= 64 ? 1 : 2) : 0;
-    static constexpr int CSLOTS = CSETS * KBOX;
+    // converted sets, one stage (KSTAGE / 2 = 128 TMEM columns) each, at
+    // columns 128 (c + 1), handed to the MMA with one barrier handshake per
+    // stage (the single MMA-issuing thread's waits had set the rate when it
+    // took them per block); as many as the accumulators and the converter
+    // warps' registers leave room for
+    static constexpr int CSETS = W4 ? (MP <= 16 ? 3 : (MP <= 32 ? 2 : 1)) : 0;
+    static constexpr uint32_t CSET_COLS = KSTAGE / 2;
     static constexpr uint32_t B_BOX = BN * BK * 2;
     static constexpr uint32_t A_BOX = MP * BK * 2;
     static constexpr uint32_t B_BYTES = W4 ? 0 : KBOX * B_BOX;
     static constexpr uint32_t A_BYTES = KBOX * A_BOX;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + RAW_B + SCALE_B;
-    static constexpr uint32_t CB_BYTES = CSLOTS * B_BOX;  // converted ring (W4)
-    // as many stages as fit in about 200 KB of shared memory (at most 16); W4
-    // takes up to 220 KB for its two rings
-    static constexpr uint32_t RING_BUDGET = (W4 ? 225280u : 204800u) - CB_BYTES;
+    // as many stages as fit in about 200 KB of shared memory (at most 16)
+    static constexpr uint32_t RING_BUDGET = 204800u;
     static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) < 16 ? (RING_BUDGET / STAGE_BYTES) : 16;
-    static constexpr uint32_t OFF_CB = 0;
-    static constexpr uint32_t OFF_B = CB_BYTES;
+    static constexpr uint32_t OFF_B = 0;
     static constexpr uint32_t OFF_A = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_RAW = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_SC = OFF_RAW + STAGES * RAW_B;
@@ -71,17 +78,35 @@ struct SkinnyCfg {
     // stages (one thread per row of B); MP = 64's epilogue needs the registers
     // that more threads would take
     static constexpr int CONV_GROUPS = CSETS;
-    static constexpr int CONV_WARPS = 4 * CONV_GROUPS;
+    // threads per row of B in a group: each takes KBOX / CONV_SPLIT of the blocks
+    static constexpr int CONV_SPLIT = TCG_CONV_SPLIT;
+    static constexpr int CONV_WARPS = 4 * CONV_SPLIT * CONV_GROUPS;
+    static_assert(!W4 || KBOX % CONV_SPLIT == 0, "a row's blocks split evenly");
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;  // MP destination rows (scattered rows)
     static constexpr uint32_t SMEM_BYTES = OFF_ROWS + MP * 4;
     static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
-    static constexpr uint32_t TMEM_COLS = (2 * MP < 32) ? 32 : 2 * MP;
-    static constexpr int THREADS = 192 + 32 * CONV_WARPS;
+    static constexpr uint32_t TMEM_COLS = W4 ? 512u : ((2 * MP < 32) ? 32u : 2u * MP);
+    // MMA-issuing warps.  One thread issues a tcgen05.mma about every 117
+    // cycles whatever its N, so at N = MP a lone issuer, not the tensor pipe,
+    // sets the rate; issuers in separate warps add up (with A in TMEM; A
+    // from shared memory saturates its reads first).  Issuer e takes the
+    // blocks j = e (mod ISSUERS) of every stage into accumulators of its
+    // own, and the epilogue adds the partial sums in issuer order.
+    static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : 1;
+    static constexpr int EPI_WARP0 = 1 + ISSUERS;    // four epilogue warps
+    static constexpr int CONV_WARP0 = EPI_WARP0 + 4;  // then the converters
+    static constexpr int THREADS = 32 * CONV_WARP0 + 32 * CONV_WARPS;
+    // TMEM columns: accumulator (buffer b, issuer e) at (b ISSUERS + e) MP,
+    // the converted sets from the next multiple of 128
+    static constexpr uint32_t CSET_COL0 = (2u * ISSUERS * MP + 127u) / 128u * 128u;
     static_assert(!W4 || KBOX == 4, "W4 stages hold 128-byte runs of codes");
     static_assert(OFF_RAW % 1024 == 0 && RAW_B % 128 == 0, "TMA destinations stay aligned");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MMA N for M = 128 is a multiple of 16");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation is a power of two");
+    static_assert(!W4 || CSET_COL0 + CSETS * CSET_COLS <= TMEM_COLS,
+                  "accumulators and converted sets fit the allocation");
+    static_assert(KBOX % ISSUERS == 0 && (W4 || ISSUERS == 1), "issuers split a stage's blocks");
     static_assert(A_BOX % 1024 == 0 && B_BOX % 1024 == 0, "box images stay 1024-aligned");
     static_assert(STAGES >= 2, "at least double buffering");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -237,14 +262,14 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             // the MMA, and (W4) each warp of the converter group that takes the stage
-            mbar_init(empty_bar(s), W4 ? 5 : 1);
+            mbar_init(empty_bar(s), W4 ? Cfg::ISSUERS + 4 * Cfg::CONV_SPLIT : 1);
         }
         for (int c = 0; c < Cfg::CSETS; ++c) {
-            mbar_init(cfull_bar(c), 4);
-            mbar_init(cempty_bar(c), 1);
+            mbar_init(cfull_bar(c), 4 * Cfg::CONV_SPLIT);
+            mbar_init(cempty_bar(c), Cfg::ISSUERS);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf_bar(b), 1);
+            mbar_init(accf_bar(b), Cfg::ISSUERS);
             mbar_init(acce_bar(b), 4);
         }
         *abort_flag = 0u;
@@ -310,8 +335,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp < static_cast<uint32_t>(Cfg::EPI_WARP0)) {
+        // ------------------------------------------------------------ MMA issuers
+        const int e = static_cast<int>(warp) - 1;  // this warp's share of each stage's blocks
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32acc(args.ab_bf16 != 0, Cfg::BN, MP);
             int s = 0;
@@ -331,7 +357,8 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                                   kWhereMmaAccEmpty))
                     break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * MP);
+                const uint32_t d_tmem =
+                    tmem_base + static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP);
                 for (int32_t kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
                                       kWhereMmaFull)) {
@@ -346,15 +373,27 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                     tc_fence_after_sync();
 #pragma unroll
                     for (int j = 0; j < KBOX; ++j) {
-                        const uint64_t bd =
-                            W4 ? sdesc_k_sw128(base + Cfg::OFF_CB + (cset * KBOX + j) * Cfg::B_BOX)
-                               : sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES + j * Cfg::B_BOX);
+                        if (j % Cfg::ISSUERS != e)
+                            continue;
                         const uint64_t ad =
                             sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES + j * Cfg::A_BOX);
+                        if constexpr (W4) {
+                            // converted rows of B in TMEM: 8 columns per K step of 16
+                            const uint32_t bt = tmem_base + Cfg::CSET_COL0 +
+                                                Cfg::CSET_COLS * static_cast<uint32_t>(cset) +
+                                                static_cast<uint32_t>(j * (Cfg::BK / 2));
 #pragma unroll
-                        for (int k = 0; k < Cfg::BK / 16; ++k)
-                            tc_mma_f16(d_tmem, bd + 2u * k, ad + 2u * k, idesc,
-                                       (kb != kb0 || j != 0 || k != 0) ? 1u : 0u);
+                            for (int k = 0; k < Cfg::BK / 16; ++k)
+                                tc_mma_f16_tmem_a(d_tmem, bt + 8u * k, ad + 2u * k, idesc,
+                                                  (kb != kb0 || j != e || k != 0) ? 1u : 0u);
+                        } else {
+                            const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES +
+                                                              j * Cfg::B_BOX);
+#pragma unroll
+                            for (int k = 0; k < Cfg::BK / 16; ++k)
+                                tc_mma_f16(d_tmem, bd + 2u * k, ad + 2u * k, idesc,
+                                           (kb != kb0 || j != 0 || k != 0) ? 1u : 0u);
+                        }
                     }
                     tc_commit(empty_bar(s));
                     if (++s == STAGES) {
@@ -380,16 +419,16 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < static_cast<uint32_t>(Cfg::CONV_WARP0)) {
         // ------------------------------------------------------------ epilogue
         const uint32_t q = warp & 3u;
-        const bool leader = warp == 2 && lane == 0;
+        const bool leader = warp == static_cast<uint32_t>(Cfg::EPI_WARP0) && lane == 0;
         const int32_t n_local = 32 * static_cast<int32_t>(q) + static_cast<int32_t>(lane);
         // scattered rows: D row of each row of A, read once (after the set-up
         // barrier, so after the previous kernel in the stream has finished)
         int32_t *drow = reinterpret_cast<int32_t *>(gbase + Cfg::OFF_ROWS);
         if (args.scatter) {
-            const int32_t e = static_cast<int32_t>(threadIdx.x) - 64;  // 0 .. 127
+            const int32_t e = static_cast<int32_t>(threadIdx.x) - 32 * Cfg::EPI_WARP0;  // 0 .. 127
             if (e < MP) {
                 int32_t r = -1;
                 if (e < args.M) {
@@ -429,15 +468,21 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             if (!ok || *abort_flag)
                 break;
             tc_fence_after_sync();
+            // the issuers' partial sums, added in issuer order
             float v[MP];
 #pragma unroll
-            for (int g = 0; g < MP / 16; ++g) {
-                uint32_t r[16];
-                tc_ld_32x32b_x16(tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * MP + 16 * g), r);
-                tc_wait_ld(r);
+            for (int e = 0; e < Cfg::ISSUERS; ++e) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    v[16 * g + i] = __uint_as_float(r[i]);
+                for (int g = 0; g < MP / 16; ++g) {
+                    uint32_t r[16];
+                    tc_ld_32x32b_x16(tmem_base + ((32u * q) << 16) +
+                                         static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP + 16 * g),
+                                     r);
+                    tc_wait_ld(r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v[16 * g + i] = e == 0 ? __uint_as_float(r[i]) : v[16 * g + i] + __uint_as_float(r[i]);
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -509,13 +554,21 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         }
     } else if constexpr (W4) {
         // ------------------------------------------------------------ converters
-        // Group g of four warps takes the stages g, g + G, ... of this CTA's
-        // share (G groups, one converted set each); thread i of the group turns
-        // row i of the stage's codes (KBOX blocks of 32 bytes, two scales each)
-        // into bf16 in the set's swizzled images, which the MMA reads as B.
-        const uint32_t ct = threadIdx.x - 192u;
-        const int32_t group = static_cast<int32_t>(ct / 128u);
-        const uint32_t row = ct % 128u;
+        // Group g of 4 * CONV_SPLIT warps takes the stages g, g + G, ... of this
+        // CTA's share (G groups, one converted set each).  A warp reaches only
+        // its own quarter of the TMEM lanes (warp % 4), so lane l of warp w
+        // turns row 32 (w % 4) + l of the stage's codes (blocks of 32 bytes,
+        // two scales each) into bf16 and stores it in that TMEM lane of the
+        // set's columns; with CONV_SPLIT threads per row each takes its own run
+        // of blocks.
+        constexpr uint32_t kPart = static_cast<uint32_t>(KBOX / Cfg::CONV_SPLIT);
+        constexpr int kUnroll = TCG_CONV_UNROLL;
+        const uint32_t cw = warp - static_cast<uint32_t>(Cfg::CONV_WARP0);
+        const int32_t group = static_cast<int32_t>(cw / (4u * Cfg::CONV_SPLIT));
+        const uint32_t quarter = warp & 3u;
+        const uint32_t row = 32u * quarter + lane;
+        const uint32_t j0 = (cw / 4u) % Cfg::CONV_SPLIT * kPart;
+        const uint32_t t_lane = tmem_base + ((32u * quarter) << 16);
         for (int64_t qs = group; qs < my_end - my_start; qs += Cfg::CONV_GROUPS) {
             const int s = static_cast<int>(qs % STAGES);
             const uint32_t ph = static_cast<uint32_t>((qs / STAGES) & 1);
@@ -527,27 +580,31 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             if (!warp_wait_bounded(cempty_bar(cset), cph ^ 1u, abort_flag, args.status,
                                    args.timeout_ns, kWhereProducerEmpty))
                 break;
+            tc_fence_after_sync();  // the stores below come after the MMA's reads of the set
             const uint32_t src = base + Cfg::OFF_RAW + s * Cfg::RAW_B + row * 128u;
             const uint32_t sc = base + Cfg::OFF_SC + s * Cfg::SCALE_B + row;
-#pragma unroll 1
-            for (uint32_t j = 0; j < static_cast<uint32_t>(KBOX); ++j) {
+            const uint32_t tcol = t_lane + Cfg::CSET_COL0 + Cfg::CSET_COLS * static_cast<uint32_t>(cset);
+#pragma unroll kUnroll
+            for (uint32_t j = j0; j < j0 + kPart; ++j) {
                 // block j: the row's 16-byte chunks 2j, 2j+1 of the 128-byte swizzled image
                 uint32_t w[8];
                 ld_shared_v4(src + (((2u * j) ^ (row & 7u)) << 4), w[0], w[1], w[2], w[3]);
                 ld_shared_v4(src + (((2u * j + 1u) ^ (row & 7u)) << 4), w[4], w[5], w[6], w[7]);
                 const uint32_t sc_lo = ue8m0_to_bf16x2(ld_shared_u8(sc + 2u * j * 128u));
                 const uint32_t sc_hi = ue8m0_to_bf16x2(ld_shared_u8(sc + (2u * j + 1u) * 128u));
-                const uint32_t dst =
-                    base + Cfg::OFF_CB + (static_cast<uint32_t>(cset) * KBOX + j) * Cfg::B_BOX + row * 128u;
+                uint32_t v[32];  // the block's 64 elements, two per column, in K order
 #pragma unroll
                 for (uint32_t k = 0; k < 8; ++k) {
-                    // word k: elements 8k .. 8k+7 -> 16-byte chunk k (128-byte swizzle)
                     uint32_t p[4];
                     e2m1x8_to_bf16(w[k], k < 4 ? sc_lo : sc_hi, p);
-                    st_shared_v4(dst + ((k ^ (row & 7u)) << 4), p[0], p[1], p[2], p[3]);
+#pragma unroll
+                    for (uint32_t e = 0; e < 4; ++e)
+                        v[4 * k + e] = p[e];
                 }
+                tc_st_32x32b_x32(tcol + 32u * j, v);
             }
-            fence_proxy_async_smem();  // the MMA reads the images through the async proxy
+            tc_wait_st();
+            tc_fence_before_sync();  // the MMA reads the set once the group has arrived
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(cfull_bar(cset));

@@ -394,6 +394,20 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T: A's row r in TMEM lane r, K along the
+// columns, two f16/bf16 elements per 32-bit column (the lower K index in the
+// low half), so one K step of 16 spans 8 columns from a_tmem.
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Pair MMA, issued by the leader CTA only: M = 256 rows, A's rows 0-127 from
 // the leader's shared memory and 128-255 from the peer's (same offsets), B's
 // N columns split in halves the same way; each CTA's TMEM receives its rows.

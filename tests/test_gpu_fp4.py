@@ -66,14 +66,22 @@ def test_fp4_quarter_bit_exact(M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 256), (64, 1000, 256), (200, 512, 512)])
 def test_fp4_equals_bf16_on_dequantised_weights(M, N, K):
-    """Where neither path splits a tile's K sum over CTAs (K = 256 for M <= 64;
-    always for M > 64, which runs the bf16 kernel itself), the sums are the same
-    values in the same order."""
+    """M > 64 runs the bf16 kernel itself on the dequantised weights: equal bit
+    for bit.  M <= 64 multiplies the same bf16 values, but its MMA issuers each
+    sum their own K blocks before the partial sums are added, so the two may
+    differ only by float32 reassociation: at most 2 K 2^-24 sum|a||w| (before
+    the alpha/beta epilogue, which both apply alike)."""
     p = _problem(M + N, M, N, K, values="normal", smin=112, smax=135)
     got = run(p)
-    want = binding.gemm_bf16(p.A.to(DEV), _dequant_bf16(p).to(DEV), p.C.to(DEV),
-                             alpha=p.alpha, beta=p.beta)
-    assert torch.equal(got, want)
+    w = _dequant_bf16(p)
+    want = binding.gemm_bf16(p.A.to(DEV), w.to(DEV), p.C.to(DEV), alpha=p.alpha, beta=p.beta)
+    if M > 64:
+        assert torch.equal(got, want)
+        return
+    absprod = p.A.double().abs() @ w.double().abs().T
+    bound = abs(p.alpha) * 2 * K * 2.0**-24 * absprod + 1e-30
+    diff = (got.double().cpu() - want.double().cpu()).abs()
+    assert bool((diff <= bound * 1.01 + 2.0**-24 * want.double().cpu().abs()).all())
 
 
 @pytest.mark.parametrize("smin,smax", [(0, 8), (100, 140), (200, 220)])
