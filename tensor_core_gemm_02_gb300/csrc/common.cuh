@@ -66,8 +66,9 @@ __device__ __forceinline__ void record_error(uint32_t *status, uint32_t code, ui
 
 // Wait for phase `parity` of `bar`, giving up after `timeout_ns` or when the
 // CTA-wide abort flag is raised.  Returns false when it gave up; the first
-// thread to time out raises the abort flag and records the error.
-static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+// thread to time out raises the abort flag and records the error.  (The loop,
+// out of line; wait_bounded below tries the barrier inline first.)
+static __device__ __noinline__ bool wait_bounded_loop(uint32_t bar, uint32_t parity,
                                           volatile uint32_t *abort_flag, uint32_t *status,
                                           uint64_t timeout_ns, uint32_t where)
 {
@@ -89,6 +90,24 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// kProbe: try the barrier inline first, so that a phase which has already
+// completed costs one probe instead of a call (whose register saves cost
+// hundreds of cycles per wait in the warp-specialised loops).  Worth it where
+// the phase has usually completed; where the waiting thread is usually early
+// and on the critical path (an MMA issuer waiting for HBM), the probe only
+// adds to each wait and the loop is called directly.
+template <bool kProbe = false>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t *abort_flag, uint32_t *status,
+                                             uint64_t timeout_ns, uint32_t where)
+{
+    if constexpr (kProbe) {
+        if (mbar_probe(bar, parity))
+            return true;
+    }
+    return wait_bounded_loop(bar, parity, abort_flag, status, timeout_ns, where);
+}
+
 // Teardown after an abort: wait (bounded, ignoring the abort flag) for copies
 // this thread issued to land before the CTA releases its shared memory.
 static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
@@ -103,12 +122,17 @@ static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, ui
 
 // Every lane of the warp waits (bounded); the warp then agrees on the result
 // so that no lane runs ahead into a warp-collective instruction alone.
+template <bool kProbe = false>
 __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile uint32_t *abort_flag,
                                                   uint32_t *status, uint64_t timeout_ns,
                                                   uint32_t where)
 {
-    const bool ok = wait_bounded(bar, parity, abort_flag, status, timeout_ns, where);
+    if constexpr (kProbe) {
+        if (__all_sync(0xffffffffu, mbar_probe(bar, parity)))
+            return true;
+    }
+    const bool ok = wait_bounded_loop(bar, parity, abort_flag, status, timeout_ns, where);
     return __all_sync(0xffffffffu, ok);
 }
 

@@ -63,6 +63,55 @@ __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t sc2, uint32_
         asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(p[j]) : "r"(sc2));
 }
 
+// Eight codes -> four bf16x2 words as bit fields: a code's sign to bit 15 and
+// its three magnitude bits to bits 6-8 make the bf16 whose value is the
+// code's times 2^-126 exactly (e = 0 codes land on bf16 subnormals), so the
+// block scale 2^(s - 127) becomes the factor 2^(s - 1): `sa`, followed by
+// `sb` when that exceeds bf16's range (see e2m1_field_scales).  Spreading a
+// byte's two codes to the two halves is one integer multiply (by 4097), and
+// moving the sign bits another: this form loads the FMA pipe where
+// e2m1x8_to_bf16 loads the ALU pipe, and a mix of the two runs faster than
+// either alone.
+template <bool TWO>
+__device__ __forceinline__ void e2m1x8_to_bf16_fields(uint32_t w, uint32_t sa, uint32_t sb,
+                                                      uint32_t (&p)[4])
+{
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t b = prmt(w, 0u, 0x4440u + static_cast<uint32_t>(c));  // byte c alone
+        const uint32_t x = b * 4097u;       // code 2c at bits 0-3, code 2c+1 at bits 16-19
+        const uint32_t u = x & 0x000F000Fu;
+        const uint32_t sg = x & 0x00080008u;
+        uint32_t r = u * 64u + sg * 4032u;  // bits 0-2 -> 6-8 and bit 3 -> 15, in each half
+        asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(sa));
+        if (TWO)
+            asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(sb));
+        p[c] = r;
+    }
+}
+
+// Factors for e2m1x8_to_bf16_fields: 2^(s - 1) when s <= 128 (sb unused),
+// else 2^127 then 2^(s - 128); 255 (NaN) as one NaN factor.  Returns whether
+// sb is needed.  Every product is exact (powers of two) unless it leaves
+// bf16's range, exactly as with the single factor 2^(s - 127).
+__device__ __forceinline__ bool e2m1_field_scales(uint32_t s, uint32_t &sa, uint32_t &sb)
+{
+    uint32_t ha, hb = 0x3F80u;
+    bool two = false;
+    if (s == 255u) {
+        ha = 0x7FC0u;
+    } else if (s <= 128u) {
+        ha = (s + 126u) << 7;
+    } else {
+        ha = 0x7F00u;
+        hb = (s - 1u) << 7;
+        two = true;
+    }
+    sa = ha | (ha << 16);
+    sb = hb | (hb << 16);
+    return two;
+}
+
 // UE8M0 scale byte -> bf16x2 with 2^(s - 127) in both halves (0 is the
 // subnormal 2^-127, 255 NaN).
 __device__ __forceinline__ uint32_t ue8m0_to_bf16x2(uint32_t s)

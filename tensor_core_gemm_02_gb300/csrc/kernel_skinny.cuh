@@ -28,13 +28,6 @@
 #include "common.cuh"
 #include "fp4.cuh"
 
-// FP4 converters: threads per row of B (1 or 2) and the unroll of their block loop
-#ifndef TCG_CONV_SPLIT
-#define TCG_CONV_SPLIT 1
-#endif
-#ifndef TCG_CONV_UNROLL
-#define TCG_CONV_UNROLL 1
-#endif
 
 namespace tcg {
 
@@ -48,18 +41,38 @@ struct SkinnyCfg {
     // W4: B arrives as FP4 codes (two per byte) with one UE8M0 scale per 32
     // elements, KBOX = 4 blocks of 64 per stage so each row of codes is read
     // in 128-byte runs (32-byte runs leave HBM mostly idle); converter warps
-    // turn a stage into bf16 in tensor memory, where the MMA takes its A
+    // turn the codes into bf16 in tensor memory, where the MMA takes its A
     // operand from (row r of B in TMEM lane r, two elements per column)
     static constexpr bool W4 = W4_;
     static constexpr uint32_t RAW_B = W4 ? BN * BK / 2 * KBOX : 0;  // 128 rows x 128 bytes of codes
     static constexpr uint32_t SCALE_B = W4 ? 2 * KBOX * BN : 0;     // 8 scale rows x 128 columns
-    // converted sets, one stage (KSTAGE / 2 = 128 TMEM columns) each, at
-    // columns 128 (c + 1), handed to the MMA with one barrier handshake per
-    // stage (the single MMA-issuing thread's waits had set the rate when it
-    // took them per block); as many as the accumulators and the converter
-    // warps' registers leave room for
-    static constexpr int CSETS = W4 ? (MP <= 16 ? 3 : (MP <= 32 ? 2 : 1)) : 0;
+
+    // MMA-issuing warps.  One thread issues a tcgen05.mma about every 117
+    // cycles whatever its N, so at N = MP a lone issuer, not the tensor pipe,
+    // sets the rate; issuers in separate warps add up (with A in TMEM; A
+    // from shared memory saturates its reads first).  Issuer e takes the
+    // blocks j = e (mod ISSUERS) of every stage into accumulators of its
+    // own, and the epilogue adds the partial sums in issuer order.
+    static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : 1;
+    static constexpr int EPI_WARP0 = 1 + ISSUERS;    // four epilogue warps
+    static constexpr int CONV_WARP0 = EPI_WARP0 + 4;  // then the converters
+    static constexpr uint32_t TMEM_COLS = W4 ? 512u : ((2 * MP < 32) ? 32u : 2u * MP);
+    // TMEM columns: accumulator (buffer b, issuer e) at (b ISSUERS + e) MP,
+    // then whole-stage converted sets (two elements per column) from the
+    // next multiple of 128 to the end of the allocation
+    static constexpr uint32_t CSET_COL0 = (2u * ISSUERS * MP + 127u) / 128u * 128u;
     static constexpr uint32_t CSET_COLS = KSTAGE / 2;
+    static constexpr int CSETS = W4 ? static_cast<int>((TMEM_COLS - CSET_COL0) / CSET_COLS) : 0;
+    // Converter warps: CONV_PER_Q for each quarter of TMEM lanes (a warp
+    // reaches only quarter warp % 4), each taking KBOX / CONV_PER_Q blocks of
+    // every stage for its 32 rows.  All of them convert every stage and move
+    // through the sets together, so none sits waiting for the MMA while a set
+    // is free, and the decode (ALU-bound) keeps the SM busy; fewer per
+    // quarter for larger MP, whose epilogue needs the registers.
+    static constexpr int CONV_PER_Q = W4 ? (MP <= 16 ? 4 : (MP <= 32 ? 2 : 1)) : 0;
+    static constexpr int CONV_WARPS = 4 * CONV_PER_Q;
+    static constexpr int THREADS = 32 * CONV_WARP0 + 32 * CONV_WARPS;
+
     static constexpr uint32_t B_BOX = BN * BK * 2;
     static constexpr uint32_t A_BOX = MP * BK * 2;
     static constexpr uint32_t B_BYTES = W4 ? 0 : KBOX * B_BOX;
@@ -74,39 +87,19 @@ struct SkinnyCfg {
     static constexpr uint32_t OFF_SC = OFF_RAW + STAGES * RAW_B;
     static constexpr uint32_t OFF_BAR = (OFF_SC + STAGES * SCALE_B + 7u) & ~7u;
     static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 2 * CSETS;
-    // converter warps: one group of four per converted set, taking alternate
-    // stages (one thread per row of B); MP = 64's epilogue needs the registers
-    // that more threads would take
-    static constexpr int CONV_GROUPS = CSETS;
-    // threads per row of B in a group: each takes KBOX / CONV_SPLIT of the blocks
-    static constexpr int CONV_SPLIT = TCG_CONV_SPLIT;
-    static constexpr int CONV_WARPS = 4 * CONV_SPLIT * CONV_GROUPS;
-    static_assert(!W4 || KBOX % CONV_SPLIT == 0, "a row's blocks split evenly");
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;  // MP destination rows (scattered rows)
     static constexpr uint32_t SMEM_BYTES = OFF_ROWS + MP * 4;
     static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
-    static constexpr uint32_t TMEM_COLS = W4 ? 512u : ((2 * MP < 32) ? 32u : 2u * MP);
-    // MMA-issuing warps.  One thread issues a tcgen05.mma about every 117
-    // cycles whatever its N, so at N = MP a lone issuer, not the tensor pipe,
-    // sets the rate; issuers in separate warps add up (with A in TMEM; A
-    // from shared memory saturates its reads first).  Issuer e takes the
-    // blocks j = e (mod ISSUERS) of every stage into accumulators of its
-    // own, and the epilogue adds the partial sums in issuer order.
-    static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : 1;
-    static constexpr int EPI_WARP0 = 1 + ISSUERS;    // four epilogue warps
-    static constexpr int CONV_WARP0 = EPI_WARP0 + 4;  // then the converters
-    static constexpr int THREADS = 32 * CONV_WARP0 + 32 * CONV_WARPS;
-    // TMEM columns: accumulator (buffer b, issuer e) at (b ISSUERS + e) MP,
-    // the converted sets from the next multiple of 128
-    static constexpr uint32_t CSET_COL0 = (2u * ISSUERS * MP + 127u) / 128u * 128u;
+
     static_assert(!W4 || KBOX == 4, "W4 stages hold 128-byte runs of codes");
+    static_assert(!W4 || (KBOX % CONV_PER_Q == 0 && CSETS >= 2), "converters split a stage's blocks");
+    static_assert(KBOX % ISSUERS == 0 && (W4 || ISSUERS == 1), "issuers split a stage's blocks");
     static_assert(OFF_RAW % 1024 == 0 && RAW_B % 128 == 0, "TMA destinations stay aligned");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MMA N for M = 128 is a multiple of 16");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation is a power of two");
     static_assert(!W4 || CSET_COL0 + CSETS * CSET_COLS <= TMEM_COLS,
                   "accumulators and converted sets fit the allocation");
-    static_assert(KBOX % ISSUERS == 0 && (W4 || ISSUERS == 1), "issuers split a stage's blocks");
     static_assert(A_BOX % 1024 == 0 && B_BOX % 1024 == 0, "box images stay 1024-aligned");
     static_assert(STAGES >= 2, "at least double buffering");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -262,10 +255,10 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             // the MMA, and (W4) each warp of the converter group that takes the stage
-            mbar_init(empty_bar(s), W4 ? Cfg::ISSUERS + 4 * Cfg::CONV_SPLIT : 1);
+            mbar_init(empty_bar(s), W4 ? Cfg::ISSUERS + Cfg::CONV_WARPS : 1);
         }
         for (int c = 0; c < Cfg::CSETS; ++c) {
-            mbar_init(cfull_bar(c), 4 * Cfg::CONV_SPLIT);
+            mbar_init(cfull_bar(c), Cfg::CONV_WARPS);
             mbar_init(cempty_bar(c), Cfg::ISSUERS);
         }
         for (int b = 0; b < 2; ++b) {
@@ -353,19 +346,19 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                 const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
                 const int64_t left = piece_end(i) - i;
                 const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + left ? nkb : kb0 + left);
-                if (!wait_bounded(acce_bar(ab), aph ^ 1u, abort_flag, args.status, args.timeout_ns,
-                                  kWhereMmaAccEmpty))
+                if (!wait_bounded<W4>(acce_bar(ab), aph ^ 1u, abort_flag, args.status,
+                                      args.timeout_ns, kWhereMmaAccEmpty))
                     break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem =
                     tmem_base + static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP);
                 for (int32_t kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
-                                      kWhereMmaFull)) {
+                    if (!wait_bounded<W4>(full_bar(s), ph, abort_flag, args.status,
+                                          args.timeout_ns, kWhereMmaFull)) {
                         alive = false;
                         break;
                     }
-                    if (W4 && !wait_bounded(cfull_bar(cset), cph, abort_flag, args.status,
+                    if (W4 && !wait_bounded<true>(cfull_bar(cset), cph, abort_flag, args.status,
                                             args.timeout_ns, kWhereMmaFull)) {
                         alive = false;  // (the stage's blocks, as bf16 in converted set cset)
                         break;
@@ -554,61 +547,85 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         }
     } else if constexpr (W4) {
         // ------------------------------------------------------------ converters
-        // Group g of 4 * CONV_SPLIT warps takes the stages g, g + G, ... of this
-        // CTA's share (G groups, one converted set each).  A warp reaches only
-        // its own quarter of the TMEM lanes (warp % 4), so lane l of warp w
-        // turns row 32 (w % 4) + l of the stage's codes (blocks of 32 bytes,
-        // two scales each) into bf16 and stores it in that TMEM lane of the
-        // set's columns; with CONV_SPLIT threads per row each takes its own run
-        // of blocks.
-        constexpr uint32_t kPart = static_cast<uint32_t>(KBOX / Cfg::CONV_SPLIT);
-        constexpr int kUnroll = TCG_CONV_UNROLL;
+        // Every converter warp takes every stage of this CTA's share: lane l of
+        // warp w turns row 32 (w % 4) + l of its run of blocks (32 bytes of
+        // codes and two scales each) into bf16 and stores it in that TMEM lane
+        // of the stage's converted set.
+        constexpr uint32_t kRun = static_cast<uint32_t>(KBOX / Cfg::CONV_PER_Q);
         const uint32_t cw = warp - static_cast<uint32_t>(Cfg::CONV_WARP0);
-        const int32_t group = static_cast<int32_t>(cw / (4u * Cfg::CONV_SPLIT));
         const uint32_t quarter = warp & 3u;
         const uint32_t row = 32u * quarter + lane;
-        const uint32_t j0 = (cw / 4u) % Cfg::CONV_SPLIT * kPart;
+        const uint32_t j0 = (cw / 4u) * kRun;
         const uint32_t t_lane = tmem_base + ((32u * quarter) << 16);
-        for (int64_t qs = group; qs < my_end - my_start; qs += Cfg::CONV_GROUPS) {
-            const int s = static_cast<int>(qs % STAGES);
-            const uint32_t ph = static_cast<uint32_t>((qs / STAGES) & 1);
-            const int cset = static_cast<int>(qs % Cfg::CSETS);
-            const uint32_t cph = static_cast<uint32_t>((qs / Cfg::CSETS) & 1);
-            if (!warp_wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
+        int s = 0;
+        uint32_t ph = 0;
+        int cset = 0;
+        uint32_t cph = 0;
+        for (int64_t q = 0; q < my_end - my_start; ++q) {
+            if (!warp_wait_bounded<true>(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
                                    kWhereMmaFull))
                 break;
-            if (!warp_wait_bounded(cempty_bar(cset), cph ^ 1u, abort_flag, args.status,
+            if (!warp_wait_bounded<true>(cempty_bar(cset), cph ^ 1u, abort_flag, args.status,
                                    args.timeout_ns, kWhereProducerEmpty))
                 break;
             tc_fence_after_sync();  // the stores below come after the MMA's reads of the set
             const uint32_t src = base + Cfg::OFF_RAW + s * Cfg::RAW_B + row * 128u;
             const uint32_t sc = base + Cfg::OFF_SC + s * Cfg::SCALE_B + row;
             const uint32_t tcol = t_lane + Cfg::CSET_COL0 + Cfg::CSET_COLS * static_cast<uint32_t>(cset);
-#pragma unroll kUnroll
-            for (uint32_t j = j0; j < j0 + kPart; ++j) {
+#pragma unroll 1
+            for (uint32_t j = j0; j < j0 + kRun; ++j) {
                 // block j: the row's 16-byte chunks 2j, 2j+1 of the 128-byte swizzled image
                 uint32_t w[8];
                 ld_shared_v4(src + (((2u * j) ^ (row & 7u)) << 4), w[0], w[1], w[2], w[3]);
                 ld_shared_v4(src + (((2u * j + 1u) ^ (row & 7u)) << 4), w[4], w[5], w[6], w[7]);
-                const uint32_t sc_lo = ue8m0_to_bf16x2(ld_shared_u8(sc + 2u * j * 128u));
-                const uint32_t sc_hi = ue8m0_to_bf16x2(ld_shared_u8(sc + (2u * j + 1u) * 128u));
                 uint32_t v[32];  // the block's 64 elements, two per column, in K order
 #pragma unroll
-                for (uint32_t k = 0; k < 8; ++k) {
+                for (uint32_t hf = 0; hf < 2; ++hf) {
+                    // scale block hf (words 4 hf .. 4 hf + 3): the first word through
+                    // the byte tables, the other three as bit fields (the mix keeps
+                    // the ALU and FMA pipes both busy)
+                    const uint32_t s8 = ld_shared_u8(sc + (2u * j + hf) * 128u);
+                    uint32_t sa, sb;
+                    const bool two = e2m1_field_scales(s8, sa, sb);
                     uint32_t p[4];
-                    e2m1x8_to_bf16(w[k], k < 4 ? sc_lo : sc_hi, p);
+                    e2m1x8_to_bf16(w[4 * hf], ue8m0_to_bf16x2(s8), p);
 #pragma unroll
                     for (uint32_t e = 0; e < 4; ++e)
-                        v[4 * k + e] = p[e];
+                        v[16 * hf + e] = p[e];
+                    if (__any_sync(0xffffffffu, two)) {
+#pragma unroll
+                        for (uint32_t k = 1; k < 4; ++k) {
+                            e2m1x8_to_bf16_fields<true>(w[4 * hf + k], sa, sb, p);
+#pragma unroll
+                            for (uint32_t e = 0; e < 4; ++e)
+                                v[16 * hf + 4 * k + e] = p[e];
+                        }
+                    } else {
+#pragma unroll
+                        for (uint32_t k = 1; k < 4; ++k) {
+                            e2m1x8_to_bf16_fields<false>(w[4 * hf + k], sa, sb, p);
+#pragma unroll
+                            for (uint32_t e = 0; e < 4; ++e)
+                                v[16 * hf + 4 * k + e] = p[e];
+                        }
+                    }
                 }
                 tc_st_32x32b_x32(tcol + 32u * j, v);
             }
             tc_wait_st();
-            tc_fence_before_sync();  // the MMA reads the set once the group has arrived
+            tc_fence_before_sync();  // the MMA reads the set once every converter has arrived
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(cfull_bar(cset));
                 mbar_arrive(empty_bar(s));
+            }
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (++cset == Cfg::CSETS) {
+                cset = 0;
+                cph ^= 1u;
             }
         }
     }

@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
             for (int32_t kb = 0; kb < args.num_k_blocks; ++kb) {
-                if (!warp_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status,
+                if (!warp_wait_bounded<true>(empty_bar(s), ph ^ 1u, abort_flag, args.status,
                                        args.timeout_ns, kWhereProducerEmpty)) {
                     alive = false;
                     break;
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(192, 1)
             };
             // wait until stage s holds K block data; false if the kernel is aborting
             auto next_full = [&](int &st) {
-                if (!wait_bounded(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
+                if (!wait_bounded<true>(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
                                   kWhereMmaFull))
                     return false;
                 tc_fence_after_sync();
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(192, 1)
             auto wait_acc_free = [&](int b) {
                 // (seeded: the epilogue's first arrival is the seed, so the first
                 // use waits for it instead of passing on a fresh barrier)
-                if (!wait_bounded(acce_bar(b), seeded ? aph : aph ^ 1u, abort_flag, args.status,
+                if (!wait_bounded<true>(acce_bar(b), seeded ? aph : aph ^ 1u, abort_flag, args.status,
                                   args.timeout_ns,
                                   kWhereMmaAccEmpty))
                     return false;
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int32_t c = 0; c < TILE_N / 32; ++c) {
                 const int unit = NSUB == 2 ? c / kUnitChunks : ab;
                 if (c % kUnitChunks == 0) {
-                    if (!warp_wait_bounded(accf_bar(unit), aph, abort_flag, args.status,
+                    if (!warp_wait_bounded<true>(accf_bar(unit), aph, abort_flag, args.status,
                                            args.timeout_ns, kWhereEpiAccFull)) {
                         alive = false;
                         break;
@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(192, 1)
                                       ((args.d_tail_direct || scatter) && col0 + 32 > args.N);
                 float v[32];
                 if (c_tma) {
-                    if (!warp_wait_bounded(c_bar(q, j), cph[j], abort_flag, args.status,
+                    if (!warp_wait_bounded<true>(c_bar(q, j), cph[j], abort_flag, args.status,
                                            args.timeout_ns, kWhereEpiC)) {
                         alive = false;
                         break;

@@ -105,6 +105,20 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 }
 
 // true once the phase with the given parity has completed
+// Non-blocking probe: has phase `parity` of `bar` completed?
+__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
