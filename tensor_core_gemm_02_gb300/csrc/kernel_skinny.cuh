@@ -579,35 +579,47 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                 ld_shared_v4(src + (((2u * j) ^ (row & 7u)) << 4), w[0], w[1], w[2], w[3]);
                 ld_shared_v4(src + (((2u * j + 1u) ^ (row & 7u)) << 4), w[4], w[5], w[6], w[7]);
                 uint32_t v[32];  // the block's 64 elements, two per column, in K order
-#pragma unroll
-                for (uint32_t hf = 0; hf < 2; ++hf) {
-                    // scale block hf (words 4 hf .. 4 hf + 3): the first word through
-                    // the byte tables, the other three as bit fields (the mix keeps
-                    // the ALU and FMA pipes both busy)
-                    const uint32_t s8 = ld_shared_u8(sc + (2u * j + hf) * 128u);
-                    uint32_t sa, sb;
-                    const bool two = e2m1_field_scales(s8, sa, sb);
+                // scale blocks 2j and 2j+1 (words 0-3 and 4-7): the first word of
+                // each through the byte tables, the other three as bit fields (the
+                // mix keeps the ALU and FMA pipes both busy); one warp vote for the
+                // block picks the field form with or without its second factor
+                const uint32_t s_lo = ld_shared_u8(sc + 2u * j * 128u);
+                const uint32_t s_hi = ld_shared_u8(sc + (2u * j + 1u) * 128u);
+                uint32_t fa[2], fb[2];
+                const bool two_lo = e2m1_field_scales(s_lo, fa[0], fb[0]);
+                const bool two_hi = e2m1_field_scales(s_hi, fa[1], fb[1]);
+                {
                     uint32_t p[4];
-                    e2m1x8_to_bf16(w[4 * hf], ue8m0_to_bf16x2(s8), p);
+                    e2m1x8_to_bf16(w[0], ue8m0_to_bf16x2(s_lo), p);
 #pragma unroll
                     for (uint32_t e = 0; e < 4; ++e)
-                        v[16 * hf + e] = p[e];
-                    if (__any_sync(0xffffffffu, two)) {
+                        v[e] = p[e];
+                    e2m1x8_to_bf16(w[4], ue8m0_to_bf16x2(s_hi), p);
 #pragma unroll
-                        for (uint32_t k = 1; k < 4; ++k) {
-                            e2m1x8_to_bf16_fields<true>(w[4 * hf + k], sa, sb, p);
+                    for (uint32_t e = 0; e < 4; ++e)
+                        v[16 + e] = p[e];
+                }
+                if (__any_sync(0xffffffffu, two_lo || two_hi)) {
 #pragma unroll
-                            for (uint32_t e = 0; e < 4; ++e)
-                                v[16 * hf + 4 * k + e] = p[e];
-                        }
-                    } else {
+                    for (uint32_t k = 1; k < 8; ++k) {
+                        if (k == 4)
+                            continue;
+                        uint32_t p[4];
+                        e2m1x8_to_bf16_fields<true>(w[k], fa[k / 4], fb[k / 4], p);
 #pragma unroll
-                        for (uint32_t k = 1; k < 4; ++k) {
-                            e2m1x8_to_bf16_fields<false>(w[4 * hf + k], sa, sb, p);
+                        for (uint32_t e = 0; e < 4; ++e)
+                            v[4 * k + e] = p[e];
+                    }
+                } else {
 #pragma unroll
-                            for (uint32_t e = 0; e < 4; ++e)
-                                v[16 * hf + 4 * k + e] = p[e];
-                        }
+                    for (uint32_t k = 1; k < 8; ++k) {
+                        if (k == 4)
+                            continue;
+                        uint32_t p[4];
+                        e2m1x8_to_bf16_fields<false>(w[k], fa[k / 4], fb[k / 4], p);
+#pragma unroll
+                        for (uint32_t e = 0; e < 4; ++e)
+                            v[4 * k + e] = p[e];
                     }
                 }
                 tc_st_32x32b_x32(tcol + 32u * j, v);
