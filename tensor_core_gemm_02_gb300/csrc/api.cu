@@ -696,53 +696,23 @@ gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
     return plan;
 }
 
-gemm_status run(const Problem &p)
+// The tile kernel in the form of `plan` over all of p (maps, arguments,
+// launch).  grid_cap > 0 bounds the persistent grid; co_tail marks a launch
+// that runs beside the previous kernel on the SMs it leaves idle.
+gemm_status launch_tile_problem(const Problem &p, const gemm_plan &plan, const DeviceInfo *dev,
+                                int grid_cap, bool co_tail)
 {
-    bool empty = false;
-    gemm_status st = validate(p, &empty);
-    if (st != GEMM_OK || empty)
-        return st;
-    if (p.reduce && p.K == 0)
-        return GEMM_OK;  // adding zero
-    DeviceInfo *dev = nullptr;
-    if ((st = device_info(&dev)) != GEMM_OK)
-        return st;
-    if (p.w4 && p.K > 0 && p.M > 64) {
-        // many rows: turn the weights into bf16 once (exact: every code times a
-        // power of two fits bf16 unless it leaves its range) and run the bf16 GEMM
-        void *wb = nullptr;
-        if ((st = get_dequant_buffer(dev->index, p.stream, kBufWeights,
-                                     static_cast<size_t>(p.N) * p.K * 2, &wb)) != GEMM_OK)
-            return st;
-        if (tcg::launch_dequant_fp4(static_cast<const uint8_t *>(p.B), p.ldb, p.bscale, p.ldbs,
-                                    static_cast<int32_t>(p.N), static_cast<int32_t>(p.K),
-                                    static_cast<uint16_t *>(wb), p.K, p.stream) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        Problem q = p;
-        q.w4 = false;
-        q.B = wb;
-        q.ldb = p.K;
-        q.bscale = nullptr;
-        return run(q);
-    }
-    const bool c_used = p.C != nullptr && p.beta != 0.0f;
-    const gemm_plan plan = apply_forced_tile(
-        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count, p.scatter, p.seed,
-                  p.w4 && p.K > 0),
-        p, dev->sm_count);
-
     GemmMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    if (plan.kernel == 2)
-        return run_skinny(p, plan, dev);
-    if (plan.kernel == 10)
-        return run_tiny(p, plan, dev);
     const TileForm form = tile_form(plan);
+    const bool c_used = p.C != nullptr && p.beta != 0.0f;
     const bool pair = form.pair;
     const int bn = form.mma_bn;
     const int bn_local = pair ? bn / 2 : bn;  // rows of B per MMA half each CTA loads
     const int64_t units = loop_tiles(form, p.M, p.N);
     int grid = plan.grid;
+    if (grid_cap > 0 && grid > grid_cap)
+        grid = grid_cap;
     if (form.cluster > 1) {
         // never more clusters than can be resident together (SMs left over
         // within a GPC stay idle)
@@ -806,6 +776,7 @@ gemm_status run(const Problem &p)
     a.scatter = p.scatter ? 1 : 0;
     a.d_rows = static_cast<int32_t>(p.d_rows);
     a.reduce = p.reduce ? 1 : 0;
+    a.co_tail = co_tail ? 1 : 0;
     if (p.seed) {
         a.seed = 1;
         a.has_c = 0;  // C went into the accumulator; the epilogue writes D = acc
@@ -815,6 +786,113 @@ gemm_status run(const Problem &p)
     const cudaError_t e =
         tcg::launch_tile(mode, bn, pair, form.nsub, form.mc, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// A clustered form places whole clusters only (within a GPC), so some SMs stay
+// idle, and its last wave of clusters may run part-full.  For gathered rows
+// the first rows then run as whole waves of the clustered form, and the
+// remaining 256-row stripes on single CTAs (128 x 256 tiles, no cluster) on
+// the idle SMs at the same time: the tail is launched right behind the
+// clustered kernel (programmatic dependent launch), so its CTAs land on the
+// SMs left free.  The stripes are chosen so the tail, at kTailRate of the
+// clustered form's rate per SM, ends within the clustered kernel's time.
+// Returns the rows for the clustered kernel, or 0 for no split.
+// (kTailRate: 16384 of 65536 rows, N = K = 4096: single 128 x 256 CTAs
+// 1.032 ms on 152 SMs, four CTA pairs sharing rows 0.397 ms on 120 SMs.)
+constexpr double kTailRate = 0.30;
+
+int64_t tail_split_rows(const Problem &p, const gemm_plan &plan, const DeviceInfo *dev)
+{
+    if (!p.gather || p.scatter || p.reduce || p.seed || p.K == 0 || g_force_kernel.load() != 0)
+        return 0;
+    const TileForm f = tile_form(plan);
+    if (f.cluster <= 2)
+        return 0;
+    const int resident = tcg::tile_max_clusters(f.mma_bn, f.pair, f.nsub, f.mc);
+    const int idle = dev->sm_count - resident * f.cluster;
+    if (resident <= 0 || idle < 8)
+        return 0;
+    const int64_t m_blocks = ceil_div(p.M, f.tile_m);
+    const int64_t per_stripe = loop_tiles(f, f.tile_m, p.N);  // units in one stripe of rows
+    const int64_t waves_now = ceil_div(m_blocks * per_stripe, resident);
+    // what one wave of the clustered kernel covers, in (row x column) cells,
+    // and what the idle SMs cover in the same time
+    const double wave_cells = static_cast<double>(resident) * f.tile_m * f.mc * f.tile_n;
+    const double tail_cells_per_wave =
+        wave_cells / (resident * f.cluster) * idle * kTailRate;
+    for (int64_t m = m_blocks - 1; m > 0; --m) {
+        if ((m * per_stripe) % resident != 0)
+            continue;
+        const int64_t waves = m * per_stripe / resident;
+        if (waves >= waves_now)
+            continue;
+        const double tail_rows = static_cast<double>(p.M - m * f.tile_m);
+        if (tail_rows * static_cast<double>(p.N) <= tail_cells_per_wave * waves)
+            return m * f.tile_m;
+        return 0;  // fewer stripes only lengthen the tail
+    }
+    return 0;
+}
+
+gemm_status run(const Problem &p)
+{
+    bool empty = false;
+    gemm_status st = validate(p, &empty);
+    if (st != GEMM_OK || empty)
+        return st;
+    if (p.reduce && p.K == 0)
+        return GEMM_OK;  // adding zero
+    DeviceInfo *dev = nullptr;
+    if ((st = device_info(&dev)) != GEMM_OK)
+        return st;
+    if (p.w4 && p.K > 0 && p.M > 64) {
+        // many rows: turn the weights into bf16 once (exact: every code times a
+        // power of two fits bf16 unless it leaves its range) and run the bf16 GEMM
+        void *wb = nullptr;
+        if ((st = get_dequant_buffer(dev->index, p.stream, kBufWeights,
+                                     static_cast<size_t>(p.N) * p.K * 2, &wb)) != GEMM_OK)
+            return st;
+        if (tcg::launch_dequant_fp4(static_cast<const uint8_t *>(p.B), p.ldb, p.bscale, p.ldbs,
+                                    static_cast<int32_t>(p.N), static_cast<int32_t>(p.K),
+                                    static_cast<uint16_t *>(wb), p.K, p.stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        Problem q = p;
+        q.w4 = false;
+        q.B = wb;
+        q.ldb = p.K;
+        q.bscale = nullptr;
+        return run(q);
+    }
+    const bool c_used = p.C != nullptr && p.beta != 0.0f;
+    const gemm_plan plan = apply_forced_tile(
+        make_plan(p.M, p.N, p.K, p.gather, c_used, dev->sm_count, p.scatter, p.seed,
+                  p.w4 && p.K > 0),
+        p, dev->sm_count);
+
+    if (plan.kernel == 2)
+        return run_skinny(p, plan, dev);
+    if (plan.kernel == 10)
+        return run_tiny(p, plan, dev);
+    const int64_t head = tail_split_rows(p, plan, dev);
+    if (head <= 0)
+        return launch_tile_problem(p, plan, dev, 0, false);
+    Problem h = p;
+    h.M = head;
+    Problem t = p;
+    t.M = p.M - head;
+    t.idx = p.idx + head;
+    if (t.C != nullptr)
+        t.C = p.C + head * p.ldc;
+    t.D = static_cast<char *>(p.D) + head * p.ldd * out_size(p.out);
+    gemm_plan tp;
+    std::memset(&tp, 0, sizeof(tp));
+    set_tile_plan(tp, 1, 256, t.M, t.N, dev->sm_count);
+    const TileForm f = tile_form(plan);
+    const int idle = dev->sm_count -
+                     tcg::tile_max_clusters(f.mma_bn, f.pair, f.nsub, f.mc) * f.cluster;
+    if ((st = launch_tile_problem(h, plan, dev, 0, false)) != GEMM_OK)
+        return st;
+    return launch_tile_problem(t, tp, dev, idle, true);
 }
 
 }  // namespace host

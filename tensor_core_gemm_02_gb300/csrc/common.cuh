@@ -46,6 +46,8 @@ struct GemmArgs {
     int32_t reduce;         // D += alpha * acc (float32 adds into D; no C)
     int32_t seed;           // the accumulator starts from C (written to TMEM before the
                             // first MMA, which then accumulates); D = acc, C not read after
+    int32_t co_tail;        // launched right behind the previous kernel onto the SMs it
+                            // left idle: no dependency wait at the start, one at the end
     uint32_t extra_tx;      // test hook: extra bytes expected on the first stage
     uint32_t *status;       // [0] first error code, [1] where a wait gave up
     uint64_t timeout_ns;    // limit of every bounded wait

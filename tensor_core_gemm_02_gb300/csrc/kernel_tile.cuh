@@ -198,8 +198,11 @@ __global__ void __launch_bounds__(192, 1)
         }
     }
     // set-up above touched only shared and tensor memory; inputs and outputs
-    // are used only after the previous kernel in the stream has finished
-    grid_dependency_wait();
+    // are used only after the previous kernel in the stream has finished (a
+    // co-launched tail skips this: the kernel it runs beside let it launch
+    // only after passing this same wait, and writes other rows of D)
+    if (!args.co_tail)
+        grid_dependency_wait();
     tc_fence_before_sync();
     if (CL > 1)
         cluster_sync_all();  // the peers' barriers exist before anything targets them
@@ -822,6 +825,10 @@ __global__ void __launch_bounds__(192, 1)
         else
             tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
+    // a co-launched tail completes only after the kernel beside it, so the next
+    // kernel in the stream, which waits for this grid, waits for both
+    if (args.co_tail)
+        grid_dependency_wait();
 }
 
 }  // namespace tcg

@@ -178,6 +178,32 @@ def test_gather_sampled():
     _sampled_check(workloads.gather_16384_of_65536())
 
 
+def test_gather_split_into_waves_and_tail_exact():
+    """16484 gathered rows, N = 4096, K = 2048: the clustered form (four CTA pairs
+    sharing rows) runs the first 15360 rows as whole waves and single CTAs on the
+    SMs it leaves idle run the other 1124 (a ragged last stripe).  Quarter-integer
+    inputs make every sum exact, so sampled entries -- around the boundary, in the
+    tail, anywhere -- match the oracle bit for bit, as does the same call with the
+    clustered form forced for all rows."""
+    p = workloads.random_problem(31, 16484, 4096, 2048, dtype="bf16", values="quarter",
+                                 with_c=True, alpha=0.5, beta=-1.0, gather_rows=4096)
+    D = run(p)
+    rng = np.random.default_rng(7)
+    ii = np.concatenate([rng.integers(0, p.M, 2048), rng.integers(15360 - 256, 15360 + 256, 1024),
+                         rng.integers(15360, p.M, 1024), np.array([15359, 15360, p.M - 1])])
+    jj = np.concatenate([rng.integers(0, p.N, 4096), np.array([0, p.N - 1, 2047])])
+    ref, _, _ = oracle.gemm_entries(p.A, p.B, ii, jj, p.C, p.alpha, p.beta, idx=p.idx)
+    got = D[torch.from_numpy(ii).to(DEV), torch.from_numpy(jj).to(DEV)]
+    assert np.array_equal(to_f64(got), ref)
+    binding.gemm_debug_force_tile(9, 512)
+    try:
+        forced = run(p)
+    finally:
+        binding.gemm_debug_force_tile(0, 0)
+    assert torch.equal(D, forced)
+    assert device_status() == binding.GEMM_OK
+
+
 def test_gather_identity_matches_plain():
     """idx = arange(M) must give exactly the plain GEMM on the same rows."""
     p = workloads.random_problem(21, 300, 400, 264, dtype="bf16", with_c=True, alpha=0.5)
