@@ -16,13 +16,19 @@
 //
 //   warp 0     producer: per stage, KBOX TMA boxes of B (128 x 64) and of A
 //              (MP x 64) at consecutive K, so each row of B is read in
-//              KBOX * 128-byte runs
-//   warp 1     MMA issuer: tcgen05.mma M=128 N=MP K=16, two TMEM accumulators
-//   warps 2-5  epilogue: tcgen05.ld, partial or final fma.rn(alpha, acc, beta*C)
-//              with coalesced plain loads/stores (lanes walk along N); with
+//              KBOX * 128-byte runs (FP4 B: the codes, 128 rows x 128 bytes,
+//              and the stage's scale rows)
+//   warps 1..I MMA issuers (I = ISSUERS: 1, or 2 / 4 for FP4 B):
+//              tcgen05.mma M=128 N=MP K=16, each issuer into two TMEM
+//              accumulators of its own (FP4 B: A operand from TMEM)
+//   next 4     epilogue: tcgen05.ld (the issuers' partial sums added in
+//              order), partial or final fma.rn(alpha, acc, beta*C) with
+//              coalesced plain loads/stores (lanes walk along N); with
 //              scattered rows, row m of the result lands in row idx[m] of D;
 //              in the accumulating form every part is added into D with
 //              float32 atomic adds instead (no workspace, no last arriver)
+//   the rest   (FP4 B) converters: E2M1 codes and UE8M0 scales to bf16 rows
+//              in tensor memory (tcgen05.st), the MMA's A operand
 #pragma once
 
 #include "common.cuh"
