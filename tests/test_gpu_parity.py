@@ -6,8 +6,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (DEV, assert_bits, assert_within, device_status, oracle_full, run,
-                         to_f64)
+from gpu_helpers import (DEV, assert_bits, assert_within, device_status, expected_bits, oracle_full,
+                         run, to_f64)
 from tensor_core_gemm_02_gb300 import binding, workloads
 from tensor_core_gemm_02_gb300.workloads import OUT_BF16, OUT_F16, OUT_F32
 
@@ -178,15 +178,18 @@ def test_gather_sampled():
     _sampled_check(workloads.gather_16384_of_65536())
 
 
-def test_gather_split_into_waves_and_tail_exact():
+@pytest.mark.parametrize("out,with_c", [(OUT_F32, True), (OUT_BF16, False)])
+def test_gather_split_into_waves_and_tail_exact(out, with_c):
     """16484 gathered rows, N = 4096, K = 2048: the clustered form (four CTA pairs
     sharing rows) runs the first 15360 rows as whole waves and single CTAs on the
     SMs it leaves idle run the other 1124 (a ragged last stripe).  Quarter-integer
     inputs make every sum exact, so sampled entries -- around the boundary, in the
-    tail, anywhere -- match the oracle bit for bit, as does the same call with the
-    clustered form forced for all rows."""
+    tail, anywhere -- match the oracle bit for bit (bf16 output: the oracle's value
+    rounded once), as does the same call with the clustered form forced for all
+    rows."""
     p = workloads.random_problem(31, 16484, 4096, 2048, dtype="bf16", values="quarter",
-                                 with_c=True, alpha=0.5, beta=-1.0, gather_rows=4096)
+                                 with_c=with_c, alpha=0.5, beta=-1.0, gather_rows=4096,
+                                 out=out)
     D = run(p)
     rng = np.random.default_rng(7)
     ii = np.concatenate([rng.integers(0, p.M, 2048), rng.integers(15360 - 256, 15360 + 256, 1024),
@@ -194,7 +197,7 @@ def test_gather_split_into_waves_and_tail_exact():
     jj = np.concatenate([rng.integers(0, p.N, 4096), np.array([0, p.N - 1, 2047])])
     ref, _, _ = oracle.gemm_entries(p.A, p.B, ii, jj, p.C, p.alpha, p.beta, idx=p.idx)
     got = D[torch.from_numpy(ii).to(DEV), torch.from_numpy(jj).to(DEV)]
-    assert np.array_equal(to_f64(got), ref)
+    assert np.array_equal(to_f64(got), expected_bits(ref, out))
     binding.gemm_debug_force_tile(9, 512)
     try:
         forced = run(p)
