@@ -10,7 +10,10 @@
 //               from zero and later ones accumulate ("mma.sync" page, section
 //               "Accumulation, transpose and alpha/beta": only the first K
 //               issue reads the start value).  tcgen05.commit frees stages.
-//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), optional C box via
+//               (Single CTAs with BN <= 128: warp 6 is a second issuer taking
+//               every other K block into an accumulator of its own.)
+//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld; the two issuers'
+//               partial sums added), optional C box via
 //               TMA, D = fma.rn(alpha, acc, beta*C) ("fma" page), convert,
 //               swizzled shared image, TMA store ("cp.async.bulk.tensor"
 //               page, section "Stores, reductions, and completion").  With
@@ -84,8 +87,15 @@ struct TileCfg {
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base
-    static constexpr uint32_t TMEM_COLS = NUM_ACC * TILE_N;     // fp32 accumulators
-    static constexpr int THREADS = 192;
+    // MMA issuers.  One thread issues a tcgen05.mma about every 117 cycles
+    // whatever its N, while a 128 x BN x 16 MMA takes the tensor pipe about
+    // BN / 2 cycles: at BN <= 128 a lone issuer, not the tensor pipe, sets
+    // the rate.  Those single-CTA forms get a second issuing warp (warp 6)
+    // that takes every other K block into an accumulator of its own; the
+    // epilogue adds the two.  (Pairs and wider tiles are tensor-bound.)
+    static constexpr int ISS = (!PAIR && MC == 1 && NSUB == 1 && BN <= 128) ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = NUM_ACC * TILE_N * ISS;  // fp32 accumulators
+    static constexpr int THREADS = 192 + 32 * (ISS - 1);
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(NSUB == 1 || NSUB == 2, "one or two halves");
@@ -113,7 +123,7 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t row, uint32_t chunk, uint32
 enum : int { kModePlain = 0, kModeScatter = 1, kModeReduce = 2, kModeSeed = 3 };
 
 template <int BN, int STAGES, bool PAIR, int NSUB, int MC, int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC,
@@ -121,6 +131,9 @@ __global__ void __launch_bounds__(192, 1)
 {
     using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
     constexpr int CL = Cfg::CLUSTER;
+    // issuers in use: one for seeded accumulators (C is the start value of the
+    // one chain of K steps, as the pages' recurrence has it)
+    constexpr int kIss = MODE == kModeSeed ? 1 : Cfg::ISS;
     constexpr uint16_t kAllCtas = static_cast<uint16_t>((1u << CL) - 1u);
     constexpr int TILE_N = Cfg::TILE_N;
     extern __shared__ uint8_t smem_raw[];
@@ -170,7 +183,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(empty_bar(s), MC);  // MC > 1: every CTA's MMA frees the shared A slices
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf_bar(b), 1);
+            mbar_init(accf_bar(b), kIss);  // each issuer's last MMAs of the tile
             mbar_init(acce_bar(b), PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
         }
         for (int q = 0; q < 4; ++q)
@@ -325,9 +338,10 @@ __global__ void __launch_bounds__(192, 1)
                 wait_drain(full_bar(ds), dph, 10000000ull);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && leader) {
+    } else if (warp == 1 || (Cfg::ISS == 2 && warp == 6)) {
+        // ------------------------------------------------------------ MMA issuers
+        const int e = warp == 1 ? 0 : 1;  // issuer e takes the K blocks kb = e (mod kIss)
+        if (lane == 0 && leader && e < kIss) {
             const uint32_t idesc = idesc_f16_f32acc(args.ab_bf16 != 0, Cfg::TILE_M, BN);
             const int32_t nkb = args.num_k_blocks;
             int s = 0;
@@ -346,12 +360,13 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t dj = d_tmem + static_cast<uint32_t>(j * BN);
 #pragma unroll
                 for (int k = 0; k < Cfg::BK / 16; ++k) {  // +32 B per K=16 step
+                    // (the first K step of this issuer's chain starts from zero)
                     if (PAIR)
                         tc_mma_f16_pair(dj, ad + 2u * k, bd + 2u * k, idesc,
-                                        (seeded || (kb | k) != 0) ? 1u : 0u);
+                                        (seeded || ((kb / kIss) | k) != 0) ? 1u : 0u);
                     else
                         tc_mma_f16(dj, ad + 2u * k, bd + 2u * k, idesc,
-                                   (seeded || (kb | k) != 0) ? 1u : 0u);
+                                   (seeded || ((kb / kIss) | k) != 0) ? 1u : 0u);
                 }
             };
             // arrive on `bar` (both CTAs of a pair) once the MMAs issued so far finish
@@ -398,8 +413,16 @@ __global__ void __launch_bounds__(192, 1)
                 if constexpr (NSUB == 1) {
                     if (!wait_acc_free(ab))
                         break;
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * TILE_N);
+                    const uint32_t d_tmem =
+                        tmem_base + static_cast<uint32_t>((ab * kIss + e) * TILE_N);
                     for (int32_t kb = 0; kb < nkb; ++kb) {
+                        if (kIss > 1 && kb % kIss != e) {
+                            if (++s == STAGES) {  // the other issuer's stage
+                                s = 0;
+                                ph ^= 1u;
+                            }
+                            continue;
+                        }
                         int st;
                         if (!next_full(st)) {
                             alive = false;
@@ -410,8 +433,8 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     if (!alive)
                         break;
-                    if (nkb == 0 && !PAIR)
-                        mbar_arrive(accf_bar(ab));  // nothing to multiply: acc reads as zero
+                    if (nkb <= e && !PAIR)
+                        mbar_arrive(accf_bar(ab));  // nothing to multiply here
                     else
                         commit_to(accf_bar(ab));
                 } else {
@@ -670,9 +693,18 @@ __global__ void __launch_bounds__(192, 1)
                 const bool have = c < nchunks;
                 uint32_t acc[32];
                 if (have) {
-                    tc_ld_32x32b_x32(
-                        tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(ab * TILE_N + 32 * c), acc);
+                    const uint32_t col = static_cast<uint32_t>(ab * kIss * TILE_N + 32 * c);
+                    tc_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + col, acc);
                     tc_wait_ld(acc);
+                    if (kIss > 1 && args.num_k_blocks > 1) {
+                        // the second issuer's partial sum (odd K blocks)
+                        uint32_t acc2[32];
+                        tc_ld_32x32b_x32(tmem_base + ((32u * q) << 16) + col + TILE_N, acc2);
+                        tc_wait_ld(acc2);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            acc[i] = __float_as_uint(__fadd_rn(__uint_as_float(acc[i]), __uint_as_float(acc2[i])));
+                    }
                 }
                 // seeded mode: these columns are read, so the next tile's C can
                 // take their place

@@ -207,8 +207,12 @@ def test_gather_split_into_waves_and_tail_exact(out, with_c):
     assert device_status() == binding.GEMM_OK
 
 
-def test_gather_identity_matches_plain():
-    """idx = arange(M) must give exactly the plain GEMM on the same rows."""
+@pytest.mark.parametrize("form", [(1, 128), (4, 512)], ids=["two_issuers", "pair512"])
+def test_gather_identity_matches_plain(form):
+    """idx = arange(M) must give exactly the plain GEMM on the same rows, with the
+    same kernel form (forms differ in how the K sum is split: two issuers'
+    partial sums, one chain per pair)."""
+    binding.gemm_debug_force_tile(*form)
     p = workloads.random_problem(21, 300, 400, 264, dtype="bf16", with_c=True, alpha=0.5)
     plain = run(p)
     p.idx = torch.arange(300, dtype=torch.int32)

@@ -75,8 +75,11 @@ def test_scatter_skinny_split_k_exact():
     assert_scatter(run(p), p, True, "skinny split-K")
 
 
-def test_scatter_identity_matches_plain():
-    """idx = arange(M) into a D of M rows gives exactly the plain GEMM."""
+@pytest.mark.parametrize("form", [(1, 128), (3, 256)], ids=["two_issuers", "pair256"])
+def test_scatter_identity_matches_plain(form):
+    """idx = arange(M) into a D of M rows gives exactly the plain GEMM (same
+    kernel form for both: forms differ in how the K sum is split)."""
+    binding.gemm_debug_force_tile(*form)
     p = workloads.random_problem(47, 300, 400, 264, dtype="bf16", with_c=True, alpha=0.5)
     plain = run(p)
     q = workloads.Problem("identity", p.A, p.B, p.C, idx=torch.arange(300, dtype=torch.int32),
@@ -86,7 +89,9 @@ def test_scatter_identity_matches_plain():
 
 
 def test_scatter_permutation_matches_plain_rows():
-    """A permutation only moves rows: D[perm[i]] equals row i of the plain GEMM."""
+    """A permutation only moves rows: D[perm[i]] equals row i of the plain GEMM
+    (tile kernel: the same form for both calls)."""
+    binding.gemm_debug_force_tile(1, 128)  # (the skinny kernel, M <= 64, ignores this)
     for M in (40, 700):  # skinny and tile kernels
         p = workloads.random_problem(48 + M, M, 330, 200, dtype="f16", alpha=1.5)
         plain = run(p)
