@@ -18,8 +18,12 @@ TFLOP/s = 2 M N K / time.  The same line also carries:
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample of rows
   variants      the other workloads (f16 1024^3 + C, 8192 x 28672 x 4096 with
                 C, the M = 16 skinny case, the gathered 16384-of-65536 rows
-                case), each timed per launch with an L2 flush in between, with
-                their own roofline (HBM-bound ones against the copy bandwidth)
+                case, scattered rows, the accumulating and FP4-weight skinny
+                cases): device time per launch from a CUDA graph of
+                back-to-back launches that cycle through copies of the operands
+                holding at least twice L2 (no launch finds its inputs in L2),
+                with their own roofline (HBM-bound ones against the copy
+                bandwidth)
 
 With --impl reference the oracle itself is timed as the comparison arm.
 Under torchrun every rank runs its own replica; rank 0 prints the JSON line.
@@ -212,10 +216,6 @@ def plan_of(p, dev):
                                    sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
 
 
-def l2_flush(buf):
-    buf.zero_()
-
-
 def launch(p, dev_tensors):
     A, B, C, idx, D = dev_tensors
     if p.fp4:
@@ -357,39 +357,55 @@ def input_bytes(p):
     return a + b + c
 
 
-def time_variant(name, dev, reps, flush):
-    """Median per-launch time.  Inputs larger than L2 run back to back (each
-    launch finds little of the previous one's data in L2); smaller ones get an
-    L2 flush (a 258 MB write) before every launch."""
+def set_bytes(tensors):
+    """Device bytes of one launch's operands (inputs and output)."""
+    return sum(t.numel() * t.element_size() for t in tensors if t is not None)
+
+
+def time_variant(name, dev, reps, flush=None):
+    """Device time per launch, without host launch gaps: a CUDA graph of back-to-back
+    launches, replayed and timed with events on its stream.  Operands smaller than
+    twice L2 are replicated so that the launches cycle through copies holding at
+    least twice L2 together: no launch finds its inputs in L2 from an earlier one
+    (a copy's data was last touched at least an L2's worth of traffic before)."""
     p = workloads.WORKLOADS[name]()
-    tensors = to_device(p, dev)
-    for _ in range(3):
-        launch(p, tensors)
+    first = to_device(p, dev)
+    one = set_bytes(first)
+    copies = 1 if one >= 2 * L2_BYTES else -(-2 * L2_BYTES // one)
+    copies = max(1, min(copies, (6 << 30) // max(one, 1)))
+    sets = [first] + [to_device(p, dev) for _ in range(copies - 1)]
+    n = -(-max(reps, copies) // copies) * copies
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for t in sets:
+            launch(p, t)
     torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(n):
+            launch(p, sets[i % copies])
     times = []
-    stream = torch.cuda.current_stream()
-    big = input_bytes(p) > L2_BYTES
-    for _ in range(reps):
-        if not big:
-            l2_flush(flush)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        launch(p, tensors)
-        e1.record(stream)
-        if not big:
+    with torch.cuda.stream(stream):  # (a graph replays on the current stream)
+        graph.replay()
+        torch.cuda.synchronize()
+        for _ in range(5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
             e1.synchronize()
-        times.append((e0, e1))
-    torch.cuda.synchronize()
-    times = [a.elapsed_time(b) for a, b in times]
+            times.append(e0.elapsed_time(e1) / n)
     status = binding.gemm_check_device_status()
     if status != binding.GEMM_OK:
         raise RuntimeError(f"{name}: device status {binding.gemm_status_string(status)}")
     ms = statistics.median(times)
     plan = plan_of(p, dev)
-    del tensors
-    return p, ms, plan, ("back-to-back launches, inputs larger than L2" if big
-                         else "L2 flushed (258 MB write) before every launch")
+    del graph, sets, first
+    torch.cuda.empty_cache()
+    return p, ms, plan, (f"CUDA graph of {n} back-to-back launches cycling through {copies} "
+                         f"cop{'y' if copies == 1 else 'ies'} of the operands "
+                         f"({copies * one / 1e6:.0f} MB, >= 2x L2 when copied); median of 5 replays")
 
 
 def oracle_rows_rate(p, seconds, threads):
@@ -463,12 +479,11 @@ def run_ours(args):
     }
 
     if rank == 0 and args.variants:
-        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
         variants = {}
         for name in ("f16_1024", "mlp_8192x28672x4096", "skinny_16x28672x4096",
                      "gather_16384_of_65536", "scatter_16384_into_65536",
                      "skinny_accumulate_16x28672x4096", "fp4_skinny_16x28672x4096"):
-            vp, ms, plan, how = time_variant(name, dev, args.variant_reps, flush)
+            vp, ms, plan, how = time_variant(name, dev, args.variant_reps)
             tflops = vp.flops / (ms * 1e-3) / 1e12
             gbs = algorithmic_bytes(vp) / (ms * 1e-3) / 1e9
             hbm_bound = name in ("skinny_16x28672x4096", "skinny_accumulate_16x28672x4096",
@@ -492,10 +507,9 @@ def run_ours(args):
                                    "frac": round(tflops / peaks["bf16_tflops"], 4)}),
                                  traffic=stored_traffic(f"{kernel_key(plan, vp)}@{name}"),
                                  kernel=kernel_key(plan, vp)),
-                "timing": f"median of per-launch CUDA events; {how}",
+                "timing": how,
             }
         result["variants"] = variants
-        del flush
 
     if rank == 0:
         threads = len(os.sched_getaffinity(0))
