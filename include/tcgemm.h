@@ -35,7 +35,12 @@
  * workspace that it allocates once and grows on demand.
  *
  * Execution: calls are asynchronous on `stream` (a cudaStream_t; NULL means
- * the legacy default stream) on the current device.
+ * the legacy default stream) on the current device.  A call may launch more
+ * than one kernel on that stream (a large gathered call runs whole waves of
+ * clustered CTAs and, beside them, single CTAs on the SMs no cluster fits;
+ * FP4 weights with M > 64 are first converted to bf16); work issued later
+ * on the stream still starts only after all of them, and every form can be
+ * captured into a CUDA graph.
  *
  * Errors:
  *  - Argument, alignment, aliasing and type errors are returned synchronously
