@@ -31,8 +31,10 @@
  * allocator; typically PyTorch).  The library never frees or retains caller
  * memory beyond the asynchronous execution of the call.  It holds, per
  * device, a small status word in its own device globals and a host-side cache
- * of TMA descriptors; the skinny (M <= 64) path also keeps a per-device
- * workspace that it allocates once and grows on demand.
+ * of TMA descriptors; per device and stream, the skinny (M <= 64) path keeps
+ * a workspace for split tiles, and the FP4 path buffers for converted weights
+ * or re-pitched scales, each allocated once and grown on demand (so calls on
+ * different streams never share them).
  *
  * Execution: calls are asynchronous on `stream` (a cudaStream_t; NULL means
  * the legacy default stream) on the current device.  A call may launch more
