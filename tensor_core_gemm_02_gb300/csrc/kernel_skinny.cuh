@@ -73,9 +73,10 @@ struct SkinnyCfg {
     // reaches only quarter warp % 4), each taking KBOX / CONV_PER_Q blocks of
     // every stage for its 32 rows.  All of them convert every stage and move
     // through the sets together, so none sits waiting for the MMA while a set
-    // is free, and the decode (ALU-bound) keeps the SM busy; fewer per
-    // quarter for larger MP, whose epilogue needs the registers.
-    static constexpr int CONV_PER_Q = W4 ? (MP <= 16 ? 4 : (MP <= 32 ? 2 : 1)) : 0;
+    // is free, and the decode (ALU-bound) keeps the SM busy; two per quarter
+    // for MP > 16 (the chunked epilogue's registers, four issuers' worth of
+    // TMEM accumulators not fitting; four there measured slower with spills).
+    static constexpr int CONV_PER_Q = W4 ? (MP <= 16 ? 4 : 2) : 0;
     static constexpr int CONV_WARPS = 4 * CONV_PER_Q;
     static constexpr int THREADS = 32 * CONV_WARP0 + 32 * CONV_WARPS;
 
@@ -125,7 +126,6 @@ __device__ __forceinline__ void epi_bar_sync()
 
 // Row of C and D for row m of A: m itself, or (scattered rows) the entry
 // that the epilogue staged in shared memory; -1 when nothing is written.
-template <int MP>
 __device__ __forceinline__ int32_t skinny_row(const GemmArgs &a, const int32_t *drow, int m)
 {
     if (a.scatter)
@@ -133,19 +133,35 @@ __device__ __forceinline__ int32_t skinny_row(const GemmArgs &a, const int32_t *
     return m < a.M ? m : -1;
 }
 
-// Final values of column n: D[r][n] = fma.rn(alpha, v[m], cb[m]) with
-// r = skinny_row(m) and cb[m] = mul.rn(beta, C[r][n]) loaded beforehand (or
-// D = mul.rn(alpha, v[m]) without C).  No loads of C or D happen here, so
-// nothing waits behind the stores.
-template <int MP>
+// The epilogue works on chunks of CH rows of A (m0 .. m0 + CH - 1) of one
+// column n of D, so its registers do not grow with MP.
+
+// cb[m] = mul.rn(beta, C[r][n]) for the chunk's rows (0 where nothing is
+// written or C is absent).
+template <int CH>
+__device__ __forceinline__ void skinny_load_cb(const GemmArgs &a, const int32_t *drow, int32_t n,
+                                               int m0, float (&cb)[CH])
+{
+#pragma unroll
+    for (int m = 0; m < CH; ++m) {
+        const int32_t r = skinny_row(a, drow, m0 + m);
+        cb[m] = (a.has_c && r >= 0 && n < a.N)
+                    ? mul_rn(a.beta, a.C[static_cast<int64_t>(r) * a.ldc + n])
+                    : 0.f;
+    }
+}
+
+// Final values: D[r][n] = fma.rn(alpha, v[m], cb[m]) with r = skinny_row(m)
+// (or D = mul.rn(alpha, v[m]) without C).
+template <int CH>
 __device__ __forceinline__ void skinny_store(const GemmArgs &a, const int32_t *drow, int32_t n,
-                                             const float (&v)[MP], const float (&cb)[MP])
+                                             int m0, const float (&v)[CH], const float (&cb)[CH])
 {
     if (n >= a.N)
         return;
 #pragma unroll
-    for (int m = 0; m < MP; ++m) {
-        const int32_t r = skinny_row<MP>(a, drow, m);
+    for (int m = 0; m < CH; ++m) {
+        const int32_t r = skinny_row(a, drow, m0 + m);
         if (r >= 0) {
             const float d = a.has_c ? fma_rn(a.alpha, v[m], cb[m]) : mul_rn(a.alpha, v[m]);
             const int64_t o = static_cast<int64_t>(r) * a.ldd + n;
@@ -161,15 +177,15 @@ __device__ __forceinline__ void skinny_store(const GemmArgs &a, const int32_t *d
 
 // Accumulating form: add mul.rn(alpha, v[m]) into D[r][n] (float32 atomic
 // adds, so the parts of a split tile need no workspace and no ordering).
-template <int MP>
+template <int CH>
 __device__ __forceinline__ void skinny_add(const GemmArgs &a, const int32_t *drow, int32_t n,
-                                           const float (&v)[MP])
+                                           int m0, const float (&v)[CH])
 {
     if (n >= a.N)
         return;
 #pragma unroll
-    for (int m = 0; m < MP; ++m) {
-        const int32_t r = skinny_row<MP>(a, drow, m);
+    for (int m = 0; m < CH; ++m) {
+        const int32_t r = skinny_row(a, drow, m0 + m);
         if (r >= 0)
             atomicAdd(static_cast<float *>(a.D) + static_cast<int64_t>(r) * a.ldd + n,
                       mul_rn(a.alpha, v[m]));
@@ -451,15 +467,33 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + left ? nkb : kb0 + left);
             i += kb1 - kb0;
             const int32_t n = t * Cfg::BN + n_local;
-            // beta * C of this column, fetched while the MMAs still run
-            float cb[MP];
-#pragma unroll
-            for (int m = 0; m < MP; ++m) {
-                const int32_t r = skinny_row<MP>(args, drow, m);
-                cb[m] = (args.has_c && r >= 0 && n < args.N)
-                            ? mul_rn(args.beta, args.C[static_cast<int64_t>(r) * args.ldc + n])
-                            : 0.f;
+            // FP4 weights with MP > 16 finish the MP rows of A in chunks of 16,
+            // so the epilogue's registers stay those of MP = 16 and leave room
+            // for the converter warps; otherwise one chunk of all MP rows.
+            // beta * C is fetched while the MMAs still run: into registers when
+            // there is one chunk, else its lines into L2.
+            constexpr int CH = (W4 && MP > 16) ? 16 : MP;
+            constexpr int NCH = MP / CH;
+            float cb0[CH];
+            if constexpr (NCH == 1) {
+                skinny_load_cb<CH>(args, drow, n, 0, cb0);
+            } else if (args.has_c && n < args.N) {
+#pragma unroll 4
+                for (int m = 0; m < MP; ++m) {
+                    const int32_t r = skinny_row(args, drow, m);
+                    if (r >= 0)
+                        prefetch_l2(args.C + static_cast<int64_t>(r) * args.ldc + n);
+                }
             }
+            auto chunk_cb = [&](int g, float (&cb)[CH]) {
+                if constexpr (NCH == 1) {
+#pragma unroll
+                    for (int m = 0; m < CH; ++m)
+                        cb[m] = cb0[m];
+                } else {
+                    skinny_load_cb<CH>(args, drow, n, CH * g, cb);
+                }
+            };
             const bool ok = warp_wait_bounded(accf_bar(ab), aph, abort_flag, args.status,
                                               args.timeout_ns, kWhereEpiAccFull);
             // all four warps agree before the named barriers below
@@ -467,20 +501,43 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             if (!ok || *abort_flag)
                 break;
             tc_fence_after_sync();
-            // the issuers' partial sums, added in issuer order
-            float v[MP];
+            const int32_t c_lo = skinny_owner(static_cast<int64_t>(t) * nkb, W, G);
+            const int32_t c_hi = skinny_owner(static_cast<int64_t>(t + 1) * nkb - 1, W, G);
+            const int32_t parts = args.reduce ? 1 : c_hi - c_lo + 1;
+            // a split tile's partial sums: slot (t, blockIdx.x - c_lo) of the workspace
+            const int32_t my_slot = static_cast<int32_t>(blockIdx.x) - c_lo;
+            float *slot0 = args.workspace + static_cast<int64_t>(t) * args.splits * (Cfg::BN * MP);
+            float *mine = slot0 + static_cast<int64_t>(my_slot) * (Cfg::BN * MP);
+#pragma unroll 1
+            for (int g = 0; g < NCH; ++g) {
+                // the issuers' partial sums of this chunk, added in issuer order
+                float v[CH];
 #pragma unroll
-            for (int e = 0; e < Cfg::ISSUERS; ++e) {
+                for (int e = 0; e < Cfg::ISSUERS; ++e) {
 #pragma unroll
-                for (int g = 0; g < MP / 16; ++g) {
-                    uint32_t r[16];
-                    tc_ld_32x32b_x16(tmem_base + ((32u * q) << 16) +
-                                         static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP + 16 * g),
-                                     r);
-                    tc_wait_ld(r);
+                    for (int h = 0; h < CH / 16; ++h) {
+                        uint32_t r[16];
+                        tc_ld_32x32b_x16(tmem_base + ((32u * q) << 16) +
+                                             static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP +
+                                                                   CH * g + 16 * h),
+                                         r);
+                        tc_wait_ld(r);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        v[16 * g + i] = e == 0 ? __uint_as_float(r[i]) : v[16 * g + i] + __uint_as_float(r[i]);
+                        for (int i = 0; i < 16; ++i)
+                            v[16 * h + i] = e == 0 ? __uint_as_float(r[i])
+                                                   : v[16 * h + i] + __uint_as_float(r[i]);
+                    }
+                }
+                if (args.reduce) {
+                    skinny_add<CH>(args, drow, n, CH * g, v);  // every part adds itself into D
+                } else if (parts == 1) {
+                    float cb[CH];
+                    chunk_cb(g, cb);
+                    skinny_store<CH>(args, drow, n, CH * g, v, cb);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < CH; ++m)
+                        __stcg(mine + (CH * g + m) * Cfg::BN + n_local, v[m]);
                 }
             }
             tc_fence_before_sync();
@@ -491,25 +548,8 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                 ab = 0;
                 aph ^= 1u;
             }
-
-            if (args.reduce) {
-                skinny_add<MP>(args, drow, n, v);  // every part adds itself into D
+            if (parts == 1)
                 continue;
-            }
-            const int32_t c_lo = skinny_owner(static_cast<int64_t>(t) * nkb, W, G);
-            const int32_t c_hi = skinny_owner(static_cast<int64_t>(t + 1) * nkb - 1, W, G);
-            const int32_t parts = c_hi - c_lo + 1;
-            if (parts == 1) {
-                skinny_store<MP>(args, drow, n, v, cb);
-                continue;
-            }
-            // partial sum of this CTA -> workspace slot (t, blockIdx.x - c_lo)
-            const int32_t my_slot = static_cast<int32_t>(blockIdx.x) - c_lo;
-            float *slot0 = args.workspace + static_cast<int64_t>(t) * args.splits * (Cfg::BN * MP);
-            float *mine = slot0 + static_cast<int64_t>(my_slot) * (Cfg::BN * MP);
-#pragma unroll
-            for (int m = 0; m < MP; ++m)
-                __stcg(mine + m * Cfg::BN + n_local, v[m]);
             // The CTA barrier orders every thread's partial before the leader's
             // device-scope fence and counter increment; for the last CTA to
             // arrive, the leader's second fence orders the other CTAs' parts
@@ -526,28 +566,27 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             if (*arrival != static_cast<uint32_t>(parts - 1))
                 continue;  // another CTA still has to add its part
             // last to arrive: add the parts in slot order (this CTA's own part
-            // from registers: the same bits it wrote), then finish the tile
-            float sum[MP];
+            // too, read back: the bits it wrote), then finish the tile
+#pragma unroll 1
+            for (int g = 0; g < NCH; ++g) {
+                float sum[CH];
 #pragma unroll
-            for (int m = 0; m < MP; ++m)
-                sum[m] = 0.f;
-            for (int p = 0; p < parts; ++p) {
-                if (p == my_slot) {
-#pragma unroll
-                    for (int m = 0; m < MP; ++m)
-                        sum[m] += v[m];
-                } else {
+                for (int m = 0; m < CH; ++m)
+                    sum[m] = 0.f;
+                for (int p = 0; p < parts; ++p) {
                     const float *src = slot0 + static_cast<int64_t>(p) * (Cfg::BN * MP);
-                    float part[MP];
+                    float part[CH];
 #pragma unroll
-                    for (int m = 0; m < MP; ++m)
-                        part[m] = __ldcg(src + m * Cfg::BN + n_local);
+                    for (int m = 0; m < CH; ++m)
+                        part[m] = __ldcg(src + (CH * g + m) * Cfg::BN + n_local);
 #pragma unroll
-                    for (int m = 0; m < MP; ++m)
+                    for (int m = 0; m < CH; ++m)
                         sum[m] += part[m];
                 }
+                float cb[CH];
+                chunk_cb(g, cb);
+                skinny_store<CH>(args, drow, n, CH * g, sum, cb);
             }
-            skinny_store<MP>(args, drow, n, sum, cb);
             if (leader)
                 args.counters[t] = 0u;  // ready for the next call
         }

@@ -61,6 +61,12 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
 // attribute); every access to inputs or outputs comes after it.
 // launch_dependents: let the next such launch begin its own set-up.
 
+// Bring a global line into L2 ahead of its use (no register, no wait).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void grid_dependency_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
