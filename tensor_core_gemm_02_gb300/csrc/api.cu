@@ -498,9 +498,12 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, i
         set_tiny_plan(p, M, N);
         return p;
     }
-    if (!gather && !seeded && M <= 64 && K > 0) {  // (seeded accumulators: tile kernel)
+    // (FP4 weights with 64 < M <= 128 run as two launches of the 64-row skinny
+    // kernel; the plan describes one of them)
+    const int64_t m_skinny = (w4 && K > 0 && M <= 128 && M > 64) ? 64 : M;
+    if (!gather && !seeded && m_skinny <= 64 && K > 0) {  // (seeded accumulators: tile kernel)
         // few rows: swap A and B so B streams through the MMA's M side
-        const int mp = skinny_rows(M);
+        const int mp = skinny_rows(m_skinny);
         const int64_t tiles = ceil_div(N, 128);
         const int64_t nkb = ceil_div(K, w4 ? tcg::skinny_w4_kstage() : tcg::skinny_kstage());
         const int64_t W = tiles * nkb;
@@ -845,6 +848,25 @@ gemm_status run(const Problem &p)
     DeviceInfo *dev = nullptr;
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
+    if (p.w4 && p.K > 0 && p.M > 64 && p.M <= 128) {
+        // up to 128 rows: two launches of the FP4 skinny kernel, rows 0-63 and
+        // the rest (each decodes the weights again, which still costs less than
+        // converting them to bf16 in memory: 64 + 64 rows, N = 28672, K = 4096:
+        // 99 against 120 us)
+        Problem h = p;
+        h.M = 64;
+        h.a_rows = 64;
+        if ((st = run(h)) != GEMM_OK)
+            return st;
+        Problem t = p;
+        t.M = p.M - 64;
+        t.a_rows = t.M;
+        t.A = static_cast<const char *>(p.A) + 64 * p.lda * 2;
+        if (t.C != nullptr)
+            t.C = p.C + 64 * p.ldc;
+        t.D = static_cast<char *>(p.D) + 64 * p.ldd * out_size(p.out);
+        return run(t);
+    }
     if (p.w4 && p.K > 0 && p.M > 64) {
         // many rows: turn the weights into bf16 once (exact: every code times a
         // power of two fits bf16 unless it leaves its range) and run the bf16 GEMM

@@ -15,21 +15,6 @@ namespace tcg {
 constexpr uint32_t kE2m1LoA = 0xC0800000u, kE2m1LoB = 0xC0804000u;
 constexpr uint32_t kE2m1HiA = 0x3F3F3F00u, kE2m1HiB = 0x40404040u;
 
-// Four codes (element i in nibble i of w) -> two bf16x2 words (elements 0,1 and
-// 2,3), multiplied by the block scale `sc2` (bf16x2, both halves the same power
-// of two, so the products are exact unless they leave bf16's range).
-__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t w, uint32_t sc2, uint32_t &p01,
-                                               uint32_t &p23)
-{
-    const uint32_t sel = w & 0x7777u;  // magnitudes (sign bits cleared)
-    const uint32_t lo = __byte_perm(kE2m1LoA, kE2m1LoB, sel);
-    const uint32_t hi = __byte_perm(kE2m1HiA, kE2m1HiB, sel);
-    p01 = __byte_perm(lo, hi, 0x5140u) | ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
-    p23 = __byte_perm(lo, hi, 0x7362u) | ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
-    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(p01) : "r"(sc2));
-    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(p23) : "r"(sc2));
-}
-
 // prmt.b32 in its default mode: byte n of the result is byte (s >> 4n) & 7 of
 // {b, a}, or, when bit 3 of that selector nibble is set, the top bit of that
 // byte copied into all eight bits (PTX ISA, prmt).

@@ -176,6 +176,10 @@ def test_fp4_argument_checks(lib):
     assert (p.kernel, p.bm) == (2, 16) and p.stages > 0
     assert binding.gemm_query_plan(16, 8, 64, fp4=True, sm_count=148).kernel == 2  # never tiny
     assert binding.gemm_query_plan(4096, 4096, 4096, fp4=True, sm_count=148).kernel == 4
+    # 64 < M <= 128: two launches of the 64-row skinny kernel
+    p = binding.gemm_query_plan(100, 28672, 4096, fp4=True, sm_count=148)
+    assert (p.kernel, p.bm) == (2, 64)
+    assert binding.gemm_query_plan(129, 28672, 4096, fp4=True, sm_count=148).kernel != 2
 
 
 def test_plan_matches_the_dispatch_rules(lib):
