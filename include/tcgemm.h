@@ -40,7 +40,7 @@
  * the legacy default stream) on the current device.  A call may launch more
  * than one kernel on that stream (a large gathered call runs whole waves of
  * clustered CTAs and, beside them, single CTAs on the SMs no cluster fits;
- * FP4 weights with M > 64 are first converted to bf16); work issued later
+ * FP4 weights with M > 128 are first converted to bf16); work issued later
  * on the stream still starts only after all of them, and every form can be
  * captured into a CUDA graph.
  *
@@ -183,8 +183,9 @@ gemm_status gemm_scatter_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16
  * 2 exponent bits with bias 1, 1 mantissa bit, codes 0..7 = 0, 0.5, 1, 1.5, 2,
  * 3, 4, 6; UE8M0 scale s = 2^(s - 127), 255 = NaN; 32 elements per scale).
  * M <= 64 streams the codes and scales with TMA and converts them to bf16 in
- * shared memory next to the tensor-core pipeline (a quarter of the bytes of a
- * bf16 B); larger M converts W to bf16 once (a per-stream buffer the library
+ * tensor memory, where the tensor-core MMA reads them (a quarter of the bytes
+ * of a bf16 B); 64 < M <= 128 runs that path twice (rows 0-63, then the
+ * rest); larger M converts W to bf16 once (a per-stream buffer the library
  * allocates) and runs the bf16 GEMM.  W's values are exact in bf16 for scales
  * up to 252; 253-254 can overflow to infinity.
  *
@@ -195,7 +196,7 @@ gemm_status gemm_scatter_rows(int64_t M, int64_t N, int64_t K, int dtype_is_bf16
  *  Bs, ldbs    K/32 rows of N scale bytes, ldbs bytes apart (row b holds the
  *              scales of elements 32b .. 32b+31 of every row of W), ldbs >= N.
  *              With a 16-byte aligned base and a pitch that is a multiple of
- *              16 the kernel reads them in place; otherwise (M <= 64) the
+ *              16 the kernel reads them in place; otherwise (M <= 128) the
  *              library first copies them to a padded buffer of its own.
  *  K           a multiple of 32 (GEMM_ERR_UNSUPPORTED otherwise).
  *  Other arguments as in gemm_bf16.  D must not overlap A, Bq or Bs.
