@@ -241,10 +241,11 @@ gemm_status gemm_seeded(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
  * page, section "Stores, reductions, and completion": the reduction form adds
  * the shared image into the global box, whose contents are the starting
  * value, so the caller initialises D).  Rounding: each element receives
- * D + mul.rn(alpha, acc) with one float32 add per part of the K sum; for
- * M > 64 there is one part, so the result is deterministic; for M <= 64 the
- * K sum of a tile may be split over several CTAs, each adding its part (in an
- * order that is not specified, so the last bits may differ from call to call
+ * D + mul.rn(alpha, acc) with one float32 add per part of the K sum; the
+ * tile kernel makes one part, so the result is deterministic; where the
+ * skinny kernel runs the call (M <= 64, see gemm_query_plan) the K sum of a
+ * tile may be split over several CTAs, each adding its part (in an order
+ * that is not specified, so the last bits may differ from call to call
  * unless every partial sum is exact).  Unlike fma.rn(alpha, acc, beta * C)
  * this is two roundings (the product, then the add).
  *
@@ -270,9 +271,11 @@ gemm_status gemm_accumulate(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
  * reserves the whole GPU up front) and latency-critical sections where the
  * implicit synchronisation of cudaMalloc/cudaFree is not allowed.
  *
- * It computes exactly what gemm_f16 / gemm_bf16 compute for M <= 64, with the
- * same kernel, but its scratch (partial tiles and arrival counters) lives in
- * one fixed device array inside the library: 16 MiB of partials plus 16384
+ * It computes what gemm_f16 / gemm_bf16 compute for M <= 64, always with the
+ * skinny kernel (those calls take it only for some shapes, the tile kernel
+ * for the rest: the two round alike, element by element, but may add the K
+ * sum in another order), and its scratch (partial tiles and arrival counters)
+ * lives in one fixed device array inside the library: 16 MiB of partials plus 16384
  * counters (16.06 MiB in all), held by every GPU that loads the library until
  * the process exits.  The call itself allocates no device memory; the caller
  * still owns A, B, C and D.
@@ -312,11 +315,18 @@ const char *gemm_status_string(int status);
 
 /*
  * The kernel choice the library makes for a problem, without launching
- * anything and without touching the GPU (for diagnostics and tests).
+ * anything and without touching the GPU (for diagnostics and tests; a form
+ * forced with gemm_debug_force_tile is applied as a call would apply it).
  * form: 0 = plain, 1 = row-gathered (gemm_gather_rows), 2 = row-scattered
  * (gemm_scatter_rows), 3 = seeded (gemm_seeded), 4 = FP4 weights
- * (gemm_bf16_e2m1); any other value is GEMM_ERR_INVALID_ARG.  has_c: C
- * is given and beta != 0.
+ * (gemm_bf16_e2m1), 5 = gemm_skinny_noalloc (kernel 0 where it returns
+ * GEMM_ERR_UNSUPPORTED for the shape); any other value is
+ * GEMM_ERR_INVALID_ARG.  has_c: C is given and beta != 0.
+ *
+ * With M <= 64 rows (bf16 / f16 B; not gathered, not seeded) the skinny
+ * kernel runs where it measured faster than the tile kernel: M <= 16 with
+ * N * K > 2^21, 16 < M <= 32 with K >= 2 N, 32 < M <= 64 with K >= 8 N or
+ * K >= max(4 N, 16384).  FP4 weights with M <= 128 always take it.
  *
  *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles, one
  *           CTA each), 2 = skinny swap-AB kernel (M <= 64), 3 = tile kernel
@@ -375,10 +385,12 @@ gemm_status gemm_debug_inject(int mode);
  * with bn = 256, kernel 7 = two CTA pairs sharing A with bn = 512,
  * kernel 8 = two CTA pairs sharing A with bn = 256, kernel 9 = four CTA pairs
  * sharing A with bn = 512, kernel 10 = the warp-level kernel with bn = 8 (it
- * then runs every problem, the skinny ones too), kernel 0 = automatic
- * choice (the default).  Problems the forced form cannot run (the M <= 64 skinny
- * path; K == 0 for pairs) keep the automatic choice.  Returns
- * GEMM_ERR_INVALID_ARG for other values.
+ * then runs every problem), kernel 2 = the skinny kernel with bn = 0 or 128
+ * (problems it can run: M <= 64, K > 0, not gathered or seeded), kernel 0 =
+ * automatic choice (the default).  Tile forms apply to every problem the tile
+ * kernel runs, M <= 64 ones included; FP4 weights keep their own paths, and
+ * problems the forced form cannot run (K == 0 for clusters and pairs) keep
+ * the automatic choice.  Returns GEMM_ERR_INVALID_ARG for other values.
  */
 gemm_status gemm_debug_force_tile(int kernel, int bn);
 

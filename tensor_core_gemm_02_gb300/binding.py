@@ -291,9 +291,9 @@ def gemm_check_device_status(stream=None) -> int:
 
 
 def gemm_query_plan(M, N, K, gather=False, has_c=False, sm_count=148, scatter=False,
-                    seeded=False, fp4=False) -> Plan:
+                    seeded=False, fp4=False, noalloc=False) -> Plan:
     p = Plan()
-    form = 1 if gather else (2 if scatter else (3 if seeded else (4 if fp4 else 0)))
+    form = 1 if gather else (2 if scatter else (3 if seeded else (4 if fp4 else (5 if noalloc else 0))))
     _check(load_library().gemm_query_plan(M, N, K, form, int(bool(has_c)),
                                           sm_count, ctypes.byref(p)), "gemm_query_plan")
     return p

@@ -413,6 +413,54 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, bool gather, bool c_used
 
 int skinny_rows(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
+// Problems the skinny kernel can run: M <= 64, K > 0, plain, scattered or
+// accumulating (gathered rows and seeded accumulators: tile kernel only).
+bool skinny_eligible(int64_t M, int64_t K, bool gather, bool seeded)
+{
+    return !gather && !seeded && M <= 64 && K > 0;
+}
+
+// Few rows of A, bf16 / f16 B: whether the skinny kernel beats the tile
+// kernel.  The skinny kernel spreads every tile's K over the SMs, which pays
+// when the tile kernel has few tiles to give them and a long K to walk in
+// each (K large against N); with more than 16 rows its epilogue and split
+// reductions cost more than the tile kernel's idle MMA rows.  Measured
+// (CUDA-graph replay, operands cold in HBM, microseconds skinny / tile):
+// M = 16: 28672 x 4096 42.0 / 45.1, 4096^2 14.1 / 16.6, 1024^2 8.9 / 6.8;
+// M = 32: 28672 x 4096 46.0 / 45.9, 4096 x 8192 23.6 / 29.3, 4096^2 23.0 / 16.6,
+// 16384 x 2048 25.4 / 16.8; M = 64: 28672 x 4096 64.4 / 47.6, 4096^2
+// 34.1 / 16.7, 1024 x 8192 26.7 / 29.1, 4096 x 16384 40.6 / 54.7, 48 rows
+// 2048 x 8192 34.3 / 29.1.
+bool skinny_wins(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 16)
+        return N * K > (int64_t(1) << 21);  // (N, K < 2^31: no overflow)
+    if (M <= 32)
+        return K >= 2 * N;
+    return K >= 8 * N || (K >= 4 * N && K >= 16384);
+}
+
+// The skinny kernel's plan for m <= 64 rows (stream-K over the SMs).
+void set_skinny_plan(gemm_plan &p, int64_t m, int64_t N, int64_t K, int sm_count, bool w4)
+{
+    // few rows: swap A and B so B streams through the MMA's M side
+    const int mp = skinny_rows(m);
+    const int64_t tiles = ceil_div(N, 128);
+    const int64_t nkb = ceil_div(K, w4 ? tcg::skinny_w4_kstage() : tcg::skinny_kstage());
+    const int64_t W = tiles * nkb;
+    // at least TCG_SKINNY_MIN_KB K blocks per CTA, so small problems are
+    // not cut into many parts whose reduction costs more than it saves
+    const int64_t want = ceil_div(W, TCG_SKINNY_MIN_KB);
+    const int64_t G = want < sm_count ? want : sm_count;
+    p.kernel = 2;
+    p.bm = mp;
+    p.bn = 128;
+    p.stages = w4 ? tcg::skinny_w4_stages(mp) : tcg::skinny_stages(mp);
+    p.tiles = tiles;
+    p.splits = tcg::skinny_max_parts(tcg::skinny_sk_tiles(tiles, G, w4), nkb, G);
+    p.grid = static_cast<int32_t>(G);
+}
+
 // Problems with at most this many multiply-adds run on the warp-level kernel.
 constexpr int64_t kTinyWork = int64_t(1) << 20;
 
@@ -499,29 +547,28 @@ gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, i
         return p;
     }
     // (FP4 weights with 64 < M <= 128 run as two launches of the 64-row skinny
-    // kernel; the plan describes one of them)
+    // kernel; the plan describes one of them; FP4 weights with M <= 64 always
+    // take the skinny kernel, which converts them on the fly)
     const int64_t m_skinny = (w4 && K > 0 && M <= 128 && M > 64) ? 64 : M;
-    if (!gather && !seeded && m_skinny <= 64 && K > 0) {  // (seeded accumulators: tile kernel)
-        // few rows: swap A and B so B streams through the MMA's M side
-        const int mp = skinny_rows(m_skinny);
-        const int64_t tiles = ceil_div(N, 128);
-        const int64_t nkb = ceil_div(K, w4 ? tcg::skinny_w4_kstage() : tcg::skinny_kstage());
-        const int64_t W = tiles * nkb;
-        // at least TCG_SKINNY_MIN_KB K blocks per CTA, so small problems are
-        // not cut into many parts whose reduction costs more than it saves
-        const int64_t want = ceil_div(W, TCG_SKINNY_MIN_KB);
-        const int64_t G = want < sm_count ? want : sm_count;
-        p.kernel = 2;
-        p.bm = mp;
-        p.bn = 128;
-        p.stages = w4 ? tcg::skinny_w4_stages(mp) : tcg::skinny_stages(mp);
-        p.tiles = tiles;
-        p.splits = tcg::skinny_max_parts(tiles, nkb, G);
-        p.grid = static_cast<int32_t>(G);
+    if (skinny_eligible(m_skinny, K, gather, seeded) && (w4 || skinny_wins(M, N, K))) {
+        set_skinny_plan(p, m_skinny, N, K, sm_count, w4);
         return p;
     }
     const TileChoice c = choose_tile(M, N, K, gather, c_used, scatter, sm_count);
     set_tile_plan(p, c.kernel, c.bn, M, N, sm_count);
+    return p;
+}
+
+gemm_plan noalloc_plan(int64_t M, int64_t N, int64_t K, bool c_used, int sm_count)
+{
+    gemm_plan p;
+    std::memset(&p, 0, sizeof(p));
+    if (!skinny_eligible(M, K, false, false))
+        return p;  // M > 64 or K == 0: not this entry point's
+    p = make_plan(M, N, K, false, c_used, sm_count);
+    if (p.kernel == 0 || p.kernel == 10)
+        return p;  // empty, or the warp-level kernel (which needs no scratch)
+    set_skinny_plan(p, M, N, K, sm_count, false);
     return p;
 }
 
@@ -641,6 +688,7 @@ gemm_status run_skinny(const Problem &p, const gemm_plan &plan, const DeviceInfo
     a.num_k_blocks =
         static_cast<int32_t>(ceil_div(p.K, p.w4 ? tcg::skinny_w4_kstage() : tcg::skinny_kstage()));
     a.num_tiles = static_cast<int32_t>(plan.tiles);
+    a.sk_tiles = static_cast<int32_t>(tcg::skinny_sk_tiles(plan.tiles, plan.grid, p.w4));
     a.group_m = 1;
     a.splits = plan.splits;
     a.scatter = p.scatter ? 1 : 0;
@@ -691,8 +739,11 @@ gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
         set_tiny_plan(plan, p.M, p.N);  // the warp-level kernel runs every problem
         return plan;
     }
-    if (plan.kernel == 2)
+    if (fk == 2) {
+        if (skinny_eligible(p.M, p.K, p.gather, p.seed))
+            set_skinny_plan(plan, p.M, p.N, p.K, sm_count, false);
         return plan;
+    }
     if (fk != 1 && p.K == 0)
         return plan;  // cluster forms need K > 0
     set_tile_plan(plan, fk, fbn, p.M, p.N, sm_count);
@@ -769,7 +820,6 @@ gemm_status launch_tile_problem(const Problem &p, const gemm_plan &plan, const D
     a.num_tiles = static_cast<int32_t>(units);
     a.group_m = a.num_m_blocks < TCG_GROUP_M ? a.num_m_blocks : TCG_GROUP_M;
     a.splits = 1;
-    a.kb_per_split = a.num_k_blocks;
     a.gather = p.gather ? 1 : 0;
     a.c_tma = c_tma ? 1 : 0;
     a.d_tma = d_tma ? 1 : 0;
@@ -1050,10 +1100,23 @@ gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int form, int has_c
 {
     if (!plan || sm_count < 1 || M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (form < 0 || form > 4)
+    if (form < 0 || form > 5)
         return GEMM_ERR_INVALID_ARG;
-    *plan = make_plan(M, N, K, form == 1, has_c != 0 || form == 3, sm_count, form == 2, form == 3,
-                      form == 4 && K > 0);
+    if (form == 5) {
+        *plan = noalloc_plan(M, N, K, has_c != 0, sm_count);
+        return GEMM_OK;
+    }
+    Problem q{};
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.gather = form == 1;
+    q.scatter = form == 2;
+    q.seed = form == 3;
+    q.w4 = form == 4 && K > 0;
+    *plan = apply_forced_tile(make_plan(M, N, K, q.gather, has_c != 0 || q.seed, sm_count,
+                                        q.scatter, q.seed, q.w4),
+                              q, sm_count);
     return GEMM_OK;
 }
 
@@ -1065,7 +1128,8 @@ gemm_status gemm_set_wait_timeout(uint64_t ns)
 
 gemm_status gemm_debug_force_tile(int kernel, int bn)
 {
-    const bool ok = (kernel == 0) || (kernel == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
+    const bool ok = (kernel == 0) || (kernel == 2 && (bn == 0 || bn == 128)) ||
+                    (kernel == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
                     (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512) ||
                     (kernel == 5 && (bn == 64 || bn == 256)) || (kernel == 6 && bn == 256) ||
                     (kernel == 7 && bn == 512) || (kernel == 8 && bn == 256) ||

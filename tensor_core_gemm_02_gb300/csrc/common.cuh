@@ -28,7 +28,7 @@ struct GemmArgs {
     int32_t num_tiles;      // output tiles
     int32_t group_m;        // tile-order group height (in m blocks)
     int32_t splits;         // K slices per tile (skinny kernel)
-    int32_t kb_per_split;   // k blocks per slice (skinny kernel)
+    int32_t sk_tiles;       // skinny kernel: tiles shared block by block (the rest go whole)
     float alpha, beta;
     int32_t has_c;          // C is read (non-NULL and beta != 0)
     int32_t out_kind;       // kOutF32 / kOutBF16 / kOutF16

@@ -63,6 +63,11 @@ CUtensorMapDataType ab_type(bool bf16);
 int64_t ceil_div(int64_t a, int64_t b);
 gemm_plan make_plan(int64_t M, int64_t N, int64_t K, bool gather, bool c_used, int sm_count,
                     bool scatter = false, bool seeded = false, bool w4 = false);
+// The skinny kernel's plan for m <= 64 rows, and the plan of the
+// allocation-free entry point (the warp-level kernel for tiny problems, the
+// skinny kernel for the rest of M <= 64, K > 0; kernel 0 otherwise).
+void set_skinny_plan(gemm_plan &p, int64_t m, int64_t N, int64_t K, int sm_count, bool w4);
+gemm_plan noalloc_plan(int64_t M, int64_t N, int64_t K, bool c_used, int sm_count);
 
 // Launch the warp-level kernel for a validated problem with a plan of kernel 10.
 gemm_status run_tiny(const Problem &p, const gemm_plan &plan, const DeviceInfo *dev);

@@ -7,12 +7,18 @@
 // ("mma.sync" page, section "Accumulation, transpose and alpha/beta": a
 // transpose is a change of view, not an exchange of values).
 //
-// Work split (stream-K): the (tile, k-block) pairs of all 128-row tiles of
-// B form one list; CTA g takes the contiguous share [W g / G, W (g+1) / G).
-// A tile touched by several CTAs gets one partial sum from each; each writes
-// its partial to the workspace, and the last to arrive (an atomic counter per
-// tile) adds them in a fixed order, applies the epilogue and resets the
-// counter.  No CTA waits for another.
+// Work split (stream-K, FP4 B with whole tiles): of the T 128-row tiles of
+// B, the first S (args.sk_tiles) are shared block by block -- their (tile,
+// k-block) pairs form one list of W = S nkb and CTA g takes the contiguous
+// share [W g / G, W (g+1) / G) -- and the other T - S, a multiple of G, go
+// whole, tile S + g + G j to CTA g.  A shared tile touched by several CTAs
+// gets one partial sum from each; each writes its partial to the workspace,
+// and the last to arrive (an atomic counter per tile) adds them in a fixed
+// order, applies the epilogue and resets the counter.  No CTA waits for
+// another.  A CTA runs its shared pieces first and its whole tiles last, so
+// the reductions overlap the whole tiles' MMAs instead of ending the kernel.
+// (bf16 / f16 B shares every tile, S = T: with whole tiles its HBM stream
+// measured 10-20% slower, FP4 B, bound by the decode, 3-12% faster.)
 //
 //   warp 0     producer: per stage, KBOX TMA boxes of B (128 x 64) and of A
 //              (MP x 64) at consecutive K, so each row of B is read in
@@ -35,7 +41,19 @@
 #include "fp4.cuh"
 
 
+// Accumulator buffers of the bf16 / f16 form (at most 512 / (MP) columns).
+#ifndef TCG_SKINNY_NACC
+#define TCG_SKINNY_NACC 4
+#endif
+
+
 namespace tcg {
+
+// A tensor-memory allocation: a power of two of at least 32 columns.
+__host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t cols)
+{
+    return cols <= 32u ? 32u : (cols <= 64u ? 64u : (cols <= 128u ? 128u : (cols <= 256u ? 256u : 512u)));
+}
 
 template <int MP_, int KBOX_, bool W4_ = false>
 struct SkinnyCfg {
@@ -62,11 +80,19 @@ struct SkinnyCfg {
     static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : 1;
     static constexpr int EPI_WARP0 = 1 + ISSUERS;    // four epilogue warps
     static constexpr int CONV_WARP0 = EPI_WARP0 + 4;  // then the converters
-    static constexpr uint32_t TMEM_COLS = W4 ? 512u : ((2 * MP < 32) ? 32u : 2u * MP);
+    // Accumulator buffers.  A CTA's share is a few pieces (a tile's tail, the
+    // next one's head, whole tiles); a short piece after a long one leaves the
+    // epilogue of the long one (partial sums out, maybe the reduction) too
+    // little MMA time to hide behind, so the bf16 kernel keeps four buffers
+    // and the MMA rarely waits for a free one.  (FP4 B: two, the rest of
+    // tensor memory holds converted weights.)
+    static constexpr int NACC = W4 ? 2 : TCG_SKINNY_NACC;
+    static constexpr uint32_t ACC_COLS = static_cast<uint32_t>(NACC * ISSUERS * MP);
+    static constexpr uint32_t TMEM_COLS = W4 ? 512u : tmem_cols_for(ACC_COLS);
     // TMEM columns: accumulator (buffer b, issuer e) at (b ISSUERS + e) MP,
     // then whole-stage converted sets (two elements per column) from the
     // next multiple of 128 to the end of the allocation
-    static constexpr uint32_t CSET_COL0 = (2u * ISSUERS * MP + 127u) / 128u * 128u;
+    static constexpr uint32_t CSET_COL0 = (ACC_COLS + 127u) / 128u * 128u;
     static constexpr uint32_t CSET_COLS = KSTAGE / 2;
     static constexpr int CSETS = W4 ? static_cast<int>((TMEM_COLS - CSET_COL0) / CSET_COLS) : 0;
     // Converter warps: CONV_PER_Q for each quarter of TMEM lanes (a warp
@@ -93,7 +119,7 @@ struct SkinnyCfg {
     static constexpr uint32_t OFF_RAW = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_SC = OFF_RAW + STAGES * RAW_B;
     static constexpr uint32_t OFF_BAR = (OFF_SC + STAGES * SCALE_B + 7u) & ~7u;
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 2 * CSETS;
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * NACC + 2 * CSETS;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;  // MP destination rows (scattered rows)
     static constexpr uint32_t SMEM_BYTES = OFF_ROWS + MP * 4;
@@ -105,6 +131,7 @@ struct SkinnyCfg {
     static_assert(OFF_RAW % 1024 == 0 && RAW_B % 128 == 0, "TMA destinations stay aligned");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MMA N for M = 128 is a multiple of 16");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation is a power of two");
+    static_assert(ACC_COLS <= TMEM_COLS && NACC >= 2, "accumulators fit the allocation");
     static_assert(!W4 || CSET_COL0 + CSETS * CSET_COLS <= TMEM_COLS,
                   "accumulators and converted sets fit the allocation");
     static_assert(A_BOX % 1024 == 0 && B_BOX % 1024 == 0, "box images stay 1024-aligned");
@@ -211,39 +238,56 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
     const uint32_t bar0 = base + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    constexpr int NACC = Cfg::NACC;
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 4 + c); };  // per converted set
-    auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 4 + Cfg::CSETS + c); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + NACC + b); };
+    auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 2 * NACC + c); };  // per converted set
+    auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 2 * NACC + Cfg::CSETS + c); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
     volatile uint32_t *arrival = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 8);
 
     const int64_t nkb = args.num_k_blocks;
-    const int64_t W = static_cast<int64_t>(args.num_tiles) * nkb;
+    const int64_t S = args.sk_tiles;
+    const int64_t W = S * nkb;  // shared K blocks
     const int64_t G = gridDim.x;
     const int64_t my_start = W * blockIdx.x / G;
     const int64_t my_end = W * (blockIdx.x + 1) / G;
+    const int64_t sk_n = my_end - my_start;
+    // whole tiles S + blockIdx.x + G j (T - S is a multiple of G)
+    const int64_t n_steps = sk_n + (args.num_tiles - S) / G * nkb;
     // The share [my_start, my_end) is the tail of one tile, whole tiles, and the
     // head of another.  The two partial pieces go first: the tiles they belong
     // to are finished by a neighbour CTA too, so doing them early moves the
-    // last-arriver reductions off the end of the kernel.  Step i of the share
-    // (0 <= i < my_end - my_start) is K block order(i); pieces stay contiguous.
+    // last-arriver reductions off the end of the kernel; the CTA's own whole
+    // tiles come last.  Step i (0 <= i < n_steps) is linear K block order(i)
+    // (tile order(i) / nkb); pieces stay contiguous.
     const int64_t b1 = (my_start + nkb - 1) / nkb * nkb;  // first tile boundary
     const int64_t b2 = my_end / nkb * nkb;                 // last tile boundary
     const bool crosses = b1 < my_end;
-    const int64_t len_a = crosses ? b1 - my_start : my_end - my_start;  // tail piece
-    const int64_t len_b = crosses ? my_end - b2 : 0;                      // head piece
+    const int64_t len_a = crosses ? b1 - my_start : sk_n;  // tail piece
+    const int64_t len_b = crosses ? my_end - b2 : 0;       // head piece
     auto order = [&](int64_t i) -> int64_t {
         if (i < len_a)
             return my_start + i;
         if (i < len_a + len_b)
             return b2 + (i - len_a);
-        return b1 + (i - len_a - len_b);
+        if (i < sk_n)
+            return b1 + (i - len_a - len_b);
+        const int64_t d = i - sk_n;
+        return (S + blockIdx.x + G * (d / nkb)) * nkb + d % nkb;
     };
-    // end, in steps, of the piece that step i belongs to
+    // end, in steps, of the piece that step i belongs to: the tail piece, the
+    // head piece, then whole tiles of nkb steps each (those of the share
+    // between the two pieces, which starts on a tile boundary, then the
+    // CTA's own)
     auto piece_end = [&](int64_t i) -> int64_t {
-        return i < len_a ? len_a : (i < len_a + len_b ? len_a + len_b : my_end - my_start);
+        if (i < len_a)
+            return len_a;
+        if (i < len_a + len_b)
+            return len_a + len_b;
+        const int64_t w0 = i < sk_n ? len_a + len_b : sk_n;
+        return w0 + ((i - w0) / nkb + 1) * nkb;
     };
 
     // stage st <- B and A boxes of linear K block q, counted on full_bar(st)
@@ -283,7 +327,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             mbar_init(cfull_bar(c), Cfg::CONV_WARPS);
             mbar_init(cempty_bar(c), Cfg::ISSUERS);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NACC; ++b) {
             mbar_init(accf_bar(b), Cfg::ISSUERS);
             mbar_init(acce_bar(b), 4);
         }
@@ -298,7 +342,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         grid_dependency_wait();
         // the ring is empty: start the B stream now instead of after the
         // tensor-memory allocation and the set-up barrier
-        for (int64_t i = 0; i < my_end - my_start && pre < STAGES; ++i, ++pre)
+        for (int64_t i = 0; i < n_steps && pre < STAGES; ++i, ++pre)
             issue_stage(pre, order(i), pre == 0 ? args.extra_tx : 0u);
     }
     if (warp == 1) {
@@ -320,7 +364,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         uint32_t ph = 0;
         int pending = 0;
         bool alive = true;
-        for (int64_t i = 0; i < my_end - my_start; ++i) {
+        for (int64_t i = 0; i < n_steps; ++i) {
             const int64_t q = order(i);
             if (i >= pre) {
                 if (!warp_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status,
@@ -362,19 +406,15 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             int cset = 0;  // converted set (W4)
             uint32_t cph = 0;
             bool alive = true;
-            for (int64_t i = 0; i < my_end - my_start && alive;) {
-                const int64_t pos = order(i);
-                const int32_t t = static_cast<int32_t>(pos / nkb);
-                const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
-                const int64_t left = piece_end(i) - i;
-                const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + left ? nkb : kb0 + left);
+            for (int64_t i = 0; i < n_steps && alive;) {
+                const int64_t i1 = piece_end(i);  // this piece: steps i .. i1 - 1
                 if (!wait_bounded<W4>(acce_bar(ab), aph ^ 1u, abort_flag, args.status,
                                       args.timeout_ns, kWhereMmaAccEmpty))
                     break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem =
                     tmem_base + static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP);
-                for (int32_t kb = kb0; kb < kb1; ++kb) {
+                for (int64_t st = i; st < i1; ++st) {
                     if (!wait_bounded<W4>(full_bar(s), ph, abort_flag, args.status,
                                           args.timeout_ns, kWhereMmaFull)) {
                         alive = false;
@@ -400,14 +440,14 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
 #pragma unroll
                             for (int k = 0; k < Cfg::BK / 16; ++k)
                                 tc_mma_f16_tmem_a(d_tmem, bt + 8u * k, ad + 2u * k, idesc,
-                                                  (kb != kb0 || j != e || k != 0) ? 1u : 0u);
+                                                  (st != i || j != e || k != 0) ? 1u : 0u);
                         } else {
                             const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES +
                                                               j * Cfg::B_BOX);
 #pragma unroll
                             for (int k = 0; k < Cfg::BK / 16; ++k)
                                 tc_mma_f16(d_tmem, bd + 2u * k, ad + 2u * k, idesc,
-                                           (kb != kb0 || j != 0 || k != 0) ? 1u : 0u);
+                                           (st != i || j != 0 || k != 0) ? 1u : 0u);
                         }
                     }
                     tc_commit(empty_bar(s));
@@ -426,11 +466,11 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                 if (!alive)
                     break;
                 tc_commit(accf_bar(ab));
-                if (++ab == 2) {
+                if (++ab == NACC) {
                     ab = 0;
                     aph ^= 1u;
                 }
-                i += kb1 - kb0;
+                i = i1;
             }
         }
         __syncwarp();
@@ -459,13 +499,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         }
         int ab = 0;
         uint32_t aph = 0;
-        for (int64_t i = 0; i < my_end - my_start;) {
-            const int64_t pos = order(i);
-            const int32_t t = static_cast<int32_t>(pos / nkb);
-            const int32_t kb0 = static_cast<int32_t>(pos - t * nkb);
-            const int64_t left = piece_end(i) - i;
-            const int32_t kb1 = static_cast<int32_t>(nkb < kb0 + left ? nkb : kb0 + left);
-            i += kb1 - kb0;
+        for (int64_t i = 0; i < n_steps;) {
+            const int32_t t = static_cast<int32_t>(order(i) / nkb);
+            i = piece_end(i);
             const int32_t n = t * Cfg::BN + n_local;
             // FP4 weights with MP > 16 finish the MP rows of A in chunks of 16,
             // so the epilogue's registers stay those of MP = 16 and leave room
@@ -501,8 +537,11 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             if (!ok || *abort_flag)
                 break;
             tc_fence_after_sync();
-            const int32_t c_lo = skinny_owner(static_cast<int64_t>(t) * nkb, W, G);
-            const int32_t c_hi = skinny_owner(static_cast<int64_t>(t + 1) * nkb - 1, W, G);
+            const bool shared_tile = t < S;
+            const int32_t c_lo =
+                shared_tile ? skinny_owner(static_cast<int64_t>(t) * nkb, W, G) : static_cast<int32_t>(blockIdx.x);
+            const int32_t c_hi =
+                shared_tile ? skinny_owner(static_cast<int64_t>(t + 1) * nkb - 1, W, G) : c_lo;
             const int32_t parts = args.reduce ? 1 : c_hi - c_lo + 1;
             // a split tile's partial sums: slot (t, blockIdx.x - c_lo) of the workspace
             const int32_t my_slot = static_cast<int32_t>(blockIdx.x) - c_lo;
@@ -544,7 +583,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(acce_bar(ab));
-            if (++ab == 2) {
+            if (++ab == NACC) {
                 ab = 0;
                 aph ^= 1u;
             }
@@ -606,7 +645,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         uint32_t ph = 0;
         int cset = 0;
         uint32_t cph = 0;
-        for (int64_t q = 0; q < my_end - my_start; ++q) {
+        for (int64_t q = 0; q < n_steps; ++q) {
             if (!warp_wait_bounded<true>(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
                                    kWhereMmaFull))
                 break;

@@ -12,6 +12,10 @@
 #ifndef TCG_PDL
 #define TCG_PDL 1
 #endif
+// skinny kernel, FP4 B: whole waves of tiles go to CTAs whole (0: every tile shared)
+#ifndef TCG_SKINNY_WHOLE
+#define TCG_SKINNY_WHOLE 1
+#endif
 
 namespace tcg {
 
@@ -60,9 +64,29 @@ cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, in
 // when W blocks are shared by G CTAs as [W g / G, W (g+1) / G).
 inline int64_t skinny_owner_host(int64_t x, int64_t W, int64_t G) { return ((x + 1) * G - 1) / W; }
 
-// Most CTAs that contribute to one tile (workspace slots per tile).
+// Tiles of the skinny kernel shared block by block when T tiles run on G
+// CTAs.  bf16 / f16 B: all of them.  FP4 B: the T mod G left over after
+// whole waves (each CTA takes floor(T / G) tiles whole), plus one wave more
+// when fewer than G / 4 are left over, so that no tile is cut into more than
+// about five parts.  The shared tiles are tiles 0 .. S-1; T - S is always a
+// multiple of G.
+inline int64_t skinny_sk_tiles(int64_t T, int64_t G, bool w4)
+{
+    if (!w4 || !TCG_SKINNY_WHOLE)
+        return T;
+    const int64_t waves = T / G;
+    int64_t S = T - waves * G;
+    if (S != 0 && waves > 0 && 4 * S < G)
+        S += G;
+    return S;
+}
+
+// Most CTAs that contribute to one shared tile (workspace slots per tile)
+// when `tiles` tiles of nkb K blocks are shared by G CTAs.
 inline int32_t skinny_max_parts(int64_t tiles, int64_t nkb, int64_t G)
 {
+    if (tiles == 0)
+        return 1;
     const int64_t W = tiles * nkb;
     if (tiles > 65536) {
         // shares are at least W / G blocks long, so a tile of nkb blocks holds at

@@ -1,5 +1,5 @@
 // launch_skinny.cu -- instantiations and launcher of the swap-AB stream-K kernel
-// (bf16/f16 B, or FP4 B with block scales converted in shared memory).
+// (bf16/f16 B, or FP4 B with block scales converted into tensor memory).
 #include <cuda_runtime.h>
 
 #include "kernel_skinny.cuh"

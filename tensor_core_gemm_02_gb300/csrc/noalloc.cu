@@ -82,7 +82,7 @@ extern "C" gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int 
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
     const gemm_plan plan =
-        make_plan(p.M, p.N, p.K, false, p.C != nullptr && p.beta != 0.0f, dev->sm_count);
+        noalloc_plan(p.M, p.N, p.K, p.C != nullptr && p.beta != 0.0f, dev->sm_count);
     if (plan.kernel == 10)
         return run_tiny(p, plan, dev);  // the warp-level kernel needs no scratch at all
     if (plan.kernel != 2)
@@ -117,6 +117,7 @@ extern "C" gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int 
     a.num_n_blocks = static_cast<int32_t>(plan.tiles);
     a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, tcg::skinny_kstage()));
     a.num_tiles = static_cast<int32_t>(plan.tiles);
+    a.sk_tiles = static_cast<int32_t>(tcg::skinny_sk_tiles(plan.tiles, plan.grid, false));
     a.group_m = 1;
     a.splits = plan.splits;
     a.workspace = partials;

@@ -38,7 +38,7 @@ def _as_bf16(ref):
 @pytest.mark.parametrize("M", [16, 48, 300, 1024])
 def test_chain_of_dependent_gemms(M):
     """Eight GEMMs on one stream, each reading the previous one's bf16 output.
-    M = 16 / 48 run the skinny kernel, larger M the tile kernels."""
+    M = 16 runs the warp-level kernel, larger M the tile kernels."""
     rng = np.random.default_rng(M)
     K = 192
     a = _ternary(rng, (M, K))
@@ -54,18 +54,18 @@ def test_chain_of_dependent_gemms(M):
 
 
 def test_chain_mixing_kernels():
-    """Skinny -> gathered tile -> skinny on one stream, each step reading the
+    """Warp-level -> gathered tile -> skinny on one stream, each step reading the
     previous one's output."""
     rng = np.random.default_rng(5)
     a = _ternary(rng, (16, 128))
     b1 = _signed_selector(rng, 256, 128)
     idx = torch.from_numpy(rng.integers(0, 16, 512).astype(np.int32))
     b2 = _signed_selector(rng, 640, 256)
-    b3 = _signed_selector(rng, 96, 640)
+    b3 = _signed_selector(rng, 64, 640)  # K >= 8 N: the skinny kernel for 40 rows
 
     d1 = binding.gemm_bf16(a.to(DEV), b1.to(DEV), out=OUT_BF16)           # 16 x 256
     d2 = binding.gemm_gather_rows(d1, idx.to(DEV), b2.to(DEV), out=OUT_BF16)  # 512 x 640
-    d3 = binding.gemm_bf16(d2[:40], b3.to(DEV), out=OUT_F32)              # 40 x 96
+    d3 = binding.gemm_bf16(d2[:40], b3.to(DEV), out=OUT_F32)              # 40 x 64
     assert device_status() == binding.GEMM_OK
 
     r1 = _as_bf16(oracle.gemm(a, b1)[0])

@@ -342,24 +342,30 @@ SKINNY_SHAPES = [(1, 3000, 640), (5, 1000, 520), (16, 4096, 1024), (17, 777, 264
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY_SHAPES)
-def test_skinny_quarter_bit_exact(M, N, K):
-    """M <= 64 goes through the swap-AB stream-K kernel; exact inputs stay exact
-    through its split partial sums."""
-    plan = binding.gemm_query_plan(M, N, K, sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
-    assert plan.kernel == 2
+@pytest.mark.parametrize("form", [(2, 0), (0, 0)], ids=["skinny", "auto"])
+def test_skinny_quarter_bit_exact(M, N, K, form):
+    """M <= 64 through the swap-AB stream-K kernel (forced), and through whatever
+    the automatic choice gives the shape; exact inputs stay exact through the
+    skinny kernel's split partial sums."""
+    binding.gemm_debug_force_tile(*form)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = binding.gemm_query_plan(M, N, K, sm_count=sms)
+    assert plan.kernel == 2 or form == (0, 0)
     for out, with_c, alpha, beta in [(OUT_F32, True, 0.5, 2.0), (OUT_BF16, False, 1.0, 0.0)]:
         p = workloads.random_problem(M + N + K, M, N, K, dtype="bf16", values="quarter",
                                      with_c=with_c, alpha=alpha, beta=beta, out=out)
         ref, _, _ = oracle_full(p)
-        assert_bits(run(p), ref, out, f"skinny {M}x{N}x{K} out={out}")
+        assert_bits(run(p), ref, out, f"kernel {plan.kernel} {M}x{N}x{K} out={out}")
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 28672, 4096), (40, 3000, 2056), (7, 513, 8192)])
-def test_skinny_normal_within_tolerance(M, N, K):
+@pytest.mark.parametrize("form", [(2, 0), (0, 0)], ids=["skinny", "auto"])
+def test_skinny_normal_within_tolerance(M, N, K, form):
+    binding.gemm_debug_force_tile(*form)
     p = workloads.random_problem(M * N + K, M, N, K, dtype="f16", with_c=True, alpha=0.5,
                                  beta=1.0, b_scale=0.02)
     ref, absprod, _ = oracle_full(p)
-    assert_within(run(p), ref, absprod, OUT_F32, f"skinny {M}x{N}x{K}")
+    assert_within(run(p), ref, absprod, OUT_F32, f"form {form} {M}x{N}x{K}")
 
 
 def test_skinny_repeated_calls_are_deterministic():
@@ -372,6 +378,7 @@ def test_skinny_repeated_calls_are_deterministic():
 
 def test_skinny_timeout_is_reported():
     p = workloads.random_problem(32, 16, 2048, 1024, dtype="bf16", values="quarter")
+    binding.gemm_debug_force_tile(2, 0)  # (the automatic choice for this shape is the tile kernel)
     binding.gemm_set_wait_timeout(50_000_000)
     binding.gemm_debug_inject(1)
     try:

@@ -91,8 +91,8 @@ def test_scatter_identity_matches_plain(form):
 def test_scatter_permutation_matches_plain_rows():
     """A permutation only moves rows: D[perm[i]] equals row i of the plain GEMM
     (tile kernel: the same form for both calls)."""
-    binding.gemm_debug_force_tile(1, 128)  # (the skinny kernel, M <= 64, ignores this)
-    for M in (40, 700):  # skinny and tile kernels
+    binding.gemm_debug_force_tile(1, 128)
+    for M in (40, 700):
         p = workloads.random_problem(48 + M, M, 330, 200, dtype="f16", alpha=1.5)
         plain = run(p)
         perm = torch.from_numpy(np.random.default_rng(M).permutation(M).astype(np.int32))

@@ -214,11 +214,25 @@ def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(16, 28672, 4096, scatter=True, sm_count=148)
     assert p.kernel == 2
     plan = binding.Plan()
-    assert lib.gemm_query_plan(64, 64, 64, 5, 0, 148, ctypes.byref(plan)) == 1
+    assert lib.gemm_query_plan(64, 64, 64, 6, 0, 148, ctypes.byref(plan)) == 1
     p = binding.gemm_query_plan(100, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bn) == (1, 64)
-    p = binding.gemm_query_plan(40, 1000, 64, sm_count=148)
-    assert p.kernel == 2 and p.bm == 64
+    # 16 < M <= 64: the tile kernel unless K is long against N
+    assert binding.gemm_query_plan(40, 1000, 64, sm_count=148).kernel == 1
+    assert binding.gemm_query_plan(64, 28672, 4096, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(32, 4096, 4096, sm_count=148).kernel != 2
+    p = binding.gemm_query_plan(32, 4096, 8192, sm_count=148)
+    assert (p.kernel, p.bm) == (2, 32)
+    p = binding.gemm_query_plan(40, 1024, 8192, sm_count=148)
+    assert (p.kernel, p.bm) == (2, 64)
+    assert binding.gemm_query_plan(64, 4096, 16384, sm_count=148).kernel == 2
+    assert binding.gemm_query_plan(48, 2048, 8192, sm_count=148).kernel != 2
+    # the allocation-free entry point always plans the skinny kernel (or the tiny one)
+    p = binding.gemm_query_plan(40, 1000, 64, noalloc=True, sm_count=148)
+    assert (p.kernel, p.bm) == (2, 64)
+    assert binding.gemm_query_plan(16, 8, 32, noalloc=True, sm_count=148).kernel == 10
+    assert binding.gemm_query_plan(65, 1000, 64, noalloc=True, sm_count=148).kernel == 0
+    assert binding.gemm_query_plan(16, 1000, 0, noalloc=True, sm_count=148).kernel == 0
     assert binding.gemm_query_plan(0, 10, 10).kernel == 0
     # at most 2^20 multiply-adds: the warp-level kernel, one 16 x 8 block per warp
     p = binding.gemm_query_plan(16, 8, 32, sm_count=148)
@@ -226,22 +240,65 @@ def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(64, 128, 128, sm_count=148)
     assert (p.kernel, p.tiles, p.grid) == (10, 4 * 16, 16)
     assert binding.gemm_query_plan(128, 128, 128, sm_count=148).kernel == 1
-    assert binding.gemm_query_plan(16, 1024, 1024, sm_count=148).kernel == 2
+    # M <= 16: the skinny kernel once N * K > 2^21
+    assert binding.gemm_query_plan(16, 1024, 1024, sm_count=148).kernel == 1
+    assert binding.gemm_query_plan(16, 1024, 2049, sm_count=148).kernel == 2
+    assert binding.gemm_query_plan(8, 4096, 4096, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(300, 200, 0, sm_count=148).kernel == 10  # K = 0: beta * C
     assert binding.gemm_query_plan(3000, 2000, 0, sm_count=148).kernel == 1
 
 
+def _skinny_steps(tiles, nkb, G, whole):
+    """Each CTA's linear K blocks in the order the skinny kernel runs them.
+    With whole tiles (FP4 B), floor(T / G) waves of tiles (one wave fewer
+    when fewer than G / 4 tiles are left over) go whole, tile S + g + G j to
+    CTA g, after its contiguous share [W g / G, W (g+1) / G) of the first S
+    tiles' W = S nkb blocks (tail piece, head piece, whole tiles between);
+    without (bf16 B), S = T."""
+    S = tiles
+    if whole:
+        waves = tiles // G
+        S = tiles - waves * G
+        if S and waves and 4 * S < G:
+            S += G
+    W = S * nkb
+    steps = []
+    for g in range(G):
+        lo, hi = W * g // G, W * (g + 1) // G
+        b1, b2 = -(-lo // nkb) * nkb, hi // nkb * nkb
+        if b1 < hi:
+            mine = list(range(lo, b1)) + list(range(b2, hi)) + list(range(b1, b2))
+        else:
+            mine = list(range(lo, hi))
+        for j in range((tiles - S) // G):
+            t = S + g + G * j
+            mine += list(range(t * nkb, (t + 1) * nkb))
+        steps.append(mine)
+    return S, steps
+
+
 def test_skinny_split_arithmetic_covers_every_block():
-    """The stream-K shares partition the k-block list and every tile's parts fit its slots."""
-    for tiles, nkb, G in [(224, 64, 148), (3, 5, 7), (1, 1, 1), (10, 3, 30), (1000, 7, 152),
-                          (4, 8, 148), (8, 16, 148), (64, 16, 148)]:
-        W = tiles * nkb
-        G = min(G, -(-W // 8))  # at least 8 K blocks per CTA
-        owner = lambda x: ((x + 1) * G - 1) // W
-        starts = [W * g // G for g in range(G)]
-        for g in range(G):
-            lo, hi = starts[g], W * (g + 1) // G
-            assert all(owner(x) == g for x in range(lo, hi))
-        most = max(owner((t + 1) * nkb - 1) - owner(t * nkb) + 1 for t in range(tiles))
-        p = binding.gemm_query_plan(16, tiles * 128, nkb * 64, sm_count=G)
-        assert p.splits == most
+    """Shared shares and whole tiles cover every K block once, and every shared
+    tile's parts fit its workspace slots."""
+    cases = [(224, 64, 148), (3, 5, 7), (1, 1, 1), (10, 3, 30), (1000, 7, 152), (4, 8, 148),
+             (8, 16, 148), (64, 16, 148), (224, 64, 152), (300, 64, 148), (304, 8, 152),
+             (150, 64, 148), (190, 16, 152), (224, 16, 152)]
+    for (tiles, nkb, G), whole in [(c, w) for c in cases for w in (False, True)]:
+        G = min(G, -(-(tiles * nkb) // 8))  # at least 8 K blocks per CTA
+        S, steps = _skinny_steps(tiles, nkb, G, whole)
+        assert (tiles - S) % G == 0 and 0 <= S <= tiles
+        flat = sorted(x for mine in steps for x in mine)
+        assert flat == list(range(tiles * nkb))
+        # every CTA's work is balanced to within one K block
+        assert max(map(len, steps)) - min(map(len, steps)) <= 1
+        owner = {x: g for g, mine in enumerate(steps) for x in mine}
+        parts = [len({owner[x] for x in range(t * nkb, (t + 1) * nkb)}) for t in range(tiles)]
+        assert all(n == 1 for n in parts[S:])  # whole tiles
+        most = max(parts[:S], default=1)
+        # bf16 B: 64 K elements per block; FP4 B: 256
+        p = binding.gemm_query_plan(16, tiles * 128, nkb * (256 if whole else 64), sm_count=G,
+                                    fp4=whole)
+        if p.kernel == 2:  # (the smallest bf16 case runs on the warp-level kernel)
+            assert p.grid == G and p.splits == most
+        else:
+            assert not whole

@@ -80,8 +80,9 @@ def test_noalloc_rejects_what_it_cannot_hold():
     A = torch.zeros((64, 4096), dtype=torch.bfloat16, device=DEV)
     B = torch.zeros((38400, 4096), dtype=torch.bfloat16, device=DEV)
     D = torch.zeros((64, 38400), device=DEV)
-    plan = binding.gemm_query_plan(64, 38400, 4096,
+    plan = binding.gemm_query_plan(64, 38400, 4096, noalloc=True,
                                    sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan.kernel == 2
     assert plan.tiles * plan.splits * 128 * 64 * 4 > 16 << 20
     assert _call(lib, 64, 38400, 4096, A, B, D, stream) == 3
     assert binding.gemm_check_device_status() == binding.GEMM_OK
