@@ -41,9 +41,9 @@
 #include "fp4.cuh"
 
 
-// Accumulator buffers of the bf16 / f16 form (at most 512 / (MP) columns).
+// Accumulator buffers of the bf16 / f16 form (at most 512 / MP).
 #ifndef TCG_SKINNY_NACC
-#define TCG_SKINNY_NACC 4
+#define TCG_SKINNY_NACC 2
 #endif
 
 
@@ -80,12 +80,9 @@ struct SkinnyCfg {
     static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : 1;
     static constexpr int EPI_WARP0 = 1 + ISSUERS;    // four epilogue warps
     static constexpr int CONV_WARP0 = EPI_WARP0 + 4;  // then the converters
-    // Accumulator buffers.  A CTA's share is a few pieces (a tile's tail, the
-    // next one's head, whole tiles); a short piece after a long one leaves the
-    // epilogue of the long one (partial sums out, maybe the reduction) too
-    // little MMA time to hide behind, so the bf16 kernel keeps four buffers
-    // and the MMA rarely waits for a free one.  (FP4 B: two, the rest of
-    // tensor memory holds converted weights.)
+    // Accumulator buffers: the MMA fills one while the epilogue drains the
+    // other.  (Four for bf16 B measured the same as two; FP4 B needs the rest
+    // of tensor memory for converted weights.)
     static constexpr int NACC = W4 ? 2 : TCG_SKINNY_NACC;
     static constexpr uint32_t ACC_COLS = static_cast<uint32_t>(NACC * ISSUERS * MP);
     static constexpr uint32_t TMEM_COLS = W4 ? 512u : tmem_cols_for(ACC_COLS);
