@@ -69,11 +69,25 @@ def _assert_close(D, p, ref, absprod, what, times=1):
                                    (129, 257, 72), (300, 520, 264), (513, 700, 1000)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_accumulate_quarter_bit_exact(M, N, K, dtype):
-    """Skinny (M <= 64, with split K tiles for the larger K) and tile kernels."""
+    """The automatic choice: warp-level, tile and (for M <= 64 where it wins)
+    skinny kernels."""
     for alpha in (0.5, -2.0):
         p = _problem(M + 3 * N + K, M, N, K, dtype=dtype, alpha=alpha)
         ref, _ = _oracle(p)
         assert_bits(run(p), ref, OUT_F32, f"{M}x{N}x{K} {dtype} alpha={alpha}")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 300, 136), (48, 520, 4096), (64, 4096, 2048),
+                                   (33, 130, 520)])
+def test_accumulate_skinny_forced_bit_exact(M, N, K):
+    """The skinny kernel on every M <= 64 shape (forced): each part of a split
+    tile adds itself into D."""
+    binding.gemm_debug_force_tile(2, 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert binding.gemm_query_plan(M, N, K, sm_count=sms).kernel == 2
+    p = _problem(M + 5 * N + K, M, N, K, dtype="bf16", alpha=0.5)
+    ref, _ = _oracle(p)
+    assert_bits(run(p), ref, OUT_F32, f"skinny {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("form", TILE_FORMS, ids=FORM_IDS)

@@ -41,12 +41,27 @@ CASES = [("bf16", OUT_F32, True, 0.5, 2.0), ("f16", OUT_BF16, False, 1.0, 0.0),
                                           (129, 257, 72, 500), (300, 520, 264, 700),
                                           (513, 700, 1000, 2000), (256, 96, 64, 256)])
 def test_scatter_quarter_bit_exact(M, N, K, d_rows):
-    """Skinny (M <= 64) and tile kernels, ragged shapes, every output type."""
+    """The automatic choice (warp-level, tile and skinny kernels), ragged
+    shapes, every output type."""
     for dtype, out, with_c, alpha, beta in CASES:
         p = workloads.random_problem(M + 7 * N + K, M, N, K, dtype=dtype, values="quarter",
                                      with_c=with_c, alpha=alpha, beta=beta, out=out,
                                      scatter_rows=d_rows)
         assert_scatter(run(p), p, True, f"{M}x{N}x{K} into {d_rows} {dtype} out={out}")
+
+
+@pytest.mark.parametrize("M,N,K,d_rows", [(16, 300, 136, 40), (48, 520, 200, 100),
+                                          (64, 1000, 520, 3000)])
+def test_scatter_skinny_forced_bit_exact(M, N, K, d_rows):
+    """The skinny kernel's scattered epilogue (forced) on ragged M <= 64 shapes."""
+    binding.gemm_debug_force_tile(2, 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert binding.gemm_query_plan(M, N, K, scatter=True, sm_count=sms).kernel == 2
+    for dtype, out, with_c, alpha, beta in CASES:
+        p = workloads.random_problem(M + 9 * N + K, M, N, K, dtype=dtype, values="quarter",
+                                     with_c=with_c, alpha=alpha, beta=beta, out=out,
+                                     scatter_rows=d_rows)
+        assert_scatter(run(p), p, True, f"skinny {M}x{N}x{K} into {d_rows} {dtype} out={out}")
 
 
 @pytest.mark.parametrize("form", TILE_FORMS, ids=FORM_IDS)
