@@ -15,6 +15,10 @@ TFLOP/s = 2 M N K / time.  The same line also carries:
   roofline      the kernel's achieved TFLOP/s against the measured dense bf16
                 peak in MEASURED_PEAKS.json (tensor-bound), and the DRAM traffic
                 per launch from the committed ncu summary when it is current
+  clocks        nvidia-smi samples every 20 ms inside the timed region (median
+                SM clock, reasons seen active) and the driver's per-reason
+                slowdown counters read at its two ends (reason_us: how long
+                each reason held the clocks down in it)
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample of rows
   variants      the other workloads (f16 1024^3 + C, 8192 x 28672 x 4096 with
                 C, the M = 16 skinny case, the gathered 16384-of-65536 rows
@@ -111,22 +115,46 @@ def stored_traffic(kernel_key):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs,
+    plus the driver's cumulative per-reason slowdown counters (microseconds) read
+    right before and right after it, which catch a reason that was active between
+    two samples."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "power.draw.instant")
+    COUNTERS = ("sw_power_cap", "sw_thermal_slowdown", "hw_thermal_slowdown",
+                "hw_power_brake_slowdown")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
 
+    def counters(self):
+        """The cumulative slowdown counters (us per reason), or None if unavailable."""
+        q = ",".join("clocks_event_reasons_counters." + c for c in self.COUNTERS)
+        try:
+            out = subprocess.run(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={q}",
+                                  "--format=csv,noheader,nounits"], capture_output=True,
+                                 text=True, timeout=10)
+            vals = [int(x.strip()) for x in out.stdout.strip().split(",")]
+        except (OSError, ValueError, subprocess.SubprocessError):
+            return None
+        return dict(zip(self.COUNTERS, vals)) if len(vals) == len(self.COUNTERS) else None
+
     def mark(self, which):
-        """Host wall-clock bounds of the timed region (samples outside are dropped)."""
+        """Host wall-clock bounds of the timed region (samples outside are dropped);
+        the slowdown counters are read just before the start and just after the end."""
+        if which == "t_start":
+            self.c_start = self.counters()
         setattr(self, which, time.time())
+        if which == "t_end":
+            self.c_end = self.counters()
 
     def __enter__(self):
         self.t_start = self.t_end = None
+        self.c_start = self.c_end = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -158,8 +186,12 @@ class ClockSampler:
                 try:
                     ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
                     mask = int(parts[5], 16) if parts[5].startswith("0x") else 0
+                    try:
+                        inst = float(parts[10]) if len(parts) > 10 else float(parts[4])
+                    except ValueError:
+                        inst = float(parts[4])
                     rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
-                                 "power": float(parts[4]), "mask": mask,
+                                 "power": float(parts[4]), "power_inst": inst, "mask": mask,
                                  "hw_slowdown": parts[6] == "Active",
                                  "hw_thermal_slowdown": parts[7] == "Active",
                                  "sw_thermal_slowdown": parts[8] == "Active",
@@ -177,9 +209,14 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         pw = sorted(r["power"] for r in rows)
         load = rows
-        reasons = sorted({k for r in rows for k in ("hw_slowdown", "hw_thermal_slowdown",
-                                                     "sw_thermal_slowdown", "sw_power_cap")
-                          if r[k]})
+        reasons = {k for r in rows for k in ("hw_slowdown", "hw_thermal_slowdown",
+                                             "sw_thermal_slowdown", "sw_power_cap") if r[k]}
+        # microseconds each reason held the clocks down inside the timed region
+        reason_us = None
+        if self.c_start is not None and self.c_end is not None:
+            reason_us = {k: self.c_end[k] - self.c_start[k] for k in self.COUNTERS}
+            reasons |= {k for k, v in reason_us.items() if v > 0}
+        reasons = sorted(reasons)
         # every reason in the active bitmask (nvidia-smi's clocks_event_reasons bits)
         names = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
                  0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
@@ -188,6 +225,10 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r["sm"] for r in load),
                 "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
                 "active_reasons": active, "samples": len(rows), "power_w_max": max(pw),
+                "power_instant_w_max": max(r["power_inst"] for r in rows),
+                "reason_us": reason_us,
+                "window_us": (round((self.t_end - self.t_start) * 1e6)
+                              if self.t_start is not None and self.t_end is not None else None),
                 "sm_mhz_samples": [r["sm"] for r in rows][:40]}
 
 

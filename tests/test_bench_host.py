@@ -90,3 +90,40 @@ def test_traffic_is_reported_only_for_current_sources(tmp_path, monkeypatch):
         {"source_hash": "current", "kernels": {"k@w": {"dram_bytes_per_launch": 5}}}))
     assert bench.stored_traffic("k@w") == 5
     assert bench.stored_traffic("other@w") is None
+
+
+def test_clock_summary_counts_reasons_between_samples(tmp_path):
+    """A slowdown reason that no 20 ms sample caught still shows up through the
+    driver's cumulative counters read at the ends of the timed region; samples
+    outside the region are dropped."""
+    c = bench.ClockSampler(0)
+    c.out.close()
+    rows = [("2026/01/01 00:00:00.000", 2070, "0x0000000000000000", "Not Active"),
+            ("2026/01/01 00:00:01.000", 2070, "0x0000000000000000", "Not Active"),
+            ("2026/01/01 00:00:01.020", 1700, "0x0000000000000000", "Not Active"),
+            ("2026/01/01 00:00:01.040", 1700, "0x0000000000000004", "Active"),
+            ("2026/01/01 00:00:09.000", 900, "0x0000000000000040", "Not Active")]
+    with open(c.out.name, "w") as f:
+        for ts, sm, mask, cap in rows:
+            f.write(f"{ts}, 0, {sm}, 2070, 300.5, {mask}, Not Active, Not Active, "
+                    f"Not Active, {cap}, 900.25\n")
+    import datetime
+    t = lambda s: datetime.datetime.strptime(s, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    c.t_start, c.t_end = t("2026/01/01 00:00:00.990"), t("2026/01/01 00:00:01.050")
+    c.c_start = {"sw_power_cap": 100, "sw_thermal_slowdown": 5, "hw_thermal_slowdown": 0,
+                 "hw_power_brake_slowdown": 0}
+    c.c_end = dict(c.c_start, sw_power_cap=30100)
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1700 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["active_reasons"] == ["sw_power_cap"]
+    assert s["reason_us"]["sw_power_cap"] == 30000 and s["reason_us"]["sw_thermal_slowdown"] == 0
+    assert s["power_instant_w_max"] == 900.25 and s["window_us"] == 60000
+    # without counters (older drivers) the samples alone decide
+    c2 = bench.ClockSampler(0)
+    c2.out.close()
+    with open(c2.out.name, "w") as f:
+        f.write("2026/01/01 00:00:01.020, 0, 1700, 2070, 300.5, 0x0000000000000000, "
+                "Not Active, Not Active, Not Active, Not Active\n")
+    c2.t_start, c2.t_end, c2.c_start, c2.c_end = None, None, None, None
+    s2 = c2.summary()
+    assert s2["reasons"] == [] and s2["reason_us"] is None and s2["power_instant_w_max"] == 300.5
