@@ -19,6 +19,9 @@ TFLOP/s = 2 M N K / time.  The same line also carries:
                 SM clock, reasons seen active) and the driver's per-reason
                 slowdown counters read at its two ends (reason_us: how long
                 each reason held the clocks down in it)
+  sustained     the headline GEMM back to back for about 4 s (--sustained-seconds),
+                once the power cap has settled, against the measured sustained
+                cuBLAS rate (bf16_tflops_sustained)
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample of rows
   variants      the other workloads (f16 1024^3 + C, 8192 x 28672 x 4096 with
                 C, the M = 16 skinny case, the gathered 16384-of-65536 rows
@@ -333,6 +336,44 @@ def time_headline(p, dev, steps, warmup, rank, world):
     return ms, clocks.summary()
 
 
+def time_sustained(p, dev, seconds):
+    """The headline GEMM back to back for about `seconds` (batches of 50 launches
+    until the host clock passes the mark), timed with CUDA events around the
+    whole run, clocks sampled meanwhile: the rate once the power cap has settled,
+    to set beside the measured sustained cuBLAS figure."""
+    tensors = to_device(p, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        launch(p, tensors)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n = 0
+    with ClockSampler(dev.index) as clocks:
+        clocks.mark("t_start")
+        e0.record(stream)
+        t0 = time.time()
+        marks = []
+        while time.time() - t0 < seconds:
+            for _ in range(50):
+                launch(p, tensors)
+            n += 50
+            marks.append(torch.cuda.Event())
+            marks[-1].record(stream)
+            # keep the host one batch ahead of the device: the queue never runs dry
+            if len(marks) > 1:
+                marks.pop(0).synchronize()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        clocks.mark("t_end")
+    ms = e0.elapsed_time(e1)
+    status = binding.gemm_check_device_status()
+    if status != binding.GEMM_OK:
+        raise RuntimeError(f"device status after the sustained run: {binding.gemm_status_string(status)}")
+    del tensors
+    return ms, n, clocks.summary()
+
+
 def time_e2e(p, dev, steps):
     """Host buffers through the C ABI, pipelined over three streams.
 
@@ -485,6 +526,18 @@ def run_ours(args):
 
     e2e_steps = min(args.steps, 20)
     e2e_ms, h2d, d2h = time_e2e(p, dev, e2e_steps)
+    sustained = None
+    if args.sustained_seconds > 0:
+        s_ms, s_n, s_clocks = time_sustained(p, dev, args.sustained_seconds)
+        s_rate = s_n * flops / (s_ms * 1e-3) / 1e12
+        s_peak = peaks.get("bf16_tflops_sustained")
+        sustained = {"value": round(s_rate, 2), "unit": "TFLOP/s", "launches": s_n,
+                     "seconds": round(s_ms * 1e-3, 3), "peak": s_peak,
+                     "frac": round(s_rate / s_peak, 4) if s_peak else None,
+                     "peak_source": f"{peaks['source']} bf16_tflops_sustained (cuBLAS, 4 s)",
+                     "clocks": {k: s_clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons",
+                                                              "reason_us", "window_us",
+                                                              "power_instant_w_max")}}
 
     result = {
         "metric": "GEMM TFLOP/s (bf16 8192^3, bf16 out)",
@@ -518,6 +571,8 @@ def run_ours(args):
                      "kernel": kernel_key(plan_of(p, dev), p),
                      "algorithmic_flops_per_launch": flops},
     }
+    if sustained is not None:
+        result["sustained"] = sustained
 
     if rank == 0 and args.variants:
         variants = {}
@@ -630,6 +685,8 @@ def main():
     ap.add_argument("--no-variants", dest="variants", action="store_false")
     ap.add_argument("--variant-reps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--sustained-seconds", type=float, default=4.0,
+                    help="length of the back-to-back sustained leg (0: skip it)")
     ap.add_argument("--case", choices=sorted(workloads.WORKLOADS), default=None,
                     help="only launch this workload's GEMM warmup + steps times (profiling)")
     args = ap.parse_args()
