@@ -544,10 +544,29 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             const int32_t my_slot = static_cast<int32_t>(blockIdx.x) - c_lo;
             float *slot0 = args.workspace + static_cast<int64_t>(t) * args.splits * (Cfg::BN * MP);
             float *mine = slot0 + static_cast<int64_t>(my_slot) * (Cfg::BN * MP);
+            // The CTA's last piece, of a split tile whose other parts are all
+            // in already (the usual case: the CTAs sharing the tile started
+            // with it): this CTA is the last to arrive whatever happens, so it
+            // skips writing its part, the fences and the counter, and adds its
+            // part from registers below.  (An earlier piece rarely finds the
+            // others in, and the extra load there measured slower.  bf16 / f16
+            // B with MP <= 32 only: keeping the part in registers spills with
+            // FP4 B's converter warps and with MP = 64; FP4 B ends on whole
+            // tiles.)
+            constexpr bool kKeep = !W4 && MP <= 32 && NCH == 1;
+            bool last_known = false;
+            if (kKeep && parts > 1 && i == n_steps) {
+                if (leader) {
+                    const uint32_t in = ld_acquire_gpu(args.counters + t);
+                    *arrival = in;
+                }
+                epi_bar_sync();
+                last_known = *arrival == static_cast<uint32_t>(parts - 1);
+            }
+            float v[CH];  // this chunk's sums (with one chunk: the CTA's whole part)
 #pragma unroll 1
             for (int g = 0; g < NCH; ++g) {
                 // the issuers' partial sums of this chunk, added in issuer order
-                float v[CH];
 #pragma unroll
                 for (int e = 0; e < Cfg::ISSUERS; ++e) {
 #pragma unroll
@@ -570,7 +589,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                     float cb[CH];
                     chunk_cb(g, cb);
                     skinny_store<CH>(args, drow, n, CH * g, v, cb);
-                } else {
+                } else if (!last_known) {
 #pragma unroll
                     for (int m = 0; m < CH; ++m)
                         __stcg(mine + (CH * g + m) * Cfg::BN + n_local, v[m]);
@@ -586,23 +605,28 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             }
             if (parts == 1)
                 continue;
-            // The CTA barrier orders every thread's partial before the leader's
-            // device-scope fence and counter increment; for the last CTA to
-            // arrive, the leader's second fence orders the other CTAs' parts
-            // before the reads below (the barrier after it passes that on).
-            epi_bar_sync();
-            if (leader) {
-                __threadfence();
-                const uint32_t before = atomicAdd(args.counters + t, 1u);
-                if (before == static_cast<uint32_t>(parts - 1))
+            if (!last_known) {
+                // The CTA barrier orders every thread's partial before the
+                // leader's device-scope fence and counter increment; for the
+                // last CTA to arrive, the leader's second fence orders the
+                // other CTAs' parts before the reads below (the barrier after
+                // it passes that on).  (With the other parts seen in beforehand,
+                // the acquire load above and its barrier did the same.)
+                epi_bar_sync();
+                if (leader) {
                     __threadfence();
-                *arrival = before;
+                    const uint32_t before = atomicAdd(args.counters + t, 1u);
+                    if (before == static_cast<uint32_t>(parts - 1))
+                        __threadfence();
+                    *arrival = before;
+                }
+                epi_bar_sync();
+                if (*arrival != static_cast<uint32_t>(parts - 1))
+                    continue;  // another CTA still has to add its part
             }
-            epi_bar_sync();
-            if (*arrival != static_cast<uint32_t>(parts - 1))
-                continue;  // another CTA still has to add its part
             // last to arrive: add the parts in slot order (this CTA's own part
-            // too, read back: the bits it wrote), then finish the tile
+            // from registers where it keeps it -- the bits it wrote or would
+            // have written -- else read back), then finish the tile
 #pragma unroll 1
             for (int g = 0; g < NCH; ++g) {
                 float sum[CH];
@@ -612,9 +636,15 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                 for (int p = 0; p < parts; ++p) {
                     const float *src = slot0 + static_cast<int64_t>(p) * (Cfg::BN * MP);
                     float part[CH];
+                    if (kKeep && p == my_slot) {
 #pragma unroll
-                    for (int m = 0; m < CH; ++m)
-                        part[m] = __ldcg(src + (CH * g + m) * Cfg::BN + n_local);
+                        for (int m = 0; m < CH; ++m)
+                            part[m] = v[m];
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < CH; ++m)
+                            part[m] = __ldcg(src + (CH * g + m) * Cfg::BN + n_local);
+                    }
 #pragma unroll
                     for (int m = 0; m < CH; ++m)
                         sum[m] += part[m];

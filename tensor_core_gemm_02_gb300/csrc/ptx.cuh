@@ -61,6 +61,18 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
 // attribute); every access to inputs or outputs comes after it.
 // launch_dependents: let the next such launch begin its own set-up.
 
+// A 32-bit global load with acquire semantics at GPU scope: writes another
+// CTA made before releasing the value it reads are visible after it.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "l"(reinterpret_cast<uint64_t>(p))
+                 : "memory");
+    return v;
+}
+
 // Bring a global line into L2 ahead of its use (no register, no wait).
 __device__ __forceinline__ void prefetch_l2(const void *p)
 {
