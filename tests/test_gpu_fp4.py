@@ -55,9 +55,13 @@ def _dequant_bf16(p):
 
 @pytest.mark.parametrize("M,N,K", [(1, 300, 64), (16, 1000, 96), (17, 777, 4096),
                                    (33, 2048, 1024), (64, 520, 2048), (16, 28672, 512),
-                                   (100, 300, 256), (300, 1000, 1024)])
+                                   (100, 300, 256), (300, 1000, 1024),
+                                   (20, 20000, 1024), (16, 39000, 1024)])
 def test_fp4_quarter_bit_exact(M, N, K):
-    """Fused skinny path (M <= 64, split K included) and dequantise-then-tile (M > 64)."""
+    """Fused skinny path (M <= 64, split K included) and dequantise-then-tile (M > 64).
+    On 152 SMs, 20 x 20000 x 1024 shares 78 tiles and gives 79 whole ones to 79
+    CTAs (ragged last tile among them); 16 x 39000 x 1024 leaves one tile over two
+    whole waves, so one wave more is shared (153 shared, 152 whole)."""
     for out, with_c in [(OUT_F32, True), (OUT_BF16, False)]:
         p = _problem(M * 7 + N + K, M, N, K, with_c=with_c, out=out)
         ref, _ = _ref(p)
