@@ -423,21 +423,19 @@ bool skinny_eligible(int64_t M, int64_t K, bool gather, bool seeded)
 // Few rows of A, bf16 / f16 B: whether the skinny kernel beats the tile
 // kernel.  The skinny kernel spreads every tile's K over the SMs, which pays
 // when the tile kernel has few tiles to give them and a long K to walk in
-// each (K large against N); with more than 16 rows its epilogue and split
-// reductions cost more than the tile kernel's idle MMA rows.  Measured
-// (CUDA-graph replay, operands cold in HBM, microseconds skinny / tile):
-// M = 16: 28672 x 4096 42.0 / 45.1, 4096^2 14.1 / 16.6, 1024^2 8.9 / 6.8;
-// M = 32: 28672 x 4096 46.0 / 45.9, 4096 x 8192 23.6 / 29.3, 4096^2 23.0 / 16.6,
-// 16384 x 2048 25.4 / 16.8; M = 64: 28672 x 4096 64.4 / 47.6, 4096^2
-// 34.1 / 16.7, 1024 x 8192 26.7 / 29.1, 4096 x 16384 40.6 / 54.7, 48 rows
-// 2048 x 8192 34.3 / 29.1.
+// each (K large against N); with more than 16 rows and a short K its
+// epilogue and split reductions cost more than the tile kernel's idle MMA
+// rows.  Measured (CUDA-graph replay, operands cold in HBM, microseconds
+// skinny / tile): M = 16: 28672 x 4096 42.0 / 45.1, 4096^2 14.1 / 16.6,
+// 1024^2 8.9 / 6.8; M = 32: 28672 x 4096 46.0 / 45.9, 4096 x 8192
+// 23.6 / 29.3, 4096^2 23.0 / 16.6, 16384 x 2048 25.4 / 16.8; M = 64:
+// 4096^2 19.4 / 16.7, 4096 x 14336 30.5 / 48.3, 2048 x 16384 23.7 / 54.4,
+// 1024 x 8192 20.0 / 29.1; 48 rows 2048 x 8192 20.4 / 29.1.
 bool skinny_wins(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 16)
         return N * K > (int64_t(1) << 21);  // (N, K < 2^31: no overflow)
-    if (M <= 32)
-        return K >= 2 * N;
-    return K >= 8 * N || (K >= 4 * N && K >= 16384);
+    return K >= 2 * N;
 }
 
 // The skinny kernel's plan for m <= 64 rows (stream-K over the SMs).

@@ -27,7 +27,8 @@
 //   warps 1..I MMA issuers (I = ISSUERS: 1, or 2 / 4 for FP4 B):
 //              tcgen05.mma M=128 N=MP K=16, each issuer into two TMEM
 //              accumulators of its own (FP4 B: A operand from TMEM)
-//   next 4     epilogue: tcgen05.ld (the issuers' partial sums added in
+//   next 4     epilogue (8 for bf16 / f16 B with MP = 64, two per TMEM lane
+//              quarter, 32 columns each): tcgen05.ld (the issuers' partial sums added in
 //              order), partial or final fma.rn(alpha, acc, beta*C) with
 //              coalesced plain loads/stores (lanes walk along N); with
 //              scattered rows, row m of the result lands in row idx[m] of D;
@@ -78,8 +79,13 @@ struct SkinnyCfg {
     // blocks j = e (mod ISSUERS) of every stage into accumulators of its
     // own, and the epilogue adds the partial sums in issuer order.
     static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : 1;
-    static constexpr int EPI_WARP0 = 1 + ISSUERS;    // four epilogue warps
-    static constexpr int CONV_WARP0 = EPI_WARP0 + 4;  // then the converters
+    // Epilogue warps: four (one per TMEM lane quarter), or eight for bf16 /
+    // f16 B with MP = 64, two per quarter, each finishing 32 of the 64
+    // columns, which halves a thread's chain of loads and stores per piece.
+    static constexpr int EPI_SPLIT = (!W4 && MP == 64) ? 2 : 1;
+    static constexpr int EPI_WARPS = 4 * EPI_SPLIT;
+    static constexpr int EPI_WARP0 = 1 + ISSUERS;
+    static constexpr int CONV_WARP0 = EPI_WARP0 + EPI_WARPS;  // then the converters
     // Accumulator buffers: the MMA fills one while the epilogue drains the
     // other.  (Four for bf16 B measured the same as two; FP4 B needs the rest
     // of tensor memory for converted weights.)
@@ -143,9 +149,11 @@ __device__ __forceinline__ int32_t skinny_owner(int64_t x, int64_t W, int64_t G)
     return static_cast<int32_t>(((x + 1) * G - 1) / W);
 }
 
+// Named barrier 1 among the epilogue's N threads.
+template <int N>
 __device__ __forceinline__ void epi_bar_sync()
 {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
 // Row of C and D for row m of A: m itself, or (scattered rows) the entry
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         }
         for (int b = 0; b < NACC; ++b) {
             mbar_init(accf_bar(b), Cfg::ISSUERS);
-            mbar_init(acce_bar(b), 4);
+            mbar_init(acce_bar(b), Cfg::EPI_WARPS);
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -476,11 +484,15 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         const uint32_t q = warp & 3u;
         const bool leader = warp == static_cast<uint32_t>(Cfg::EPI_WARP0) && lane == 0;
         const int32_t n_local = 32 * static_cast<int32_t>(q) + static_cast<int32_t>(lane);
+        // this warp's columns of the MP: [mb, mb + MPH)
+        constexpr int MPH = MP / Cfg::EPI_SPLIT;
+        const int mb = static_cast<int>((warp - static_cast<uint32_t>(Cfg::EPI_WARP0)) / 4u) * MPH;
+        constexpr int EPI_THREADS = 32 * Cfg::EPI_WARPS;
         // scattered rows: D row of each row of A, read once (after the set-up
         // barrier, so after the previous kernel in the stream has finished)
         int32_t *drow = reinterpret_cast<int32_t *>(gbase + Cfg::OFF_ROWS);
         if (args.scatter) {
-            const int32_t e = static_cast<int32_t>(threadIdx.x) - 32 * Cfg::EPI_WARP0;  // 0 .. 127
+            const int32_t e = static_cast<int32_t>(threadIdx.x) - 32 * Cfg::EPI_WARP0;  // epilogue thread
             if (e < MP) {
                 int32_t r = -1;
                 if (e < args.M) {
@@ -492,7 +504,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                 }
                 drow[e] = r;
             }
-            epi_bar_sync();
+            epi_bar_sync<EPI_THREADS>();
         }
         int ab = 0;
         uint32_t aph = 0;
@@ -502,17 +514,17 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             const int32_t n = t * Cfg::BN + n_local;
             // FP4 weights with MP > 16 finish the MP rows of A in chunks of 16,
             // so the epilogue's registers stay those of MP = 16 and leave room
-            // for the converter warps; otherwise one chunk of all MP rows.
-            // beta * C is fetched while the MMAs still run: into registers when
-            // there is one chunk, else its lines into L2.
-            constexpr int CH = (W4 && MP > 16) ? 16 : MP;
-            constexpr int NCH = MP / CH;
+            // for the converter warps; otherwise one chunk of the warp's MPH
+            // rows.  beta * C is fetched while the MMAs still run: into
+            // registers when there is one chunk, else its lines into L2.
+            constexpr int CH = (W4 && MP > 16) ? 16 : MPH;
+            constexpr int NCH = MPH / CH;
             float cb0[CH];
             if constexpr (NCH == 1) {
-                skinny_load_cb<CH>(args, drow, n, 0, cb0);
+                skinny_load_cb<CH>(args, drow, n, mb, cb0);
             } else if (args.has_c && n < args.N) {
 #pragma unroll 4
-                for (int m = 0; m < MP; ++m) {
+                for (int m = mb; m < mb + MPH; ++m) {
                     const int32_t r = skinny_row(args, drow, m);
                     if (r >= 0)
                         prefetch_l2(args.C + static_cast<int64_t>(r) * args.ldc + n);
@@ -524,13 +536,13 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                     for (int m = 0; m < CH; ++m)
                         cb[m] = cb0[m];
                 } else {
-                    skinny_load_cb<CH>(args, drow, n, CH * g, cb);
+                    skinny_load_cb<CH>(args, drow, n, mb + CH * g, cb);
                 }
             };
             const bool ok = warp_wait_bounded(accf_bar(ab), aph, abort_flag, args.status,
                                               args.timeout_ns, kWhereEpiAccFull);
-            // all four warps agree before the named barriers below
-            epi_bar_sync();
+            // all epilogue warps agree before the named barriers below
+            epi_bar_sync<EPI_THREADS>();
             if (!ok || *abort_flag)
                 break;
             tc_fence_after_sync();
@@ -553,14 +565,14 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             // B with MP <= 32 only: keeping the part in registers spills with
             // FP4 B's converter warps and with MP = 64; FP4 B ends on whole
             // tiles.)
-            constexpr bool kKeep = !W4 && MP <= 32 && NCH == 1;
+            constexpr bool kKeep = !W4 && MPH <= 32 && NCH == 1;
             bool last_known = false;
             if (kKeep && parts > 1 && i == n_steps) {
                 if (leader) {
                     const uint32_t in = ld_acquire_gpu(args.counters + t);
                     *arrival = in;
                 }
-                epi_bar_sync();
+                epi_bar_sync<EPI_THREADS>();
                 last_known = *arrival == static_cast<uint32_t>(parts - 1);
             }
             float v[CH];  // this chunk's sums (with one chunk: the CTA's whole part)
@@ -574,7 +586,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                         uint32_t r[16];
                         tc_ld_32x32b_x16(tmem_base + ((32u * q) << 16) +
                                              static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP +
-                                                                   CH * g + 16 * h),
+                                                                   mb + CH * g + 16 * h),
                                          r);
                         tc_wait_ld(r);
 #pragma unroll
@@ -584,15 +596,15 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                     }
                 }
                 if (args.reduce) {
-                    skinny_add<CH>(args, drow, n, CH * g, v);  // every part adds itself into D
+                    skinny_add<CH>(args, drow, n, mb + CH * g, v);  // every part adds itself into D
                 } else if (parts == 1) {
                     float cb[CH];
                     chunk_cb(g, cb);
-                    skinny_store<CH>(args, drow, n, CH * g, v, cb);
+                    skinny_store<CH>(args, drow, n, mb + CH * g, v, cb);
                 } else if (!last_known) {
 #pragma unroll
                     for (int m = 0; m < CH; ++m)
-                        __stcg(mine + (CH * g + m) * Cfg::BN + n_local, v[m]);
+                        __stcg(mine + (mb + CH * g + m) * Cfg::BN + n_local, v[m]);
                 }
             }
             tc_fence_before_sync();
@@ -612,7 +624,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                 // other CTAs' parts before the reads below (the barrier after
                 // it passes that on).  (With the other parts seen in beforehand,
                 // the acquire load above and its barrier did the same.)
-                epi_bar_sync();
+                epi_bar_sync<EPI_THREADS>();
                 if (leader) {
                     __threadfence();
                     const uint32_t before = atomicAdd(args.counters + t, 1u);
@@ -620,7 +632,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                         __threadfence();
                     *arrival = before;
                 }
-                epi_bar_sync();
+                epi_bar_sync<EPI_THREADS>();
                 if (*arrival != static_cast<uint32_t>(parts - 1))
                     continue;  // another CTA still has to add its part
             }
@@ -643,7 +655,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                     } else {
 #pragma unroll
                         for (int m = 0; m < CH; ++m)
-                            part[m] = __ldcg(src + (CH * g + m) * Cfg::BN + n_local);
+                            part[m] = __ldcg(src + (mb + CH * g + m) * Cfg::BN + n_local);
                     }
 #pragma unroll
                     for (int m = 0; m < CH; ++m)
@@ -651,7 +663,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                 }
                 float cb[CH];
                 chunk_cb(g, cb);
-                skinny_store<CH>(args, drow, n, CH * g, sum, cb);
+                skinny_store<CH>(args, drow, n, mb + CH * g, sum, cb);
             }
             if (leader)
                 args.counters[t] = 0u;  // ready for the next call

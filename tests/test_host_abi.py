@@ -225,15 +225,15 @@ def test_plan_matches_the_dispatch_rules(lib):
     assert (p.kernel, p.bm) == (2, 32)
     p = binding.gemm_query_plan(40, 1024, 8192, sm_count=148)
     assert (p.kernel, p.bm) == (2, 64)
+    assert binding.gemm_query_plan(64, 4096, 4096, sm_count=148).kernel != 2
     assert binding.gemm_query_plan(64, 4096, 16384, sm_count=148).kernel == 2
-    assert binding.gemm_query_plan(48, 2048, 8192, sm_count=148).kernel != 2
-    # the rule's edges: K >= 2N for 17..32 rows, K >= 8N or K >= max(4N, 16384) above
+    assert binding.gemm_query_plan(48, 2048, 8192, sm_count=148).kernel == 2
+    assert binding.gemm_query_plan(64, 4096, 14336, sm_count=148).kernel == 2
+    # the rule's edge: K >= 2N for 17..64 rows
     assert binding.gemm_query_plan(17, 1024, 2048, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(32, 1024, 2047, sm_count=148).kernel == 1
-    assert binding.gemm_query_plan(33, 1024, 8192, sm_count=148).kernel == 2
-    assert binding.gemm_query_plan(64, 1024, 8184, sm_count=148).kernel == 1
-    assert binding.gemm_query_plan(33, 4096, 16384, sm_count=148).kernel == 2
-    assert binding.gemm_query_plan(33, 4104, 16384, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(33, 1024, 2048, sm_count=148).kernel == 2
+    assert binding.gemm_query_plan(64, 1024, 2040, sm_count=148).kernel == 1
     # scattered and accumulating calls follow the same rule; gathered rows never
     assert binding.gemm_query_plan(32, 4096, 4096, scatter=True, sm_count=148).kernel != 2
     assert binding.gemm_query_plan(16, 4096, 4096, scatter=True, sm_count=148).kernel == 2
