@@ -562,9 +562,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             // skips writing its part, the fences and the counter, and adds its
             // part from registers below.  (An earlier piece rarely finds the
             // others in, and the extra load there measured slower.  bf16 / f16
-            // B with MP <= 32 only: keeping the part in registers spills with
-            // FP4 B's converter warps and with MP = 64; FP4 B ends on whole
-            // tiles.)
+            // B only, at most 32 columns a thread: keeping the part in
+            // registers spills beside FP4 B's converter warps, and FP4 B ends
+            // on whole tiles.)
             constexpr bool kKeep = !W4 && MPH <= 32 && NCH == 1;
             bool last_known = false;
             if (kKeep && parts > 1 && i == n_steps) {
