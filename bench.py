@@ -33,7 +33,10 @@ TFLOP/s = 2 M N K / time.  The same line also carries:
                 bandwidth)
 
 With --impl reference the oracle itself is timed as the comparison arm.
-Under torchrun every rank runs its own replica; rank 0 prints the JSON line.
+
+One GPU only.  The library's clustered forms use TMA multicast within one
+GPU's memory, and the GEMM has no exchange step to run across GPUs, so the
+bench refuses --gpus other than 1 and any launch with WORLD_SIZE > 1.
 """
 from __future__ import annotations
 
@@ -57,29 +60,22 @@ from tensor_core_gemm_02_gb300 import binding, workloads  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 HEADLINE = "bf16_8192"
+# dense bf16 / f16 tcgen05 rate of one SM: a 128 x N x 16 MMA (2 * 128 * N * 16
+# flop) keeps the tensor pipe busy for N / 2 cycles
+FLOP_PER_CLK_PER_SM = 8192
 
 
 # ----------------------------------------------------------------- plumbing
 
-def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
+def single_gpu_only(gpus):
+    """Exit with a message unless this is one process on one GPU."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", str(rank)))
-    return rank, world, local
-
-
-def slowest_rank(ms_step, world, device):
-    """The largest per-step time over all ranks (every rank must call this)."""
-    if world <= 1:
-        return ms_step
-    t = torch.tensor([ms_step], dtype=torch.float64, device=device)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    return float(t.item())
-
-
-def job_throughput(flops_per_rank_step, ms_step, world):
-    """Whole-job TFLOP/s: every rank's work over the slowest rank's step time."""
-    return world * flops_per_rank_step / (ms_step * 1e-3) / 1e12
+    if gpus != 1 or world != 1:
+        sys.stderr.write(
+            f"bench.py runs on one GPU only (--gpus {gpus}, WORLD_SIZE {world}): the "
+            "library's clustered forms multicast TMA loads within one GPU's memory and "
+            "the GEMM has no step that spans GPUs\n")
+        sys.exit(2)
 
 
 def measured_peaks():
@@ -307,14 +303,12 @@ def algorithmic_bytes(p):
 
 # ----------------------------------------------------------------- our arm
 
-def time_headline(p, dev, steps, warmup, rank, world):
+def time_headline(p, dev, steps, warmup):
     tensors = to_device(p, dev)
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         launch(p, tensors)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
@@ -326,8 +320,6 @@ def time_headline(p, dev, steps, warmup, rank, world):
         e1.record(stream)
         torch.cuda.synchronize()
         clocks.mark("t_end")
-    if world > 1:
-        torch.distributed.barrier()
     ms = e0.elapsed_time(e1)
     status = binding.gemm_check_device_status()
     if status != binding.GEMM_OK:
@@ -508,21 +500,34 @@ def oracle_rows_rate(p, seconds, threads):
     return 2.0 * rows * p.N * p.K / dt, rows, dt
 
 
+def spec_peak(sms, clocks, achieved):
+    """The chip's dense bf16 tensor peak from its SM count, the per-SM rate and
+    the SM clock: at the maximum clock and at the median clock sampled during
+    the timed region, with the achieved rate (TFLOP/s) as a fraction of each."""
+    out = {"flop_per_clk_per_sm": FLOP_PER_CLK_PER_SM, "sms": sms,
+           "source": "one SM's tensor pipe runs a 128 x N x 16 bf16 MMA in N/2 cycles "
+                     "(8192 flop per clock); x SMs x SM clock"}
+    for key, mhz in (("max", clocks.get("sm_max_mhz")), ("median", clocks.get("sm_mhz"))):
+        if mhz:
+            peak = FLOP_PER_CLK_PER_SM * sms * mhz * 1e6 / 1e12
+            out[f"{key}_mhz"] = mhz
+            out[f"peak_at_{key}_mhz"] = round(peak, 1)
+            out[f"frac_at_{key}_mhz"] = round(achieved / peak, 4)
+    return out
+
+
 def run_ours(args):
-    rank, world, local = dist_env()
-    if world > 1:
-        torch.distributed.init_process_group("nccl")
-    dev = torch.device("cuda", local % torch.cuda.device_count())
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     binding.load_library()
     peaks = measured_peaks()
 
     p = workloads.WORKLOADS[HEADLINE]()
     flops = p.flops
-    ms_total, clocks = time_headline(p, dev, args.steps, args.warmup, rank, world)
-    ms_step = slowest_rank(ms_total / args.steps, world, dev)
-    value = job_throughput(flops, ms_step, world)
-    achieved = flops / (ms_step * 1e-3) / 1e12
+    ms_total, clocks = time_headline(p, dev, args.steps, args.warmup)
+    ms_step = ms_total / args.steps
+    value = flops / (ms_step * 1e-3) / 1e12
+    achieved = value
 
     e2e_steps = min(args.steps, 20)
     e2e_ms, h2d, d2h = time_e2e(p, dev, e2e_steps)
@@ -543,7 +548,7 @@ def run_ours(args):
         "metric": "GEMM TFLOP/s (bf16 8192^3, bf16 out)",
         "value": round(value, 2),
         "unit": "TFLOP/s",
-        "n_gpus": world,
+        "n_gpus": 1,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
@@ -553,11 +558,11 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) / N(0,0.02) bf16)",
         "config": {"workload": "bf16 GEMM M=N=K=8192, A~N(0,1), B~N(0,0.02), C=0, bf16 out",
-                   "M": 8192, "N": 8192, "K": 8192, "parallelism": f"replicas x{world}",
+                   "M": 8192, "N": 8192, "K": 8192, "parallelism": "one GPU",
                    "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": round(e2e_ms, 4),
                 "how": "pinned host A, B -> device, gemm_bf16, D -> pinned host, every step; "
@@ -569,12 +574,15 @@ def run_ours(args):
                      "peak_source": f"{peaks['source']} bf16_tflops (burst)",
                      "traffic": stored_traffic(f"{kernel_key(plan_of(p, dev), p)}@{HEADLINE}"),
                      "kernel": kernel_key(plan_of(p, dev), p),
-                     "algorithmic_flops_per_launch": flops},
+                     "algorithmic_flops_per_launch": flops,
+                     "chip_dense_bf16_peak": spec_peak(
+                         torch.cuda.get_device_properties(dev).multi_processor_count,
+                         clocks, achieved)},
     }
     if sustained is not None:
         result["sustained"] = sustained
 
-    if rank == 0 and args.variants:
+    if args.variants:
         variants = {}
         for name in ("f16_1024", "mlp_8192x28672x4096", "skinny_16x28672x4096",
                      "gather_16384_of_65536", "scatter_16384_into_65536",
@@ -607,26 +615,19 @@ def run_ours(args):
             }
         result["variants"] = variants
 
-    if rank == 0:
-        threads = len(os.sched_getaffinity(0))
-        rate, rows, dt = oracle_rows_rate(p, args.cpu_seconds, threads)
-        result["cpu_baseline"] = {"value": round(rate / 1e12, 6), "unit": "TFLOP/s",
-                                  "cores": threads, "kind": "oracle",
-                                  "sample": f"{rows} full output rows of the 8192^3 bf16 GEMM "
-                                            f"(fp64 oracle, {dt:.1f} s)"}
-        print(json.dumps(result), flush=True)
-    if world > 1:
-        torch.distributed.barrier()
-        torch.distributed.destroy_process_group()
+    threads = len(os.sched_getaffinity(0))
+    rate, rows, dt = oracle_rows_rate(p, args.cpu_seconds, threads)
+    result["cpu_baseline"] = {"value": round(rate / 1e12, 6), "unit": "TFLOP/s",
+                              "cores": threads, "kind": "oracle",
+                              "sample": f"{rows} full output rows of the 8192^3 bf16 GEMM "
+                                        f"(fp64 oracle, {dt:.1f} s)"}
+    print(json.dumps(result), flush=True)
 
 
 # ----------------------------------------------------------------- reference arm
 
 def run_reference(args):
     """The oracle as the comparison arm: each step computes a bounded sample of rows."""
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return
     p = workloads.WORKLOADS[HEADLINE]()
     threads = len(os.sched_getaffinity(0))
     import oracle
@@ -648,7 +649,7 @@ def run_reference(args):
     print(json.dumps({
         "impl": "reference",
         "metric": "GEMM TFLOP/s (bf16 8192^3, bf16 out)",
-        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "bf16 GEMM M=N=K=8192, A~N(0,1), B~N(0,0.02), C=0, bf16 out",
@@ -690,6 +691,7 @@ def main():
     ap.add_argument("--case", choices=sorted(workloads.WORKLOADS), default=None,
                     help="only launch this workload's GEMM warmup + steps times (profiling)")
     args = ap.parse_args()
+    single_gpu_only(args.gpus)
     if args.case:
         run_case(args)
         return

@@ -1,14 +1,11 @@
-"""Host-side logic of bench.py that needs no GPU: the whole-job aggregation over
-ranks (two gloo processes on the CPU), kernel naming and the traffic lookup."""
+"""Host-side logic of bench.py that needs no GPU: the one-GPU guard, the chip
+peak arithmetic, kernel naming and the traffic lookup."""
 import json
 import os
-import socket
 import sys
 
 import pytest
 import torch
-import torch.distributed as dist
-import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
@@ -17,39 +14,31 @@ import bench  # noqa: E402
 from tensor_core_gemm_02_gb300 import binding, workloads  # noqa: E402
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
+def test_more_than_one_gpu_is_refused(monkeypatch):
+    """The bench runs on one GPU: --gpus 2, or a launch under torchrun with
+    WORLD_SIZE 2, exits with status 2 before touching a GPU."""
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    bench.single_gpu_only(1)  # the default passes
+    with pytest.raises(SystemExit) as e:
+        bench.single_gpu_only(2)
+    assert e.value.code == 2
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit) as e:
+        bench.single_gpu_only(1)
+    assert e.value.code == 2
 
 
-def _rank_main(rank, world, port, out):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    local_ms = [2.0, 3.0][rank]  # rank 1 is the slow one
-    ms = bench.slowest_rank(local_ms, world, torch.device("cpu"))
-    value = bench.job_throughput(1e12, ms, world)
-    out[rank] = (ms, value)
-    dist.barrier()
-    dist.destroy_process_group()
-
-
-def test_two_rank_aggregation_takes_the_slowest_rank():
-    port = _free_port()
-    with mp.Manager() as m:
-        out = m.dict()
-        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
-        res = dict(out)
-    for rank in (0, 1):
-        ms, value = res[rank]
-        assert ms == 3.0
-        # 2 ranks x 1 TFLOP each over 3 ms
-        assert abs(value - 2 * 1e12 / 3e-3 / 1e12) < 1e-9
-
-
-def test_single_rank_needs_no_process_group():
-    assert bench.slowest_rank(1.5, 1, torch.device("cpu")) == 1.5
-    assert bench.job_throughput(2e12, 2.0, 1) == pytest.approx(1000.0)
+def test_spec_peak_from_sms_and_clock():
+    """152 SMs x 8192 flop per clock at 2070 MHz is 2577.4 TFLOP/s; at a sampled
+    median of 1650 MHz, 2054.5; the achieved rate is divided by each."""
+    s = bench.spec_peak(152, {"sm_max_mhz": 2070.0, "sm_mhz": 1650.0}, 1800.0)
+    assert s["peak_at_max_mhz"] == pytest.approx(152 * 8192 * 2.07e9 / 1e12, abs=0.06)
+    assert s["peak_at_median_mhz"] == pytest.approx(152 * 8192 * 1.65e9 / 1e12, abs=0.06)
+    assert s["frac_at_max_mhz"] == pytest.approx(1800.0 / (152 * 8192 * 2.07e9 / 1e12), abs=1e-4)
+    assert s["frac_at_median_mhz"] == pytest.approx(1800.0 / (152 * 8192 * 1.65e9 / 1e12),
+                                                    abs=1e-4)
+    # no clock samples: no peak figures, no division
+    assert "peak_at_median_mhz" not in bench.spec_peak(152, {"sm_mhz": None}, 1800.0)
 
 
 def test_kernel_keys_name_the_launched_instance():
