@@ -44,6 +44,11 @@
  * on the stream still starts only after all of them, and every form can be
  * captured into a CUDA graph.
  *
+ * Per-device state (the status word's address, the workspaces, the address of
+ * the allocation-free entry point's array) is set up by the first call on a
+ * device and kept for the life of the process; it does not survive
+ * cudaDeviceReset, after which the library must not be called again.
+ *
  * Errors:
  *  - Argument, alignment, aliasing and type errors are returned synchronously
  *    before anything is launched, following the descriptor legality rule that
@@ -290,8 +295,11 @@ gemm_status gemm_accumulate(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
  * The first call on a device looks up the array's device address (and sets up
  * the library's per-device state); make that first call before any stream
  * capture.  Every call on a device shares the one array, which keeps what the
- * last call left there: each call clears the counters it needs on `stream`
- * before launching.  Calls whose executions overlap on the GPU (different
+ * last call left there: a call whose tiles are split over several CTAs (the
+ * K sum of a 128-column tile of N shared out) first clears, on `stream`, the
+ * arrival counters it uses; a call without split tiles uses no scratch and
+ * clears nothing.  gemm_check_device_status also clears them after a
+ * device-side error.  Calls whose executions overlap on the GPU (different
  * streams, no ordering between them) race on the array and give wrong results.
  */
 gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,

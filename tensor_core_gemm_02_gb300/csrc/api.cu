@@ -1074,6 +1074,8 @@ gemm_status gemm_check_device_status(void *stream)
             return GEMM_ERR_CUDA;
         if ((st = reset_workspaces(dev->index)) != GEMM_OK)
             return st;
+        if ((st = reset_static_scratch(dev->index)) != GEMM_OK)
+            return st;
     }
     return static_cast<gemm_status>(h[0]);
 }

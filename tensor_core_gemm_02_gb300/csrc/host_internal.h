@@ -75,5 +75,9 @@ gemm_status run_tiny(const Problem &p, const gemm_plan &plan, const DeviceInfo *
 // Kernel arguments common to every kernel (sizes, epilogue, status, timeout).
 void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev);
 
+// Clear the allocation-free entry point's counters on `device` (after a
+// device-side error; noalloc.cu).
+gemm_status reset_static_scratch(int device);
+
 }  // namespace host
 }  // namespace tcg

@@ -61,6 +61,29 @@ gemm_status static_scratch(int device, unsigned char **out)
 
 }  // namespace
 
+namespace tcg {
+namespace host {
+
+// After a device-side error: clear the array's counters on `device` (current),
+// if this entry point has run there (synchronous; nothing else may be running).
+gemm_status reset_static_scratch(int device)
+{
+    if (device < 0 || device >= kMaxDevices)
+        return GEMM_OK;
+    unsigned char *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        base = g_static_ptr[device];
+    }
+    if (base && cudaMemset(base + kStaticPartialBytes, 0, kStaticCounters * sizeof(uint32_t)) !=
+                    cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+}  // namespace host
+}  // namespace tcg
+
 extern "C" gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype_is_bf16,
                                            const void *A, int64_t lda, const void *B,
                                            int64_t ldb, const float *C, int64_t ldc, void *D,
@@ -98,8 +121,13 @@ extern "C" gemm_status gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int 
         return st;
     float *partials = reinterpret_cast<float *>(scratch);
     uint32_t *counters = reinterpret_cast<uint32_t *>(scratch + kStaticPartialBytes);
-    // the array keeps whatever the previous call left: the counters must start at zero
-    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(plan.tiles) * sizeof(uint32_t),
+    // The array keeps whatever the previous call left.  Only tiles split over
+    // several CTAs use counters, and those must start at zero: a kernel that
+    // completes returns them to zero, but one that gave up half way (a wait
+    // that ran out of time) may not have, so they are cleared here.  Without
+    // split tiles nothing is read from the array and nothing is cleared.
+    if (plan.splits > 1 &&
+        cudaMemsetAsync(counters, 0, static_cast<size_t>(plan.tiles) * sizeof(uint32_t),
                         p.stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
 

@@ -80,6 +80,23 @@ def test_worked_example_bit_exact():
     assert np.array_equal(to_f64(D), stored)
 
 
+@pytest.mark.parametrize("form", TILE_FORMS + [(2, 128)], ids=FORM_IDS + ["skinny"])
+def test_worked_example_every_form(form):
+    """The same 16 x 8 x 32 inputs through every kernel form, forced: a 16 x 8
+    corner of a 128- or 256-row tile, so the TMA boxes of A (128 x 64 or more)
+    and B read mostly out-of-bounds zero fill (K = 32 of a 64-wide block, 8 of
+    up to 512 columns; the second CTA of a pair and all but one CTA of a
+    cluster load boxes that lie wholly outside), and D's stores are clipped to
+    8 columns and 16 rows.  D must equal the stored exact result bit for bit."""
+    binding.gemm_debug_force_tile(*form)
+    p = workloads.worked_16x8x32()
+    plan = binding.gemm_query_plan(p.M, p.N, p.K, sm_count=148)
+    assert plan.kernel == form[0]
+    D = run(p)
+    stored = np.loadtxt(os.path.join(GOLDEN, "worked_16x8x32.txt"))
+    assert np.array_equal(to_f64(D), stored), f"form {form}"
+
+
 QUARTER_SHAPES = [(1, 1, 8), (16, 8, 32), (5, 3, 24), (127, 255, 64), (128, 256, 64),
                   (129, 257, 72), (300, 520, 264), (257, 129, 520), (64, 640, 136),
                   (384, 96, 1000)]
@@ -140,32 +157,29 @@ def test_f16_1024_full():
     assert_within(run(p), ref, absprod, p.out, p.name)
 
 
-def _sample_coords(M, N, n, seed):
-    rng = np.random.default_rng(seed)
-    ii = rng.integers(0, M, n)
-    jj = rng.integers(0, N, n)
-    # tile corners and the last row / column
-    edge_i = np.array([0, 127, 128, M - 1, M - 1, 0, 255, 256])
-    edge_j = np.array([0, 255, 256, N - 1, 0, N - 1, 31, 32])
-    return np.concatenate([ii, edge_i]), np.concatenate([jj, edge_j])
-
-
-def _sampled_check(p, n=4096, seed=0):
+def _full_check(p, rows_per_chunk=512):
+    """Every element of D against the oracle, a block of rows at a time (the
+    oracle's float64 result for the whole matrix would not need to be held)."""
     D = run(p)
     torch.cuda.synchronize()
-    ii, jj = _sample_coords(p.M, p.N, n, seed)
-    ref, absprod, _ = oracle.gemm_entries(p.A, p.B, ii, jj, p.C, p.alpha, p.beta, idx=p.idx)
-    got = D[torch.from_numpy(ii).to(DEV), torch.from_numpy(jj).to(DEV)]
-    assert_within(to_f64(got), ref, absprod, p.out, p.name)
-    return D
+    got_all = D.cpu()
+    del D
+    for i0 in range(0, p.M, rows_per_chunk):
+        i1 = min(p.M, i0 + rows_per_chunk)
+        ref, absprod, bad = oracle.gemm(p.A, p.B, p.C, p.alpha, p.beta, idx=p.idx,
+                                        rows=(i0, i1))
+        assert not bad
+        assert_within(to_f64(got_all[i0:i1]), ref, absprod, p.out, f"{p.name} rows {i0}..{i1}")
 
 
-def test_bf16_8192_sampled():
-    _sampled_check(workloads.bf16_8192())
+def test_bf16_8192_full():
+    """bf16 8192^3, bf16 out: all 67,108,864 elements."""
+    _full_check(workloads.bf16_8192())
 
 
-def test_mlp_sampled():
-    _sampled_check(workloads.mlp_8192x28672x4096())
+def test_mlp_full():
+    """8192 x 28672 x 4096 with D = fma(0.5, A B^T, 1.0 C): all 234,881,024 elements."""
+    _full_check(workloads.mlp_8192x28672x4096(), rows_per_chunk=256)
 
 
 def test_skinny_full():
@@ -174,8 +188,9 @@ def test_skinny_full():
     assert_within(run(p), ref, absprod, p.out, p.name)
 
 
-def test_gather_sampled():
-    _sampled_check(workloads.gather_16384_of_65536())
+def test_gather_full():
+    """16384 rows gathered from a 65536-row table, N = K = 4096: all 67,108,864 elements."""
+    _full_check(workloads.gather_16384_of_65536())
 
 
 @pytest.mark.parametrize("out,with_c", [(OUT_F32, True), (OUT_BF16, False)])
