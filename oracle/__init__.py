@@ -1,5 +1,6 @@
 """fp64 CPU oracle for D = alpha * A @ B.T + beta * C (plain, gathered and
-scattered forms, and FP4 block-scaled weights).
+scattered forms, FP4 block-scaled weights, and both operands FP4 with block
+scales).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product path
@@ -61,6 +62,9 @@ def _bind(lib):
     lib.oracle_w4_rows.argtypes = [i64, i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
                                    dbl, dbl, vp, vp, i64]
     lib.oracle_w4_rows.restype = None
+    lib.oracle_e2m1_rows.argtypes = [i64, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                     vp, i64, dbl, dbl, vp, vp, i64]
+    lib.oracle_e2m1_rows.restype = None
     lib.oracle_init()
     return lib
 
@@ -316,6 +320,44 @@ def w4(A, Wq, Ws, C=None, alpha=1.0, beta=1.0, dtype=None, threads=None):
             lib.oracle_w4_rows(lo, hi, N, K, code_a, _ptr(a), a.shape[1], _ptr(wq), wq.shape[1],
                                _ptr(ws), N, _ptr(c), N, float(alpha), float(beta),
                                ref.ctypes.data + off, absprod.ctypes.data + off, N)
+
+    with ThreadPoolExecutor(max_workers=nthr) as ex:
+        list(ex.map(lambda p: run(*p), zip(bounds[:-1], bounds[1:])))
+    return ref, absprod
+
+
+def e2m1(Aq, As, Bq, Bs, C=None, alpha=1.0, beta=1.0, threads=None, rows=None):
+    """alpha * A @ B.T + beta * C with both operands FP4: packed E2M1 codes Aq
+    (M x K/2 uint8) and Bq (N x K/2 uint8), even k in the low nibble, and UE8M0
+    block scales As (K/32 x M uint8) and Bs (K/32 x N uint8), one per 32
+    elements along K.  ``rows`` = (i0, i1) limits the computation to a row
+    range.  Returns (ref, absprod) as float64 arrays of shape (i1 - i0, N)."""
+    lib = load()
+    aq = np.ascontiguousarray(np.asarray(Aq, np.uint8))
+    a_s = np.ascontiguousarray(np.asarray(As, np.uint8))
+    bq = np.ascontiguousarray(np.asarray(Bq, np.uint8))
+    b_s = np.ascontiguousarray(np.asarray(Bs, np.uint8))
+    c = _f32(C)
+    M, K = aq.shape[0], 2 * aq.shape[1]
+    N = bq.shape[0]
+    if K % 32 or bq.shape[1] != K // 2 or a_s.shape != (K // 32, M) or b_s.shape != (K // 32, N):
+        raise ValueError("Aq must be M x K/2, Bq N x K/2, As K/32 x M, Bs K/32 x N, "
+                         "K a multiple of 32")
+    if c is not None and c.shape != (M, N):
+        raise ValueError("C must be M x N")
+    i0, i1 = rows if rows is not None else (0, M)
+    ref = np.empty((i1 - i0, N), np.float64)
+    absprod = np.empty((i1 - i0, N), np.float64)
+    nthr = threads or default_threads()
+    bounds = np.linspace(i0, i1, min(nthr, max(1, i1 - i0)) + 1).astype(np.int64)
+
+    def run(lo, hi):
+        lo, hi = int(lo), int(hi)
+        if hi > lo:
+            off = (lo - i0) * N * 8
+            lib.oracle_e2m1_rows(lo, hi, N, K, _ptr(aq), aq.shape[1], _ptr(a_s), M, _ptr(bq),
+                                 bq.shape[1], _ptr(b_s), N, _ptr(c), N, float(alpha),
+                                 float(beta), ref.ctypes.data + off, absprod.ctypes.data + off, N)
 
     with ThreadPoolExecutor(max_workers=nthr) as ex:
         list(ex.map(lambda p: run(*p), zip(bounds[:-1], bounds[1:])))

@@ -287,3 +287,51 @@ void oracle_w4_rows(int64_t i0, int64_t i1, int64_t N, int64_t K, int dtype,
         }
     }
 }
+
+/*
+ * Both operands FP4 with block scales (the block-scaled tensor-core product):
+ * rows [i0, i1) of D = alpha * A * B^T + beta * C with
+ *   A[i][k] = e2m1(code of element k in row i of Aq) * ue8m0(As[k / 32][i]),
+ *   B[j][k] = e2m1(code of element k in row j of Bq) * ue8m0(Bs[k / 32][j]).
+ * Rows of Aq and Bq hold K / 2 bytes, element k in the low nibble of byte
+ * k / 2 when k is even and in the high nibble when k is odd (ldaq, ldbq bytes
+ * apart); As holds K / 32 rows of M scale bytes (ldas apart) and Bs K / 32 rows
+ * of N (ldbs apart), one scale per 32 consecutive elements along K, as the OCP
+ * Microscaling definition the float4_e2m1fn name refers to groups them ("cp.async.bulk.tensor"
+ * page, section "Interleave and packed FP4", gives the operand format).
+ * ref and abs_out as in oracle_gemm_rows.
+ */
+static double fp4_element(const uint8_t *codes, const uint8_t *scales, int64_t lds,
+                          int64_t row, int64_t k)
+{
+    int byte = codes[k / 2];
+    int code = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
+    return oracle_decode_e2m1(code) * oracle_decode_ue8m0(scales[(k / 32) * lds + row]);
+}
+
+void oracle_e2m1_rows(int64_t i0, int64_t i1, int64_t N, int64_t K,
+                      const uint8_t *Aq, int64_t ldaq, const uint8_t *As, int64_t ldas,
+                      const uint8_t *Bq, int64_t ldbq, const uint8_t *Bs, int64_t ldbs,
+                      const float *C, int64_t ldc, double alpha, double beta,
+                      double *ref, double *abs_out, int64_t ldr)
+{
+    for (int64_t i = i0; i < i1; ++i) {
+        const uint8_t *arow = Aq + i * ldaq;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint8_t *brow = Bq + j * ldbq;
+            double dot = 0.0, dot_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = fp4_element(arow, As, ldas, i, k);
+                double b = fp4_element(brow, Bs, ldbs, j, k);
+                dot += a * b;
+                dot_abs += fabs(a) * fabs(b);
+            }
+            double d = alpha * dot;
+            if (C && beta != 0.0)
+                d += beta * (double)C[i * ldc + j];
+            ref[(i - i0) * ldr + j] = d;
+            if (abs_out)
+                abs_out[(i - i0) * ldr + j] = dot_abs;
+        }
+    }
+}

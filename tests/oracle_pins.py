@@ -274,8 +274,65 @@ def pin_w4_nibble_order_and_blocks():
     assert np.array_equal(ref, want)
 
 
+def _fp4_operand(rng, rows, K, codes=(0, 16), scales=(118, 137)):
+    """Packed codes (rows x K/2) and scales (K/32 x rows) drawn from the given ranges."""
+    lo = rng.integers(*codes, (rows, K // 2))
+    hi = rng.integers(*codes, (rows, K // 2))
+    q = (lo | (hi << 4)).astype(np.uint8)
+    s = rng.integers(*scales, (K // 32, rows)).astype(np.uint8)
+    return q, s
+
+
+def pin_e2m1_matches_numpy():
+    """Both operands FP4: against numpy dequantisation of each and a float64 matmul."""
+    rng = np.random.default_rng(17)
+    M, N, K = 7, 9, 160
+    aq, a_s = _fp4_operand(rng, M, K)
+    bq, b_s = _fp4_operand(rng, N, K)
+    c = (rng.integers(-4, 5, (M, N)) / 4).astype(np.float32)
+    ref, absprod = oracle.e2m1(aq, a_s, bq, b_s, c, alpha=0.5, beta=-2.0)
+    a = _dequant_numpy(aq, a_s)
+    b = _dequant_numpy(bq, b_s)
+    assert np.array_equal(ref, 0.5 * (a @ b.T) - 2.0 * c.astype(np.float64))
+    assert np.array_equal(absprod, np.abs(a) @ np.abs(b).T)
+    # a row range is the same rows of the full result
+    part, _ = oracle.e2m1(aq, a_s, bq, b_s, c, alpha=0.5, beta=-2.0, rows=(2, 5))
+    assert np.array_equal(part, ref[2:5])
+    # beta = 0 leaves C out (even NaN), C absent likewise
+    nan_c = np.full((M, N), np.nan, np.float32)
+    r0, _ = oracle.e2m1(aq, a_s, bq, b_s, nan_c, alpha=1.0, beta=0.0)
+    r1, _ = oracle.e2m1(aq, a_s, bq, b_s)
+    assert np.array_equal(r0, a @ b.T) and np.array_equal(r1, a @ b.T)
+
+
+def pin_e2m1_identity_picks():
+    """One operand the identity (code 2 = 1.0, scale 127) picks single elements of
+    the other: D = B^T dequantised (A = I) and D = A dequantised (B = I), with
+    scales that differ per row and per 32-element block, so a transposed scale,
+    a swapped nibble or a scale shared between the operands shows."""
+    K = 64
+    eye_q = np.zeros((K, K // 2), np.uint8)
+    for k in range(K):
+        eye_q[k, k // 2] |= 2 << (4 * (k % 2))
+    eye_s = np.full((K // 32, K), 127, np.uint8)
+    rng = np.random.default_rng(19)
+    xq, xs = _fp4_operand(rng, 5, K, scales=(124, 131))
+    want = _dequant_numpy(xq, xs)                        # 5 x K
+    d_a, _ = oracle.e2m1(eye_q, eye_s, xq, xs)           # A = I: D = X^T
+    assert np.array_equal(d_a, want.T)
+    d_b, _ = oracle.e2m1(xq, xs, eye_q, eye_s)           # B = I: D = X
+    assert np.array_equal(d_b, want)
+    # closed-form spot values: row 0 of X, element 1 (high nibble of byte 0)
+    # and element 33 (block 1)
+    code1 = int(xq[0, 0]) >> 4
+    code33 = int(xq[0, 16]) >> 4
+    v = lambda c: (-1.0 if c & 8 else 1.0) * E2M1_TABLE[c & 7]
+    assert d_b[0, 1] == v(code1) * 2.0 ** (int(xs[0, 0]) - 127)
+    assert d_b[0, 33] == v(code33) * 2.0 ** (int(xs[1, 0]) - 127)
+
+
 ALL_PINS = [pin_decode_f16, pin_decode_bf16, pin_worked_example_exact,
             pin_matches_numpy_random_shapes, pin_two_a_plus_one, pin_fma_separation,
             pin_alpha_beta_c_cases, pin_gather_invariants, pin_entries_match_rows,
             pin_scatter_rows, pin_fp4_decode, pin_w4_matches_numpy,
-            pin_w4_nibble_order_and_blocks]
+            pin_w4_nibble_order_and_blocks, pin_e2m1_matches_numpy, pin_e2m1_identity_picks]

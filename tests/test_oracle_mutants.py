@@ -51,6 +51,20 @@ MUTANTS = [
      "    return v;\n}\n\ndouble oracle_decode_ue8m0"),
     ("ue8m0_bias", "ldexp(1.0, s - 127)", "ldexp(1.0, s - 128)"),
     ("fp4_scale_transposed", "Ws[(k / 32) * lds + j]", "Ws[j * lds + (k / 32)]"),
+    # (swapping the nibble order of both FP4 operands alike permutes K the same
+    # way on both sides, within a 32-element block: the products are unchanged,
+    # so that mistake cannot be told apart and is not planted; the order is
+    # pinned where an FP4 operand meets a 16-bit one)
+    ("e2m1_scale_block_16", "scales[(k / 32) * lds + row]", "scales[(k / 16) * lds + row]"),
+    ("e2m1_scale_transposed", "scales[(k / 32) * lds + row]", "scales[row * lds + (k / 32)]"),
+    ("e2m1_a_scaled_by_b_scales", "fp4_element(arow, As, ldas, i, k)", "fp4_element(arow, Bs, ldbs, i, k)"),
+    ("e2m1_a_scale_of_b_row", "fp4_element(arow, As, ldas, i, k)", "fp4_element(arow, As, ldas, 0, k)"),
+    ("e2m1_b_row_stride_ignored", "const uint8_t *brow = Bq + j * ldbq;", "const uint8_t *brow = Bq + j;"),
+    ("e2m1_a_row_stride_ignored", "const uint8_t *arow = Aq + i * ldaq;", "const uint8_t *arow = Aq + i;"),
+    ("e2m1_alpha_dropped", "double d = alpha * dot;", "double d = dot;"),
+    ("e2m1_c_wrong_sign", "d += beta * (double)C[i * ldc + j];", "d -= beta * (double)C[i * ldc + j];"),
+    ("e2m1_last_k_dropped", "for (int64_t k = 0; k < K; ++k) {\n                double a = fp4_element",
+     "for (int64_t k = 0; k + 1 < K; ++k) {\n                double a = fp4_element"),
     ("sign_bit_ignored_f16", "    return sign ? -v : v;\n}\n\n/* bfloat16", "    return v;\n}\n\n/* bfloat16"),
 ]
 
