@@ -215,6 +215,54 @@ gemm_status gemm_bf16_e2m1(int64_t M, int64_t N, int64_t K,
                            int out, float alpha, float beta, void *stream);
 
 /*
+ * Both operands FP4: D = fma.rn(alpha, A * B^T, beta * C) with
+ *     A[i][k] = e2m1(code of element k of row i of Aq) * 2^(As[k / 32][i] - 127),
+ *     B[j][k] = e2m1(code of element k of row j of Bq) * 2^(Bs[k / 32][j] - 127),
+ * computed by the tensor cores' block-scaled MMAs (fp32 accumulation).  The
+ * "cp.async.bulk.tensor" page (section "Interleave and packed FP4") gives
+ * float4_e2m1fn as an operand format and its 16U4_ALIGN16B load image; code
+ * values and scales are those of the OCP Microscaling definition that name
+ * refers to (E2M1 codes 0..7 = 0, 0.5, 1, 1.5, 2, 3, 4, 6, bit 3 the sign;
+ * UE8M0 scale s = 2^(s - 127), 255 = NaN; one scale per 32 elements along K).
+ *
+ *  Aq, ldaq    M rows of K/2 bytes, ldaq bytes apart: element k of a row is
+ *              the low nibble of byte k/2 when k is even, the high nibble when
+ *              odd.  ldaq >= K/2.
+ *  As, ldas    K/32 rows of M scale bytes, ldas bytes apart (row b holds the
+ *              scales of elements 32b .. 32b+31 of every row of A), ldas >= M.
+ *  Bq, ldbq    N rows of K/2 bytes (as Aq), ldbq >= K/2.
+ *  Bs, ldbs    K/32 rows of N scale bytes (as As), ldbs >= N.
+ *              Scales with a 16-byte aligned base and a pitch that is a
+ *              multiple of 16 are read in place; otherwise the library first
+ *              copies them to a padded buffer of its own (per device and stream,
+ *              allocated once and grown on demand).
+ *  K           a multiple of 32 (GEMM_ERR_UNSUPPORTED otherwise).
+ *  image       how the codes reach the tensor cores:
+ *              GEMM_FP4_PACKED (0): as stored, two per byte (MMA kind::mxf4);
+ *                Aq, Bq 16-byte aligned, ldaq, ldbq multiples of 16.
+ *              GEMM_FP4_ALIGN16B (1): through the 16U4_ALIGN16B load image,
+ *                sixteen codes in the low 8 bytes of each 16-byte shared block
+ *                (MMA kind::mxf8f6f4, half the rate of the packed form); the
+ *                page's rules apply: K a multiple of 128 (GEMM_ERR_UNSUPPORTED
+ *                otherwise), Aq, Bq 32-byte aligned and ldaq, ldbq multiples of
+ *                32 (GEMM_ERR_ALIGNMENT otherwise).
+ *              The two forms take the same products; they may add them in a
+ *              different order (bit-identical wherever every partial sum is
+ *              exact in float32).
+ *  C, D, out, alpha, beta, stream as in gemm_f16.  D must not overlap Aq, As,
+ *  Bq or Bs.  K == 0: D = beta * C.
+ */
+enum { GEMM_FP4_PACKED = 0, GEMM_FP4_ALIGN16B = 1 };
+gemm_status gemm_e2m1(int64_t M, int64_t N, int64_t K,
+                      const uint8_t *Aq, int64_t ldaq,
+                      const uint8_t *As, int64_t ldas,
+                      const uint8_t *Bq, int64_t ldbq,
+                      const uint8_t *Bs, int64_t ldbs,
+                      const float *C, int64_t ldc,
+                      void *D, int64_t ldd,
+                      int out, float alpha, float beta, int image, void *stream);
+
+/*
  * Seeded form, the pages' recurrence taken literally: D = C + A * B^T where C
  * is the accumulator's starting value.  The first K issue reads C and every
  * later one reads the running fp32 sum ("mma.sync" page, section
@@ -328,8 +376,9 @@ const char *gemm_status_string(int status);
  * form: 0 = plain, 1 = row-gathered (gemm_gather_rows), 2 = row-scattered
  * (gemm_scatter_rows), 3 = seeded (gemm_seeded), 4 = FP4 weights
  * (gemm_bf16_e2m1), 5 = gemm_skinny_noalloc (kernel 0 where it returns
- * GEMM_ERR_UNSUPPORTED for the shape); any other value is
- * GEMM_ERR_INVALID_ARG.  has_c: C is given and beta != 0.
+ * GEMM_ERR_UNSUPPORTED for the shape), 6 / 7 = gemm_e2m1 with packed codes /
+ * the 16U4_ALIGN16B image; any other value is GEMM_ERR_INVALID_ARG.
+ * has_c: C is given and beta != 0.
  *
  * With M <= 64 rows (bf16 / f16 B; not gathered, not seeded) the skinny
  * kernel runs where it measured faster than the tile kernel: M <= 16 with
@@ -349,7 +398,10 @@ const char *gemm_status_string(int status);
  *           9 = four CTA pairs (a cluster of 8) with 256 x 512 tiles, each
  *           CTA loading a quarter of its A rows for the four, 10 = the
  *           warp-level kernel (mma.sync.m16n8k16, one 16 x 8 block of D per
- *           warp; problems of at most 2^20 multiply-adds)
+ *           warp; problems of at most 2^20 multiply-adds), 11 / 12 = the tile
+ *           kernel on FP4 operands with block scales (single CTAs, 128 x bn
+ *           tiles, bn 128 or 256; MMA kind::mxf4 on packed codes / kind::mxf8f6f4
+ *           on the 16U4_ALIGN16B image)
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)
@@ -393,7 +445,8 @@ gemm_status gemm_debug_inject(int mode);
  * with bn = 256, kernel 7 = two CTA pairs sharing A with bn = 512,
  * kernel 8 = two CTA pairs sharing A with bn = 256, kernel 9 = four CTA pairs
  * sharing A with bn = 512, kernel 10 = the warp-level kernel with bn = 8 (it
- * then runs every problem), kernel 2 = the skinny kernel with bn = 0 or 128
+ * then runs every problem), kernels 11 / 12 = the FP4 tile width bn in {128,
+ * 256} for gemm_e2m1 (only), kernel 2 = the skinny kernel with bn = 0 or 128
  * (problems it can run: M <= 64, K > 0, not gathered or seeded), kernel 0 =
  * automatic choice (the default).  Tile forms apply to every problem the tile
  * kernel runs, M <= 64 ones included; FP4 weights keep their own paths, and

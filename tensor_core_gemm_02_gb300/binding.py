@@ -57,6 +57,8 @@ def load_library(path: str = LIB_PATH):
                                      vp, i64, i32, f32, f32, vp]
     lib.gemm_bf16_e2m1.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                    i32, f32, f32, vp]
+    lib.gemm_e2m1.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                              i32, f32, f32, i32, vp]
     lib.gemm_seeded.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, i32, vp]
     lib.gemm_accumulate.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, f32, vp]
     lib.gemm_scatter_rows.argtypes = [i64, i64, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64,
@@ -71,7 +73,7 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_debug_inject.argtypes = [i32]
     lib.gemm_debug_force_tile.argtypes = [i32, i32]
     for name in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows", "gemm_accumulate",
-                 "gemm_seeded", "gemm_bf16_e2m1",
+                 "gemm_seeded", "gemm_bf16_e2m1", "gemm_e2m1",
                  "gemm_skinny_noalloc",
                  "gemm_check_device_status",
                  "gemm_query_plan", "gemm_set_wait_timeout", "gemm_debug_inject",
@@ -221,6 +223,34 @@ def gemm_bf16_e2m1(A, Bq, Bs, C=None, D=None, *, alpha=1.0, beta=1.0, out=OUT_F3
     return D
 
 
+FP4_PACKED, FP4_ALIGN16B = 0, 1
+
+
+def gemm_e2m1(Aq, As, Bq, Bs, C=None, D=None, *, alpha=1.0, beta=1.0, out=OUT_F32,
+              image=FP4_PACKED, stream=None):
+    """D = fma.rn(alpha, A @ B.T, beta * C) with both operands FP4: packed E2M1
+    codes Aq (M x K/2 uint8) and Bq (N x K/2 uint8), even k in the low nibble,
+    and UE8M0 block scales As (K/32 x M uint8) and Bs (K/32 x N uint8).
+    image: FP4_PACKED (codes as stored, MMA kind::mxf4) or FP4_ALIGN16B (the
+    16U4_ALIGN16B load image, MMA kind::mxf8f6f4)."""
+    for name, t in (("Aq", Aq), ("As", As), ("Bq", Bq), ("Bs", Bs)):
+        if t.dtype != torch.uint8 or t.dim() != 2:
+            raise TypeError(f"{name} must be a 2-D uint8 tensor")
+    M, K = Aq.shape[0], 2 * Aq.shape[1]
+    N = Bq.shape[0]
+    if Bq.shape[1] * 2 != K or tuple(As.shape) != (K // 32, M) or tuple(Bs.shape) != (K // 32, N):
+        raise ValueError("Aq must be M x K/2, Bq N x K/2, As K/32 x M and Bs K/32 x N")
+    if C is not None and (C.dtype != torch.float32 or tuple(C.shape) != (M, N)):
+        raise ValueError("C must be float32 M x N")
+    D = _out_tensor(D, M, N, out, Aq.device)
+    st = load_library().gemm_e2m1(
+        M, N, K, _ptr(Aq), _ld(Aq), _ptr(As), _ld(As), _ptr(Bq), _ld(Bq), _ptr(Bs), _ld(Bs),
+        _ptr(C), _ld(C) if C is not None else 0, _ptr(D), _ld(D), out, float(alpha), float(beta),
+        int(image), _stream_ptr(stream))
+    _check(st, "gemm_e2m1")
+    return D
+
+
 def gemm_seeded(A, B, C, D=None, *, out=OUT_F32, stream=None):
     """D = C + A @ B.T with C (float32 M x N) as the accumulator's starting value:
     every K step of the tensor-core sum accumulates onto it."""
@@ -291,9 +321,12 @@ def gemm_check_device_status(stream=None) -> int:
 
 
 def gemm_query_plan(M, N, K, gather=False, has_c=False, sm_count=148, scatter=False,
-                    seeded=False, fp4=False, noalloc=False) -> Plan:
+                    seeded=False, fp4=False, noalloc=False, e2m1=None) -> Plan:
+    """e2m1: None, or FP4_PACKED / FP4_ALIGN16B for gemm_e2m1's plan."""
     p = Plan()
     form = 1 if gather else (2 if scatter else (3 if seeded else (4 if fp4 else (5 if noalloc else 0))))
+    if e2m1 is not None:
+        form = 6 + int(e2m1)
     _check(load_library().gemm_query_plan(M, N, K, form, int(bool(has_c)),
                                           sm_count, ctypes.byref(p)), "gemm_query_plan")
     return p

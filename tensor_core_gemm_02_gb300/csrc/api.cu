@@ -598,8 +598,8 @@ void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev)
 // Buffers of the FP4 paths, one per (device, stream, use), grown
 // geometrically: kBufWeights holds the bf16 copy of the weights for M > 64,
 // kBufScales a copy of the scales with a 16-byte row pitch for the TMA loads
-// of the M <= 64 path when the caller's pitch or base is not 16-byte aligned.
-enum { kBufWeights = 0, kBufScales = 1 };
+// of the M <= 64 path when the caller's pitch or base is not 16-byte aligned
+// (kBufScalesA / kBufScalesB: the same for gemm_e2m1's two operands).
 struct DequantBuffer {
     int device = -1;
     cudaStream_t stream = nullptr;
@@ -727,12 +727,18 @@ gemm_status run_tiny(const Problem &p, const gemm_plan &plan, const DeviceInfo *
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+void forced_tile(int *kernel, int *bn)
+{
+    *kernel = g_force_kernel.load();
+    *bn = g_force_bn.load();
+}
+
 // Test hook: replace the automatic tile form by a forced one where it can run.
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || plan.kernel == 0 || p.w4)
-        return plan;  // (FP4 weights run only on their own paths)
+    if (fk == 0 || fk == 11 || fk == 12 || plan.kernel == 0 || p.w4)
+        return plan;  // (FP4 weights run only on their own paths; 11 / 12 are FP4 x FP4 forms)
     if (fk == 10) {
         set_tiny_plan(plan, p.M, p.N);  // the warp-level kernel runs every problem
         return plan;
@@ -1100,10 +1106,14 @@ gemm_status gemm_query_plan(int64_t M, int64_t N, int64_t K, int form, int has_c
 {
     if (!plan || sm_count < 1 || M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (form < 0 || form > 5)
+    if (form < 0 || form > 7)
         return GEMM_ERR_INVALID_ARG;
     if (form == 5) {
         *plan = noalloc_plan(M, N, K, has_c != 0, sm_count);
+        return GEMM_OK;
+    }
+    if (form == 6 || form == 7) {
+        *plan = e2m1_plan(M, N, K, form - 6, sm_count);
         return GEMM_OK;
     }
     Problem q{};
@@ -1133,7 +1143,8 @@ gemm_status gemm_debug_force_tile(int kernel, int bn)
                     (kernel == 3 && bn == 256) || (kernel == 4 && bn == 512) ||
                     (kernel == 5 && (bn == 64 || bn == 256)) || (kernel == 6 && bn == 256) ||
                     (kernel == 7 && bn == 512) || (kernel == 8 && bn == 256) ||
-                    (kernel == 9 && bn == 512) || (kernel == 10 && bn == 8);
+                    (kernel == 9 && bn == 512) || (kernel == 10 && bn == 8) ||
+                    ((kernel == 11 || kernel == 12) && (bn == 128 || bn == 256));
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

@@ -79,5 +79,23 @@ void fill_common(GemmArgs &a, const Problem &p, const DeviceInfo *dev);
 // device-side error; noalloc.cu).
 gemm_status reset_static_scratch(int device);
 
+// Buffers the library keeps per (device, stream, use), grown geometrically:
+// bf16 weights converted from FP4, and block scales copied to a 16-byte row
+// pitch for TMA (B's for gemm_bf16_e2m1; A's and B's for gemm_e2m1).
+enum { kBufWeights = 0, kBufScales = 1, kBufScalesA = 2, kBufScalesB = 3 };
+gemm_status get_dequant_buffer(int device, cudaStream_t stream, int use, size_t bytes, void **out);
+
+// The form forced by gemm_debug_force_tile (kernel 0: none).
+void forced_tile(int *kernel, int *bn);
+
+bool aligned16(const void *p);
+uint64_t span_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t esize);
+bool overlap(const void *a, uint64_t an, const void *b, uint64_t bn);
+int out_size(int out);
+
+// Plan of gemm_e2m1 (kernel 11: packed codes, kind::mxf4; 12: the 16U4 image,
+// kind::mxf8f6f4), with a forced form applied.
+gemm_plan e2m1_plan(int64_t M, int64_t N, int64_t K, int image, int sm_count);
+
 }  // namespace host
 }  // namespace tcg

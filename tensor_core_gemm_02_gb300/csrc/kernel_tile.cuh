@@ -51,9 +51,15 @@
 
 namespace tcg {
 
-template <int BN_, int STAGES_, bool PAIR_ = false, int NSUB_ = 1, int MC_ = 1>
+template <int BN_, int STAGES_, bool PAIR_ = false, int NSUB_ = 1, int MC_ = 1, int MX_ = 0>
 struct TileCfg {
     static constexpr bool PAIR = PAIR_;
+    // MX: operand kind.  0 = f16/bf16 (tcgen05 kind::f16); 1 = FP4 E2M1 codes
+    // packed two per byte (kind::mxf4); 2 = FP4 codes in the 16U4_ALIGN16B TMA
+    // image, sixteen codes in the low 8 bytes of each 16-byte block
+    // (kind::mxf8f6f4).  The FP4 kinds carry UE8M0 block scales (one per 32
+    // elements along K) through shared memory into TMEM.  Single CTAs only.
+    static constexpr int MX = MX_;
     // MC > 1: MC CTAs (or MC pairs) work on MC neighbouring tiles of one
     // block row; each loads 1/MC of the shared A box and multicasts it to the
     // others, so per CTA the A traffic (or the number of gather4 issues) drops
@@ -64,26 +70,53 @@ struct TileCfg {
     // step into one 2*BN-column accumulator), so each row of A feeds twice the
     // work; without a second accumulator the epilogue no longer overlaps.
     static constexpr int NSUB = NSUB_;
-    static constexpr int NUM_ACC = NSUB == 1 ? 2 : 1;
     static constexpr int BM = 128;                  // rows of A (and D) per CTA
     static constexpr int TILE_M = PAIR ? 256 : 128;  // rows per output tile
     static constexpr int BN = BN_;       // N of one MMA
     static constexpr int TILE_N = BN * NSUB;
+    // Accumulators: two (the epilogue of one tile overlaps the next tile's
+    // MMAs), except for two-half tiles and for FP4 tiles 256 wide, whose block
+    // scales need TMEM columns beside the one 256-column accumulator.
+    static constexpr int NUM_ACC = (NSUB == 1 && !(MX != 0 && BN == 256)) ? 2 : 1;
     static constexpr int BN_LOCAL = PAIR ? BN / 2 : BN;  // rows of B per half each CTA loads
-    static constexpr int BK = 64;  // 64 x 16-bit = one 128-byte swizzle row
+    // K elements per stage: one 128-byte swizzle row of each operand row
+    // (64 x 16-bit, 256 packed FP4 codes, or 128 codes in the 16U4 image)
+    static constexpr int BK = MX == 0 ? 64 : (MX == 1 ? 256 : 128);
+    static constexpr int MMA_K = MX == 0 ? 16 : (MX == 1 ? 64 : 32);  // K of one MMA (32 bytes)
     static constexpr int STAGES = STAGES_;
-    static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr uint32_t ROW_BYTES = 128;
+    static constexpr uint32_t A_BYTES = BM * ROW_BYTES;
     static constexpr int A_SLICE_ROWS = BM / MC;  // rows of A this CTA loads for the cluster
     static constexpr uint32_t A_SLICE_BYTES = A_BYTES / MC;
-    static constexpr uint32_t B_SUB_BYTES = BN_LOCAL * BK * 2;
+    static constexpr uint32_t B_SUB_BYTES = BN_LOCAL * ROW_BYTES;
     static constexpr uint32_t B_BYTES = NSUB * B_SUB_BYTES;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    // Block scales of a stage (FP4): SF_KB rows of 32-element blocks, as TMA
+    // loads them from the K/32 x rows scale matrices (BM bytes for A, TILE_N
+    // for B per row), then rearranged by the scale warp into 512-byte tiles
+    // (128 rows x 4 blocks: row l + 32 q of the tile, block b at byte
+    // 16 l + 4 q + b) that tcgen05.cp copies into 4 TMEM columns each: the A
+    // tiles (one per 128-element K chunk), then per chunk the B row tiles.
+    static constexpr int SF_KB = MX ? BK / 32 : 0;
+    static constexpr int SF_CHUNKS = MX ? BK / 128 : 0;
+    static constexpr int SF_B_ROWTILES = MX ? (TILE_N + 127) / 128 : 0;
+    static constexpr int SF_TILES = SF_CHUNKS * (1 + SF_B_ROWTILES);
+    static constexpr uint32_t SF_STAGE_BYTES = SF_KB * (BM + TILE_N);
+    static constexpr uint32_t SF_CP_BYTES = SF_TILES * 512;
+    static constexpr uint32_t SF_COLS = SF_TILES * 4;  // TMEM columns per stage
+    // bytes the stage barrier expects: codes in the 16U4 image count their
+    // payload, not the padding ("cp.async.bulk.tensor" page, section
+    // "Interleave and packed FP4")
+    static constexpr uint32_t STAGE_TX =
+        (MX == 2 ? STAGE_BYTES / 2 : STAGE_BYTES) + SF_STAGE_BYTES;
     static constexpr uint32_t EPI_BUF = 32 * 128;  // 32 rows x 128 B
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = STAGES * A_BYTES;
-    static constexpr uint32_t OFF_EPI = STAGES * STAGE_BYTES;
+    static constexpr uint32_t OFF_SFS = STAGES * STAGE_BYTES;             // scales as loaded
+    static constexpr uint32_t OFF_SFC = OFF_SFS + STAGES * SF_STAGE_BYTES;  // rearranged
+    static constexpr uint32_t OFF_EPI = OFF_SFC + STAGES * SF_CP_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_EPI + 8 * EPI_BUF;  // 4 warps x 2 buffers
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 8;
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 8 + (MX ? STAGES : 0);
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base
@@ -93,9 +126,12 @@ struct TileCfg {
     // the rate.  Those single-CTA forms get a second issuing warp (warp 6)
     // that takes every other K block into an accumulator of its own; the
     // epilogue adds the two.  (Pairs and wider tiles are tensor-bound.)
-    static constexpr int ISS = (!PAIR && MC == 1 && NSUB == 1 && BN <= 128) ? 2 : 1;
-    static constexpr uint32_t TMEM_COLS = NUM_ACC * TILE_N * ISS;  // fp32 accumulators
-    static constexpr int THREADS = 192 + 32 * (ISS - 1);
+    static constexpr int ISS = (!PAIR && MC == 1 && NSUB == 1 && BN <= 128 && MX == 0) ? 2 : 1;
+    static constexpr uint32_t ACC_COLS = NUM_ACC * TILE_N * ISS;  // fp32 accumulators
+    static constexpr uint32_t SF_COL0 = ACC_COLS;                 // first scale column (FP4)
+    static constexpr uint32_t TMEM_COLS = MX ? 512u : ACC_COLS;
+    // warp 6: the second MMA issuer, or (FP4) the scale warp
+    static constexpr int THREADS = 192 + 32 * (ISS - 1) + (MX ? 32 : 0);
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(NSUB == 1 || NSUB == 2, "one or two halves");
@@ -105,6 +141,9 @@ struct TileCfg {
     static_assert(!PAIR || (BN % 32 == 0 && BN_LOCAL % 8 == 0), "pair splits B in 8-row groups");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
+    static_assert(MX == 0 || (!PAIR && MC == 1 && NSUB == 1 && (BN == 128 || BN == 256)),
+                  "FP4 operands: single CTAs, tiles 128 or 256 wide");
+    static_assert(MX == 0 || SF_COL0 + STAGES * SF_COLS <= 512, "TMEM for the block scales");
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled box image
@@ -122,14 +161,16 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t row, uint32_t chunk, uint32
 // into D, and accumulators seeded with C.
 enum : int { kModePlain = 0, kModeScatter = 1, kModeReduce = 2, kModeSeed = 3 };
 
-template <int BN, int STAGES, bool PAIR, int NSUB, int MC, int MODE>
-__global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 1)
+template <int BN, int STAGES, bool PAIR, int NSUB, int MC, int MODE, int MX = 0>
+__global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREADS, 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC,
-                     const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
+                     const __grid_constant__ CUtensorMap tmD,
+                     const __grid_constant__ CUtensorMap tmSFA,
+                     const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args)
 {
-    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>;
     constexpr int CL = Cfg::CLUSTER;
     // issuers in use: one for seeded accumulators (C is the start value of the
     // one chain of K steps, as the pages' recurrence has it)
@@ -150,6 +191,8 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     auto c_bar = [&](int q, int j) { return bar0 + 8u * (2 * STAGES + 4 + 2 * q + j); };
+    // (FP4) stage s's scales are rearranged for tcgen05.cp
+    auto sf_bar = [&](int st) { return bar0 + 8u * (2 * STAGES + 12 + st); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
 
@@ -189,12 +232,19 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 
         for (int q = 0; q < 4; ++q)
             for (int j = 0; j < 2; ++j)
                 mbar_init(c_bar(q, j), 1);
+        if (MX)
+            for (int st = 0; st < STAGES; ++st)
+                mbar_init(sf_bar(st), 1);
         *abort_flag = 0u;
         fence_mbar_init();
         fence_proxy_async_smem();
         if (args.num_k_blocks > 0) {  // with K == 0 the A/B descriptors are left empty
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            if (MX) {
+                tma_prefetch_desc(&tmSFA);
+                tma_prefetch_desc(&tmSFB);
+            }
         }
         if (args.has_c && args.c_tma)
             tma_prefetch_desc(&tmC);
@@ -268,7 +318,7 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 
                 }
                 if (lane == 0 && leader) {
                     // the leader's barrier counts the bytes of both CTAs of a pair
-                    const uint32_t bytes = (PAIR ? 2u : 1u) * Cfg::STAGE_BYTES + (first ? args.extra_tx : 0u);
+                    const uint32_t bytes = (PAIR ? 2u : 1u) * Cfg::STAGE_TX + (first ? args.extra_tx : 0u);
                     mbar_arrive_expect_tx(full_bar(s), bytes);
                 }
                 first = false;
@@ -276,7 +326,19 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 
                 const int32_t k0 = kb * Cfg::BK;
                 const uint32_t sa = base + Cfg::OFF_A + s * Cfg::A_BYTES;
                 const uint32_t sb = base + Cfg::OFF_B + s * Cfg::B_BYTES;
-                if (PAIR) {
+                if constexpr (MX != 0) {
+                    // FP4: the codes of A and B (128-byte rows: x is K / 2 bytes for
+                    // packed codes, K elements for the 16U4 image, kb * 128 either
+                    // way), and the stage's SF_KB rows of A's and B's block scales
+                    if (lane == 0) {
+                        const uint32_t sfs = base + Cfg::OFF_SFS + s * Cfg::SF_STAGE_BYTES;
+                        tma_load_2d(sa, &tmA, full_bar(s), kb * 128, m0);
+                        tma_load_2d(sb, &tmB, full_bar(s), kb * 128, nb0);
+                        tma_load_2d(sfs, &tmSFA, full_bar(s), m0, kb * Cfg::SF_KB);
+                        tma_load_2d(sfs + Cfg::SF_KB * Cfg::BM, &tmSFB, full_bar(s), nb0,
+                                    kb * Cfg::SF_KB);
+                    }
+                } else if (PAIR) {
                     const uint32_t fb = lead(full_bar(s));
                     if (MC > 1) {
                         if (args.gather) {
@@ -358,15 +420,40 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 
                 const uint64_t bd =
                     sdesc_k_sw128(base + Cfg::OFF_B + st * Cfg::B_BYTES + j * Cfg::B_SUB_BYTES);
                 const uint32_t dj = d_tmem + static_cast<uint32_t>(j * BN);
+                if constexpr (MX != 0) {
+                    // the stage's scale tiles into its TMEM columns, then four
+                    // block-scaled MMAs of 32 bytes of K each; MMA k reads the
+                    // scales of its 128-element chunk, the byte(s) its scale ids pick
+                    const uint32_t sfc = base + Cfg::OFF_SFC + st * Cfg::SF_CP_BYTES;
+                    const uint32_t sfcol = tmem_base + Cfg::SF_COL0 + st * Cfg::SF_COLS;
 #pragma unroll
-                for (int k = 0; k < Cfg::BK / 16; ++k) {  // +32 B per K=16 step
-                    // (the first K step of this issuer's chain starts from zero)
-                    if (PAIR)
-                        tc_mma_f16_pair(dj, ad + 2u * k, bd + 2u * k, idesc,
-                                        (seeded || ((kb / kIss) | k) != 0) ? 1u : 0u);
-                    else
-                        tc_mma_f16(dj, ad + 2u * k, bd + 2u * k, idesc,
-                                   (seeded || ((kb / kIss) | k) != 0) ? 1u : 0u);
+                    for (int ti = 0; ti < Cfg::SF_TILES; ++ti)
+                        tc_cp_32x128b_warpx4(sfcol + 4u * ti, sdesc_rows16(sfc + 512u * ti));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        constexpr uint32_t kFmt = MX == 1 ? 1u : 5u;  // E2M1 in each kind's coding
+                        const uint32_t chunk = (k * Cfg::MMA_K) / 128;
+                        const uint32_t sfid = ((k * Cfg::MMA_K) % 128) / 32;
+                        const uint32_t id = idesc_mx(kFmt, 128, BN, sfid, sfid);
+                        const uint32_t sfa = sfcol + 4u * chunk;
+                        const uint32_t sfb = sfcol + 4u * Cfg::SF_CHUNKS + 4u * Cfg::SF_B_ROWTILES * chunk;
+                        const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+                        if (MX == 1)
+                            tc_mma_mxf4(dj, ad + 2u * k, bd + 2u * k, id, sfa, sfb, acc);
+                        else
+                            tc_mma_mxf8f6f4(dj, ad + 2u * k, bd + 2u * k, id, sfa, sfb, acc);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < Cfg::BK / 16; ++k) {  // +32 B per K=16 step
+                        // (the first K step of this issuer's chain starts from zero)
+                        if (PAIR)
+                            tc_mma_f16_pair(dj, ad + 2u * k, bd + 2u * k, idesc,
+                                            (seeded || ((kb / kIss) | k) != 0) ? 1u : 0u);
+                        else
+                            tc_mma_f16(dj, ad + 2u * k, bd + 2u * k, idesc,
+                                       (seeded || ((kb / kIss) | k) != 0) ? 1u : 0u);
+                    }
                 }
             };
             // arrive on `bar` (both CTAs of a pair) once the MMAs issued so far finish
@@ -390,6 +477,10 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 
             auto next_full = [&](int &st) {
                 if (!wait_bounded<true>(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
                                   kWhereMmaFull))
+                    return false;
+                // (FP4: and for the scale warp to have rearranged the stage's scales)
+                if (MX && !wait_bounded<true>(sf_bar(s), ph, abort_flag, args.status,
+                                              args.timeout_ns, kWhereMmaFull))
                     return false;
                 tc_fence_after_sync();
                 st = s;
@@ -502,6 +593,55 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC>::THREADS, 
             }
         }
         __syncwarp();
+    } else if (MX != 0 && warp == 6) {
+        // ------------------------------------------------------------ scale warp
+        // For every stage: wait for its loads, rearrange the scale rows as loaded
+        // (row b of the stage: one byte per row of A, then of B) into 512-byte
+        // tiles -- lane l writes 16 bytes, rows l, l + 32, l + 64, l + 96 of the
+        // tile, four 32-element blocks each -- and hand them to the MMA thread
+        // (tcgen05.cp reads them through the async proxy, hence the fence).
+        if constexpr (MX != 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool alive = true;
+            for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
+                for (int32_t kb = 0; kb < args.num_k_blocks; ++kb) {
+                    if (!warp_wait_bounded<true>(full_bar(s), ph, abort_flag, args.status,
+                                                 args.timeout_ns, kWhereMmaFull)) {
+                        alive = false;
+                        break;
+                    }
+                    const uint32_t src = base + Cfg::OFF_SFS + s * Cfg::SF_STAGE_BYTES;
+                    const uint32_t dst = base + Cfg::OFF_SFC + s * Cfg::SF_CP_BYTES;
+#pragma unroll
+                    for (int ti = 0; ti < Cfg::SF_TILES; ++ti) {
+                        const bool a_tile = ti < Cfg::SF_CHUNKS;
+                        const int c = a_tile ? ti : (ti - Cfg::SF_CHUNKS) / Cfg::SF_B_ROWTILES;
+                        const int rt = a_tile ? 0 : (ti - Cfg::SF_CHUNKS) % Cfg::SF_B_ROWTILES;
+                        const uint32_t pitch = a_tile ? Cfg::BM : Cfg::TILE_N;
+                        const uint32_t rows = src + (a_tile ? 0u : Cfg::SF_KB * Cfg::BM) + 128u * rt +
+                                              4u * c * pitch + lane;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            w[q] = 0u;
+#pragma unroll
+                            for (int b = 0; b < 4; ++b)
+                                w[q] |= ld_shared_u8(rows + b * pitch + 32u * q) << (8 * b);
+                        }
+                        st_shared_v4(dst + 512u * ti + 16u * lane, w[0], w[1], w[2], w[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(sf_bar(s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may read

@@ -20,10 +20,12 @@
 namespace tcg {
 
 struct GemmMaps {
-    CUtensorMap a;  // A tiles, or the gather table (box of one row)
-    CUtensorMap b;  // B tiles
-    CUtensorMap c;  // C boxes (float32), unused when C is not read
-    CUtensorMap d;  // D boxes
+    CUtensorMap a;    // A tiles, or the gather table (box of one row); FP4: A's codes
+    CUtensorMap b;    // B tiles; FP4: B's codes
+    CUtensorMap c;    // C boxes (float32), unused when C is not read
+    CUtensorMap d;    // D boxes
+    CUtensorMap sfa;  // FP4 operands: A's block scales (K/32 rows of M bytes)
+    CUtensorMap sfb;  // FP4 operands: B's block scales (K/32 rows of N bytes)
 };
 
 // Tile kernel forms: 128 x bn tiles on single CTAs (mc = 1), or on clusters of
@@ -37,6 +39,17 @@ int tile_max_clusters(int bn, bool pair, int nsub, int mc);
 // accumulators (kModePlain ... kModeSeed)
 cudaError_t launch_tile(int mode, int bn, bool pair, int nsub, int mc, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream);
+
+// The tile kernel with FP4 E2M1 operands and UE8M0 block scales (plain
+// epilogue, single CTAs, 128 x bn tiles, bn 128 or 256).  mx 1: codes packed
+// two per byte, kind::mxf4; mx 2: codes in the 16U4_ALIGN16B image,
+// kind::mxf8f6f4.  maps.a / maps.b: the codes (128-byte boxes of 128 / bn
+// rows, 128-byte swizzle); maps.sfa / maps.sfb: the scales (uint8 boxes of
+// 128 / bn columns by K_stage / 32 rows).  tile_mx_kstage: K elements per stage.
+int tile_mx_stages(int mx, int bn);
+int tile_mx_kstage(int mx);
+cudaError_t launch_tile_mx(int mx, int bn, const GemmMaps &maps, const GemmArgs &args, int grid,
+                           cudaStream_t stream);
 
 // Warp-level tiny-GEMM kernel: one 16 x 8 block of D per warp.
 int tiny_warps_per_cta();

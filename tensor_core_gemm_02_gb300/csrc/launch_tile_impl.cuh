@@ -15,11 +15,11 @@
 namespace tcg {
 
 // attr must hold two entries
-template <int BN, int STAGES, bool PAIR, int NSUB, int MC>
+template <int BN, int STAGES, bool PAIR, int NSUB, int MC, int MX = 0>
 inline void tile_fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid,
                              cudaStream_t stream)
 {
-    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>;
     cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
@@ -40,20 +40,20 @@ inline void tile_fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr,
     cfg.numAttrs = n;
 }
 
-template <int BN, int STAGES, bool PAIR, int NSUB, int MC, int MODE>
+template <int BN, int STAGES, bool PAIR, int NSUB, int MC, int MODE, int MX = 0>
 cudaError_t tile_launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                              cudaStream_t stream)
 {
-    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC>;
-    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, MODE>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>;
+    auto kfn = tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, MODE, MX>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_ALLOC));
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    tile_fill_config<BN, STAGES, PAIR, NSUB, MC>(cfg, attr, grid, stream);
-    return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, maps.d, args);
+    tile_fill_config<BN, STAGES, PAIR, NSUB, MC, MX>(cfg, attr, grid, stream);
+    return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, maps.d, maps.sfa, maps.sfb, args);
 }
 
 // Every form of the tile kernel, for epilogue mode MODE.

@@ -440,6 +440,52 @@ __device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tm
         : "memory");
 }
 
+// Block-scaled MMA on FP4 E2M1 operands with UE8M0 scales, one scale per 32
+// elements along K (the OCP Microscaling grouping that the float4_e2m1fn
+// operand format of the "cp.async.bulk.tensor" page, section "Interleave and
+// packed FP4", refers to).  A and B come from 128-byte swizzled shared images
+// through descriptors, the scales from TMEM at sfa_tmem / sfb_tmem (layout:
+// sf_tile_cols below), the byte within each 32-bit scale column chosen by the
+// scale-factor ids of the instruction descriptor.
+//   mxf4:     codes packed two per byte, K = 64 per instruction (32 bytes of a
+//             row), two scales per row per instruction (scale_vec::2X).
+//   mxf8f6f4: codes in the 16U4_ALIGN16B image (sixteen codes in the low 8
+//             bytes of each 16-byte block), K = 32 per instruction (32 bytes of
+//             a row), one scale per row per instruction (scale_vec::1X).
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared memory -> TMEM copy of one scale tile: 32 rows of 16 bytes, written
+// to the four 32-lane quarters alike (lane q*32 + l, columns col .. col+3 get
+// row l).  Issued by the MMA thread; it completes in order before the MMAs
+// issued after it by the same thread.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t src_desc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
+                 : "memory");
+}
+
 // Pair MMA, issued by the leader CTA only: M = 256 rows, A's rows 0-127 from
 // the leader's shared memory and 128-255 from the peer's (same offsets), B's
 // N columns split in halves the same way; each CTA's TMEM receives its rows.
@@ -585,6 +631,33 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t smem_addr)
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
     return d;
+}
+
+// Shared-memory descriptor of an unswizzled image made of 8-row groups of
+// 16-byte rows, the groups 128 bytes apart (the source of tcgen05.cp 32x128b:
+// 32 rows of 16 bytes, contiguous).  16-byte aligned base; layout 0 = none.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
+// Instruction descriptor of the block-scaled kinds (mxf4, mxf8f6f4), dense,
+// fp32 accumulator, both operands K-major, UE8M0 scales.
+//   bits  4-5   B scale-factor id (byte of B's 32-bit scale column)
+//   bits  7-9   A format, bits 10-12 B format (E2M1: 1 for mxf4, 5 for mxf8f6f4)
+//   bits 17-22  N >> 3
+//   bit  23     scale type (1 = UE8M0)
+//   bits 24-28  M >> 4
+//   bits 29-30  A scale-factor id
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t fmt, uint32_t m, uint32_t n, uint32_t sfa_id,
+                                                uint32_t sfb_id)
+{
+    return (sfb_id << 4) | (fmt << 7) | (fmt << 10) | ((n >> 3) << 17) | (1u << 23) |
+           ((m >> 4) << 24) | (sfa_id << 29);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16, dense, fp32 accumulator,

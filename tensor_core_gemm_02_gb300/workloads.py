@@ -43,6 +43,14 @@ torch ``.to(torch.bfloat16)``, both round-to-nearest-even):
                    byte) and scales integers(118, 121, (128, 28672)) uint8
                    (2^-9 .. 2^-7: weights of the size of 0.02 * N(0,1));
                    C (16, 28672) N(0,1) float32; alpha = 0.5, beta = 1; fp32 out.
+  e2m1_16x28672x4096
+                   seed 7: both operands FP4 (e2m1_problem, values="random"):
+                   A (16 x 4096) codes integers(0, 16) per nibble and scales
+                   integers(125, 130), B (28672 x 4096) codes likewise and
+                   scales integers(118, 121); C (16, 28672) N(0,1) float32;
+                   alpha = 0.5, beta = 1; fp32 out.
+  e2m1_8192        seed 8: both operands FP4 as above, M = N = K = 8192; no C;
+                   bf16 out.
 """
 from __future__ import annotations
 
@@ -75,10 +83,19 @@ class Problem:
     accumulate: bool = False        # D += alpha * A @ B.T into float32 D = D0
     Bs: torch.Tensor | None = None  # FP4 weights: B holds codes (N x K/2 uint8), Bs the
                                     # UE8M0 scales (K/32 x N uint8)
+    As: torch.Tensor | None = None  # both operands FP4: A holds codes (M x K/2 uint8), As the
+                                    # scales (K/32 x M uint8)
+    image: int = 0                  # (both FP4) 0 packed codes, 1 the 16U4_ALIGN16B image
 
     @property
     def fp4(self) -> bool:
-        return self.Bs is not None
+        """FP4 weights with bf16 activations (gemm_bf16_e2m1)."""
+        return self.Bs is not None and self.As is None
+
+    @property
+    def e2m1(self) -> bool:
+        """Both operands FP4 (gemm_e2m1)."""
+        return self.As is not None
 
     @property
     def M(self) -> int:
@@ -90,7 +107,7 @@ class Problem:
 
     @property
     def K(self) -> int:
-        return int(self.A.shape[1])
+        return int(self.A.shape[1]) * (2 if self.As is not None else 1)
 
     @property
     def flops(self) -> int:
@@ -184,6 +201,66 @@ def scatter_16384_into_65536() -> Problem:
                    out=OUT_F32, scatter=True, d_rows=65536)
 
 
+def fp4_operand(rng, rows: int, K: int, codes=(0, 16), scales=(118, 121)):
+    """Packed E2M1 codes (rows x K/2 uint8; two independent draws per byte, the
+    low nibble first) and UE8M0 scales (K/32 x rows uint8) from the ranges."""
+    lo = rng.integers(*codes, (rows, K // 2))
+    hi = rng.integers(*codes, (rows, K // 2))
+    q = torch.from_numpy((lo | (hi << 4)).astype(np.uint8))
+    s = torch.from_numpy(rng.integers(*scales, (K // 32, rows)).astype(np.uint8))
+    return q, s
+
+
+def e2m1_problem(seed: int, M: int, N: int, K: int, values: str = "random", with_c: bool = False,
+                 alpha: float = 1.0, beta: float = 1.0, out: int = OUT_F32,
+                 image: int = 0) -> Problem:
+    """Both operands FP4, seeded.  values="exact": codes 0..4 with either sign
+    (|value| <= 2) and scales 126..128, so every product is a multiple of 2^-4
+    below 16 and every partial sum of K <= 2^16 products is exact in float32;
+    C quarter-integers.  values="random": every code, A's scales 125..129
+    (values of the size of N(0,1)), B's 118..120 (of 0.02 N(0,1)); C N(0,1).
+    Draw order: A's codes, A's scales, B's codes, B's scales, C."""
+    rng = np.random.default_rng(seed)
+    if values == "exact":
+        ca, sa, cb, sb = (0, 5), (126, 129), (0, 5), (126, 129)
+    else:
+        ca, sa, cb, sb = (0, 16), (125, 130), (0, 16), (118, 121)
+
+    def draw(rows, codes, scales):
+        if values == "exact":  # a sign bit drawn apart from the magnitude
+            mag = rng.integers(*codes, (rows, K))
+            sgn = rng.integers(0, 2, (rows, K)) << 3
+            c = mag | sgn
+            q = torch.from_numpy((c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8))
+            s = torch.from_numpy(rng.integers(*scales, (K // 32, rows)).astype(np.uint8))
+            return q, s
+        return fp4_operand(rng, rows, K, codes, scales)
+
+    Aq, As = draw(M, ca, sa)
+    Bq, Bs = draw(N, cb, sb)
+    C = None
+    if with_c:
+        C = (torch.from_numpy((rng.integers(-4, 5, (M, N)) / 4).astype(np.float32)) if values == "exact"
+             else torch.from_numpy(rng.standard_normal((M, N), dtype=np.float32)))
+    return Problem(f"e2m1_{values}_{M}x{N}x{K}", Aq, Bq, C, alpha=alpha, beta=beta, out=out,
+                   Bs=Bs, As=As, image=image)
+
+
+def e2m1_16x28672x4096() -> Problem:
+    """Both operands FP4, the decode shape: 16 activation rows, FP4 weights of
+    the MLP shape, C, alpha = 0.5, fp32 out (seed 7)."""
+    p = e2m1_problem(7, 16, 28672, 4096, with_c=True, alpha=0.5, beta=1.0)
+    p.name = "e2m1_16x28672x4096"
+    return p
+
+
+def e2m1_8192() -> Problem:
+    """Both operands FP4, M = N = K = 8192, no C, bf16 out (seed 8)."""
+    p = e2m1_problem(8, 8192, 8192, 8192, alpha=1.0, beta=0.0, out=OUT_BF16)
+    p.name = "e2m1_8192"
+    return p
+
+
 WORKLOADS = {
     "worked_16x8x32": worked_16x8x32,
     "f16_1024": f16_1024,
@@ -194,6 +271,8 @@ WORKLOADS = {
     "scatter_16384_into_65536": scatter_16384_into_65536,
     "skinny_accumulate_16x28672x4096": skinny_accumulate_16x28672x4096,
     "fp4_skinny_16x28672x4096": fp4_skinny_16x28672x4096,
+    "e2m1_16x28672x4096": e2m1_16x28672x4096,
+    "e2m1_8192": e2m1_8192,
 }
 
 

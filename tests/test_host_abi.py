@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gemm_f16", "gemm_bf16", "gemm_gather_rows", "gemm_scatter_rows",
-              "gemm_accumulate", "gemm_seeded", "gemm_bf16_e2m1", "gemm_check_device_status",
+              "gemm_accumulate", "gemm_seeded", "gemm_bf16_e2m1", "gemm_e2m1",
+              "gemm_check_device_status",
               "gemm_status_string"):
         assert n in names
 
@@ -182,6 +183,52 @@ def test_fp4_argument_checks(lib):
     assert binding.gemm_query_plan(129, 28672, 4096, fp4=True, sm_count=148).kernel != 2
 
 
+def test_e2m1_argument_checks(lib):
+    """Both operands FP4: every rule of gemm_e2m1's contract is checked before any
+    CUDA call (fake device addresses)."""
+    f = lib.gemm_e2m1
+    ok = dict(M=128, N=256, K=256, Aq=A0, ldaq=128, As=I0, ldas=128, Bq=B0, ldbq=128, Bs=C0,
+              ldbs=256, C=None, ldc=0, D=D0, ldd=256, out=0, alpha=1.0, beta=0.0, image=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["M"], a["N"], a["K"], a["Aq"], a["ldaq"], a["As"], a["ldas"], a["Bq"],
+                 a["ldbq"], a["Bs"], a["ldbs"], a["C"], a["ldc"], a["D"], a["ldd"], a["out"],
+                 a["alpha"], a["beta"], a["image"], None)
+
+    assert call(M=0) == 0 and call(N=0) == 0            # nothing to do
+    assert call(M=-1) == 1 and call(image=2) == 1 and call(out=5) == 1
+    assert call(Aq=None) == 1 and call(As=None) == 1 and call(Bs=None) == 1
+    assert call(ldaq=64) == 1 and call(ldbq=100) == 1   # shorter than K / 2 bytes
+    assert call(ldas=100) == 1 and call(ldbs=255) == 1  # scale rows shorter than M / N
+    assert call(K=48) == 3                              # not whole 32-element blocks
+    assert call(image=1, K=160, ldaq=96, ldbq=96) == 3  # the 16U4 image: K % 128
+    assert call(Aq=A0 + 8) == 2 and call(ldbq=136) == 2  # 16-byte rules of the packed form
+    assert call(image=1, Aq=A0 + 16) == 2               # the 16U4 image: 32-byte origins
+    assert call(image=1, ldaq=144) == 2                 # and 32-byte strides
+    assert call(D=A0 + 64) == 4 and call(D=I0) == 4 and call(D=C0) == 4  # D over Aq, As, Bs
+    assert call(C=D0 + 16, ldc=256, beta=1.0) == 4
+    assert call(M=1 << 31) == 3
+
+
+def test_e2m1_plan(lib):
+    """gemm_e2m1: kernel 11 for packed codes, 12 for the 16U4 image; 256-wide tiles
+    unless 128-wide ones take fewer waves; forced widths apply to it alone."""
+    p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=0, sm_count=148)
+    assert (p.kernel, p.bn, p.bm, p.grid) == (11, 256, 128, 148) and p.stages == 3
+    p = binding.gemm_query_plan(16, 28672, 4096, e2m1=1, sm_count=148)
+    assert (p.kernel, p.bn, p.tiles, p.grid) == (12, 256, 112, 112)
+    p = binding.gemm_query_plan(1024, 1024, 1024, e2m1=0, sm_count=148)
+    assert (p.bn, p.tiles) == (128, 64)  # one wave either way: the narrower, cheaper tile
+    binding.gemm_debug_force_tile(11, 128)
+    try:
+        assert binding.gemm_query_plan(8192, 8192, 8192, e2m1=0, sm_count=148).bn == 128
+        assert binding.gemm_query_plan(8192, 8192, 8192, sm_count=148).kernel == 4  # not bf16's
+    finally:
+        binding.gemm_debug_force_tile(0, 0)
+    assert binding.gemm_query_plan(0, 8, 32, e2m1=0, sm_count=148).kernel == 0
+
+
 def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bm, p.bn, p.grid) == (4, 256, 512, 148)
@@ -214,7 +261,7 @@ def test_plan_matches_the_dispatch_rules(lib):
     p = binding.gemm_query_plan(16, 28672, 4096, scatter=True, sm_count=148)
     assert p.kernel == 2
     plan = binding.Plan()
-    assert lib.gemm_query_plan(64, 64, 64, 6, 0, 148, ctypes.byref(plan)) == 1
+    assert lib.gemm_query_plan(64, 64, 64, 8, 0, 148, ctypes.byref(plan)) == 1
     p = binding.gemm_query_plan(100, 8192, 8192, sm_count=148)
     assert (p.kernel, p.bn) == (1, 64)
     # 16 < M <= 64: the tile kernel unless K is long against N
