@@ -60,6 +60,12 @@ from tensor_core_gemm_02_gb300 import binding, workloads  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 HEADLINE = "bf16_8192"
+# dense FP4 (block-scaled) / bf16 and FP8 / bf16 tensor rates: the nominal
+# ratios (4.5 and 2.25 PFLOP/s against 2.25), and the ratios one SM's tensor
+# pipe shows for one thread issuing 128 x 256 MMAs back to back (kind::mxf4 and
+# mxf4nvf4: 32768 flop per clock; kind::mxf8f6f4: 16384; kind::f16: 8192)
+FP4_NOMINAL_RATIO, FP4_MEASURED_RATIO = 6.0, 4.0
+FP8_NOMINAL_RATIO, FP8_MEASURED_RATIO = 2.0, 2.0
 # dense bf16 / f16 tcgen05 rate of one SM: a 128 x N x 16 MMA (2 * 128 * N * 16
 # flop) keeps the tensor pipe busy for N / 2 cycles
 FLOP_PER_CLK_PER_SM = 8192
@@ -236,6 +242,8 @@ def kernel_key(plan, p=None):
     profiles/traffic.json): tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, MODE>,
     MODE 0 plain, 1 scattered rows, 2 reduce-add; skinny_gemm_kernel<MP, KBOX, W4>."""
     mode = 0 if p is None else (1 if p.scatter else (2 if p.accumulate else 0))
+    if plan.kernel in (11, 12):  # FP4 operands with block scales
+        return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1, 1, 0, {plan.kernel - 10}>"
     if plan.kernel == 2:  # (FP4 stages hold four 64-wide K blocks)
         return ("skinny_gemm_kernel<{}, 4, 1>" if p is not None and p.fp4
                 else "skinny_gemm_kernel<{}, 1, 0>").format(plan.bm)
@@ -250,6 +258,10 @@ def kernel_key(plan, p=None):
 
 
 def plan_of(p, dev):
+    if p.e2m1:
+        return binding.gemm_query_plan(
+            p.M, p.N, p.K, e2m1=p.image,
+            sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
     return binding.gemm_query_plan(p.M, p.N, p.K, gather=p.idx is not None and not p.scatter,
                                    scatter=p.scatter, fp4=p.fp4,
                                    has_c=p.C is not None and p.beta != 0,
@@ -257,7 +269,11 @@ def plan_of(p, dev):
 
 
 def launch(p, dev_tensors):
-    A, B, C, idx, D = dev_tensors
+    A, B, C, idx, D = dev_tensors[:5]
+    if p.e2m1:
+        As, Bs = dev_tensors[5:]
+        return binding.gemm_e2m1(A, As, B, Bs, C, D, alpha=p.alpha, beta=p.beta, out=p.out,
+                                 image=p.image)
     if p.fp4:
         return binding.gemm_bf16_e2m1(A, B, idx, C, D, alpha=p.alpha, beta=p.beta, out=p.out)
     if p.accumulate:
@@ -285,6 +301,8 @@ def to_device(p, dev):
              torch.zeros((p.d_rows, p.N), dtype=workloads.OUT_TORCH[p.out], device=dev))
     else:
         D = torch.empty((p.M, p.N), dtype=workloads.OUT_TORCH[p.out], device=dev)
+    if p.e2m1:
+        return A, B, C, idx, D, p.As.to(dev), p.Bs.to(dev)
     return A, B, C, idx, D
 
 
@@ -292,6 +310,11 @@ def algorithmic_bytes(p):
     """Bytes the GEMM must move at least once: A (or the gathered rows), B, C, D, idx
     (scattered form: the M rows of C read and of D written; accumulating form: D
     read and written)."""
+    if p.e2m1:  # codes and scales of both operands
+        a = p.M * p.K // 2 + p.As.numel()
+        b = p.N * p.K // 2 + p.Bs.numel()
+        c = p.M * p.N * 4 if (p.C is not None and p.beta != 0) else 0
+        return a + b + c + p.M * p.N * workloads.OUT_TORCH[p.out].itemsize
     esz = p.A.element_size()
     a = p.M * p.K * esz
     b = p.N * p.K * esz if not p.fp4 else p.N * p.K // 2 + p.Bs.numel()  # FP4: codes + scales
@@ -420,15 +443,6 @@ def time_e2e(p, dev, steps):
     h2d = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size()
     d2h = D_h[0].numel() * D_h[0].element_size()
     return ms, h2d, d2h
-
-
-def input_bytes(p):
-    """Bytes of input the GEMM reads (the gathered form: the rows it gathers)."""
-    gathered = p.idx is not None and not p.scatter
-    a = (int(torch.unique(p.idx).numel()) if gathered else p.M) * p.K * p.A.element_size()
-    b = p.N * p.K * p.B.element_size() if not p.fp4 else p.N * p.K // 2 + p.Bs.numel()
-    c = p.M * p.N * 4 if (p.C is not None and p.beta != 0) else 0
-    return a + b + c
 
 
 def set_bytes(tensors):
@@ -586,16 +600,26 @@ def run_ours(args):
         variants = {}
         for name in ("f16_1024", "mlp_8192x28672x4096", "skinny_16x28672x4096",
                      "gather_16384_of_65536", "scatter_16384_into_65536",
-                     "skinny_accumulate_16x28672x4096", "fp4_skinny_16x28672x4096"):
+                     "skinny_accumulate_16x28672x4096", "fp4_skinny_16x28672x4096",
+                     "e2m1_16x28672x4096", "e2m1_8192"):
             vp, ms, plan, how = time_variant(name, dev, args.variant_reps)
             tflops = vp.flops / (ms * 1e-3) / 1e12
             gbs = algorithmic_bytes(vp) / (ms * 1e-3) / 1e9
             hbm_bound = name in ("skinny_16x28672x4096", "skinny_accumulate_16x28672x4096",
-                                 "fp4_skinny_16x28672x4096")
+                                 "fp4_skinny_16x28672x4096", "e2m1_16x28672x4096")
+            # the tensor peak of the variant's operand kind (FP4: block-scaled MMAs)
+            if vp.e2m1:
+                nominal = FP4_NOMINAL_RATIO if vp.image == 0 else FP8_NOMINAL_RATIO
+                measured = FP4_MEASURED_RATIO if vp.image == 0 else FP8_MEASURED_RATIO
+            else:
+                nominal = measured = 1.0
+            t_peak = peaks["bf16_tflops"] * nominal
             variants[name] = {
                 "ms": round(ms, 5), "TFLOP/s": round(tflops, 2), "GB/s": round(gbs, 1),
                 "algorithmic_bytes": algorithmic_bytes(vp),
                 "kernel": {1: "tile (single CTA)", 2: "skinny (swap-AB, stream-K)",
+                           11: "tile (single CTA, FP4 block-scaled, kind::mxf4)",
+                           12: "tile (single CTA, FP4 block-scaled, kind::mxf8f6f4)",
                            3: "tile (CTA pair)", 4: "tile (CTA pair, two N halves)",
                            5: "tile (4-CTA cluster, A multicast)",
                            6: "tile (8-CTA cluster, A multicast)",
@@ -607,8 +631,14 @@ def run_ours(args):
                                    "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
                                   if hbm_bound else
                                   {"bound": "tensor", "achieved": round(tflops, 2),
-                                   "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                                   "frac": round(tflops / peaks["bf16_tflops"], 4)}),
+                                   "peak": round(t_peak, 1), "unit": "TFLOP/s",
+                                   "frac": round(tflops / t_peak, 4),
+                                   **({"peak_source": f"measured bf16 x {nominal:g} (nominal "
+                                                      f"ratio); x {measured:g} (per-SM MMA rate "
+                                                      f"measured): {peaks['bf16_tflops'] * measured:.1f}",
+                                       "frac_of_measured_mma_rate":
+                                           round(tflops / (peaks["bf16_tflops"] * measured), 4)}
+                                      if vp.e2m1 else {})}),
                                  traffic=stored_traffic(f"{kernel_key(plan, vp)}@{name}"),
                                  kernel=kernel_key(plan, vp)),
                 "timing": how,

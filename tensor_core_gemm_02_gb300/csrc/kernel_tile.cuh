@@ -597,9 +597,12 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
         // ------------------------------------------------------------ scale warp
         // For every stage: wait for its loads, rearrange the scale rows as loaded
         // (row b of the stage: one byte per row of A, then of B) into 512-byte
-        // tiles -- lane l writes 16 bytes, rows l, l + 32, l + 64, l + 96 of the
-        // tile, four 32-element blocks each -- and hand them to the MMA thread
-        // (tcgen05.cp reads them through the async proxy, hence the fence).
+        // tiles (row l + 32 q, block b at byte 16 l + 4 q + b) and hand them to
+        // the MMA thread (tcgen05.cp reads them through the async proxy, hence
+        // the fence).  Per tile, lane l loads the 32-bit words of rows 4l .. 4l+3
+        // for its four blocks, transposes the 4 x 4 bytes so that each word
+        // holds one row's four blocks, and stores row r's word at 16 (r % 32) +
+        // 4 (r / 32).
         if constexpr (MX != 0) {
             int s = 0;
             uint32_t ph = 0;
@@ -611,25 +614,34 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
                         alive = false;
                         break;
                     }
-                    const uint32_t src = base + Cfg::OFF_SFS + s * Cfg::SF_STAGE_BYTES;
-                    const uint32_t dst = base + Cfg::OFF_SFC + s * Cfg::SF_CP_BYTES;
+                    const uint8_t *src = gbase + Cfg::OFF_SFS + s * Cfg::SF_STAGE_BYTES;
+                    uint8_t *dst = gbase + Cfg::OFF_SFC + s * Cfg::SF_CP_BYTES;
+                    uint32_t w[Cfg::SF_TILES][4];
 #pragma unroll
                     for (int ti = 0; ti < Cfg::SF_TILES; ++ti) {
                         const bool a_tile = ti < Cfg::SF_CHUNKS;
                         const int c = a_tile ? ti : (ti - Cfg::SF_CHUNKS) / Cfg::SF_B_ROWTILES;
                         const int rt = a_tile ? 0 : (ti - Cfg::SF_CHUNKS) % Cfg::SF_B_ROWTILES;
                         const uint32_t pitch = a_tile ? Cfg::BM : Cfg::TILE_N;
-                        const uint32_t rows = src + (a_tile ? 0u : Cfg::SF_KB * Cfg::BM) + 128u * rt +
-                                              4u * c * pitch + lane;
-                        uint32_t w[4];
+                        const uint8_t *rows = src + (a_tile ? 0u : Cfg::SF_KB * Cfg::BM) + 128u * rt +
+                                              4u * c * pitch + 4u * lane;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            w[q] = 0u;
+                        for (int b = 0; b < 4; ++b)
+                            w[ti][b] = *reinterpret_cast<const uint32_t *>(rows + b * pitch);
+                    }
 #pragma unroll
-                            for (int b = 0; b < 4; ++b)
-                                w[q] |= ld_shared_u8(rows + b * pitch + 32u * q) << (8 * b);
-                        }
-                        st_shared_v4(dst + 512u * ti + 16u * lane, w[0], w[1], w[2], w[3]);
+                    for (int ti = 0; ti < Cfg::SF_TILES; ++ti) {
+                        // w[b] byte i = block b of row 4 lane + i  ->  o[i] byte b
+                        const uint32_t t0 = __byte_perm(w[ti][0], w[ti][1], 0x5140);
+                        const uint32_t t1 = __byte_perm(w[ti][0], w[ti][1], 0x7362);
+                        const uint32_t t2 = __byte_perm(w[ti][2], w[ti][3], 0x5140);
+                        const uint32_t t3 = __byte_perm(w[ti][2], w[ti][3], 0x7362);
+                        const uint32_t o[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
+                                               __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
+                        uint8_t *tile = dst + 512u * ti + 4u * (lane / 8u);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            *reinterpret_cast<uint32_t *>(tile + 16u * ((4u * lane + i) % 32u)) = o[i];
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
