@@ -737,8 +737,8 @@ void forced_tile(int *kernel, int *bn)
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || fk == 11 || fk == 12 || plan.kernel == 0 || p.w4)
-        return plan;  // (FP4 weights run only on their own paths; 11 / 12 are FP4 x FP4 forms)
+    if (fk == 0 || (fk >= 11 && fk <= 14) || plan.kernel == 0 || p.w4)
+        return plan;  // (FP4 weights run only on their own paths; 11-14 are FP4 x FP4 forms)
     if (fk == 10) {
         set_tiny_plan(plan, p.M, p.N);  // the warp-level kernel runs every problem
         return plan;
@@ -1144,7 +1144,8 @@ gemm_status gemm_debug_force_tile(int kernel, int bn)
                     (kernel == 5 && (bn == 64 || bn == 256)) || (kernel == 6 && bn == 256) ||
                     (kernel == 7 && bn == 512) || (kernel == 8 && bn == 256) ||
                     (kernel == 9 && bn == 512) || (kernel == 10 && bn == 8) ||
-                    ((kernel == 11 || kernel == 12) && (bn == 128 || bn == 256));
+                    ((kernel == 11 || kernel == 12) && (bn == 128 || bn == 256)) ||
+                    ((kernel == 13 || kernel == 14) && bn == 256);
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

@@ -17,6 +17,15 @@
 
 #include "host_internal.h"
 
+// Whether the automatic plan picks CTA pairs for FP4 operands.  Measured
+// (8192^3, packed codes): pairs 450 us, single CTAs 291 us -- the pairs' scale
+// path (each CTA's scale warp, the peer's arrival at the leader, the copies
+// into both CTAs' tensor memory) holds every stage back -- so single CTAs
+// (0); pairs stay available to gemm_debug_force_tile.
+#ifndef TCG_MX_AUTO_PAIRS
+#define TCG_MX_AUTO_PAIRS 0
+#endif
+
 namespace tcg {
 namespace host {
 
@@ -136,8 +145,16 @@ gemm_status run_e2m1(const E2m1Problem &p)
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
     const gemm_plan plan = e2m1_plan(p.M, p.N, p.K, p.image, dev->sm_count);
-    const int mx = plan.kernel == 11 ? 1 : 2;
+    const int mx = (plan.kernel == 11 || plan.kernel == 13) ? 1 : 2;
+    const bool pair = plan.kernel >= 13;
     const int bn = plan.bn;
+    int grid = plan.grid;
+    if (pair) {
+        // never more pairs than can be resident together
+        const int resident = tcg::tile_max_pairs_or(mx, dev->sm_count / 2);
+        const int64_t pairs = plan.tiles < resident ? plan.tiles : resident;
+        grid = static_cast<int>(2 * pairs);
+    }
     const bool c_used = p.C != nullptr && p.beta != 0.0f;
 
     GemmMaps maps;
@@ -158,8 +175,8 @@ gemm_status run_e2m1(const E2m1Problem &p)
         const uint64_t inner = mx == 1 ? static_cast<uint64_t>(p.K / 2) : static_cast<uint64_t>(p.K);
         const uint32_t sf_rows = static_cast<uint32_t>(kstage / 32);
         if (!encode_2d(&maps.a, code_t, p.Aq, inner, p.M, p.ldaq, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&maps.b, code_t, p.Bq, inner, p.N, p.ldbq, 128, static_cast<uint32_t>(bn),
-                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&maps.b, code_t, p.Bq, inner, p.N, p.ldbq, 128,
+                       static_cast<uint32_t>(pair ? bn / 2 : bn), CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, as, p.M, p.K / 32, ldas, 128, sf_rows,
                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
             !encode_2d(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bs, p.N, p.K / 32, ldbs,
@@ -196,7 +213,7 @@ gemm_status run_e2m1(const E2m1Problem &p)
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     fill_common(a, q, dev);
-    a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, 128));
+    a.num_m_blocks = static_cast<int32_t>(ceil_div(p.M, pair ? 256 : 128));
     a.num_n_blocks = static_cast<int32_t>(ceil_div(p.N, bn));
     a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, kstage));
     a.num_tiles = a.num_m_blocks * a.num_n_blocks;
@@ -205,14 +222,18 @@ gemm_status run_e2m1(const E2m1Problem &p)
     a.c_tma = c_tma ? 1 : 0;
     a.d_tma = d_tma ? 1 : 0;
     a.d_tail_direct = (p.N * out_size(p.out)) % 16 != 0 ? 1 : 0;
-    const cudaError_t e = tcg::launch_tile_mx(mx, bn, maps, a, plan.grid, p.stream);
+    const cudaError_t e = tcg::launch_tile_mx(mx, bn, pair, maps, a, grid, p.stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 }  // namespace
 
-// Tile width: the one with fewer waves of 128 x bn tiles over the SMs (cost
-// waves x (bn + 32), as for the other single-CTA forms), 256 on a tie.
+// Form: CTA pairs with 256 x 256 tiles (each SM moves 2/3 of the operand bytes
+// per MMA that a single CTA with a 128 x 256 tile moves, which FP4 operands,
+// four times the MMA rate of 16-bit ones on the same bytes, need) when M > 128
+// and there are at least as many pair tiles as half the pairs; otherwise single
+// CTAs, 128 x bn with the width that takes fewer waves (cost waves x (bn + 32),
+// as for the other single-CTA forms), 256 on a tie.  A forced form applies.
 gemm_plan e2m1_plan(int64_t M, int64_t N, int64_t K, int image, int sm_count)
 {
     gemm_plan p;
@@ -221,23 +242,31 @@ gemm_plan e2m1_plan(int64_t M, int64_t N, int64_t K, int image, int sm_count)
         return p;
     int fk = 0, fbn = 0;
     forced_tile(&fk, &fbn);
+    const int mx = image == 0 ? 1 : 2;
+    const int pairs = sm_count / 2;
+    bool pair = false;
     int bn = 256;
-    if (fk == 11 || fk == 12) {
+    if (fk >= 11 && fk <= 14) {
+        pair = fk >= 13;
         bn = fbn;
     } else {
-        const int64_t w256 = ceil_div(ceil_div(M, 128) * ceil_div(N, 256), sm_count);
-        const int64_t w128 = ceil_div(ceil_div(M, 128) * ceil_div(N, 128), sm_count);
-        if (w128 * (128 + 32) < w256 * (256 + 32))
-            bn = 128;
+        const int64_t pair_tiles = ceil_div(M, 256) * ceil_div(N, 256);
+        pair = TCG_MX_AUTO_PAIRS && M > 128 && pairs > 0 && 2 * pair_tiles >= pairs;
+        if (!pair) {
+            const int64_t w256 = ceil_div(ceil_div(M, 128) * ceil_div(N, 256), sm_count);
+            const int64_t w128 = ceil_div(ceil_div(M, 128) * ceil_div(N, 128), sm_count);
+            if (w128 * (128 + 32) < w256 * (256 + 32))
+                bn = 128;
+        }
     }
-    const int mx = image == 0 ? 1 : 2;
-    p.kernel = image == 0 ? 11 : 12;
-    p.bm = 128;
+    p.kernel = (image == 0 ? 11 : 12) + (pair ? 2 : 0);
+    p.bm = pair ? 256 : 128;
     p.bn = bn;
-    p.stages = tcg::tile_mx_stages(mx, bn);
-    p.tiles = ceil_div(M, 128) * ceil_div(N, bn);
+    p.stages = tcg::tile_mx_stages(mx, bn, pair);
+    p.tiles = ceil_div(M, p.bm) * ceil_div(N, bn);
     p.splits = 1;
-    p.grid = static_cast<int32_t>(p.tiles < sm_count ? p.tiles : sm_count);
+    const int64_t sets = pair ? pairs : sm_count;
+    p.grid = static_cast<int32_t>((pair ? 2 : 1) * (p.tiles < sets ? p.tiles : sets));
     (void)K;
     return p;
 }

@@ -110,6 +110,30 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     return wait_bounded_loop(bar, parity, abort_flag, status, timeout_ns, where);
 }
 
+// As wait_bounded, with the barrier read as an acquire at cluster scope (for
+// phases that the other CTA of a pair completes after writing its shared memory).
+static __device__ __noinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                         volatile uint32_t *abort_flag, uint32_t *status,
+                                                         uint64_t timeout_ns, uint32_t where)
+{
+    if (mbar_test_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test_cluster(bar, parity))
+            return true;
+        if ((it & 63u) == 0u) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1u;
+                record_error(status, kStatusTimeout, where);
+                return false;
+            }
+        }
+    }
+}
+
 // Teardown after an abort: wait (bounded, ignoring the abort flag) for copies
 // this thread issued to land before the CTA releases its shared memory.
 static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)

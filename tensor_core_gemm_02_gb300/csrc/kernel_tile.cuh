@@ -58,7 +58,8 @@ struct TileCfg {
     // packed two per byte (kind::mxf4); 2 = FP4 codes in the 16U4_ALIGN16B TMA
     // image, sixteen codes in the low 8 bytes of each 16-byte block
     // (kind::mxf8f6f4).  The FP4 kinds carry UE8M0 block scales (one per 32
-    // elements along K) through shared memory into TMEM.  Single CTAs only.
+    // elements along K) through shared memory into TMEM.  Single CTAs, or CTA
+    // pairs (each CTA holds the scales of its own rows of A and of all of B's).
     static constexpr int MX = MX_;
     // MC > 1: MC CTAs (or MC pairs) work on MC neighbouring tiles of one
     // block row; each loads 1/MC of the shared A box and multicasts it to the
@@ -104,11 +105,11 @@ struct TileCfg {
     static constexpr uint32_t SF_STAGE_BYTES = SF_KB * (BM + TILE_N);
     static constexpr uint32_t SF_CP_BYTES = SF_TILES * 512;
     static constexpr uint32_t SF_COLS = SF_TILES * 4;  // TMEM columns per stage
-    // bytes the stage barrier expects: codes in the 16U4 image count their
-    // payload, not the padding ("cp.async.bulk.tensor" page, section
-    // "Interleave and packed FP4")
-    static constexpr uint32_t STAGE_TX =
-        (MX == 2 ? STAGE_BYTES / 2 : STAGE_BYTES) + SF_STAGE_BYTES;
+    // bytes one CTA's code loads report per stage: codes in the 16U4 image count
+    // their payload, not the padding ("cp.async.bulk.tensor" page, section
+    // "Interleave and packed FP4"); the scale rows complete on a barrier of
+    // their own (SF_STAGE_BYTES)
+    static constexpr uint32_t STAGE_TX = MX == 2 ? STAGE_BYTES / 2 : STAGE_BYTES;
     static constexpr uint32_t EPI_BUF = 32 * 128;  // 32 rows x 128 B
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = STAGES * A_BYTES;
@@ -116,7 +117,7 @@ struct TileCfg {
     static constexpr uint32_t OFF_SFC = OFF_SFS + STAGES * SF_STAGE_BYTES;  // rearranged
     static constexpr uint32_t OFF_EPI = OFF_SFC + STAGES * SF_CP_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_EPI + 8 * EPI_BUF;  // 4 warps x 2 buffers
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 8 + (MX ? STAGES : 0);
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 8 + (MX ? 2 * STAGES : 0);
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base
@@ -141,8 +142,8 @@ struct TileCfg {
     static_assert(!PAIR || (BN % 32 == 0 && BN_LOCAL % 8 == 0), "pair splits B in 8-row groups");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
-    static_assert(MX == 0 || (!PAIR && MC == 1 && NSUB == 1 && (BN == 128 || BN == 256)),
-                  "FP4 operands: single CTAs, tiles 128 or 256 wide");
+    static_assert(MX == 0 || (MC == 1 && NSUB == 1 && (BN == 256 || (BN == 128 && !PAIR))),
+                  "FP4 operands: single CTAs with tiles 128 or 256 wide, or pairs with 256 x 256 tiles");
     static_assert(MX == 0 || SF_COL0 + STAGES * SF_COLS <= 512, "TMEM for the block scales");
 };
 
@@ -191,8 +192,10 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     auto c_bar = [&](int q, int j) { return bar0 + 8u * (2 * STAGES + 4 + 2 * q + j); };
-    // (FP4) stage s's scales are rearranged for tcgen05.cp
-    auto sf_bar = [&](int st) { return bar0 + 8u * (2 * STAGES + 12 + st); };
+    // (FP4) stage s's scale rows have landed in this CTA / have been rearranged
+    // for tcgen05.cp (in the leader: by the scale warps of both CTAs of a pair)
+    auto sf_full_bar = [&](int st) { return bar0 + 8u * (2 * STAGES + 12 + st); };
+    auto sf_bar = [&](int st) { return bar0 + 8u * (3 * STAGES + 12 + st); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
 
@@ -233,8 +236,10 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
             for (int j = 0; j < 2; ++j)
                 mbar_init(c_bar(q, j), 1);
         if (MX)
-            for (int st = 0; st < STAGES; ++st)
-                mbar_init(sf_bar(st), 1);
+            for (int st = 0; st < STAGES; ++st) {
+                mbar_init(sf_full_bar(st), 1);
+                mbar_init(sf_bar(st), PAIR ? 2 : 1);
+            }
         *abort_flag = 0u;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -323,22 +328,21 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
                 }
                 first = false;
                 __syncwarp();
-                const int32_t k0 = kb * Cfg::BK;
+                // inner coordinate: K elements (16-bit codes and the 16U4 image) or
+                // bytes (packed FP4 codes); FP4 rows of a stage are 128 of either
+                const int32_t k0 = MX ? kb * 128 : kb * Cfg::BK;
                 const uint32_t sa = base + Cfg::OFF_A + s * Cfg::A_BYTES;
                 const uint32_t sb = base + Cfg::OFF_B + s * Cfg::B_BYTES;
-                if constexpr (MX != 0) {
-                    // FP4: the codes of A and B (128-byte rows: x is K / 2 bytes for
-                    // packed codes, K elements for the 16U4 image, kb * 128 either
-                    // way), and the stage's SF_KB rows of A's and B's block scales
-                    if (lane == 0) {
-                        const uint32_t sfs = base + Cfg::OFF_SFS + s * Cfg::SF_STAGE_BYTES;
-                        tma_load_2d(sa, &tmA, full_bar(s), kb * 128, m0);
-                        tma_load_2d(sb, &tmB, full_bar(s), kb * 128, nb0);
-                        tma_load_2d(sfs, &tmSFA, full_bar(s), m0, kb * Cfg::SF_KB);
-                        tma_load_2d(sfs + Cfg::SF_KB * Cfg::BM, &tmSFB, full_bar(s), nb0,
-                                    kb * Cfg::SF_KB);
-                    }
-                } else if (PAIR) {
+                if (MX && lane == 0) {
+                    // FP4: the stage's SF_KB rows of block scales, this CTA's rows of A
+                    // and all of the tile's rows of B, on this CTA's own barrier
+                    const uint32_t sfs = base + Cfg::OFF_SFS + s * Cfg::SF_STAGE_BYTES;
+                    mbar_arrive_expect_tx(sf_full_bar(s), Cfg::SF_STAGE_BYTES);
+                    tma_load_2d(sfs, &tmSFA, sf_full_bar(s), m0, kb * Cfg::SF_KB);
+                    tma_load_2d(sfs + Cfg::SF_KB * Cfg::BM, &tmSFB, sf_full_bar(s), nb * TILE_N,
+                                kb * Cfg::SF_KB);
+                }
+                if (PAIR) {
                     const uint32_t fb = lead(full_bar(s));
                     if (MC > 1) {
                         if (args.gather) {
@@ -400,6 +404,18 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
                 wait_drain(full_bar(ds), dph, 10000000ull);
             }
         }
+        if (MX && !alive && lane == 0) {
+            // (FP4) each CTA's scale rows land on its own barriers: drain those too
+            int ds = s;
+            uint32_t dph = ph;
+            for (int i = 0; i < pending; ++i) {
+                if (--ds < 0) {
+                    ds = STAGES - 1;
+                    dph ^= 1u;
+                }
+                wait_drain(sf_full_bar(ds), dph, 10000000ull);
+            }
+        }
     } else if (warp == 1 || (Cfg::ISS == 2 && warp == 6)) {
         // ------------------------------------------------------------ MMA issuers
         const int e = warp == 1 ? 0 : 1;  // issuer e takes the K blocks kb = e (mod kIss)
@@ -427,19 +443,27 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
                     const uint32_t sfc = base + Cfg::OFF_SFC + st * Cfg::SF_CP_BYTES;
                     const uint32_t sfcol = tmem_base + Cfg::SF_COL0 + st * Cfg::SF_COLS;
 #pragma unroll
-                    for (int ti = 0; ti < Cfg::SF_TILES; ++ti)
-                        tc_cp_32x128b_warpx4(sfcol + 4u * ti, sdesc_rows16(sfc + 512u * ti));
+                    for (int ti = 0; ti < Cfg::SF_TILES; ++ti) {
+                        if (PAIR)
+                            tc_cp_32x128b_warpx4_pair(sfcol + 4u * ti, sdesc_rows16(sfc + 512u * ti));
+                        else
+                            tc_cp_32x128b_warpx4(sfcol + 4u * ti, sdesc_rows16(sfc + 512u * ti));
+                    }
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         constexpr uint32_t kFmt = MX == 1 ? 1u : 5u;  // E2M1 in each kind's coding
                         const uint32_t chunk = (k * Cfg::MMA_K) / 128;
                         const uint32_t sfid = ((k * Cfg::MMA_K) % 128) / 32;
-                        const uint32_t id = idesc_mx(kFmt, 128, BN, sfid, sfid);
+                        const uint32_t id = idesc_mx(kFmt, Cfg::TILE_M, BN, sfid, sfid);
                         const uint32_t sfa = sfcol + 4u * chunk;
                         const uint32_t sfb = sfcol + 4u * Cfg::SF_CHUNKS + 4u * Cfg::SF_B_ROWTILES * chunk;
                         const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-                        if (MX == 1)
+                        if (MX == 1 && PAIR)
+                            tc_mma_mxf4_pair(dj, ad + 2u * k, bd + 2u * k, id, sfa, sfb, acc);
+                        else if (MX == 1)
                             tc_mma_mxf4(dj, ad + 2u * k, bd + 2u * k, id, sfa, sfb, acc);
+                        else if (PAIR)
+                            tc_mma_mxf8f6f4_pair(dj, ad + 2u * k, bd + 2u * k, id, sfa, sfb, acc);
                         else
                             tc_mma_mxf8f6f4(dj, ad + 2u * k, bd + 2u * k, id, sfa, sfb, acc);
                     }
@@ -478,9 +502,13 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
                 if (!wait_bounded<true>(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
                                   kWhereMmaFull))
                     return false;
-                // (FP4: and for the scale warp to have rearranged the stage's scales)
-                if (MX && !wait_bounded<true>(sf_bar(s), ph, abort_flag, args.status,
-                                              args.timeout_ns, kWhereMmaFull))
+                // (FP4: and for the scale warp(s) to have rearranged the stage's
+                // scales; a pair's peer wrote its own, hence the cluster scope)
+                if (MX && !(PAIR ? (mbar_probe_cluster(sf_bar(s), ph) ||
+                                    wait_bounded_cluster(sf_bar(s), ph, abort_flag, args.status,
+                                                         args.timeout_ns, kWhereMmaFull))
+                                 : wait_bounded<true>(sf_bar(s), ph, abort_flag, args.status,
+                                                      args.timeout_ns, kWhereMmaFull)))
                     return false;
                 tc_fence_after_sync();
                 st = s;
@@ -609,7 +637,7 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
             bool alive = true;
             for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
                 for (int32_t kb = 0; kb < args.num_k_blocks; ++kb) {
-                    if (!warp_wait_bounded<true>(full_bar(s), ph, abort_flag, args.status,
+                    if (!warp_wait_bounded<true>(sf_full_bar(s), ph, abort_flag, args.status,
                                                  args.timeout_ns, kWhereMmaFull)) {
                         alive = false;
                         break;
@@ -645,8 +673,12 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(sf_bar(s));
+                    if (lane == 0) {
+                        if (PAIR && !leader)
+                            mbar_arrive_cluster(lead(sf_bar(s)));
+                        else
+                            mbar_arrive(sf_bar(s));
+                    }
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;

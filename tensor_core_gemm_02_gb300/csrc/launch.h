@@ -41,15 +41,23 @@ cudaError_t launch_tile(int mode, int bn, bool pair, int nsub, int mc, const Gem
                         const GemmArgs &args, int grid, cudaStream_t stream);
 
 // The tile kernel with FP4 E2M1 operands and UE8M0 block scales (plain
-// epilogue, single CTAs, 128 x bn tiles, bn 128 or 256).  mx 1: codes packed
-// two per byte, kind::mxf4; mx 2: codes in the 16U4_ALIGN16B image,
-// kind::mxf8f6f4.  maps.a / maps.b: the codes (128-byte boxes of 128 / bn
-// rows, 128-byte swizzle); maps.sfa / maps.sfb: the scales (uint8 boxes of
-// 128 / bn columns by K_stage / 32 rows).  tile_mx_kstage: K elements per stage.
-int tile_mx_stages(int mx, int bn);
+// epilogue): single CTAs with 128 x bn tiles (bn 128 or 256), or CTA pairs with
+// 256 x 256 tiles (pair = true, bn 256).  mx 1: codes packed two per byte,
+// kind::mxf4; mx 2: codes in the 16U4_ALIGN16B image, kind::mxf8f6f4.
+// maps.a / maps.b: the codes (128-byte boxes of 128 / bn rows -- pairs: bn / 2
+// -- with 128-byte swizzle); maps.sfa / maps.sfb: the scales (uint8 boxes of
+// 128 / bn columns by K_stage / 32 rows).  tile_mx_kstage: K elements per
+// stage; tile_mx_max_pairs: pairs that can be resident at once (0 if unknown).
+int tile_mx_stages(int mx, int bn, bool pair);
 int tile_mx_kstage(int mx);
-cudaError_t launch_tile_mx(int mx, int bn, const GemmMaps &maps, const GemmArgs &args, int grid,
-                           cudaStream_t stream);
+int tile_mx_max_pairs(int mx);
+inline int tile_max_pairs_or(int mx, int fallback)
+{
+    const int r = tile_mx_max_pairs(mx);
+    return r > 0 ? r : fallback;
+}
+cudaError_t launch_tile_mx(int mx, int bn, bool pair, const GemmMaps &maps, const GemmArgs &args,
+                           int grid, cudaStream_t stream);
 
 // Warp-level tiny-GEMM kernel: one 16 x 8 block of D per warp.
 int tiny_warps_per_cta();

@@ -6,7 +6,7 @@ float32, whatever order the tensor cores add them in: those results compare
 bit for bit (16-bit outputs: the float32 value rounded once).  Random codes
 and scales compare within the parity tolerance.  Every kernel form runs:
 packed codes (MMA kind::mxf4) and the 16U4_ALIGN16B image (kind::mxf8f6f4),
-tiles 128 and 256 wide.
+single CTAs with tiles 128 and 256 wide and CTA pairs with 256 x 256 tiles.
 """
 import numpy as np
 import pytest
@@ -19,8 +19,8 @@ from tensor_core_gemm_02_gb300.workloads import OUT_BF16, OUT_F16, OUT_F32
 
 pytestmark = pytest.mark.gpu
 
-FORMS = [(11, 256), (11, 128), (12, 256), (12, 128)]
-FORM_IDS = ["packed256", "packed128", "align16b256", "align16b128"]
+FORMS = [(11, 256), (11, 128), (12, 256), (12, 128), (13, 256), (14, 256)]
+FORM_IDS = ["packed256", "packed128", "align16b256", "align16b128", "packed_pair", "align16b_pair"]
 
 
 @pytest.fixture(autouse=True)
@@ -51,7 +51,7 @@ CASES = [(OUT_F32, True, 0.5, 2.0), (OUT_BF16, False, 2.0, 0.0), (OUT_F16, True,
 def test_exact_every_form_bit_exact(form, M, N, K):
     """Ragged shapes over several tiles, K over several stages and partial ones."""
     binding.gemm_debug_force_tile(*form)
-    image = 0 if form[0] == 11 else 1
+    image = 0 if form[0] in (11, 13) else 1
     for out, with_c, alpha, beta in CASES:
         p = workloads.e2m1_problem(M + 3 * N + K + out, M, N, K, values="exact", with_c=with_c,
                                    alpha=alpha, beta=beta, out=out, image=image)
@@ -59,7 +59,7 @@ def test_exact_every_form_bit_exact(form, M, N, K):
         assert_bits(run_e2m1(p), ref, out, f"form {form} {M}x{N}x{K} out={out}")
 
 
-@pytest.mark.parametrize("form", FORMS[:2], ids=FORM_IDS[:2])
+@pytest.mark.parametrize("form", [FORMS[0], FORMS[1], FORMS[4]], ids=[FORM_IDS[0], FORM_IDS[1], FORM_IDS[4]])
 @pytest.mark.parametrize("K", [32, 96, 160, 288])
 def test_packed_k_not_a_multiple_of_128(form, K):
     """Packed codes take any whole number of 32-element blocks: the last stage's
@@ -79,6 +79,26 @@ def test_decode_shape_full_exact(image):
     assert_bits(run_e2m1(p), ref, OUT_F32, f"decode shape image={image}")
 
 
+@pytest.mark.parametrize("form", FORMS, ids=FORM_IDS)
+def test_timeout_reports_and_recovers(form):
+    """A stage that never completes (the test hook adds bytes to its expected
+    count): the wait runs out, the status says so, nothing hangs, and the next
+    call is exact."""
+    binding.gemm_debug_force_tile(*form)
+    p = workloads.e2m1_problem(21, 512, 512, 512, values="exact",
+                               image=0 if form[0] in (11, 13) else 1)
+    binding.gemm_set_wait_timeout(50_000_000)
+    binding.gemm_debug_inject(1)
+    try:
+        run_e2m1(p)
+        assert device_status() == binding.GEMM_ERR_TIMEOUT
+    finally:
+        binding.gemm_debug_inject(0)
+        binding.gemm_set_wait_timeout(0)
+    ref, _ = oracle_e2m1(p)
+    assert_bits(run_e2m1(p), ref, OUT_F32, "after timeout")
+
+
 @pytest.mark.parametrize("image", [0, 1])
 def test_1024_cubed_full_exact(image):
     """A multiple of 128 rows: 1024^3, exact inputs, bf16 out, every element."""
@@ -93,7 +113,7 @@ def test_random_within_tolerance(form):
     """Every code and scales of the workloads' ranges: within the parity tolerance."""
     binding.gemm_debug_force_tile(*form)
     p = workloads.e2m1_problem(90, 384, 1000, 2048, with_c=True, alpha=0.5, beta=1.0,
-                               image=0 if form[0] == 11 else 1)
+                               image=0 if form[0] in (11, 13) else 1)
     ref, absprod = oracle_e2m1(p)
     assert_within(run_e2m1(p), ref, absprod, OUT_F32, f"form {form}")
 

@@ -212,18 +212,33 @@ def test_e2m1_argument_checks(lib):
 
 
 def test_e2m1_plan(lib):
-    """gemm_e2m1: kernel 11 for packed codes, 12 for the 16U4 image; 256-wide tiles
-    unless 128-wide ones take fewer waves; forced widths apply to it alone."""
+    """gemm_e2m1: single CTAs (11 packed codes, 12 the 16U4 image), 256 wide unless
+    128-wide tiles take fewer waves; CTA pairs with 256 x 256 tiles (13 / 14) when
+    forced; forced forms apply to gemm_e2m1 alone."""
     p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=0, sm_count=148)
-    assert (p.kernel, p.bn, p.bm, p.grid) == (11, 256, 128, 148) and p.stages == 3
+    assert (p.kernel, p.bn, p.bm, p.grid, p.stages) == (11, 256, 128, 148, 3)
+    p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=1, sm_count=148)
+    assert (p.kernel, p.bm) == (12, 128)
+    binding.gemm_debug_force_tile(13, 256)
+    try:
+        p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=0, sm_count=148)
+        assert (p.kernel, p.bn, p.bm, p.grid, p.stages) == (13, 256, 256, 148, 5)
+    finally:
+        binding.gemm_debug_force_tile(0, 0)
     p = binding.gemm_query_plan(16, 28672, 4096, e2m1=1, sm_count=148)
     assert (p.kernel, p.bn, p.tiles, p.grid) == (12, 256, 112, 112)
     p = binding.gemm_query_plan(1024, 1024, 1024, e2m1=0, sm_count=148)
-    assert (p.bn, p.tiles) == (128, 64)  # one wave either way: the narrower, cheaper tile
+    assert (p.kernel, p.bn, p.tiles) == (11, 128, 64)  # 16 pair tiles: single CTAs, narrower
     binding.gemm_debug_force_tile(11, 128)
     try:
         assert binding.gemm_query_plan(8192, 8192, 8192, e2m1=0, sm_count=148).bn == 128
         assert binding.gemm_query_plan(8192, 8192, 8192, sm_count=148).kernel == 4  # not bf16's
+    finally:
+        binding.gemm_debug_force_tile(0, 0)
+    binding.gemm_debug_force_tile(14, 256)
+    try:
+        p = binding.gemm_query_plan(300, 200, 256, e2m1=1, sm_count=148)
+        assert (p.kernel, p.bm, p.tiles, p.grid) == (14, 256, 2, 4)
     finally:
         binding.gemm_debug_force_tile(0, 0)
     assert binding.gemm_query_plan(0, 8, 32, e2m1=0, sm_count=148).kernel == 0
