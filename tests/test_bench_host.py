@@ -43,6 +43,10 @@ def test_spec_peak_from_sms_and_clock():
 
 def test_kernel_keys_name_the_launched_instance():
     binding.load_library()
+    p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=0, sm_count=148)
+    assert bench.kernel_key(p) == "tile_gemm_kernel<256, 3, 0, 1, 1, 0, 1>"
+    p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=1, sm_count=148)
+    assert bench.kernel_key(p) == "tile_gemm_kernel<256, 3, 0, 1, 1, 0, 2>"
     p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
     assert bench.kernel_key(p) == "tile_gemm_kernel<256, 4, 1, 2, 1, 0>"
     p = binding.gemm_query_plan(8192, 28672, 4096, has_c=True, sm_count=148)
