@@ -239,11 +239,14 @@ class ClockSampler:
 
 def kernel_key(plan, p=None):
     """The kernel instance a plan launches for problem p, as ncu names it (for
-    profiles/traffic.json): tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, MODE>,
-    MODE 0 plain, 1 scattered rows, 2 reduce-add; skinny_gemm_kernel<MP, KBOX, W4>."""
+    profiles/traffic.json): tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, MODE, MX>,
+    MODE 0 plain, 1 scattered rows, 2 reduce-add, MX the operand kind (0 16-bit,
+    1 packed FP4, 2 the 16U4 FP4 image); skinny_gemm_kernel<MP, KBOX, W4>."""
     mode = 0 if p is None else (1 if p.scatter else (2 if p.accumulate else 0))
-    if plan.kernel in (11, 12):  # FP4 operands with block scales
-        return f"tile_gemm_kernel<{plan.bn}, {plan.stages}, 0, 1, 1, 0, {plan.kernel - 10}>"
+    if plan.kernel in (11, 12, 13, 14):  # FP4 operands with block scales (last: operand kind)
+        pair = 1 if plan.kernel >= 13 else 0
+        return (f"tile_gemm_kernel<{plan.bn}, {plan.stages}, {pair}, 1, 1, 0, "
+                f"{1 if plan.kernel in (11, 13) else 2}>")
     if plan.kernel == 2:  # (FP4 stages hold four 64-wide K blocks)
         return ("skinny_gemm_kernel<{}, 4, 1>" if p is not None and p.fp4
                 else "skinny_gemm_kernel<{}, 1, 0>").format(plan.bm)
@@ -254,7 +257,7 @@ def kernel_key(plan, p=None):
     if form is None:
         mc = {5: 4, 6: 8}.get(plan.kernel, 1)
         form = f"{plan.bn}, {plan.stages}, 0, 1, {mc}"
-    return f"tile_gemm_kernel<{form}, {mode}>"
+    return f"tile_gemm_kernel<{form}, {mode}, 0>"  # (last: operand kind 0, 16-bit)
 
 
 def plan_of(p, dev):
