@@ -241,15 +241,18 @@ def kernel_key(plan, p=None):
     """The kernel instance a plan launches for problem p, as ncu names it (for
     profiles/traffic.json): tile_gemm_kernel<BN, STAGES, PAIR, NSUB, MC, MODE, MX>,
     MODE 0 plain, 1 scattered rows, 2 reduce-add, MX the operand kind (0 16-bit,
-    1 packed FP4, 2 the 16U4 FP4 image); skinny_gemm_kernel<MP, KBOX, W4>."""
+    1 packed FP4, 2 the 16U4 FP4 image); skinny_gemm_kernel<MP, KBOX, W4, MX>
+    (W4 FP4 weights, MX both operands FP4)."""
     mode = 0 if p is None else (1 if p.scatter else (2 if p.accumulate else 0))
     if plan.kernel in (11, 12, 13, 14):  # FP4 operands with block scales (last: operand kind)
         pair = 1 if plan.kernel >= 13 else 0
         return (f"tile_gemm_kernel<{plan.bn}, {plan.stages}, {pair}, 1, 1, 0, "
                 f"{1 if plan.kernel in (11, 13) else 2}>")
+    if plan.kernel == 15:  # both operands FP4, M <= 64
+        return f"skinny_gemm_kernel<{plan.bm}, 1, 0, 1>"
     if plan.kernel == 2:  # (FP4 stages hold four 64-wide K blocks)
-        return ("skinny_gemm_kernel<{}, 4, 1>" if p is not None and p.fp4
-                else "skinny_gemm_kernel<{}, 1, 0>").format(plan.bm)
+        return ("skinny_gemm_kernel<{}, 4, 1, 0>" if p is not None and p.fp4
+                else "skinny_gemm_kernel<{}, 1, 0, 0>").format(plan.bm)
     if plan.kernel == 10:
         return "tiny_gemm_kernel"
     form = {3: "256, 6, 1, 1, 1", 4: "256, 4, 1, 2, 1", 7: "256, 4, 1, 2, 2",
@@ -623,6 +626,7 @@ def run_ours(args):
                 "kernel": {1: "tile (single CTA)", 2: "skinny (swap-AB, stream-K)",
                            11: "tile (single CTA, FP4 block-scaled, kind::mxf4)",
                            12: "tile (single CTA, FP4 block-scaled, kind::mxf8f6f4)",
+                           15: "skinny (swap-AB, stream-K, FP4 block-scaled, kind::mxf4)",
                            3: "tile (CTA pair)", 4: "tile (CTA pair, two N halves)",
                            5: "tile (4-CTA cluster, A multicast)",
                            6: "tile (8-CTA cluster, A multicast)",

@@ -249,6 +249,11 @@ gemm_status gemm_bf16_e2m1(int64_t M, int64_t N, int64_t K,
  *              The two forms take the same products; they may add them in a
  *              different order (bit-identical wherever every partial sum is
  *              exact in float32).
+ *  Kernels: M <= 64 with packed codes runs on the skinny swap-AB kernel (128
+ *  rows of B per tile on the MMA's M side, A's rows padded to 16 / 32 / 64 on
+ *  its N side, the K blocks of all tiles shared out over the SMs, a tile's
+ *  parts added in a fixed order by the last CTA to finish); otherwise the tile
+ *  kernel (gemm_query_plan forms 6 / 7).
  *  C, D, out, alpha, beta, stream as in gemm_f16.  D must not overlap Aq, As,
  *  Bq or Bs.  K == 0: D = beta * C.
  */
@@ -401,7 +406,9 @@ const char *gemm_status_string(int status);
  *           warp; problems of at most 2^20 multiply-adds), 11 / 12 = the tile
  *           kernel on FP4 operands with block scales (single CTAs, 128 x bn
  *           tiles, bn 128 or 256; MMA kind::mxf4 on packed codes / kind::mxf8f6f4
- *           on the 16U4_ALIGN16B image)
+ *           on the 16U4_ALIGN16B image), 13 / 14 = the same on CTA pairs
+ *           with 256 x 256 tiles, 15 = the skinny kernel on packed FP4
+ *           operands (M <= 64, K > 0; block-scaled MMA kind::mxf4)
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)
@@ -446,7 +453,10 @@ gemm_status gemm_debug_inject(int mode);
  * kernel 8 = two CTA pairs sharing A with bn = 256, kernel 9 = four CTA pairs
  * sharing A with bn = 512, kernel 10 = the warp-level kernel with bn = 8 (it
  * then runs every problem), kernels 11 / 12 = the FP4 tile width bn in {128,
- * 256} for gemm_e2m1 (only), kernel 2 = the skinny kernel with bn = 0 or 128
+ * 256} for gemm_e2m1 (only), kernels 13 / 14 = FP4 CTA pairs with bn = 256
+ * (gemm_e2m1 only), kernel 15 = the FP4 skinny kernel with bn = 128 (gemm_e2m1
+ * with packed codes, M <= 64, K > 0; other calls keep the automatic choice;
+ * forcing 11 - 14 keeps gemm_e2m1 on the tile kernel at M <= 64), kernel 2 = the skinny kernel with bn = 0 or 128
  * (problems it can run: M <= 64, K > 0, not gathered or seeded), kernel 0 =
  * automatic choice (the default).  Tile forms apply to every problem the tile
  * kernel runs, M <= 64 ones included; FP4 weights keep their own paths, and

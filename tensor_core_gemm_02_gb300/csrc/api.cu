@@ -44,17 +44,6 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 
-// Scratch of the skinny kernel: per-split partial tiles and per-tile arrival
-// counters.  One per (device, stream), so calls on different streams never
-// share it; calls on one stream are ordered by the stream.
-struct Workspace {
-    int device = -1;
-    cudaStream_t stream = nullptr;
-    float *partials = nullptr;
-    size_t partial_bytes = 0;
-    uint32_t *counters = nullptr;
-    size_t counter_count = 0;
-};
 std::mutex g_ws_mu;
 std::vector<Workspace> g_ws;
 
@@ -737,8 +726,8 @@ void forced_tile(int *kernel, int *bn)
 gemm_plan apply_forced_tile(gemm_plan plan, const Problem &p, int sm_count)
 {
     const int fk = g_force_kernel.load(), fbn = g_force_bn.load();
-    if (fk == 0 || (fk >= 11 && fk <= 14) || plan.kernel == 0 || p.w4)
-        return plan;  // (FP4 weights run only on their own paths; 11-14 are FP4 x FP4 forms)
+    if (fk == 0 || (fk >= 11 && fk <= 15) || plan.kernel == 0 || p.w4)
+        return plan;  // (FP4 weights run only on their own paths; 11-15 are FP4 x FP4 forms)
     if (fk == 10) {
         set_tiny_plan(plan, p.M, p.N);  // the warp-level kernel runs every problem
         return plan;
@@ -1145,7 +1134,7 @@ gemm_status gemm_debug_force_tile(int kernel, int bn)
                     (kernel == 7 && bn == 512) || (kernel == 8 && bn == 256) ||
                     (kernel == 9 && bn == 512) || (kernel == 10 && bn == 8) ||
                     ((kernel == 11 || kernel == 12) && (bn == 128 || bn == 256)) ||
-                    ((kernel == 13 || kernel == 14) && bn == 256);
+                    ((kernel == 13 || kernel == 14) && bn == 256) || (kernel == 15 && bn == 128);
     if (!ok)
         return GEMM_ERR_INVALID_ARG;
     g_force_kernel.store(kernel);

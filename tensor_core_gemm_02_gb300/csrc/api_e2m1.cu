@@ -135,6 +135,64 @@ gemm_status tma_scales(const DeviceInfo *dev, cudaStream_t stream, int use, cons
     return GEMM_OK;
 }
 
+// Few rows of A, packed codes: the swap-AB stream-K skinny kernel with
+// block-scaled MMAs (128 rows of B on the MMA's M side, the padded rows of A on
+// its N side, the K blocks of all tiles shared out over the SMs).
+gemm_status run_e2m1_skinny(const E2m1Problem &p, const gemm_plan &plan, const DeviceInfo *dev)
+{
+    const int mp = plan.bm;
+    GemmMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const uint8_t *as = nullptr, *bs = nullptr;
+    int64_t ldas = 0, ldbs = 0;
+    gemm_status st;
+    if ((st = tma_scales(dev, p.stream, kBufScalesA, p.As, p.ldas, p.M, p.K / 32, &as, &ldas)) != GEMM_OK ||
+        (st = tma_scales(dev, p.stream, kBufScalesB, p.Bs, p.ldbs, p.N, p.K / 32, &bs, &ldbs)) != GEMM_OK)
+        return st;
+    const uint32_t sf_rows = static_cast<uint32_t>(tcg::skinny_mx_kstage() / 32);
+    if (!encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.Aq, p.K / 2, p.M, p.ldaq, 128,
+                   static_cast<uint32_t>(mp), CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.Bq, p.K / 2, p.N, p.ldbq, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_UINT8, bs, p.N, p.K / 32, ldbs, 128, sf_rows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, as, p.M, p.K / 32, ldas,
+                   static_cast<uint32_t>(mp), sf_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return GEMM_ERR_CUDA;
+    Problem q{};  // (the fields fill_common reads)
+    q.M = p.M;
+    q.N = p.N;
+    q.K = p.K;
+    q.C = p.C;
+    q.ldc = p.ldc;
+    q.D = p.D;
+    q.ldd = p.ldd;
+    q.out = p.out;
+    q.alpha = p.alpha;
+    q.beta = p.beta;
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    fill_common(a, q, dev);
+    a.num_m_blocks = 1;
+    a.num_n_blocks = static_cast<int32_t>(plan.tiles);
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(p.K, tcg::skinny_mx_kstage()));
+    a.num_tiles = static_cast<int32_t>(plan.tiles);
+    a.sk_tiles = static_cast<int32_t>(plan.tiles);  // every tile shared block by block
+    a.group_m = 1;
+    a.splits = plan.splits;
+    if (plan.splits > 1) {
+        Workspace w;
+        const size_t bytes = static_cast<size_t>(plan.tiles) * plan.splits * 128 * mp * sizeof(float);
+        if ((st = get_workspace(dev->index, p.stream, bytes, static_cast<size_t>(plan.tiles), &w)) !=
+            GEMM_OK)
+            return st;
+        a.workspace = w.partials;
+        a.counters = w.counters;
+    }
+    const cudaError_t e = tcg::launch_skinny_mx(mp, maps, a, plan.grid, p.stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 gemm_status run_e2m1(const E2m1Problem &p)
 {
     bool empty = false;
@@ -145,6 +203,8 @@ gemm_status run_e2m1(const E2m1Problem &p)
     if ((st = device_info(&dev)) != GEMM_OK)
         return st;
     const gemm_plan plan = e2m1_plan(p.M, p.N, p.K, p.image, dev->sm_count);
+    if (plan.kernel == 15)
+        return run_e2m1_skinny(p, plan, dev);
     const int mx = (plan.kernel == 11 || plan.kernel == 13) ? 1 : 2;
     const bool pair = plan.kernel >= 13;
     const int bn = plan.bn;
@@ -228,7 +288,8 @@ gemm_status run_e2m1(const E2m1Problem &p)
 
 }  // namespace
 
-// Form: CTA pairs with 256 x 256 tiles (each SM moves 2/3 of the operand bytes
+// Forms: M <= 64 with packed codes: the skinny kernel (kernel 15).  Otherwise
+// CTA pairs with 256 x 256 tiles (each SM moves 2/3 of the operand bytes
 // per MMA that a single CTA with a 128 x 256 tile moves, which FP4 operands,
 // four times the MMA rate of 16-bit ones on the same bytes, need) when M > 128
 // and there are at least as many pair tiles as half the pairs; otherwise single
@@ -242,6 +303,26 @@ gemm_plan e2m1_plan(int64_t M, int64_t N, int64_t K, int image, int sm_count)
         return p;
     int fk = 0, fbn = 0;
     forced_tile(&fk, &fbn);
+    // M <= 64 with packed codes (and K > 0): the skinny kernel, unless a tile
+    // form is forced; forced (kernel 15) wherever it can run
+    const bool skinny_ok = image == 0 && M <= 64 && K > 0;
+    if (skinny_ok && (fk == 15 || !(fk >= 11 && fk <= 14))) {
+        const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+        const int64_t tiles = ceil_div(N, 128);
+        const int64_t nkb = ceil_div(K, tcg::skinny_mx_kstage());
+        // at least kSkinnyMinBlocks K blocks (of 256 elements) per CTA
+        constexpr int64_t kSkinnyMinBlocks = 4;
+        const int64_t want = ceil_div(tiles * nkb, kSkinnyMinBlocks);
+        const int64_t G = want < sm_count ? want : sm_count;
+        p.kernel = 15;
+        p.bm = mp;
+        p.bn = 128;
+        p.stages = tcg::skinny_mx_stages(mp);
+        p.tiles = tiles;
+        p.splits = tcg::skinny_max_parts(tiles, nkb, G);
+        p.grid = static_cast<int32_t>(G);
+        return p;
+    }
     const int mx = image == 0 ? 1 : 2;
     const int pairs = sm_count / 2;
     bool pair = false;

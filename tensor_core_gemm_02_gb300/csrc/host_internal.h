@@ -48,6 +48,23 @@ struct Problem {
     int64_t ldbs = 0;
 };
 
+// Scratch of the skinny kernel: per-split partial tiles and per-tile arrival
+// counters.  One per (device, stream), so calls on different streams never
+// share it; calls on one stream are ordered by the stream.
+struct Workspace {
+    int device = -1;
+    cudaStream_t stream = nullptr;
+    float *partials = nullptr;
+    size_t partial_bytes = 0;
+    uint32_t *counters = nullptr;
+    size_t counter_count = 0;
+};
+
+// Workspace of (device, stream) with room for `bytes` of partials and `count`
+// counters (allocated on first use, grown geometrically; counters start at zero).
+gemm_status get_workspace(int device, cudaStream_t stream, size_t bytes, size_t count,
+                          Workspace *out);
+
 // Per-device state (SM count, status word address); first call sets it up.
 gemm_status device_info(DeviceInfo **out);
 

@@ -35,7 +35,10 @@
 //              in the accumulating form every part is added into D with
 //              float32 atomic adds instead (no workspace, no last arriver)
 //   the rest   (FP4 B) converters: E2M1 codes and UE8M0 scales to bf16 rows
-//              in tensor memory (tcgen05.st), the MMA's A operand
+//              in tensor memory (tcgen05.st), the MMA's A operand; or (both
+//              operands FP4, MX) one scale warp: the stage's scale rows of B
+//              and A rearranged into the tiles tcgen05.cp copies into tensor
+//              memory, where the block-scaled MMA (kind::mxf4) reads them
 #pragma once
 
 #include "common.cuh"
@@ -56,11 +59,15 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t cols)
     return cols <= 32u ? 32u : (cols <= 64u ? 64u : (cols <= 128u ? 128u : (cols <= 256u ? 256u : 512u)));
 }
 
-template <int MP_, int KBOX_, bool W4_ = false>
+template <int MP_, int KBOX_, bool W4_ = false, bool MX_ = false>
 struct SkinnyCfg {
     static constexpr int MP = MP_;      // padded rows of A = MMA N
     static constexpr int BN = 128;      // rows of B per tile = MMA M
-    static constexpr int BK = 64;       // K of one 128-byte swizzled box
+    // MX: A and B both FP4 E2M1, codes packed two per byte, with UE8M0 scales
+    // per 32 elements: a 128-byte box holds 256 elements of a row, and the MMA
+    // is the block-scaled kind::mxf4 (K = 64 per instruction)
+    static constexpr bool MX = MX_;
+    static constexpr int BK = MX ? 256 : 64;  // K of one 128-byte swizzled box
     static constexpr int KBOX = KBOX_;  // boxes per stage: each row of B is read KBOX*128 B at a time
     static constexpr int KSTAGE = BK * KBOX;
     // W4: B arrives as FP4 codes (two per byte) with one UE8M0 scale per 32
@@ -70,7 +77,15 @@ struct SkinnyCfg {
     // operand from (row r of B in TMEM lane r, two elements per column)
     static constexpr bool W4 = W4_;
     static constexpr uint32_t RAW_B = W4 ? BN * BK / 2 * KBOX : 0;  // 128 rows x 128 bytes of codes
-    static constexpr uint32_t SCALE_B = W4 ? 2 * KBOX * BN : 0;     // 8 scale rows x 128 columns
+    // scale rows (32-element blocks) of a stage: B's 128 columns, (MX) A's MP
+    static constexpr int SF_KB = (W4 || MX) ? KSTAGE / 32 : 0;
+    static constexpr uint32_t SCALE_B = SF_KB * BN;
+    static constexpr uint32_t SCALE_A = MX ? SF_KB * MP : 0;
+    // (MX) the stage's scales rearranged for tcgen05.cp 32x128b.warpx4: 512-byte
+    // tiles of 128 rows x four 32-element blocks (row l + 32 q, block b at byte
+    // 16 l + 4 q + b) -- B's two 128-element chunks, then A's (rows >= MP zero)
+    static constexpr int SF_TILES = MX ? 2 * (KSTAGE / 128) : 0;
+    static constexpr uint32_t SF_CP = SF_TILES * 512;
 
     // MMA-issuing warps.  One thread issues a tcgen05.mma about every 117
     // cycles whatever its N, so at N = MP a lone issuer, not the tensor pipe,
@@ -91,7 +106,7 @@ struct SkinnyCfg {
     // of tensor memory for converted weights.)
     static constexpr int NACC = W4 ? 2 : TCG_SKINNY_NACC;
     static constexpr uint32_t ACC_COLS = static_cast<uint32_t>(NACC * ISSUERS * MP);
-    static constexpr uint32_t TMEM_COLS = W4 ? 512u : tmem_cols_for(ACC_COLS);
+    static constexpr uint32_t TMEM_COLS = (W4 || MX) ? 512u : tmem_cols_for(ACC_COLS);
     // TMEM columns: accumulator (buffer b, issuer e) at (b ISSUERS + e) MP,
     // then whole-stage converted sets (two elements per column) from the
     // next multiple of 128 to the end of the allocation
@@ -107,22 +122,29 @@ struct SkinnyCfg {
     // TMEM accumulators not fitting; four there measured slower with spills).
     static constexpr int CONV_PER_Q = W4 ? (MP <= 16 ? 4 : 2) : 0;
     static constexpr int CONV_WARPS = 4 * CONV_PER_Q;
-    static constexpr int THREADS = 32 * CONV_WARP0 + 32 * CONV_WARPS;
+    static constexpr int SCALE_WARPS = MX ? 1 : 0;  // (MX) after the epilogue
+    static constexpr int THREADS = 32 * CONV_WARP0 + 32 * (CONV_WARPS + SCALE_WARPS);
 
-    static constexpr uint32_t B_BOX = BN * BK * 2;
-    static constexpr uint32_t A_BOX = MP * BK * 2;
+    static constexpr uint32_t B_BOX = BN * 128;  // 128 rows of one 128-byte box
+    static constexpr uint32_t A_BOX = MP * 128;
     static constexpr uint32_t B_BYTES = W4 ? 0 : KBOX * B_BOX;
     static constexpr uint32_t A_BYTES = KBOX * A_BOX;
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + RAW_B + SCALE_B;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + RAW_B + SCALE_B + SCALE_A;  // TMA
     // as many stages as fit in about 200 KB of shared memory (at most 16)
     static constexpr uint32_t RING_BUDGET = 204800u;
-    static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) < 16 ? (RING_BUDGET / STAGE_BYTES) : 16;
+    static constexpr uint32_t STAGE_SMEM = STAGE_BYTES + SF_CP;
+    static constexpr int STAGES = (RING_BUDGET / STAGE_SMEM) < 16 ? (RING_BUDGET / STAGE_SMEM) : 16;
     static constexpr uint32_t OFF_B = 0;
     static constexpr uint32_t OFF_A = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_RAW = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_SC = OFF_RAW + STAGES * RAW_B;
-    static constexpr uint32_t OFF_BAR = (OFF_SC + STAGES * SCALE_B + 7u) & ~7u;
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * NACC + 2 * CSETS;
+    static constexpr uint32_t OFF_SCA = OFF_SC + STAGES * SCALE_B;
+    static constexpr uint32_t OFF_SFC = OFF_SCA + STAGES * SCALE_A;
+    static constexpr uint32_t OFF_BAR = (OFF_SFC + STAGES * SF_CP + 7u) & ~7u;
+    // (MX: one more per stage, the scale warp's hand-over to the MMA thread)
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * NACC + 2 * CSETS + (MX ? STAGES : 0);
+    static constexpr uint32_t SF_COL0 = ACC_COLS;     // (MX) scale tiles of stage s at
+    static constexpr uint32_t SF_COLS = SF_TILES * 4;  // SF_COL0 + s SF_COLS
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;  // MP destination rows (scattered rows)
     static constexpr uint32_t SMEM_BYTES = OFF_ROWS + MP * 4;
@@ -140,6 +162,9 @@ struct SkinnyCfg {
     static_assert(A_BOX % 1024 == 0 && B_BOX % 1024 == 0, "box images stay 1024-aligned");
     static_assert(STAGES >= 2, "at least double buffering");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(!(W4 && MX) && (!MX || (KBOX == 1 && SF_COL0 + STAGES * SF_COLS <= TMEM_COLS)),
+                  "both-FP4 stages: one box per operand, scale tiles in TMEM");
+    static_assert(OFF_SFC % 16 == 0 && OFF_SCA % 16 == 0, "scale images 16-byte aligned");
 };
 
 // The CTA that owns linear k-block x when W blocks are split over G CTAs as
@@ -224,13 +249,14 @@ __device__ __forceinline__ void skinny_add(const GemmArgs &a, const int32_t *dro
     }
 }
 
-template <int MP, int KBOX, bool W4>
-__global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
+template <int MP, int KBOX, bool W4, bool MX = false>
+__global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmS, const GemmArgs args)
+                       const __grid_constant__ CUtensorMap tmS,
+                       const __grid_constant__ CUtensorMap tmSA, const GemmArgs args)
 {
-    using Cfg = SkinnyCfg<MP, KBOX, W4>;
+    using Cfg = SkinnyCfg<MP, KBOX, W4, MX>;
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -248,6 +274,8 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + NACC + b); };
     auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 2 * NACC + c); };  // per converted set
     auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * STAGES + 2 * NACC + Cfg::CSETS + c); };
+    // (MX) stage s's scales are rearranged for tcgen05.cp
+    auto sfr_bar = [&](int st) { return bar0 + 8u * (2 * STAGES + 2 * NACC + 2 * Cfg::CSETS + st); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
     volatile uint32_t *arrival = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 8);
@@ -300,7 +328,17 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         const int32_t t = static_cast<int32_t>(q / nkb);
         const int32_t kb = static_cast<int32_t>(q - t * nkb);
         mbar_arrive_expect_tx(full_bar(st), Cfg::STAGE_BYTES + extra);
-        if constexpr (W4) {
+        if constexpr (MX) {
+            // one 128-byte box of codes of B (128 rows) and of A (MP rows), x in
+            // bytes; the stage's scale rows of B (128 columns) and of A (MP)
+            tma_load_2d(base + Cfg::OFF_B + st * Cfg::B_BYTES, &tmB, full_bar(st), kb * 128,
+                        t * Cfg::BN);
+            tma_load_2d(base + Cfg::OFF_A + st * Cfg::A_BYTES, &tmA, full_bar(st), kb * 128, 0);
+            tma_load_2d(base + Cfg::OFF_SC + st * Cfg::SCALE_B, &tmS, full_bar(st), t * Cfg::BN,
+                        kb * Cfg::SF_KB);
+            tma_load_2d(base + Cfg::OFF_SCA + st * Cfg::SCALE_A, &tmSA, full_bar(st), 0,
+                        kb * Cfg::SF_KB);
+        } else if constexpr (W4) {
             // 128 rows x 128 bytes of codes (128-byte swizzle), the stage's
             // eight scale rows, and KBOX boxes of A
             tma_load_2d(base + Cfg::OFF_RAW + st * Cfg::RAW_B, &tmB, full_bar(st),
@@ -332,6 +370,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             mbar_init(cfull_bar(c), Cfg::CONV_WARPS);
             mbar_init(cempty_bar(c), Cfg::ISSUERS);
         }
+        if (MX)
+            for (int st = 0; st < STAGES; ++st)
+                mbar_init(sfr_bar(st), 1);
         for (int b = 0; b < NACC; ++b) {
             mbar_init(accf_bar(b), Cfg::ISSUERS);
             mbar_init(acce_bar(b), Cfg::EPI_WARPS);
@@ -341,8 +382,10 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (W4)
+        if (W4 || MX)
             tma_prefetch_desc(&tmS);
+        if (MX)
+            tma_prefetch_desc(&tmSA);
         // inputs are read only once the previous kernel in the stream is done
         grid_dependency_wait();
         // the ring is empty: start the B stream now instead of after the
@@ -430,9 +473,35 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
                         alive = false;  // (the stage's blocks, as bf16 in converted set cset)
                         break;
                     }
+                    if (MX && !wait_bounded<true>(sfr_bar(s), ph, abort_flag, args.status,
+                                                  args.timeout_ns, kWhereMmaFull)) {
+                        alive = false;  // (the stage's scales, rearranged by the scale warp)
+                        break;
+                    }
                     tc_fence_after_sync();
+                    if constexpr (MX) {
+                        // the stage's scale tiles into its TMEM columns, then four
+                        // block-scaled MMAs (M = 128 rows of B, N = MP rows of A,
+                        // K = 64 each, 32 bytes along the 128-byte rows); MMA k reads
+                        // chunk k / 2's tiles, scale bytes 2 (k % 2) and up
+                        const uint32_t sfc = base + Cfg::OFF_SFC + s * Cfg::SF_CP;
+                        const uint32_t sfcol = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_COLS;
 #pragma unroll
-                    for (int j = 0; j < KBOX; ++j) {
+                        for (int ti = 0; ti < Cfg::SF_TILES; ++ti)
+                            tc_cp_32x128b_warpx4(sfcol + 4u * ti, sdesc_rows16(sfc + 512u * ti));
+                        const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES);
+                        const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t chunk = static_cast<uint32_t>(k / 2);
+                            const uint32_t sfid = static_cast<uint32_t>((k % 2) * 2);
+                            tc_mma_mxf4(d_tmem, bd + 2u * k, ad + 2u * k,
+                                        idesc_mx(1u, Cfg::BN, MP, sfid, sfid), sfcol + 4u * chunk,
+                                        sfcol + 8u + 4u * chunk, (st != i || k != 0) ? 1u : 0u);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < (MX ? 0 : KBOX); ++j) {
                         if (j % Cfg::ISSUERS != e)
                             continue;
                         const uint64_t ad =
@@ -761,6 +830,55 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4>::THREADS, 1)
             if (++cset == Cfg::CSETS) {
                 cset = 0;
                 cph ^= 1u;
+            }
+        }
+    } else if constexpr (MX) {
+        // ------------------------------------------------------------ scale warp
+        // Per stage: the scale rows as loaded (row b: one byte per row of B, then
+        // one per row of A) into the tiles tcgen05.cp takes -- lane l loads the
+        // 32-bit words of rows 4l .. 4l+3 for four blocks, transposes the 4 x 4
+        // bytes so each word holds one row's four blocks, and stores row r's word
+        // at 16 (r % 32) + 4 (r / 32) of the tile (rows of A past MP zero) --
+        // then hands the stage to the MMA thread (tcgen05.cp reads through the
+        // async proxy, hence the fence).
+        int s = 0;
+        uint32_t ph = 0;
+        for (int64_t q = 0; q < n_steps; ++q) {
+            if (!warp_wait_bounded<true>(full_bar(s), ph, abort_flag, args.status, args.timeout_ns,
+                                         kWhereMmaFull))
+                break;
+            const uint8_t *srcb = gbase + Cfg::OFF_SC + s * Cfg::SCALE_B;
+            const uint8_t *srca = gbase + Cfg::OFF_SCA + s * Cfg::SCALE_A;
+            uint8_t *dst = gbase + Cfg::OFF_SFC + s * Cfg::SF_CP;
+#pragma unroll
+            for (int ti = 0; ti < Cfg::SF_TILES; ++ti) {
+                const bool b_tile = ti < Cfg::SF_TILES / 2;
+                const int c = ti % (Cfg::SF_TILES / 2);
+                const uint32_t pitch = b_tile ? static_cast<uint32_t>(Cfg::BN) : static_cast<uint32_t>(MP);
+                const uint8_t *src = (b_tile ? srcb : srca) + 4u * c * pitch + 4u * lane;
+                const bool have = b_tile || 4u * lane < static_cast<uint32_t>(MP);
+                uint32_t w[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    w[b] = have ? *reinterpret_cast<const uint32_t *>(src + b * pitch) : 0u;
+                const uint32_t t0 = __byte_perm(w[0], w[1], 0x5140);
+                const uint32_t t1 = __byte_perm(w[0], w[1], 0x7362);
+                const uint32_t t2 = __byte_perm(w[2], w[3], 0x5140);
+                const uint32_t t3 = __byte_perm(w[2], w[3], 0x7362);
+                const uint32_t o[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
+                                       __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
+                uint8_t *tile = dst + 512u * ti + 4u * (lane / 8u);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint32_t *>(tile + 16u * ((4u * lane + i) % 32u)) = o[i];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(sfr_bar(s));
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
             }
         }
     }

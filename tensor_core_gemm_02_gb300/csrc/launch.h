@@ -78,6 +78,14 @@ cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldq, const uint8_t 
 cudaError_t launch_skinny_w4(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
                              cudaStream_t stream);
 int skinny_kstage();  // K elements per pipeline stage (and per stream-K unit)
+// Both operands FP4 (packed codes, UE8M0 scales per 32), M <= 64: maps.a / maps.b
+// the codes of A / B (uint8, 128-byte boxes of mp / 128 rows, 128-byte
+// swizzle), maps.c / maps.sfa the scales of B / A (uint8 boxes of 128 / mp
+// columns by K_stage / 32 rows); block-scaled MMA kind::mxf4.
+int skinny_mx_kstage();
+int skinny_mx_stages(int mp);
+cudaError_t launch_skinny_mx(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
+                             cudaStream_t stream);
 cudaError_t launch_skinny(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
                           cudaStream_t stream);
 

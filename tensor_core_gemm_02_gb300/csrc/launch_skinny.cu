@@ -1,5 +1,6 @@
 // launch_skinny.cu -- instantiations and launcher of the swap-AB stream-K kernel
-// (bf16/f16 B, or FP4 B with block scales converted into tensor memory).
+// (bf16/f16 B, FP4 B with block scales converted into tensor memory, or both
+// operands FP4 on the block-scaled MMA).
 #include <cuda_runtime.h>
 
 #include "kernel_skinny.cuh"
@@ -14,13 +15,13 @@ namespace tcg {
 
 namespace {
 
-template <int MP, bool W4>
+template <int MP, bool W4, bool MX = false>
 cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                                cudaStream_t stream)
 {
-    constexpr int KBOX = W4 ? 4 : TCG_SKINNY_KBOX;
-    using Cfg = SkinnyCfg<MP, KBOX, W4>;
-    auto kfn = skinny_gemm_kernel<MP, KBOX, W4>;
+    constexpr int KBOX = W4 ? 4 : (MX ? 1 : TCG_SKINNY_KBOX);
+    using Cfg = SkinnyCfg<MP, KBOX, W4, MX>;
+    auto kfn = skinny_gemm_kernel<MP, KBOX, W4, MX>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_ALLOC));
     if (e != cudaSuccess)
@@ -35,7 +36,7 @@ cudaError_t launch_skinny_impl(const GemmMaps &maps, const GemmArgs &args, int g
     attr[0].val.programmaticStreamSerializationAllowed = TCG_PDL;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, args);
+    return cudaLaunchKernelEx(&cfg, kfn, maps.a, maps.b, maps.c, maps.sfa, args);
 }
 
 }  // namespace
@@ -81,6 +82,29 @@ cudaError_t launch_skinny_w4(int mp, const GemmMaps &maps, const GemmArgs &args,
     case 16: return launch_skinny_impl<16, true>(maps, args, grid, stream);
     case 32: return launch_skinny_impl<32, true>(maps, args, grid, stream);
     case 64: return launch_skinny_impl<64, true>(maps, args, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int skinny_mx_kstage() { return SkinnyCfg<16, 1, false, true>::KSTAGE; }
+
+int skinny_mx_stages(int mp)
+{
+    switch (mp) {
+    case 16: return SkinnyCfg<16, 1, false, true>::STAGES;
+    case 32: return SkinnyCfg<32, 1, false, true>::STAGES;
+    case 64: return SkinnyCfg<64, 1, false, true>::STAGES;
+    default: return 0;
+    }
+}
+
+cudaError_t launch_skinny_mx(int mp, const GemmMaps &maps, const GemmArgs &args, int grid,
+                             cudaStream_t stream)
+{
+    switch (mp) {
+    case 16: return launch_skinny_impl<16, false, true>(maps, args, grid, stream);
+    case 32: return launch_skinny_impl<32, false, true>(maps, args, grid, stream);
+    case 64: return launch_skinny_impl<64, false, true>(maps, args, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -47,12 +47,14 @@ def test_kernel_keys_name_the_launched_instance():
     assert bench.kernel_key(p) == "tile_gemm_kernel<256, 3, 0, 1, 1, 0, 1>"
     p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=1, sm_count=148)
     assert bench.kernel_key(p) == "tile_gemm_kernel<256, 3, 0, 1, 1, 0, 2>"
+    p = binding.gemm_query_plan(16, 28672, 4096, e2m1=0, sm_count=148)
+    assert bench.kernel_key(p) == "skinny_gemm_kernel<16, 1, 0, 1>"
     p = binding.gemm_query_plan(8192, 8192, 8192, sm_count=148)
     assert bench.kernel_key(p) == "tile_gemm_kernel<256, 4, 1, 2, 1, 0, 0>"
     p = binding.gemm_query_plan(8192, 28672, 4096, has_c=True, sm_count=148)
     assert bench.kernel_key(p) == "tile_gemm_kernel<256, 6, 1, 1, 1, 0, 0>"
     p = binding.gemm_query_plan(16, 28672, 4096, sm_count=148)
-    assert bench.kernel_key(p) == "skinny_gemm_kernel<16, 1, 0>"
+    assert bench.kernel_key(p) == "skinny_gemm_kernel<16, 1, 0, 0>"
     p = binding.gemm_query_plan(1024, 1024, 1024, sm_count=148)
     assert bench.kernel_key(p) == "tile_gemm_kernel<64, 8, 0, 1, 1, 0, 0>"
     p = binding.gemm_query_plan(16384, 4096, 4096, gather=True, sm_count=148)
@@ -68,7 +70,7 @@ def test_kernel_keys_name_the_launched_instance():
     assert bench.kernel_key(p, sc) == "tile_gemm_kernel<256, 6, 1, 1, 1, 1, 0>"
     fp = workloads.Problem("f", torch.zeros(1, 1), torch.zeros(1, 1), Bs=torch.zeros(1, 1))
     p = binding.gemm_query_plan(16, 28672, 4096, fp4=True, sm_count=148)
-    assert bench.kernel_key(p, fp) == "skinny_gemm_kernel<16, 4, 1>"
+    assert bench.kernel_key(p, fp) == "skinny_gemm_kernel<16, 4, 1, 0>"
 
 
 def test_traffic_is_reported_only_for_current_sources(tmp_path, monkeypatch):

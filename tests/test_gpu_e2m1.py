@@ -6,7 +6,8 @@ float32, whatever order the tensor cores add them in: those results compare
 bit for bit (16-bit outputs: the float32 value rounded once).  Random codes
 and scales compare within the parity tolerance.  Every kernel form runs:
 packed codes (MMA kind::mxf4) and the 16U4_ALIGN16B image (kind::mxf8f6f4),
-single CTAs with tiles 128 and 256 wide and CTA pairs with 256 x 256 tiles.
+single CTAs with tiles 128 and 256 wide, CTA pairs with 256 x 256 tiles, and the
+swap-AB stream-K skinny form for M <= 64 (packed codes).
 """
 import numpy as np
 import pytest
@@ -68,6 +69,38 @@ def test_packed_k_not_a_multiple_of_128(form, K):
     p = workloads.e2m1_problem(K, 200, 300, K, values="exact", with_c=True, alpha=0.5)
     ref, _ = oracle_e2m1(p)
     assert_bits(run_e2m1(p), ref, OUT_F32, f"form {form} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 4096), (16, 8, 32), (16, 28672, 1024), (17, 640, 96),
+                                   (33, 1000, 2048), (48, 256, 512), (64, 4096, 4096),
+                                   (64, 130, 8192)])
+def test_skinny_every_shape_bit_exact(M, N, K):
+    """The swap-AB stream-K skinny form (M <= 64, packed codes): partial tiles of
+    B, K split over CTAs, padded rows of A, every output type."""
+    binding.gemm_debug_force_tile(15, 128)
+    plan = binding.gemm_query_plan(M, N, K, e2m1=0, sm_count=148)
+    assert plan.kernel == 15
+    for out, with_c, alpha, beta in CASES:
+        p = workloads.e2m1_problem(M * 11 + N + K + out, M, N, K, values="exact",
+                                   with_c=with_c, alpha=alpha, beta=beta, out=out)
+        ref, _ = oracle_e2m1(p)
+        assert_bits(run_e2m1(p), ref, out, f"skinny {M}x{N}x{K} out={out}")
+
+
+def test_skinny_random_within_tolerance_and_timeout():
+    binding.gemm_debug_force_tile(15, 128)
+    p = workloads.e2m1_problem(91, 40, 3000, 4096, with_c=True, alpha=0.5, beta=1.0)
+    ref, absprod = oracle_e2m1(p)
+    assert_within(run_e2m1(p), ref, absprod, OUT_F32, "skinny random")
+    binding.gemm_set_wait_timeout(50_000_000)
+    binding.gemm_debug_inject(1)
+    try:
+        run_e2m1(p)
+        assert device_status() == binding.GEMM_ERR_TIMEOUT
+    finally:
+        binding.gemm_debug_inject(0)
+        binding.gemm_set_wait_timeout(0)
+    assert_within(run_e2m1(p), ref, absprod, OUT_F32, "skinny after timeout")
 
 
 @pytest.mark.parametrize("image", [0, 1])

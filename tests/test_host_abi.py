@@ -212,9 +212,10 @@ def test_e2m1_argument_checks(lib):
 
 
 def test_e2m1_plan(lib):
-    """gemm_e2m1: single CTAs (11 packed codes, 12 the 16U4 image), 256 wide unless
-    128-wide tiles take fewer waves; CTA pairs with 256 x 256 tiles (13 / 14) when
-    forced; forced forms apply to gemm_e2m1 alone."""
+    """gemm_e2m1: M <= 64 with packed codes on the skinny kernel (15); otherwise single
+    CTAs (11 packed codes, 12 the 16U4 image), 256 wide unless 128-wide tiles take
+    fewer waves; CTA pairs with 256 x 256 tiles (13 / 14) when forced; forced forms
+    apply to gemm_e2m1 alone."""
     p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=0, sm_count=148)
     assert (p.kernel, p.bn, p.bm, p.grid, p.stages) == (11, 256, 128, 148, 3)
     p = binding.gemm_query_plan(8192, 8192, 8192, e2m1=1, sm_count=148)
@@ -226,9 +227,19 @@ def test_e2m1_plan(lib):
     finally:
         binding.gemm_debug_force_tile(0, 0)
     p = binding.gemm_query_plan(16, 28672, 4096, e2m1=1, sm_count=148)
-    assert (p.kernel, p.bn, p.tiles, p.grid) == (12, 256, 112, 112)
+    assert (p.kernel, p.bn, p.tiles, p.grid) == (12, 256, 112, 112)  # the 16U4 image: tiles
+    p = binding.gemm_query_plan(16, 28672, 4096, e2m1=0, sm_count=148)
+    assert (p.kernel, p.bm, p.bn, p.tiles, p.grid) == (15, 16, 128, 224, 148)  # packed: skinny
+    assert binding.gemm_query_plan(64, 1024, 512, e2m1=0, sm_count=148).kernel == 15
+    assert binding.gemm_query_plan(65, 1024, 512, e2m1=0, sm_count=148).kernel == 11
+    assert binding.gemm_query_plan(16, 1024, 0, e2m1=0, sm_count=148).kernel == 11  # K == 0
     p = binding.gemm_query_plan(1024, 1024, 1024, e2m1=0, sm_count=148)
-    assert (p.kernel, p.bn, p.tiles) == (11, 128, 64)  # 16 pair tiles: single CTAs, narrower
+    assert (p.kernel, p.bn, p.tiles) == (11, 128, 64)  # single CTAs, the narrower tile
+    binding.gemm_debug_force_tile(11, 256)
+    try:  # a forced tile form takes small M too
+        assert binding.gemm_query_plan(16, 28672, 4096, e2m1=0, sm_count=148).kernel == 11
+    finally:
+        binding.gemm_debug_force_tile(0, 0)
     binding.gemm_debug_force_tile(11, 128)
     try:
         assert binding.gemm_query_plan(8192, 8192, 8192, e2m1=0, sm_count=148).bn == 128
