@@ -162,6 +162,37 @@ __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
     return __all_sync(0xffffffffu, ok);
 }
 
+// As warp_wait_bounded, with the loop inline: loads the waiting threads
+// still have in flight stay in flight (around a call, the live registers are
+// saved first, and saving a register waits for the load that fills it).
+__device__ __forceinline__ bool warp_wait_bounded_inline(uint32_t bar, uint32_t parity,
+                                                         volatile uint32_t *abort_flag,
+                                                         uint32_t *status, uint64_t timeout_ns,
+                                                         uint32_t where)
+{
+    bool ok = true;
+    if (!mbar_test(bar, parity)) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_test(bar, parity))
+                break;
+            if ((it & 63u) == 0u) {
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (global_timer_ns() - t0 > timeout_ns) {
+                    *abort_flag = 1u;
+                    record_error(status, kStatusTimeout, where);
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Persistent tile order: output tiles in M, N order (the pages' repeat order
 // puts M before N and K innermost), visited in groups of `group_m` block rows
 // so that CTAs running at the same time share A and B panels in L2.

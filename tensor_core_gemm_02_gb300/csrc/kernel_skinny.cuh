@@ -15,8 +15,9 @@
 // gets one partial sum from each; each writes its partial to the workspace,
 // and the last to arrive (an atomic counter per tile) adds them in a fixed
 // order, applies the epilogue and resets the counter.  No CTA waits for
-// another.  A CTA runs its shared pieces first and its whole tiles last, so
-// the reductions overlap the whole tiles' MMAs instead of ending the kernel.
+// another.  A CTA runs its tail piece first, its whole tiles next and its head
+// piece last (FP4 B: both pieces first), so that the hand-ins overlap the
+// whole tiles' MMAs and the last piece finishes its tile from registers.
 // (bf16 / f16 B shares every tile, S = T: with whole tiles its HBM stream
 // measured 10-20% slower, FP4 B, bound by the decode, 3-12% faster.)
 //
@@ -24,9 +25,10 @@
 //              (MP x 64) at consecutive K, so each row of B is read in
 //              KBOX * 128-byte runs (FP4 B: the codes, 128 rows x 128 bytes,
 //              and the stage's scale rows)
-//   warps 1..I MMA issuers (I = ISSUERS: 1, or 2 / 4 for FP4 B):
-//              tcgen05.mma M=128 N=MP K=16, each issuer into two TMEM
-//              accumulators of its own (FP4 B: A operand from TMEM)
+//   warps 1..I MMA issuers (I = ISSUERS: 1, or 2 / 4 for FP4 B and for
+//              both operands FP4): tcgen05.mma M=128 N=MP K=16 (both FP4:
+//              block-scaled, K=64), each issuer into two TMEM accumulators of
+//              its own (FP4 B: A operand from TMEM)
 //   next 4     epilogue (8 for bf16 / f16 B with MP = 64, two per TMEM lane
 //              quarter, 32 columns each): tcgen05.ld (the issuers' partial sums added in
 //              order), partial or final fma.rn(alpha, acc, beta*C) with
@@ -46,6 +48,9 @@
 
 
 // Accumulator buffers of the bf16 / f16 form (at most 512 / MP).
+#ifndef TCG_SKINNY_MX_ISSUERS16
+#define TCG_SKINNY_MX_ISSUERS16 4
+#endif
 #ifndef TCG_SKINNY_NACC
 #define TCG_SKINNY_NACC 2
 #endif
@@ -93,7 +98,11 @@ struct SkinnyCfg {
     // from shared memory saturates its reads first).  Issuer e takes the
     // blocks j = e (mod ISSUERS) of every stage into accumulators of its
     // own, and the epilogue adds the partial sums in issuer order.
-    static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : 1;
+    // Both operands FP4 (MX): a stage is four block-scaled MMAs; issuer e takes
+    // MX_PER of them (consecutive, so one 128-element chunk of scales), copying
+    // that chunk's scale tiles into TMEM columns of its own.
+    static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : (MX ? (MP <= 16 ? TCG_SKINNY_MX_ISSUERS16 : 2) : 1);
+    static constexpr int MX_PER = MX ? 4 / ISSUERS : 0;
     // Epilogue warps: four (one per TMEM lane quarter), or eight for bf16 /
     // f16 B with MP = 64, two per quarter, each finishing 32 of the 64
     // columns, which halves a thread's chain of loads and stores per piece.
@@ -143,8 +152,10 @@ struct SkinnyCfg {
     static constexpr uint32_t OFF_BAR = (OFF_SFC + STAGES * SF_CP + 7u) & ~7u;
     // (MX: one more per stage, the scale warp's hand-over to the MMA thread)
     static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * NACC + 2 * CSETS + (MX ? STAGES : 0);
-    static constexpr uint32_t SF_COL0 = ACC_COLS;     // (MX) scale tiles of stage s at
-    static constexpr uint32_t SF_COLS = SF_TILES * 4;  // SF_COL0 + s SF_COLS
+    // (MX) scale columns of stage s, issuer e: SF_COL0 + (s ISSUERS + e) 8 (B's
+    // chunk, then A's, four columns each)
+    static constexpr uint32_t SF_COL0 = ACC_COLS;
+    static constexpr uint32_t SF_COLS = MX ? ISSUERS * 8 : 0;  // a stage's
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;  // MP destination rows (scattered rows)
     static constexpr uint32_t SMEM_BYTES = OFF_ROWS + MP * 4;
@@ -152,7 +163,8 @@ struct SkinnyCfg {
 
     static_assert(!W4 || KBOX == 4, "W4 stages hold 128-byte runs of codes");
     static_assert(!W4 || (KBOX % CONV_PER_Q == 0 && CSETS >= 2), "converters split a stage's blocks");
-    static_assert(KBOX % ISSUERS == 0 && (W4 || ISSUERS == 1), "issuers split a stage's blocks");
+    static_assert(W4 ? KBOX % ISSUERS == 0 : (MX ? (ISSUERS == 2 || ISSUERS == 4) : ISSUERS == 1),
+                  "issuers split a stage's blocks (MX: each within one chunk of scales)");
     static_assert(OFF_RAW % 1024 == 0 && RAW_B % 128 == 0, "TMA destinations stay aligned");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MMA N for M = 128 is a multiple of 16");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation is a power of two");
@@ -193,43 +205,94 @@ __device__ __forceinline__ int32_t skinny_row(const GemmArgs &a, const int32_t *
 // The epilogue works on chunks of CH rows of A (m0 .. m0 + CH - 1) of one
 // column n of D, so its registers do not grow with MP.
 
-// cb[m] = mul.rn(beta, C[r][n]) for the chunk's rows (0 where nothing is
-// written or C is absent).
+// c[m] = C[r][n] for the chunk's rows (0 where nothing is written or C is
+// absent).  The loads are left in flight: beta is applied where the values
+// are used (skinny_beta_c), so a warp that fetches C early does not stall on it.
+//
+// One epilogue warp per TMEM lane quarter runs these, so each is a straight
+// run of independent loads or stores: the per-call conditions are tested
+// once, and row m is a fixed stride from row 0 (scattered rows excepted).
 template <int CH>
-__device__ __forceinline__ void skinny_load_cb(const GemmArgs &a, const int32_t *drow, int32_t n,
-                                               int m0, float (&cb)[CH])
+__device__ __forceinline__ void skinny_load_c(const GemmArgs &a, const int32_t *drow, int32_t n,
+                                              int m0, float (&c)[CH])
 {
 #pragma unroll
-    for (int m = 0; m < CH; ++m) {
-        const int32_t r = skinny_row(a, drow, m0 + m);
-        cb[m] = (a.has_c && r >= 0 && n < a.N)
-                    ? mul_rn(a.beta, a.C[static_cast<int64_t>(r) * a.ldc + n])
-                    : 0.f;
+    for (int m = 0; m < CH; ++m)
+        c[m] = 0.f;
+    if (!a.has_c || n >= a.N)
+        return;
+    if (a.scatter) {
+#pragma unroll
+        for (int m = 0; m < CH; ++m) {
+            const int32_t r = drow[m0 + m];
+            if (r >= 0)
+                c[m] = a.C[static_cast<int64_t>(r) * a.ldc + n];
+        }
+        return;
     }
+    const float *p = a.C + static_cast<int64_t>(m0) * a.ldc + n;
+    const int32_t rows = a.M - m0;  // rows m < rows exist
+#pragma unroll
+    for (int m = 0; m < CH; ++m)
+        if (m < rows)
+            c[m] = p[static_cast<int64_t>(m) * a.ldc];
+}
+
+// cb[m] = mul.rn(beta, c[m])
+template <int CH>
+__device__ __forceinline__ void skinny_beta_c(const GemmArgs &a, const float (&c)[CH], float (&cb)[CH])
+{
+#pragma unroll
+    for (int m = 0; m < CH; ++m)
+        cb[m] = mul_rn(a.beta, c[m]);
 }
 
 // Final values: D[r][n] = fma.rn(alpha, v[m], cb[m]) with r = skinny_row(m)
 // (or D = mul.rn(alpha, v[m]) without C).
+template <typename T, int CH, typename Cvt>
+__device__ __forceinline__ void skinny_store_rows(const GemmArgs &a, const int32_t *drow, int32_t n,
+                                                  int m0, const float (&d)[CH], Cvt cvt)
+{
+    T *D = static_cast<T *>(a.D);
+    if (a.scatter) {
+#pragma unroll
+        for (int m = 0; m < CH; ++m) {
+            const int32_t r = drow[m0 + m];
+            if (r >= 0)
+                D[static_cast<int64_t>(r) * a.ldd + n] = cvt(d[m]);
+        }
+        return;
+    }
+    T *p = D + static_cast<int64_t>(m0) * a.ldd + n;
+    const int32_t rows = a.M - m0;
+#pragma unroll
+    for (int m = 0; m < CH; ++m)
+        if (m < rows)
+            p[static_cast<int64_t>(m) * a.ldd] = cvt(d[m]);
+}
+
 template <int CH>
 __device__ __forceinline__ void skinny_store(const GemmArgs &a, const int32_t *drow, int32_t n,
                                              int m0, const float (&v)[CH], const float (&cb)[CH])
 {
     if (n >= a.N)
         return;
+    float d[CH];
+    if (a.has_c) {
 #pragma unroll
-    for (int m = 0; m < CH; ++m) {
-        const int32_t r = skinny_row(a, drow, m0 + m);
-        if (r >= 0) {
-            const float d = a.has_c ? fma_rn(a.alpha, v[m], cb[m]) : mul_rn(a.alpha, v[m]);
-            const int64_t o = static_cast<int64_t>(r) * a.ldd + n;
-            if (a.out_kind == kOutF32)
-                static_cast<float *>(a.D)[o] = d;
-            else if (a.out_kind == kOutBF16)
-                static_cast<unsigned short *>(a.D)[o] = f32_to_bf16_rn(d);
-            else
-                static_cast<unsigned short *>(a.D)[o] = f32_to_f16_rn(d);
-        }
+        for (int m = 0; m < CH; ++m)
+            d[m] = fma_rn(a.alpha, v[m], cb[m]);
+    } else {
+#pragma unroll
+        for (int m = 0; m < CH; ++m)
+            d[m] = mul_rn(a.alpha, v[m]);
     }
+    if (a.out_kind == kOutF32)
+        skinny_store_rows<float>(a, drow, n, m0, d, [](float x) { return x; });
+    else if (a.out_kind == kOutBF16)
+        skinny_store_rows<unsigned short>(a, drow, n, m0, d, [](float x) { return f32_to_bf16_rn(x); });
+    else
+        skinny_store_rows<unsigned short>(a, drow, n, m0, d, [](float x) { return f32_to_f16_rn(x); });
 }
 
 // Accumulating form: add mul.rn(alpha, v[m]) into D[r][n] (float32 atomic
@@ -240,13 +303,26 @@ __device__ __forceinline__ void skinny_add(const GemmArgs &a, const int32_t *dro
 {
     if (n >= a.N)
         return;
+    float d[CH];
 #pragma unroll
-    for (int m = 0; m < CH; ++m) {
-        const int32_t r = skinny_row(a, drow, m0 + m);
-        if (r >= 0)
-            atomicAdd(static_cast<float *>(a.D) + static_cast<int64_t>(r) * a.ldd + n,
-                      mul_rn(a.alpha, v[m]));
+    for (int m = 0; m < CH; ++m)
+        d[m] = mul_rn(a.alpha, v[m]);
+    float *D = static_cast<float *>(a.D);
+    if (a.scatter) {
+#pragma unroll
+        for (int m = 0; m < CH; ++m) {
+            const int32_t r = drow[m0 + m];
+            if (r >= 0)
+                atomicAdd(D + static_cast<int64_t>(r) * a.ldd + n, d[m]);
+        }
+        return;
     }
+    float *p = D + static_cast<int64_t>(m0) * a.ldd + n;
+    const int32_t rows = a.M - m0;
+#pragma unroll
+    for (int m = 0; m < CH; ++m)
+        if (m < rows)
+            atomicAdd(p + static_cast<int64_t>(m) * a.ldd, d[m]);
 }
 
 template <int MP, int KBOX, bool W4, bool MX = false>
@@ -279,6 +355,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Cfg::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 4);
     volatile uint32_t *arrival = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 8);
+    // (the last piece's early read of its tile's counter: a slot of its own, as
+    // slower epilogue warps may still be reading `arrival` of the piece before)
+    volatile uint32_t *seen = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::OFF_MISC + 12);
 
     const int64_t nkb = args.num_k_blocks;
     const int64_t S = args.sk_tiles;
@@ -290,43 +369,78 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
     // whole tiles S + blockIdx.x + G j (T - S is a multiple of G)
     const int64_t n_steps = sk_n + (args.num_tiles - S) / G * nkb;
     // The share [my_start, my_end) is the tail of one tile, whole tiles, and the
-    // head of another.  The two partial pieces go first: the tiles they belong
-    // to are finished by a neighbour CTA too, so doing them early moves the
-    // last-arriver reductions off the end of the kernel; the CTA's own whole
-    // tiles come last.  Step i (0 <= i < n_steps) is linear K block order(i)
-    // (tile order(i) / nkb); pieces stay contiguous.
+    // head of another.  The tail piece goes first.  Where the epilogue can
+    // finish a tile from registers (kHeadLast: not FP4 B), the head piece goes
+    // last: the next CTA handed in its part of that tile with its own first
+    // piece, so this CTA finishes the tile without writing its part, and the
+    // tail piece's hand-in (its tile is finished by the previous CTA) overlaps
+    // the whole tiles' MMAs.  FP4 B runs both pieces first, then the whole
+    // tiles, so that its reductions (through the workspace) do not end the
+    // kernel.  Step i (0 <= i < n_steps) is linear K block order(i) (tile
+    // order(i) / nkb); pieces stay contiguous.
     const int64_t b1 = (my_start + nkb - 1) / nkb * nkb;  // first tile boundary
     const int64_t b2 = my_end / nkb * nkb;                 // last tile boundary
     const bool crosses = b1 < my_end;
     const int64_t len_a = crosses ? b1 - my_start : sk_n;  // tail piece
     const int64_t len_b = crosses ? my_end - b2 : 0;       // head piece
+    constexpr bool kHeadLast = !W4;
+    const int64_t ms = kHeadLast ? len_a : len_a + len_b;  // first step of the share's whole tiles
+    const int64_t os = sk_n - len_b + (kHeadLast ? 0 : len_b);  // ... of the own tiles
+    const int64_t oe = n_steps - (kHeadLast ? len_b : 0);  // end of the own tiles
+    const int64_t hs = kHeadLast ? oe : len_a;             // first step of the head piece
     auto order = [&](int64_t i) -> int64_t {
         if (i < len_a)
             return my_start + i;
-        if (i < len_a + len_b)
-            return b2 + (i - len_a);
-        if (i < sk_n)
-            return b1 + (i - len_a - len_b);
-        const int64_t d = i - sk_n;
+        if (i >= hs && i < hs + len_b)
+            return b2 + (i - hs);
+        if (i >= ms && i < os)
+            return b1 + (i - ms);
+        const int64_t d = i - os;
         return (S + blockIdx.x + G * (d / nkb)) * nkb + d % nkb;
     };
     // end, in steps, of the piece that step i belongs to: the tail piece, the
-    // head piece, then whole tiles of nkb steps each (those of the share
-    // between the two pieces, which starts on a tile boundary, then the
-    // CTA's own)
+    // head piece, or a whole tile of nkb steps (those of the share, which
+    // start on a tile boundary, and the CTA's own)
     auto piece_end = [&](int64_t i) -> int64_t {
         if (i < len_a)
             return len_a;
-        if (i < len_a + len_b)
-            return len_a + len_b;
-        const int64_t w0 = i < sk_n ? len_a + len_b : sk_n;
+        if (i >= hs && i < hs + len_b)
+            return hs + len_b;
+        const int64_t w0 = i < os ? ms : os;
         return w0 + ((i - w0) / nkb + 1) * nkb;
     };
 
-    // stage st <- B and A boxes of linear K block q, counted on full_bar(st)
-    auto issue_stage = [&](int st, int64_t q, uint32_t extra) {
-        const int32_t t = static_cast<int32_t>(q / nkb);
-        const int32_t kb = static_cast<int32_t>(q - t * nkb);
+    // (tile, K block) of successive steps without divisions: one thread's
+    // 64-bit divisions cost hundreds of cycles, and the producer's time per
+    // step bounds the stream.  The divisions of order() are taken only where
+    // a run of consecutive K blocks starts (the tail piece, the share's whole
+    // tiles, the own tiles, the head piece); inside the own tiles the next
+    // tile is G further on.
+    struct Cursor {
+        int64_t i;
+        int32_t t, kb;
+    };
+    auto cursor_at = [&](int64_t i, Cursor &c) {
+        const int64_t q = order(i);
+        c.i = i;
+        c.t = static_cast<int32_t>(q / nkb);
+        c.kb = static_cast<int32_t>(q - static_cast<int64_t>(c.t) * nkb);
+    };
+    auto cursor_next = [&](Cursor &c) {
+        ++c.i;
+        if (c.i == len_a || c.i == ms || c.i == os || c.i == oe || c.i == hs || c.i == hs + len_b) {
+            if (c.i < n_steps)
+                cursor_at(c.i, c);
+            return;
+        }
+        if (++c.kb == nkb) {
+            c.kb = 0;
+            c.t += c.i > os && c.i < oe ? static_cast<int32_t>(G) : 1;
+        }
+    };
+
+    // stage st <- B and A boxes of K block kb of tile t, counted on full_bar(st)
+    auto issue_stage = [&](int st, int32_t t, int32_t kb, uint32_t extra) {
         mbar_arrive_expect_tx(full_bar(st), Cfg::STAGE_BYTES + extra);
         if constexpr (MX) {
             // one 128-byte box of codes of B (128 rows) and of A (MP rows), x in
@@ -364,7 +478,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             // the MMA, and (W4) each warp of the converter group that takes the stage
-            mbar_init(empty_bar(s), W4 ? Cfg::ISSUERS + Cfg::CONV_WARPS : 1);
+            mbar_init(empty_bar(s), W4 ? Cfg::ISSUERS + Cfg::CONV_WARPS : Cfg::ISSUERS);
         }
         for (int c = 0; c < Cfg::CSETS; ++c) {
             mbar_init(cfull_bar(c), Cfg::CONV_WARPS);
@@ -390,8 +504,12 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
         grid_dependency_wait();
         // the ring is empty: start the B stream now instead of after the
         // tensor-memory allocation and the set-up barrier
-        for (int64_t i = 0; i < n_steps && pre < STAGES; ++i, ++pre)
-            issue_stage(pre, order(i), pre == 0 ? args.extra_tx : 0u);
+        Cursor c;
+        cursor_at(0, c);
+        for (int64_t i = 0; i < n_steps && pre < STAGES; ++i, ++pre) {
+            issue_stage(pre, c.t, c.kb, pre == 0 ? args.extra_tx : 0u);
+            cursor_next(c);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -412,16 +530,20 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
         uint32_t ph = 0;
         int pending = 0;
         bool alive = true;
+        Cursor c;
         for (int64_t i = 0; i < n_steps; ++i) {
-            const int64_t q = order(i);
             if (i >= pre) {
+                if (i == pre)
+                    cursor_at(i, c);
+                else
+                    cursor_next(c);
                 if (!warp_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status,
                                        args.timeout_ns, kWhereProducerEmpty)) {
                     alive = false;
                     break;
                 }
                 if (lane == 0)
-                    issue_stage(s, q, 0u);
+                    issue_stage(s, c.t, c.kb, 0u);
                 __syncwarp();
             }
             pending = min(pending + 1, STAGES);
@@ -463,8 +585,8 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
                 const uint32_t d_tmem =
                     tmem_base + static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP);
                 for (int64_t st = i; st < i1; ++st) {
-                    if (!wait_bounded<W4>(full_bar(s), ph, abort_flag, args.status,
-                                          args.timeout_ns, kWhereMmaFull)) {
+                    if (!wait_bounded<W4 || MX>(full_bar(s), ph, abort_flag, args.status,
+                                                args.timeout_ns, kWhereMmaFull)) {
                         alive = false;
                         break;
                     }
@@ -480,24 +602,29 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
                     }
                     tc_fence_after_sync();
                     if constexpr (MX) {
-                        // the stage's scale tiles into its TMEM columns, then four
-                        // block-scaled MMAs (M = 128 rows of B, N = MP rows of A,
-                        // K = 64 each, 32 bytes along the 128-byte rows); MMA k reads
-                        // chunk k / 2's tiles, scale bytes 2 (k % 2) and up
+                        // this issuer's MMAs k0 .. k0 + MX_PER - 1 of the stage's four
+                        // block-scaled ones (M = 128 rows of B, N = MP rows of A, K = 64
+                        // each, 32 bytes along the 128-byte rows), all in 128-element
+                        // chunk k0 / 2: that chunk's scale tiles of B and A into the
+                        // issuer's TMEM columns first; MMA k reads scale bytes 2 (k % 2)
+                        // and up
+                        const int k0 = e * Cfg::MX_PER;
+                        const uint32_t chunk = static_cast<uint32_t>(k0 / 2);
                         const uint32_t sfc = base + Cfg::OFF_SFC + s * Cfg::SF_CP;
-                        const uint32_t sfcol = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_COLS;
-#pragma unroll
-                        for (int ti = 0; ti < Cfg::SF_TILES; ++ti)
-                            tc_cp_32x128b_warpx4(sfcol + 4u * ti, sdesc_rows16(sfc + 512u * ti));
+                        const uint32_t sfcol =
+                            tmem_base + Cfg::SF_COL0 + static_cast<uint32_t>((s * Cfg::ISSUERS + e) * 8);
+                        tc_cp_32x128b_warpx4(sfcol, sdesc_rows16(sfc + 512u * chunk));
+                        tc_cp_32x128b_warpx4(sfcol + 4u,
+                                             sdesc_rows16(sfc + 512u * (Cfg::SF_TILES / 2 + chunk)));
                         const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES);
                         const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t chunk = static_cast<uint32_t>(k / 2);
+                        for (int kk = 0; kk < Cfg::MX_PER; ++kk) {
+                            const int k = k0 + kk;
                             const uint32_t sfid = static_cast<uint32_t>((k % 2) * 2);
                             tc_mma_mxf4(d_tmem, bd + 2u * k, ad + 2u * k,
-                                        idesc_mx(1u, Cfg::BN, MP, sfid, sfid), sfcol + 4u * chunk,
-                                        sfcol + 8u + 4u * chunk, (st != i || k != 0) ? 1u : 0u);
+                                        idesc_mx(1u, Cfg::BN, MP, sfid, sfid), sfcol, sfcol + 4u,
+                                        (st != i || kk != 0) ? 1u : 0u);
                         }
                     }
 #pragma unroll
@@ -575,9 +702,30 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
             }
             epi_bar_sync<EPI_THREADS>();
         }
+        // C of a piece's tile into L2 two pieces ahead (the first two now), so
+        // that the epilogue's loads of C do not wait for HBM behind the MMAs:
+        // one 128-byte line (32 columns) of a row of A per thread and pass
+        const bool pf_c = args.has_c && !args.reduce;
+        const int32_t et = static_cast<int32_t>(threadIdx.x) - 32 * Cfg::EPI_WARP0;
+        auto prefetch_c = [&](int64_t ip) {
+            const int32_t tp = static_cast<int32_t>(order(ip) / nkb);
+            for (int32_t j = et; j < MP * (Cfg::BN / 32); j += EPI_THREADS) {
+                const int32_t r = skinny_row(args, drow, j / (Cfg::BN / 32));
+                const int32_t n0 = tp * Cfg::BN + 32 * (j % (Cfg::BN / 32));
+                if (r >= 0 && n0 < args.N)
+                    prefetch_l2(args.C + static_cast<int64_t>(r) * args.ldc + n0);
+            }
+        };
+        int64_t ipf = 0;  // first step of the next piece whose C is to be prefetched
+        for (int k = 0; k < 2 && pf_c && ipf < n_steps; ++k, ipf = piece_end(ipf))
+            prefetch_c(ipf);
         int ab = 0;
         uint32_t aph = 0;
         for (int64_t i = 0; i < n_steps;) {
+            if (pf_c && ipf < n_steps) {
+                prefetch_c(ipf);
+                ipf = piece_end(ipf);
+            }
             const int32_t t = static_cast<int32_t>(order(i) / nkb);
             i = piece_end(i);
             const int32_t n = t * Cfg::BN + n_local;
@@ -588,9 +736,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
             // registers when there is one chunk, else its lines into L2.
             constexpr int CH = (W4 && MP > 16) ? 16 : MPH;
             constexpr int NCH = MPH / CH;
-            float cb0[CH];
+            float c0[CH];  // (one chunk) C, still in flight
             if constexpr (NCH == 1) {
-                skinny_load_cb<CH>(args, drow, n, mb, cb0);
+                skinny_load_c<CH>(args, drow, n, mb, c0);
             } else if (args.has_c && n < args.N) {
 #pragma unroll 4
                 for (int m = mb; m < mb + MPH; ++m) {
@@ -599,22 +747,15 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
                         prefetch_l2(args.C + static_cast<int64_t>(r) * args.ldc + n);
                 }
             }
-            auto chunk_cb = [&](int g, float (&cb)[CH]) {
+            auto chunk_cb = [&](int g, float (&cb)[CH]) {  // beta * C of chunk g
                 if constexpr (NCH == 1) {
-#pragma unroll
-                    for (int m = 0; m < CH; ++m)
-                        cb[m] = cb0[m];
+                    skinny_beta_c<CH>(args, c0, cb);
                 } else {
-                    skinny_load_cb<CH>(args, drow, n, mb + CH * g, cb);
+                    float c[CH];
+                    skinny_load_c<CH>(args, drow, n, mb + CH * g, c);
+                    skinny_beta_c<CH>(args, c, cb);
                 }
             };
-            const bool ok = warp_wait_bounded(accf_bar(ab), aph, abort_flag, args.status,
-                                              args.timeout_ns, kWhereEpiAccFull);
-            // all epilogue warps agree before the named barriers below
-            epi_bar_sync<EPI_THREADS>();
-            if (!ok || *abort_flag)
-                break;
-            tc_fence_after_sync();
             const bool shared_tile = t < S;
             const int32_t c_lo =
                 shared_tile ? skinny_owner(static_cast<int64_t>(t) * nkb, W, G) : static_cast<int32_t>(blockIdx.x);
@@ -634,36 +775,63 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
             // B only, at most 32 columns a thread: keeping the part in
             // registers spills beside FP4 B's converter warps, and FP4 B ends
             // on whole tiles.)
+            // Its counter is read before the wait for this CTA's own sums, and
+            // (a tile of two parts) the other CTA's part with it, so neither
+            // round trip follows the last MMA.
             constexpr bool kKeep = !W4 && MPH <= 32 && NCH == 1;
             bool last_known = false;
+            float other[CH];  // (kKeep, two parts) the other CTA's part
+            bool have_other = false;
             if (kKeep && parts > 1 && i == n_steps) {
                 if (leader) {
                     const uint32_t in = ld_acquire_gpu(args.counters + t);
-                    *arrival = in;
+                    *seen = in;
                 }
                 epi_bar_sync<EPI_THREADS>();
-                last_known = *arrival == static_cast<uint32_t>(parts - 1);
+                last_known = *seen == static_cast<uint32_t>(parts - 1);
+                if (last_known && parts == 2) {
+                    const float *src = slot0 + static_cast<int64_t>(1 - my_slot) * (Cfg::BN * MP);
+#pragma unroll
+                    for (int m = 0; m < CH; ++m)
+                        other[m] = __ldcg(src + (mb + m) * Cfg::BN + n_local);
+                    have_other = true;
+                }
             }
+            // (inline: the loads of C and of the other part stay in flight)
+            const bool ok = warp_wait_bounded_inline(accf_bar(ab), aph, abort_flag, args.status,
+                                                     args.timeout_ns, kWhereEpiAccFull);
+            // all epilogue warps agree before the named barriers below
+            epi_bar_sync<EPI_THREADS>();
+            if (!ok || *abort_flag)
+                break;
+            tc_fence_after_sync();
             float v[CH];  // this chunk's sums (with one chunk: the CTA's whole part)
 #pragma unroll 1
             for (int g = 0; g < NCH; ++g) {
-                // the issuers' partial sums of this chunk, added in issuer order
+                // the issuers' partial sums of this chunk (all loads first, one
+                // wait), added in issuer order
+                uint32_t r[Cfg::ISSUERS][CH / 16][16];
 #pragma unroll
-                for (int e = 0; e < Cfg::ISSUERS; ++e) {
+                for (int e = 0; e < Cfg::ISSUERS; ++e)
 #pragma unroll
-                    for (int h = 0; h < CH / 16; ++h) {
-                        uint32_t r[16];
+                    for (int h = 0; h < CH / 16; ++h)
                         tc_ld_32x32b_x16(tmem_base + ((32u * q) << 16) +
                                              static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP +
                                                                    mb + CH * g + 16 * h),
-                                         r);
-                        tc_wait_ld(r);
+                                         r[e][h]);
+#pragma unroll
+                for (int e = 0; e < Cfg::ISSUERS; ++e)
+#pragma unroll
+                    for (int h = 0; h < CH / 16; ++h)
+                        tc_wait_ld(r[e][h]);  // (the first waits; the rest tie the registers)
+#pragma unroll
+                for (int e = 0; e < Cfg::ISSUERS; ++e)
+#pragma unroll
+                    for (int h = 0; h < CH / 16; ++h)
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            v[16 * h + i] = e == 0 ? __uint_as_float(r[i])
-                                                   : v[16 * h + i] + __uint_as_float(r[i]);
-                    }
-                }
+                            v[16 * h + i] = e == 0 ? __uint_as_float(r[e][h][i])
+                                                   : v[16 * h + i] + __uint_as_float(r[e][h][i]);
                 if (args.reduce) {
                     skinny_add<CH>(args, drow, n, mb + CH * g, v);  // every part adds itself into D
                 } else if (parts == 1) {
@@ -721,6 +889,10 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
 #pragma unroll
                         for (int m = 0; m < CH; ++m)
                             part[m] = v[m];
+                    } else if (kKeep && have_other) {
+#pragma unroll
+                        for (int m = 0; m < CH; ++m)
+                            part[m] = other[m];
                     } else {
 #pragma unroll
                         for (int m = 0; m < CH; ++m)
