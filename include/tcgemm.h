@@ -387,7 +387,8 @@ const char *gemm_status_string(int status);
  *
  * With M <= 64 rows (bf16 / f16 B; not gathered, not seeded) the skinny
  * kernel runs where it measured faster than the tile kernel: M <= 16 with
- * N * K > 2^21, 16 < M <= 64 with K >= 2 N.  FP4 weights with M <= 128
+ * N * K > 2^21, 16 < M <= 64 with K >= 2 N, and also 16 < M <= 32 with
+ * K >= N and N * K > 2^21.  FP4 weights with M <= 128
  * always take it.
  *
  *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles, one

@@ -419,11 +419,19 @@ bool skinny_eligible(int64_t M, int64_t K, bool gather, bool seeded)
 // 1024^2 8.9 / 6.8; M = 32: 28672 x 4096 46.0 / 45.9, 4096 x 8192
 // 23.6 / 29.3, 4096^2 23.0 / 16.6, 16384 x 2048 25.4 / 16.8; M = 64:
 // 4096^2 19.4 / 16.7, 4096 x 14336 30.5 / 48.3, 2048 x 16384 23.7 / 54.4,
-// 1024 x 8192 20.0 / 29.1; 48 rows 2048 x 8192 20.4 / 29.1.
+// 1024 x 8192 20.0 / 29.1; 48 rows 2048 x 8192 20.4 / 29.1.  After the
+// skinny epilogue's straight-line loads and stores (same method): M = 32:
+// 4096^2 14.0 / 16.8, 28672 x 4096 44.1 / 45.7, 16384 x 2048 20.4 / 17.2,
+// 4096 x 8192 19.5 / 35.5; M = 64: 4096^2 22.6 / 16.9, 28672 x 4096
+// 53.8 / 46.7, 1024 x 8192 21.0 / 34.6; 48 x 8192^2 36.3 / 31.3; M = 16:
+// 1024^2 7.7 / 6.8.
 bool skinny_wins(int64_t M, int64_t N, int64_t K)
 {
+    const bool big = N * K > (int64_t(1) << 21);  // (N, K < 2^31: no overflow)
     if (M <= 16)
-        return N * K > (int64_t(1) << 21);  // (N, K < 2^31: no overflow)
+        return big;
+    if (M <= 32)
+        return K >= 2 * N || (big && K >= N);
     return K >= 2 * N;
 }
 

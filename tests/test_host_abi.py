@@ -293,7 +293,10 @@ def test_plan_matches_the_dispatch_rules(lib):
     # 16 < M <= 64: the tile kernel unless K is long against N
     assert binding.gemm_query_plan(40, 1000, 64, sm_count=148).kernel == 1
     assert binding.gemm_query_plan(64, 28672, 4096, sm_count=148).kernel != 2
-    assert binding.gemm_query_plan(32, 4096, 4096, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(32, 4096, 4096, sm_count=148).kernel == 2  # K >= N, 17..32 rows
+    assert binding.gemm_query_plan(32, 16384, 2048, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(32, 1024, 1024, sm_count=148).kernel != 2  # N K <= 2^21
+    assert binding.gemm_query_plan(33, 4096, 4096, sm_count=148).kernel != 2
     p = binding.gemm_query_plan(32, 4096, 8192, sm_count=148)
     assert (p.kernel, p.bm) == (2, 32)
     p = binding.gemm_query_plan(40, 1024, 8192, sm_count=148)
@@ -302,13 +305,14 @@ def test_plan_matches_the_dispatch_rules(lib):
     assert binding.gemm_query_plan(64, 4096, 16384, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(48, 2048, 8192, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(64, 4096, 14336, sm_count=148).kernel == 2
-    # the rule's edge: K >= 2N for 17..64 rows
+    # the rule's edge: K >= 2N for 17..64 rows (17..32 rows also K >= N when N K > 2^21)
     assert binding.gemm_query_plan(17, 1024, 2048, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(32, 1024, 2047, sm_count=148).kernel == 1
     assert binding.gemm_query_plan(33, 1024, 2048, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(64, 1024, 2040, sm_count=148).kernel == 1
     # scattered and accumulating calls follow the same rule; gathered rows never
-    assert binding.gemm_query_plan(32, 4096, 4096, scatter=True, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(48, 4096, 4096, scatter=True, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(32, 4096, 4096, scatter=True, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(16, 4096, 4096, scatter=True, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(16, 4096, 4096, gather=True, sm_count=148).kernel != 2
     # the allocation-free entry point always plans the skinny kernel (or the tiny one)
