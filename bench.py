@@ -520,13 +520,20 @@ def oracle_rows_rate(p, seconds, threads):
     return 2.0 * rows * p.N * p.K / dt, rows, dt
 
 
+# NVIDIA's published dense (no 2:4 sparsity) bf16 / fp16 tensor figure for one GB300
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0
+
+
 def spec_peak(sms, clocks, achieved):
-    """The chip's dense bf16 tensor peak from its SM count, the per-SM rate and
-    the SM clock: at the maximum clock and at the median clock sampled during
-    the timed region, with the achieved rate (TFLOP/s) as a fraction of each."""
+    """The chip's dense bf16 tensor peak: NVIDIA's published dense figure, and
+    from its SM count, the per-SM rate and the SM clock at the maximum clock and
+    at the median clock sampled during the timed region, with the achieved rate
+    (TFLOP/s) as a fraction of each."""
     out = {"flop_per_clk_per_sm": FLOP_PER_CLK_PER_SM, "sms": sms,
            "source": "one SM's tensor pipe runs a 128 x N x 16 bf16 MMA in N/2 cycles "
-                     "(8192 flop per clock); x SMs x SM clock"}
+                     "(8192 flop per clock); x SMs x SM clock",
+           "nominal_dense_tflops": NOMINAL_DENSE_BF16_TFLOPS,
+           "frac_of_nominal": round(achieved / NOMINAL_DENSE_BF16_TFLOPS, 4)}
     for key, mhz in (("max", clocks.get("sm_max_mhz")), ("median", clocks.get("sm_mhz"))):
         if mhz:
             peak = FLOP_PER_CLK_PER_SM * sms * mhz * 1e6 / 1e12

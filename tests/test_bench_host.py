@@ -35,6 +35,7 @@ def test_spec_peak_from_sms_and_clock():
     assert s["peak_at_max_mhz"] == pytest.approx(152 * 8192 * 2.07e9 / 1e12, abs=0.06)
     assert s["peak_at_median_mhz"] == pytest.approx(152 * 8192 * 1.65e9 / 1e12, abs=0.06)
     assert s["frac_at_max_mhz"] == pytest.approx(1800.0 / (152 * 8192 * 2.07e9 / 1e12), abs=1e-4)
+    assert s["frac_of_nominal"] == pytest.approx(1800.0 / 2250.0)  # the published dense figure
     assert s["frac_at_median_mhz"] == pytest.approx(1800.0 / (152 * 8192 * 1.65e9 / 1e12),
                                                     abs=1e-4)
     # no clock samples: no peak figures, no division

@@ -212,7 +212,7 @@ def test_e2m1_argument_checks(lib):
 
 
 def test_e2m1_plan(lib):
-    """gemm_e2m1: M <= 64 with packed codes on the skinny kernel (15); otherwise single
+    """gemm_e2m1: M <= 32 with packed codes on the skinny kernel (15); otherwise single
     CTAs (11 packed codes, 12 the 16U4 image), 256 wide unless 128-wide tiles take
     fewer waves; CTA pairs with 256 x 256 tiles (13 / 14) when forced; forced forms
     apply to gemm_e2m1 alone."""
@@ -230,8 +230,15 @@ def test_e2m1_plan(lib):
     assert (p.kernel, p.bn, p.tiles, p.grid) == (12, 256, 112, 112)  # the 16U4 image: tiles
     p = binding.gemm_query_plan(16, 28672, 4096, e2m1=0, sm_count=148)
     assert (p.kernel, p.bm, p.bn, p.tiles, p.grid) == (15, 16, 128, 224, 148)  # packed: skinny
-    assert binding.gemm_query_plan(64, 1024, 512, e2m1=0, sm_count=148).kernel == 15
+    assert binding.gemm_query_plan(32, 1024, 512, e2m1=0, sm_count=148).kernel == 15
+    assert binding.gemm_query_plan(33, 1024, 512, e2m1=0, sm_count=148).kernel == 11
     assert binding.gemm_query_plan(65, 1024, 512, e2m1=0, sm_count=148).kernel == 11
+    binding.gemm_debug_force_tile(15, 128)
+    try:  # forced, the skinny form takes up to 64 rows
+        assert binding.gemm_query_plan(64, 1024, 512, e2m1=0, sm_count=148).kernel == 15
+        assert binding.gemm_query_plan(65, 1024, 512, e2m1=0, sm_count=148).kernel == 11
+    finally:
+        binding.gemm_debug_force_tile(0, 0)
     assert binding.gemm_query_plan(16, 1024, 0, e2m1=0, sm_count=148).kernel == 11  # K == 0
     p = binding.gemm_query_plan(1024, 1024, 1024, e2m1=0, sm_count=148)
     assert (p.kernel, p.bn, p.tiles) == (11, 128, 64)  # single CTAs, the narrower tile
