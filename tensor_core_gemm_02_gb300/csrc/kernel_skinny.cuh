@@ -51,6 +51,9 @@
 #ifndef TCG_SKINNY_MX_ISSUERS16
 #define TCG_SKINNY_MX_ISSUERS16 4
 #endif
+#ifndef TCG_SKINNY_BF16_ISSUERS16
+#define TCG_SKINNY_BF16_ISSUERS16 4
+#endif
 #ifndef TCG_SKINNY_NACC
 #define TCG_SKINNY_NACC 2
 #endif
@@ -95,13 +98,17 @@ struct SkinnyCfg {
     // MMA-issuing warps.  One thread issues a tcgen05.mma about every 117
     // cycles whatever its N, so at N = MP a lone issuer, not the tensor pipe,
     // sets the rate; issuers in separate warps add up (with A in TMEM; A
-    // from shared memory saturates its reads first).  Issuer e takes the
-    // blocks j = e (mod ISSUERS) of every stage into accumulators of its
-    // own, and the epilogue adds the partial sums in issuer order.
+    // from shared memory saturates its reads first).  FP4 B: issuer e takes
+    // the blocks j = e (mod ISSUERS) of every stage; bf16 / f16 B with MP = 16:
+    // four issuers, issuer e the K step e of each box (16 x 28672 x 4096:
+    // 41.2 -> 39.9 us; for MP = 32 / 64 more issuers measured slower).  Each
+    // issuer has accumulators of its own, and the epilogue adds the partial
+    // sums in issuer order.
     // Both operands FP4 (MX): a stage is four block-scaled MMAs; issuer e takes
     // MX_PER of them (consecutive, so one 128-element chunk of scales), copying
     // that chunk's scale tiles into TMEM columns of its own.
-    static constexpr int ISSUERS = W4 ? (MP <= 16 ? 4 : 2) : (MX ? (MP <= 16 ? TCG_SKINNY_MX_ISSUERS16 : 2) : 1);
+    static constexpr int ISSUERS =
+        W4 ? (MP <= 16 ? 4 : 2) : (MX ? (MP <= 16 ? TCG_SKINNY_MX_ISSUERS16 : 2) : (MP <= 16 ? TCG_SKINNY_BF16_ISSUERS16 : 1));
     static constexpr int MX_PER = MX ? 4 / ISSUERS : 0;
     // Epilogue warps: four (one per TMEM lane quarter), or eight for bf16 /
     // f16 B with MP = 64, two per quarter, each finishing 32 of the 64
@@ -163,8 +170,9 @@ struct SkinnyCfg {
 
     static_assert(!W4 || KBOX == 4, "W4 stages hold 128-byte runs of codes");
     static_assert(!W4 || (KBOX % CONV_PER_Q == 0 && CSETS >= 2), "converters split a stage's blocks");
-    static_assert(W4 ? KBOX % ISSUERS == 0 : (MX ? (ISSUERS == 2 || ISSUERS == 4) : ISSUERS == 1),
-                  "issuers split a stage's blocks (MX: each within one chunk of scales)");
+    static_assert(W4 ? KBOX % ISSUERS == 0 : (MX ? (ISSUERS == 2 || ISSUERS == 4) : (BK / 16) % ISSUERS == 0),
+                  "issuers split a stage's blocks (MX: each within one chunk of scales; bf16 / "
+                  "f16 B: each box's K steps)");
     static_assert(OFF_RAW % 1024 == 0 && RAW_B % 128 == 0, "TMA destinations stay aligned");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MMA N for M = 128 is a multiple of 16");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation is a power of two");
@@ -420,23 +428,21 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
         int64_t i;
         int32_t t, kb;
     };
-    auto cursor_at = [&](int64_t i, Cursor &c) {
+    // (by value: a cursor whose address is taken lives on the stack)
+    auto cursor_at = [&](int64_t i) -> Cursor {
         const int64_t q = order(i);
-        c.i = i;
-        c.t = static_cast<int32_t>(q / nkb);
-        c.kb = static_cast<int32_t>(q - static_cast<int64_t>(c.t) * nkb);
+        const int32_t t = static_cast<int32_t>(q / nkb);
+        return Cursor{i, t, static_cast<int32_t>(q - static_cast<int64_t>(t) * nkb)};
     };
-    auto cursor_next = [&](Cursor &c) {
+    auto cursor_next = [&](Cursor c) -> Cursor {
         ++c.i;
-        if (c.i == len_a || c.i == ms || c.i == os || c.i == oe || c.i == hs || c.i == hs + len_b) {
-            if (c.i < n_steps)
-                cursor_at(c.i, c);
-            return;
-        }
+        if (c.i == len_a || c.i == ms || c.i == os || c.i == oe || c.i == hs || c.i == hs + len_b)
+            return c.i < n_steps ? cursor_at(c.i) : c;
         if (++c.kb == nkb) {
             c.kb = 0;
             c.t += c.i > os && c.i < oe ? static_cast<int32_t>(G) : 1;
         }
+        return c;
     };
 
     // stage st <- B and A boxes of K block kb of tile t, counted on full_bar(st)
@@ -504,11 +510,10 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
         grid_dependency_wait();
         // the ring is empty: start the B stream now instead of after the
         // tensor-memory allocation and the set-up barrier
-        Cursor c;
-        cursor_at(0, c);
+        Cursor c = cursor_at(0);
         for (int64_t i = 0; i < n_steps && pre < STAGES; ++i, ++pre) {
             issue_stage(pre, c.t, c.kb, pre == 0 ? args.extra_tx : 0u);
-            cursor_next(c);
+            c = cursor_next(c);
         }
     }
     if (warp == 1) {
@@ -530,13 +535,10 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
         uint32_t ph = 0;
         int pending = 0;
         bool alive = true;
-        Cursor c;
+        Cursor c{0, 0, 0};
         for (int64_t i = 0; i < n_steps; ++i) {
             if (i >= pre) {
-                if (i == pre)
-                    cursor_at(i, c);
-                else
-                    cursor_next(c);
+                c = i == pre ? cursor_at(i) : cursor_next(c);
                 if (!warp_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status,
                                        args.timeout_ns, kWhereProducerEmpty)) {
                     alive = false;
@@ -629,7 +631,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
                     }
 #pragma unroll
                     for (int j = 0; j < (MX ? 0 : KBOX); ++j) {
-                        if (j % Cfg::ISSUERS != e)
+                        if (W4 && j % Cfg::ISSUERS != e)
                             continue;
                         const uint64_t ad =
                             sdesc_k_sw128(base + Cfg::OFF_A + s * Cfg::A_BYTES + j * Cfg::A_BOX);
@@ -645,10 +647,14 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
                         } else {
                             const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_B + s * Cfg::B_BYTES +
                                                               j * Cfg::B_BOX);
+                            // (several issuers: issuer e takes K steps e KPER .. of each box)
+                            constexpr int KPER = (Cfg::BK / 16) / Cfg::ISSUERS;
 #pragma unroll
-                            for (int k = 0; k < Cfg::BK / 16; ++k)
+                            for (int kk = 0; kk < KPER; ++kk) {
+                                const int k = e * KPER + kk;
                                 tc_mma_f16(d_tmem, bd + 2u * k, ad + 2u * k, idesc,
-                                           (st != i || j != 0 || k != 0) ? 1u : 0u);
+                                           (st != i || j != 0 || kk != 0) ? 1u : 0u);
+                            }
                         }
                     }
                     tc_commit(empty_bar(s));
@@ -776,11 +782,13 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
             // registers spills beside FP4 B's converter warps, and FP4 B ends
             // on whole tiles.)
             // Its counter is read before the wait for this CTA's own sums, and
-            // (a tile of two parts) the other CTA's part with it, so neither
+            // (a tile of two parts, 16 columns a thread: 32 more registers
+            // spill beside 32 columns) the other CTA's part with it, so neither
             // round trip follows the last MMA.
             constexpr bool kKeep = !W4 && MPH <= 32 && NCH == 1;
+            constexpr bool kPreOther = kKeep && CH <= 16;
             bool last_known = false;
-            float other[CH];  // (kKeep, two parts) the other CTA's part
+            float other[kPreOther ? CH : 1];  // (kPreOther, two parts) the other CTA's part
             bool have_other = false;
             if (kKeep && parts > 1 && i == n_steps) {
                 if (leader) {
@@ -789,12 +797,14 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
                 }
                 epi_bar_sync<EPI_THREADS>();
                 last_known = *seen == static_cast<uint32_t>(parts - 1);
-                if (last_known && parts == 2) {
-                    const float *src = slot0 + static_cast<int64_t>(1 - my_slot) * (Cfg::BN * MP);
+                if constexpr (kPreOther) {
+                    if (last_known && parts == 2) {
+                        const float *src = slot0 + static_cast<int64_t>(1 - my_slot) * (Cfg::BN * MP);
 #pragma unroll
-                    for (int m = 0; m < CH; ++m)
-                        other[m] = __ldcg(src + (mb + m) * Cfg::BN + n_local);
-                    have_other = true;
+                        for (int m = 0; m < CH; ++m)
+                            other[m] = __ldcg(src + (mb + m) * Cfg::BN + n_local);
+                        have_other = true;
+                    }
                 }
             }
             // (inline: the loads of C and of the other part stay in flight)
@@ -808,30 +818,49 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
             float v[CH];  // this chunk's sums (with one chunk: the CTA's whole part)
 #pragma unroll 1
             for (int g = 0; g < NCH; ++g) {
-                // the issuers' partial sums of this chunk (all loads first, one
-                // wait), added in issuer order
-                uint32_t r[Cfg::ISSUERS][CH / 16][16];
+                // the issuers' partial sums of this chunk, added in issuer order:
+                // with several issuers (not FP4 B, whose converter warps leave
+                // few registers) all loads first and one wait, else one 16-column
+                // load and wait at a time
+                auto tmem_col = [&](int e, int h) {
+                    return tmem_base + ((32u * q) << 16) +
+                           static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP + mb + CH * g + 16 * h);
+                };
+                if constexpr (Cfg::ISSUERS > 1 && !W4) {
+                    uint32_t r[Cfg::ISSUERS][CH / 16][16];
 #pragma unroll
-                for (int e = 0; e < Cfg::ISSUERS; ++e)
+                    for (int e = 0; e < Cfg::ISSUERS; ++e)
 #pragma unroll
-                    for (int h = 0; h < CH / 16; ++h)
-                        tc_ld_32x32b_x16(tmem_base + ((32u * q) << 16) +
-                                             static_cast<uint32_t>((ab * Cfg::ISSUERS + e) * MP +
-                                                                   mb + CH * g + 16 * h),
-                                         r[e][h]);
+                        for (int h = 0; h < CH / 16; ++h)
+                            tc_ld_32x32b_x16(tmem_col(e, h), r[e][h]);
 #pragma unroll
-                for (int e = 0; e < Cfg::ISSUERS; ++e)
+                    for (int e = 0; e < Cfg::ISSUERS; ++e)
 #pragma unroll
-                    for (int h = 0; h < CH / 16; ++h)
-                        tc_wait_ld(r[e][h]);  // (the first waits; the rest tie the registers)
+                        for (int h = 0; h < CH / 16; ++h)
+                            tc_wait_ld(r[e][h]);  // (the first waits; the rest tie the registers)
 #pragma unroll
-                for (int e = 0; e < Cfg::ISSUERS; ++e)
+                    for (int e = 0; e < Cfg::ISSUERS; ++e)
 #pragma unroll
-                    for (int h = 0; h < CH / 16; ++h)
+                        for (int h = 0; h < CH / 16; ++h)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            v[16 * h + i] = e == 0 ? __uint_as_float(r[e][h][i])
-                                                   : v[16 * h + i] + __uint_as_float(r[e][h][i]);
+                            for (int i = 0; i < 16; ++i)
+                                v[16 * h + i] = e == 0 ? __uint_as_float(r[e][h][i])
+                                                       : v[16 * h + i] + __uint_as_float(r[e][h][i]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < Cfg::ISSUERS; ++e) {
+#pragma unroll
+                        for (int h = 0; h < CH / 16; ++h) {
+                            uint32_t r[16];
+                            tc_ld_32x32b_x16(tmem_col(e, h), r);
+                            tc_wait_ld(r);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[16 * h + i] = e == 0 ? __uint_as_float(r[i])
+                                                       : v[16 * h + i] + __uint_as_float(r[i]);
+                        }
+                    }
+                }
                 if (args.reduce) {
                     skinny_add<CH>(args, drow, n, mb + CH * g, v);  // every part adds itself into D
                 } else if (parts == 1) {
@@ -889,10 +918,10 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
 #pragma unroll
                         for (int m = 0; m < CH; ++m)
                             part[m] = v[m];
-                    } else if (kKeep && have_other) {
+                    } else if (kPreOther && have_other) {
 #pragma unroll
                         for (int m = 0; m < CH; ++m)
-                            part[m] = other[m];
+                            part[m] = other[kPreOther ? m : 0];
                     } else {
 #pragma unroll
                         for (int m = 0; m < CH; ++m)
