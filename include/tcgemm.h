@@ -249,7 +249,7 @@ gemm_status gemm_bf16_e2m1(int64_t M, int64_t N, int64_t K,
  *              The two forms take the same products; they may add them in a
  *              different order (bit-identical wherever every partial sum is
  *              exact in float32).
- *  Kernels: M <= 32 with packed codes runs on the skinny swap-AB kernel (128
+ *  Kernels: M <= 64 with packed codes runs on the skinny swap-AB kernel (128
  *  rows of B per tile on the MMA's M side, A's rows padded to 16 / 32 / 64 on
  *  its N side, the K blocks of all tiles shared out over the SMs, a tile's
  *  parts added in a fixed order by the last CTA to finish); otherwise the tile
@@ -387,8 +387,8 @@ const char *gemm_status_string(int status);
  *
  * With M <= 64 rows (bf16 / f16 B; not gathered, not seeded) the skinny
  * kernel runs where it measured faster than the tile kernel: M <= 16 with
- * N * K > 2^21, 16 < M <= 64 with K >= 2 N, and also 16 < M <= 32 with
- * K >= N and N * K > 2^21.  FP4 weights with M <= 128
+ * N * K > 2^21; 16 < M <= 64 with K >= 2 N, or with K >= N and
+ * N * K > 2^21.  FP4 weights with M <= 128
  * always take it.
  *
  *  kernel   0 = none (empty problem), 1 = tile kernel (128-row tiles, one
@@ -409,8 +409,7 @@ const char *gemm_status_string(int status);
  *           tiles, bn 128 or 256; MMA kind::mxf4 on packed codes / kind::mxf8f6f4
  *           on the 16U4_ALIGN16B image), 13 / 14 = the same on CTA pairs
  *           with 256 x 256 tiles, 15 = the skinny kernel on packed FP4
- *           operands (M <= 32, K > 0, or up to 64 rows when forced;
- *           block-scaled MMA kind::mxf4)
+ *           operands (M <= 64, K > 0; block-scaled MMA kind::mxf4)
  *  bm, bn   output tile; for the skinny kernel bm is the padded M and bn 128
  *  stages   shared-memory ring depth
  *  tiles    output tiles; splits = K slices per tile (skinny kernel)

@@ -424,15 +424,16 @@ bool skinny_eligible(int64_t M, int64_t K, bool gather, bool seeded)
 // 4096^2 14.0 / 16.8, 28672 x 4096 44.1 / 45.7, 16384 x 2048 20.4 / 17.2,
 // 4096 x 8192 19.5 / 35.5; M = 64: 4096^2 22.6 / 16.9, 28672 x 4096
 // 53.8 / 46.7, 1024 x 8192 21.0 / 34.6; 48 x 8192^2 36.3 / 31.3; M = 16:
-// 1024^2 7.7 / 6.8.
+// 1024^2 7.7 / 6.8.  After the skinny epilogue's register spills at MP = 64
+// were removed: M = 64: 4096^2 14.9 / 16.9, 2048^2 10.1 / 10.4, 28672 x 4096
+// 47.1 / 47.5, 8192 x 4096 19.7 / 17.8, 14336 x 4096 29.4 / 26.7; 40 x 4096^2
+// 14.7 / 16.8; 48 x 8192^2 31.2 / 31.5; 33 x 28672 x 4096 44.9 / 45.8.
 bool skinny_wins(int64_t M, int64_t N, int64_t K)
 {
     const bool big = N * K > (int64_t(1) << 21);  // (N, K < 2^31: no overflow)
     if (M <= 16)
         return big;
-    if (M <= 32)
-        return K >= 2 * N || (big && K >= N);
-    return K >= 2 * N;
+    return K >= 2 * N || (big && K >= N);
 }
 
 // The skinny kernel's plan for m <= 64 rows (stream-K over the SMs).

@@ -303,16 +303,15 @@ gemm_plan e2m1_plan(int64_t M, int64_t N, int64_t K, int image, int sm_count)
         return p;
     int fk = 0, fbn = 0;
     forced_tile(&fk, &fbn);
-    // M <= 32 with packed codes (and K > 0): the skinny kernel, unless a tile
-    // form is forced; forced (kernel 15) wherever it can run (M <= 64).  With
-    // 33..64 rows its N = 64 MMAs, two dependent ones per issuer and stage,
-    // take ~1150 cycles a stage against ~650 for the stage's data, and the tile
-    // kernel measured faster (microseconds, skinny / tile, C, fp32 out, graph
-    // replay over operand copies): 64 x 28672 x 4096 32.3 / 21.3, 64 x 4096^2
-    // 15.1 / 12.2, 48 x 8192^2 22.8 / 27.3; 32 x 28672 x 4096 17.3 / 21.7,
-    // 16 x 4096^2 8.1 / 12.0.
+    // M <= 64 with packed codes (and K > 0): the skinny kernel, unless a tile
+    // form is forced; forced (kernel 15) wherever it can run.  Measured
+    // (microseconds, skinny / tile, C, fp32 out, graph replay over operand
+    // copies): 16 x 4096^2 8.1 / 12.0, 32 x 28672 x 4096 17.3 / 21.7,
+    // 33 x 28672 x 4096 20.9 / 23.8, 64 x 28672 x 4096 18.4 / 21.3, 64 x 4096^2
+    // 9.9 / 12.2, 48 x 8192^2 14.8 / 19.3, 64 x 2048 x 8192 12.2 / 18.6,
+    // 64 x 1024^2 5.3 / 6.7.
     const bool skinny_ok = image == 0 && M <= 64 && K > 0;
-    if (skinny_ok && (fk == 15 || (M <= 32 && !(fk >= 11 && fk <= 14)))) {
+    if (skinny_ok && (fk == 15 || !(fk >= 11 && fk <= 14))) {
         const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
         const int64_t tiles = ceil_div(N, 128);
         const int64_t nkb = ceil_div(K, tcg::skinny_mx_kstage());

@@ -51,6 +51,9 @@
 #ifndef TCG_SKINNY_MX_ISSUERS16
 #define TCG_SKINNY_MX_ISSUERS16 4
 #endif
+#ifndef TCG_SKINNY_MX_ISSUERS32
+#define TCG_SKINNY_MX_ISSUERS32 2
+#endif
 #ifndef TCG_SKINNY_BF16_ISSUERS16
 #define TCG_SKINNY_BF16_ISSUERS16 4
 #endif
@@ -108,7 +111,9 @@ struct SkinnyCfg {
     // MX_PER of them (consecutive, so one 128-element chunk of scales), copying
     // that chunk's scale tiles into TMEM columns of its own.
     static constexpr int ISSUERS =
-        W4 ? (MP <= 16 ? 4 : 2) : (MX ? (MP <= 16 ? TCG_SKINNY_MX_ISSUERS16 : 2) : (MP <= 16 ? TCG_SKINNY_BF16_ISSUERS16 : 1));
+        W4 ? (MP <= 16 ? 4 : 2)
+           : (MX ? (MP <= 16 ? TCG_SKINNY_MX_ISSUERS16 : (MP <= 32 ? TCG_SKINNY_MX_ISSUERS32 : 2))
+                 : (MP <= 16 ? TCG_SKINNY_BF16_ISSUERS16 : 1));
     static constexpr int MX_PER = MX ? 4 / ISSUERS : 0;
     // Epilogue warps: four (one per TMEM lane quarter), or eight for bf16 /
     // f16 B with MP = 64, two per quarter, each finishing 32 of the 64
@@ -708,30 +713,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP, KBOX, W4, MX>::THREADS, 1)
             }
             epi_bar_sync<EPI_THREADS>();
         }
-        // C of a piece's tile into L2 two pieces ahead (the first two now), so
-        // that the epilogue's loads of C do not wait for HBM behind the MMAs:
-        // one 128-byte line (32 columns) of a row of A per thread and pass
-        const bool pf_c = args.has_c && !args.reduce;
-        const int32_t et = static_cast<int32_t>(threadIdx.x) - 32 * Cfg::EPI_WARP0;
-        auto prefetch_c = [&](int64_t ip) {
-            const int32_t tp = static_cast<int32_t>(order(ip) / nkb);
-            for (int32_t j = et; j < MP * (Cfg::BN / 32); j += EPI_THREADS) {
-                const int32_t r = skinny_row(args, drow, j / (Cfg::BN / 32));
-                const int32_t n0 = tp * Cfg::BN + 32 * (j % (Cfg::BN / 32));
-                if (r >= 0 && n0 < args.N)
-                    prefetch_l2(args.C + static_cast<int64_t>(r) * args.ldc + n0);
-            }
-        };
-        int64_t ipf = 0;  // first step of the next piece whose C is to be prefetched
-        for (int k = 0; k < 2 && pf_c && ipf < n_steps; ++k, ipf = piece_end(ipf))
-            prefetch_c(ipf);
         int ab = 0;
         uint32_t aph = 0;
         for (int64_t i = 0; i < n_steps;) {
-            if (pf_c && ipf < n_steps) {
-                prefetch_c(ipf);
-                ipf = piece_end(ipf);
-            }
             const int32_t t = static_cast<int32_t>(order(i) / nkb);
             i = piece_end(i);
             const int32_t n = t * Cfg::BN + n_local;

@@ -212,7 +212,7 @@ def test_e2m1_argument_checks(lib):
 
 
 def test_e2m1_plan(lib):
-    """gemm_e2m1: M <= 32 with packed codes on the skinny kernel (15); otherwise single
+    """gemm_e2m1: M <= 64 with packed codes on the skinny kernel (15); otherwise single
     CTAs (11 packed codes, 12 the 16U4 image), 256 wide unless 128-wide tiles take
     fewer waves; CTA pairs with 256 x 256 tiles (13 / 14) when forced; forced forms
     apply to gemm_e2m1 alone."""
@@ -230,12 +230,11 @@ def test_e2m1_plan(lib):
     assert (p.kernel, p.bn, p.tiles, p.grid) == (12, 256, 112, 112)  # the 16U4 image: tiles
     p = binding.gemm_query_plan(16, 28672, 4096, e2m1=0, sm_count=148)
     assert (p.kernel, p.bm, p.bn, p.tiles, p.grid) == (15, 16, 128, 224, 148)  # packed: skinny
-    assert binding.gemm_query_plan(32, 1024, 512, e2m1=0, sm_count=148).kernel == 15
-    assert binding.gemm_query_plan(33, 1024, 512, e2m1=0, sm_count=148).kernel == 11
+    assert binding.gemm_query_plan(33, 1024, 512, e2m1=0, sm_count=148).kernel == 15
+    assert binding.gemm_query_plan(64, 1024, 512, e2m1=0, sm_count=148).kernel == 15
     assert binding.gemm_query_plan(65, 1024, 512, e2m1=0, sm_count=148).kernel == 11
     binding.gemm_debug_force_tile(15, 128)
-    try:  # forced, the skinny form takes up to 64 rows
-        assert binding.gemm_query_plan(64, 1024, 512, e2m1=0, sm_count=148).kernel == 15
+    try:  # forced, the skinny form still takes at most 64 rows
         assert binding.gemm_query_plan(65, 1024, 512, e2m1=0, sm_count=148).kernel == 11
     finally:
         binding.gemm_debug_force_tile(0, 0)
@@ -300,25 +299,26 @@ def test_plan_matches_the_dispatch_rules(lib):
     # 16 < M <= 64: the tile kernel unless K is long against N
     assert binding.gemm_query_plan(40, 1000, 64, sm_count=148).kernel == 1
     assert binding.gemm_query_plan(64, 28672, 4096, sm_count=148).kernel != 2
-    assert binding.gemm_query_plan(32, 4096, 4096, sm_count=148).kernel == 2  # K >= N, 17..32 rows
+    assert binding.gemm_query_plan(32, 4096, 4096, sm_count=148).kernel == 2  # K >= N, N K > 2^21
     assert binding.gemm_query_plan(32, 16384, 2048, sm_count=148).kernel != 2
     assert binding.gemm_query_plan(32, 1024, 1024, sm_count=148).kernel != 2  # N K <= 2^21
-    assert binding.gemm_query_plan(33, 4096, 4096, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(33, 4096, 4096, sm_count=148).kernel == 2
+    assert binding.gemm_query_plan(64, 8192, 4096, sm_count=148).kernel != 2  # K < N
     p = binding.gemm_query_plan(32, 4096, 8192, sm_count=148)
     assert (p.kernel, p.bm) == (2, 32)
     p = binding.gemm_query_plan(40, 1024, 8192, sm_count=148)
     assert (p.kernel, p.bm) == (2, 64)
-    assert binding.gemm_query_plan(64, 4096, 4096, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(64, 4096, 4096, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(64, 4096, 16384, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(48, 2048, 8192, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(64, 4096, 14336, sm_count=148).kernel == 2
-    # the rule's edge: K >= 2N for 17..64 rows (17..32 rows also K >= N when N K > 2^21)
+    # the rule's edge: K >= 2N for 17..64 rows, or K >= N when N K > 2^21
     assert binding.gemm_query_plan(17, 1024, 2048, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(32, 1024, 2047, sm_count=148).kernel == 1
     assert binding.gemm_query_plan(33, 1024, 2048, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(64, 1024, 2040, sm_count=148).kernel == 1
     # scattered and accumulating calls follow the same rule; gathered rows never
-    assert binding.gemm_query_plan(48, 4096, 4096, scatter=True, sm_count=148).kernel != 2
+    assert binding.gemm_query_plan(48, 8192, 4096, scatter=True, sm_count=148).kernel != 2
     assert binding.gemm_query_plan(32, 4096, 4096, scatter=True, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(16, 4096, 4096, scatter=True, sm_count=148).kernel == 2
     assert binding.gemm_query_plan(16, 4096, 4096, gather=True, sm_count=148).kernel != 2

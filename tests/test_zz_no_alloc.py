@@ -58,12 +58,12 @@ def _twice(p, check):
         check(D, call)
 
 
-# (M, N, K): 1, 16, 33, 48 and 64 rows.  For 33..64 rows with K < 2N (4096 x 4096)
+# (M, N, K): 1, 16, 33, 48 and 64 rows.  For 17..64 rows with K < N (8192 x 4096)
 # gemm_bf16 itself runs the tile kernel, while this entry point always runs the
 # skinny one (64 rows: its eight-warp epilogue); 16 x 8 x 32 is small enough for
 # the warp-level kernel.
-SHAPES = [(1, 4096, 4096), (16, 28672, 4096), (33, 4096, 4096), (48, 2048, 8192),
-          (64, 4096, 4096), (64, 640, 136), (16, 8, 32)]
+SHAPES = [(1, 4096, 4096), (16, 28672, 4096), (33, 8192, 4096), (48, 2048, 8192),
+          (64, 8192, 4096), (64, 640, 136), (16, 8, 32)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
