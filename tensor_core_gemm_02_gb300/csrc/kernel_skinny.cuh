@@ -25,11 +25,11 @@
 //              (MP x 64) at consecutive K, so each row of B is read in
 //              KBOX * 128-byte runs (FP4 B: the codes, 128 rows x 128 bytes,
 //              and the stage's scale rows)
-//   warps 1..I MMA issuers (I = ISSUERS: 1, or 2 / 4 for FP4 B and for
-//              both operands FP4): tcgen05.mma M=128 N=MP K=16 (both FP4:
-//              block-scaled, K=64), each issuer into two TMEM accumulators of
-//              its own (FP4 B: A operand from TMEM)
-//   next 4     epilogue (8 for bf16 / f16 B with MP = 64, two per TMEM lane
+//   warps 1..I MMA issuers (I = ISSUERS: 4 for MP = 16, 2 for FP4 B and for
+//              both operands FP4 with MP = 32 / 64, else 1): tcgen05.mma M=128
+//              N=MP K=16 (both FP4: block-scaled, K=64), each issuer into two
+//              TMEM accumulators of its own (FP4 B: A operand from TMEM)
+//   next 4     epilogue (8 for MP = 64 except FP4 B, two per TMEM lane
 //              quarter, 32 columns each): tcgen05.ld (the issuers' partial sums added in
 //              order), partial or final fma.rn(alpha, acc, beta*C) with
 //              coalesced plain loads/stores (lanes walk along N); with
@@ -115,9 +115,9 @@ struct SkinnyCfg {
            : (MX ? (MP <= 16 ? TCG_SKINNY_MX_ISSUERS16 : (MP <= 32 ? TCG_SKINNY_MX_ISSUERS32 : 2))
                  : (MP <= 16 ? TCG_SKINNY_BF16_ISSUERS16 : 1));
     static constexpr int MX_PER = MX ? 4 / ISSUERS : 0;
-    // Epilogue warps: four (one per TMEM lane quarter), or eight for bf16 /
-    // f16 B with MP = 64, two per quarter, each finishing 32 of the 64
-    // columns, which halves a thread's chain of loads and stores per piece.
+    // Epilogue warps: four (one per TMEM lane quarter), or eight with MP = 64
+    // (bf16 / f16 B and both operands FP4), two per quarter, each finishing 32
+    // of the 64 columns, which halves a thread's chain of loads and stores.
     static constexpr int EPI_SPLIT = (!W4 && MP == 64) ? 2 : 1;
     static constexpr int EPI_WARPS = 4 * EPI_SPLIT;
     static constexpr int EPI_WARP0 = 1 + ISSUERS;
