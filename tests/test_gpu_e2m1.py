@@ -225,3 +225,18 @@ def test_nan_scale_gives_nan():
     keep = np.ones(128, bool)
     keep[5] = False
     assert np.array_equal(got[keep], ref[keep].astype(np.float32).astype(np.float64))
+
+
+def test_skinny_nan_scale_gives_nan():
+    """The skinny form (16 rows, K split over CTAs): a NaN scale byte of A makes
+    its row of D NaN through the split tiles' partial sums; the other rows are
+    exact."""
+    p = workloads.e2m1_problem(14, 16, 2000, 4096, values="exact", alpha=1.0, beta=0.0)
+    assert binding.gemm_query_plan(16, 2000, 4096, e2m1=0).kernel == 15
+    p.As[40, 5] = 255   # block 40 of row 5 of A
+    ref, _ = oracle_e2m1(p)
+    got = to_f64(run_e2m1(p))
+    assert np.isnan(got[5]).all() and np.isnan(ref[5]).all()
+    keep = np.ones(16, bool)
+    keep[5] = False
+    assert np.array_equal(got[keep], ref[keep].astype(np.float32).astype(np.float64))
