@@ -223,6 +223,12 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
             st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(abort_flag)), rank ^ 1u), 1u);
     };
 
+    // Single CTAs loading plain boxes: the first tile's first stages are issued
+    // right after the barriers exist, before the tensor-memory allocation and
+    // the set-up barrier (one-wave problems spend a good part of their time
+    // reaching the first full stage).  `pre` stages; the producer skips them.
+    constexpr bool kPrefill = !PAIR && MC == 1 && MX == 0;
+    int pre = 0;
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -255,6 +261,25 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
             tma_prefetch_desc(&tmC);
         if (args.d_tma)
             tma_prefetch_desc(&tmD);
+        if constexpr (kPrefill) {
+            if (!args.gather && args.num_k_blocks > 0 && cta_set < args.num_tiles) {
+                // (inputs are read only once the previous kernel in the stream is done)
+                if (!args.co_tail)
+                    grid_dependency_wait();
+                int32_t mb, nb;
+                tile_coords(cta_set, args, mb, nb);
+                const int32_t m0 = mb * Cfg::TILE_M, nb0 = nb * TILE_N;
+                const int32_t n = min(STAGES, args.num_k_blocks);
+                for (; pre < n; ++pre) {
+                    const int32_t k0 = pre * Cfg::BK;
+                    mbar_arrive_expect_tx(full_bar(pre), Cfg::STAGE_TX + (pre == 0 ? args.extra_tx : 0u));
+                    tma_load_2d(base + Cfg::OFF_A + pre * Cfg::A_BYTES, &tmA, full_bar(pre), k0, m0);
+                    for (int j = 0; j < NSUB; ++j)
+                        tma_load_2d(base + Cfg::OFF_B + pre * Cfg::B_BYTES + j * Cfg::B_SUB_BYTES, &tmB,
+                                    full_bar(pre), k0, nb0 + j * BN);
+                }
+            }
+        }
     }
     if (warp == 1) {
         if (PAIR) {
@@ -288,6 +313,7 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
         int pending = 0;  // stages issued and not yet seen consumed (for teardown)
         bool first = true;
         bool alive = true;
+        int pre_left = __shfl_sync(0xffffffffu, pre, 0);  // prefilled stages of the first tile
         for (int32_t t = cta_set; t < args.num_tiles && alive; t += cta_sets) {
             int32_t mb, nb;
             tile_coords(t, args, mb, nb);
@@ -316,6 +342,16 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
                 }
             }
             for (int32_t kb = 0; kb < args.num_k_blocks; ++kb) {
+                if (pre_left > 0) {  // issued before the set-up barrier
+                    --pre_left;
+                    first = false;
+                    pending = min(pending + 1, STAGES);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    continue;
+                }
                 if (!warp_wait_bounded<true>(empty_bar(s), ph ^ 1u, abort_flag, args.status,
                                        args.timeout_ns, kWhereProducerEmpty)) {
                     alive = false;
