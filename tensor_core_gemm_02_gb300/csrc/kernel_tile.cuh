@@ -223,11 +223,12 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
             st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(abort_flag)), rank ^ 1u), 1u);
     };
 
-    // Single CTAs loading plain boxes: the first tile's first stages are issued
-    // right after the barriers exist, before the tensor-memory allocation and
-    // the set-up barrier (one-wave problems spend a good part of their time
-    // reaching the first full stage).  `pre` stages; the producer skips them.
-    constexpr bool kPrefill = !PAIR && MC == 1 && MX == 0;
+    // Single CTAs loading plain boxes (and, FP4, the stage's scale rows): the
+    // first tile's first stages are issued right after the barriers exist,
+    // before the tensor-memory allocation and the set-up barrier (one-wave
+    // problems spend a good part of their time reaching the first full stage).
+    // `pre` stages; the producer skips them.
+    constexpr bool kPrefill = !PAIR && MC == 1;
     int pre = 0;
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -271,7 +272,14 @@ __global__ void __launch_bounds__(TileCfg<BN, STAGES, PAIR, NSUB, MC, MX>::THREA
                 const int32_t m0 = mb * Cfg::TILE_M, nb0 = nb * TILE_N;
                 const int32_t n = min(STAGES, args.num_k_blocks);
                 for (; pre < n; ++pre) {
-                    const int32_t k0 = pre * Cfg::BK;
+                    const int32_t k0 = MX ? pre * 128 : pre * Cfg::BK;
+                    if (MX) {
+                        const uint32_t sfs = base + Cfg::OFF_SFS + pre * Cfg::SF_STAGE_BYTES;
+                        mbar_arrive_expect_tx(sf_full_bar(pre), Cfg::SF_STAGE_BYTES);
+                        tma_load_2d(sfs, &tmSFA, sf_full_bar(pre), m0, pre * Cfg::SF_KB);
+                        tma_load_2d(sfs + Cfg::SF_KB * Cfg::BM, &tmSFB, sf_full_bar(pre), nb * TILE_N,
+                                    pre * Cfg::SF_KB);
+                    }
                     mbar_arrive_expect_tx(full_bar(pre), Cfg::STAGE_TX + (pre == 0 ? args.extra_tx : 0u));
                     tma_load_2d(base + Cfg::OFF_A + pre * Cfg::A_BYTES, &tmA, full_bar(pre), k0, m0);
                     for (int j = 0; j < NSUB; ++j)
